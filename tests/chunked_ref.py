@@ -1,0 +1,181 @@
+"""Chunked fp64 restatements of the KDA forward pass, used only to pin the oracle.
+
+The oracle walks the recurrence one token at a time.  The functions here reach
+the same result by the chunk-parallel route that the FlashKDA pages describe
+(guancyxx.cn FlashKDA article, sections 2.1 and 2.2: chunking, the "L / Mqk"
+construction, the matrix inversion, and the chunk-wise delta-rule recurrence),
+so agreement to ~1e-10 pins the oracle's recurrence against an independent
+formulation, and at the same time checks the algebra that a chunked GPU kernel
+relies on.
+
+Derivation (per chunk, local rows i = 0..C-1, S0 = state at chunk start,
+G_i = sum_{s<=i} a_s per channel, Gamma_i = exp(G_i)):
+  u_j := b_j (v_j - S'_j^T k^_j) satisfies (I + A) U = diag(b) (V - (K^ . Gamma) S0),
+  with A[i, j] = b_i sum_c k^_ic k^_jc exp(G_ic - G_jc) for j < i.  Hence
+  U = T diag(b) V - T diag(b) (K^ . Gamma) S0 with T = (I + A)^{-1},
+  O = scale ((Q^ . Gamma) S0 + Aqk U), Aqk[i, j] = sum_c q^_ic k^_jc exp(G_ic - G_jc), j <= i,
+  S_next = Diag(Gamma_last) S0 + (K^ . Gamma_last / Gamma)^T U.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from gated_delta_rule_23_gb300.inputs import bf16_to_f32
+
+
+def prepare(p):
+    """Widen a problem's inputs and apply the per-token maps (norm, beta sigmoid, gate) in fp64."""
+    f = lambda a: bf16_to_f32(a).astype(np.float64)
+    q, k, v, g, beta = f(p.q), f(p.k), f(p.v), f(p.g), f(p.beta)
+    qh = q / np.sqrt((q * q).sum(-1, keepdims=True) + 1e-6)
+    kh = k / np.sqrt((k * k).sum(-1, keepdims=True) + 1e-6)
+    b = 1.0 / (1.0 + np.exp(-beta))
+    z = np.exp(p.A_log.astype(np.float64))[None, None, :, None] * (g + p.dt_bias.astype(np.float64)[None, None])
+    a = p.lower_bound / (1.0 + np.exp(-z))
+    return qh, kh, v, b, a
+
+
+def seq_ranges(p):
+    if p.cu_seqlens is None:
+        return [(n, 0, p.T) for n in range(p.B)]
+    return [(n, int(p.cu_seqlens[n]), int(p.cu_seqlens[n + 1])) for n in range(p.N)]
+
+
+def inv_forward_substitution(A):
+    """(I + A)^{-1} for strictly lower-triangular A, row by row."""
+    C = A.shape[0]
+    T = np.eye(C)
+    for i in range(1, C):
+        T[i, :i] = -A[i, :i] @ T[:i, :i]
+    return T
+
+
+def inv_neumann(A):
+    """(I + A)^{-1} = (I - A)(I + A^2)(I + A^4)... : exact once A^(2^m) = 0 (A nilpotent)."""
+    C = A.shape[0]
+    T = np.eye(C) - A
+    P = A @ A
+    m = 2
+    while m < C:
+        T = T @ (np.eye(C) + P)
+        P = P @ P
+        m *= 2
+    return T
+
+
+def inv_blocked(A, blk=16):
+    """(I + A)^{-1} by 16x16 diagonal inverses and block merges T_ba = -T_bb sum_k A_bk T_ka."""
+    C = A.shape[0]
+    nb = (C + blk - 1) // blk
+    T = np.zeros_like(A)
+    sl = lambda b: slice(b * blk, min(C, (b + 1) * blk))
+    for b in range(nb):
+        T[sl(b), sl(b)] = inv_forward_substitution(A[sl(b), sl(b)])
+    for d in range(1, nb):
+        for b in range(d, nb):
+            a = b - d
+            acc = sum(A[sl(b), sl(m)] @ T[sl(m), sl(a)] for m in range(a, b))
+            T[sl(b), sl(a)] = -T[sl(b), sl(b)] @ acc
+    return T
+
+
+def chunked_direct(p, C=64, inverse=inv_forward_substitution):
+    """Chunk-parallel form with exp(G_i - G_j) taken directly (masked before exp)."""
+    qh, kh, v, b, a = prepare(p)
+    H = p.H
+    out = np.zeros(qh.shape)
+    final = np.zeros((p.N, H, 128, 128))
+    init = p.initial_state_f64()
+    for n, bos, eos in seq_ranges(p):
+        bidx = 0 if p.cu_seqlens is not None else n
+        for h in range(H):
+            S = np.zeros((128, 128)) if init is None else init[n, h].T.copy()
+            for c0 in range(bos, eos, C):
+                c1 = min(eos, c0 + C)
+                sl = (bidx, slice(c0, c1), h)
+                Q, K, V, B, Ag = qh[sl], kh[sl], v[sl], b[sl], a[sl]
+                L = c1 - c0
+                G = np.cumsum(Ag, axis=0)                      # [L, 128]
+                diff = G[:, None, :] - G[None, :, :]           # [i, j, c]
+                low = np.tril(np.ones((L, L), dtype=bool))
+                decay = np.exp(np.where(low[:, :, None], diff, -np.inf))
+                Aqk = np.einsum("ic,jc,ijc->ij", Q, K, decay)
+                Akk = B[:, None] * np.einsum("ic,jc,ijc->ij", K, K, decay)
+                Akk = np.tril(Akk, -1)
+                Tm = inverse(Akk)
+                Gam = np.exp(G)
+                W = Tm @ (B[:, None] * (K * Gam))
+                Ut = Tm @ (B[:, None] * V)
+                U = Ut - W @ S
+                out[sl] = p.scale * ((Q * Gam) @ S + Aqk @ U)
+                Kt = K * np.exp(G[-1][None, :] - G)
+                S = np.exp(G[-1])[:, None] * S + Kt.T @ U
+            final[n, h] = S.T
+    return out, final
+
+
+def chunked_subblock(p, C=64, blk=16):
+    """Chunk-parallel form with the decay factorised through 16-row sub-blocks.
+
+    Within a chunk no factor exp(G_i - G_j) is formed from a cumulative sum that
+    spans more than one 16-row block with a positive exponent.  Per channel:
+      alpha = exp(a); P_i = prod of alpha over block(i) up to and including i;
+      E_j = prod of alpha over block(j) after j; D_b = product over block b.
+    For i in block b' and j in block b <= b':
+      exp(G_i - G_j) = P_i * E_j * s(b', b),  s(b, b) = 1 / D_b,
+      s(b', b) = prod_{b < m < b'} D_m for b' > b.
+    Chunk-start factors: exp(G_i) = P_i prod_{m < b(i)} D_m and
+    exp(G_last - G_j) = E_j prod_{m > b(j)} D_m.
+    With lower_bound >= -5 every P, E, D and 1/D lies in [2^-115.5, 2^115.5].
+    """
+    qh, kh, v, b, a = prepare(p)
+    H = p.H
+    out = np.zeros(qh.shape)
+    final = np.zeros((p.N, H, 128, 128))
+    init = p.initial_state_f64()
+    for n, bos, eos in seq_ranges(p):
+        bidx = 0 if p.cu_seqlens is not None else n
+        for h in range(H):
+            S = np.zeros((128, 128)) if init is None else init[n, h].T.copy()
+            for c0 in range(bos, eos, C):
+                c1 = min(eos, c0 + C)
+                L = c1 - c0
+                sl = (bidx, slice(c0, c1), h)
+                Q = np.zeros((C, 128)); K = np.zeros((C, 128)); V = np.zeros((C, 128))
+                B = np.zeros(C); al = np.ones((C, 128))
+                Q[:L], K[:L], V[:L], B[:L], al[:L] = qh[sl], kh[sl], v[sl], b[sl], np.exp(a[sl])
+                nb = C // blk
+                P = np.ones((C, 128)); E = np.ones((C, 128)); D = np.ones((nb, 128))
+                for bb in range(nb):
+                    r = slice(bb * blk, (bb + 1) * blk)
+                    P[r] = np.cumprod(al[r], axis=0)
+                    E[r] = np.concatenate([np.cumprod(al[r][::-1], axis=0)[::-1][1:], np.ones((1, 128))])
+                    D[bb] = P[r][-1]
+                pre = np.ones((nb, 128)); post = np.ones((nb, 128))
+                for bb in range(1, nb):
+                    pre[bb] = pre[bb - 1] * D[bb - 1]
+                for bb in range(nb - 2, -1, -1):
+                    post[bb] = post[bb + 1] * D[bb + 1]
+                Akk = np.zeros((C, C)); Aqk = np.zeros((C, C))
+                for b1 in range(nb):
+                    ri = slice(b1 * blk, (b1 + 1) * blk)
+                    Lk, Lq = K[ri] * P[ri], Q[ri] * P[ri]
+                    for b0 in range(b1 + 1):
+                        rj = slice(b0 * blk, (b0 + 1) * blk)
+                        s = 1.0 / D[b0] if b0 == b1 else np.prod(D[b0 + 1:b1], axis=0)
+                        R = K[rj] * E[rj] * s
+                        Akk[ri, rj] = Lk @ R.T
+                        Aqk[ri, rj] = Lq @ R.T
+                Akk = np.tril(Akk, -1) * B[:, None]
+                Aqk = np.tril(Aqk)
+                Tm = inv_blocked(Akk, blk)
+                Gam = P * np.repeat(pre, blk, axis=0)
+                Tb = Tm * B[None, :]
+                W = Tb @ (K * Gam)
+                U = Tb @ V - W @ S
+                O = p.scale * ((Q * Gam) @ S + Aqk @ U)
+                out[sl] = O[:L]
+                Kt = K * E * np.repeat(post, blk, axis=0)
+                S = (pre[-1] * D[-1])[:, None] * S + Kt.T @ U
+            final[n, h] = S.T
+    return out, final
