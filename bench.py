@@ -1,0 +1,355 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA chunked forward pass on GB300.
+
+Default workload: fixed-length prefill, B = 1, T = 8192, H = 96, K = V = 128, bf16
+initial and final state (the H = 96 fixed-length row of the FlashKDA benchmark
+tables).  One step = one kda_fwd launch over the whole workload.  Inputs (1.0 GB)
+exceed the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle instead (the
+reference arm for this method: a deliberately plain program on the host cores).
+Under torchrun each rank runs its own replica of the workload (weak scaling, no
+collective on the data path); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "KDA fwd ms & tokens·heads/s at T=8192 H=96; % of HBM/tensor roofline"
+UNIT = "tokens·heads/s"
+KERNEL_SRC = os.path.join(ROOT, "gated_delta_rule_23_gb300", "csrc", "kda_fwd.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kda_fwd_kernel_T8192_H96_bf16state.md")
+# FlashKDA on GB200, H=96 fixed length, T=8192: 1.01 ms (guancyxx.cn FlashKDA article, section 三,
+# GB200 table) -> tokens*heads per second.  Another machine: context, not the target.
+PAGES_GB200_TOKHEADS_PER_S = 8192 * 96 / 1.01e-3
+
+
+def workload_config(p, idx):
+    st = {STATE_BF16: "bf16", STATE_FP32: "fp32"}.get(p.state_dtype, "none")
+    return {
+        "workload": WORKLOADS[idx], "B": p.B, "T": p.T, "H": p.H, "K": 128, "V": 128,
+        "state_dtype": st, "initial_state": p.initial_state is not None, "final_state": p.want_final,
+        "varlen_lengths": None if p.cu_seqlens is None else [int(x) for x in np.diff(p.cu_seqlens)],
+        "l2": "inputs larger than L2 (no flush)",
+    }
+
+
+def algorithmic_bytes(p):
+    """HBM bytes one launch must move: q, k, v, g, beta in; out; states; parameters."""
+    th = p.token_heads()
+    b = th * (4 * 128 * 2 + 2 + 128 * 2)
+    es = {STATE_BF16: 2, STATE_FP32: 4}.get(p.state_dtype, 0)
+    per_state = p.N * p.H * 128 * 128 * es
+    b += per_state * ((p.initial_state is not None) + bool(p.want_final and es))
+    b += p.H * 4 + p.H * 128 * 4 + (0 if p.cu_seqlens is None else 8 * (p.N + 1))
+    return b
+
+
+def kernel_source_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(p):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms between start() and stop()."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.samples = []
+        self.proc = None
+        self.window = None
+        self.device_index = device_index
+
+    def _gpu_id(self):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def start(self):
+        gid = self._gpu_id()
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gid:
+            cmd += ["-i", gid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._reader, daemon=True).start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 7:
+                continue
+            rows.append((ts, parts))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for r in rows if self.window and self.window[0] - 0.2 <= r[0] <= self.window[1] + 0.2]
+        if not inside:   # timed region shorter than one sampling period: nearest sample
+            mid = sum(self.window) / 2 if self.window else rows[-1][0]
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1][0]) for r in inside if num(r[1][0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[1][3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][1][1]), "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((num(r[1][2]) or 0.0) for r in inside)}
+
+
+def cpu_baseline(p, idx, max_heads=24):
+    """The oracle, as it stands, on a bounded sample: the first heads over every token."""
+    import oracle
+    from gated_delta_rule_23_gb300.inputs import subset_heads
+    nh = min(p.H, max_heads)
+    sub = subset_heads(p, list(range(nh)))
+    threads = min(oracle.default_threads(), nh * p.N)
+    t0 = time.perf_counter()
+    oracle.kda_fwd_problem(sub, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": sub.token_heads() / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{nh} of {p.H} heads, all {int(p.seq_lengths().sum())} tokens of workload {idx}; "
+                      f"fp64 token-by-token recurrence, {dt:.2f} s wall"}
+
+
+def run_reference(args, p, idx, rank):
+    """Reference arm: the CPU oracle timed per step on a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+    from gated_delta_rule_23_gb300.inputs import subset_heads
+    threads = oracle.default_threads()
+    nh = min(p.H, threads)
+    ntok = min(1024, p.T)
+    sub = subset_heads(p, list(range(nh)))
+    if sub.cu_seqlens is None:
+        import dataclasses
+        sub = dataclasses.replace(sub, q=sub.q[:, :ntok].copy(), k=sub.k[:, :ntok].copy(), v=sub.v[:, :ntok].copy(),
+                                  g=sub.g[:, :ntok].copy(), beta=sub.beta[:, :ntok].copy())
+    else:   # the first sequences up to ~ntok tokens
+        import dataclasses
+        cu = sub.cu_seqlens
+        n_keep = max(1, int(np.searchsorted(cu, ntok, side="right")) - 1)
+        end = int(cu[n_keep])
+        sub = dataclasses.replace(sub, q=sub.q[:, :end].copy(), k=sub.k[:, :end].copy(), v=sub.v[:, :end].copy(),
+                                  g=sub.g[:, :end].copy(), beta=sub.beta[:, :end].copy(), cu_seqlens=cu[:n_keep + 1].copy(),
+                                  initial_state=None if sub.initial_state is None else sub.initial_state[:n_keep].copy())
+    for _ in range(args.warmup):
+        oracle.kda_fwd_problem(sub, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kda_fwd_problem(sub, nthreads=threads)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = sub.token_heads() / dt
+    sample = f"{nh} heads x {int(sub.seq_lengths().sum())} tokens of workload {idx} per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(p, idx),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, p, idx, rank, world):
+    import torch
+    import torch.distributed as dist
+    from gated_delta_rule_23_gb300 import KDAHostRunner, kda_fwd
+    from tests.gpu_util import to_device
+
+    dev = to_device(p)
+    out = torch.empty_like(dev["q"])
+    fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda") if dev["sdt"] is not None else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+                p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    sampler.mark(t_host0, t_host1)
+    sampler.stop()
+    ms_step = ms_total / args.steps
+
+    # end to end through the public API with host buffers (copies inside the timed region)
+    has_init = p.initial_state is not None
+    runner = KDAHostRunner(p.B, p.T, p.H, N=(None if p.cu_seqlens is None else p.N), state_dtype=dev["sdt"],
+                           has_initial=has_init, want_final=p.want_final and dev["sdt"] is not None)
+    pin = lambda t: t.cpu().pin_memory()
+    host = dict(q=pin(dev["q"]), k=pin(dev["k"]), v=pin(dev["v"]), g=pin(dev["g"]), beta=pin(dev["beta"]),
+                A_log=pin(dev["A_log"]), dt_bias=pin(dev["dt_bias"]),
+                init=pin(dev["init"]) if has_init else None, cu=pin(dev["cu"]) if dev["cu"] is not None else None)
+    out_h = torch.empty(p.q.shape, dtype=torch.bfloat16).pin_memory()
+    fin_h = torch.empty(runner.fin.shape, dtype=runner.fin.dtype).pin_memory() if runner.fin is not None else None
+
+    def e2e_step():
+        runner.run(host["q"], host["k"], host["v"], host["g"], host["beta"], p.scale, host["A_log"],
+                   host["dt_bias"], p.lower_bound, initial_state=host["init"], cu_seqlens=host["cu"],
+                   out_host=out_h, final_host=fin_h)
+
+    for _ in range(2):
+        e2e_step()
+    runner.stream.synchronize()
+    n_e2e = max(3, min(args.steps, 10))
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(runner.stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    f1.record(runner.stream)
+    runner.stream.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / n_e2e
+
+    if rank != 0:
+        return
+    th = p.token_heads() * world
+    hbm, tc, peak_src = peaks()
+    abytes = algorithmic_bytes(p)
+    achieved = abytes / (ms_step * 1e-3) / 1e9
+    traffic = measured_traffic(p)
+    line = {
+        "metric": METRIC, "value": th / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (th / world) / (ms_step * 1e-3) / PAGES_GB200_TOKHEADS_PER_S,
+        "dtype": "bf16", "precision": "bf16 inputs/outputs; tf32 and fp16 tensor-core operands; fp32 accumulation "
+                                      "and fp32 state master",
+        "data": "synthetic", "config": workload_config(p, idx),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                     "algorithmic_bytes_per_launch": abytes, "kernel": "kda_fwd_kernel",
+                     "roofline_ms": abytes / (hbm * 1e9) * 1e3},
+        "cpu_baseline": cpu_baseline(p, idx),
+        "e2e": {"value": th / world / (e2e_ms * 1e-3) * world, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": runner.h2d_bytes(p.cu_seqlens is not None),
+                "d2h_bytes_per_step": runner.d2h_bytes()},
+        "clocks": sampler.summary(),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, help="0-4; 2 = T=8192 H=96 fixed length")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, make_workload(args.workload), args.workload, rank)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    p = make_workload(args.workload)
+    run_ours(args, p, args.workload, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -32,8 +32,13 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); return the uint16 bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     u = x.view(np.uint32)
-    bias = ((u >> 16) & 1) + np.uint32(0x7FFF)
-    return ((u + bias) >> 16).astype(np.uint16)
+    r = np.empty(u.shape, np.uint32)          # in-place uint32 ops: no temporaries, no int64 promotion
+    np.right_shift(u, 16, out=r)
+    np.bitwise_and(r, np.uint32(1), out=r)
+    np.add(r, np.uint32(0x7FFF), out=r)
+    np.add(r, u, out=r)
+    np.right_shift(r, 16, out=r)
+    return r.astype(np.uint16)
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:

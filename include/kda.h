@@ -1,0 +1,120 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * The operation is the forward pass of KDA, a per-head gated delta rule, as the
+ * FlashKDA pages state it: the guancyxx.cn FlashKDA article, section 一
+ * ("什么是 Delta Attention": a recurrent state S of shape [K, V] with a learned
+ * decay) and section 2.2 (a token-parallel intra-chunk stage and a head-parallel
+ * chunk-wise delta-rule recurrence), and the FlashKDA README mirror
+ * (ai-feeds.com), section "内核 API" (argument table of flash_kda.fwd) and section
+ * "将 FlashKDA 用作 FLA 后端" (L2 norm of q/k, beta sigmoid and gate inside the
+ * kernel, transposed [V, K] state layout).
+ *
+ * Per sequence n and head h, with K = V = 128 and token t of the sequence:
+ *   q^ = q_t / sqrt(|q_t|^2 + 1e-6),  k^ = k_t / sqrt(|k_t|^2 + 1e-6)
+ *   b  = sigmoid(beta_t)
+ *   a_c = lower_bound * sigmoid(exp(A_log[h]) * (g_t[c] + dt_bias[h][c]))   c = 0..127
+ *   S' = Diag(exp(a)) S_{t-1};  S_t = S' + k^ (b (v_t - S'^T k^))^T;  o_t = scale * S_t^T q^
+ * The pages name g, A_log, dt_bias and lower_bound but print no formula for the
+ * gate; the form above is the one this library implements (bounded in
+ * (lower_bound, 0)).  The 1e-6 inside the norm is likewise this library's choice.
+ *
+ * Layouts (row-major, element strides implied, all device pointers unless noted):
+ *   q, k, v, g, out : bf16 [B, T, H, 128]          (B = N without cu_seqlens, B = 1 with it)
+ *   beta            : bf16 [B, T, H]               (logits; the sigmoid is applied inside)
+ *   A_log           : fp32 [H];  dt_bias : fp32 [H, 128]
+ *   initial_state, final_state : [N, H, 128 (V), 128 (K)], element [n][h][v][k] = S[k][v],
+ *                     bf16 or fp32 as state_dtype says
+ *   cu_seqlens      : int64 [N + 1], cumulative sequence lengths (varlen mode)
+ *
+ * Ownership: the caller allocates and owns every buffer, including out and
+ * final_state.  The library allocates no memory and keeps no state beyond a
+ * per-device "attributes set" flag.  Calls are asynchronous on `stream`; results
+ * are valid once the stream has been synchronised.  initial_state may equal
+ * final_state (in-place update).  Calls on different streams may run concurrently
+ * if their output buffers do not overlap.
+ *
+ * Numerics: the kernel evaluates the chunked form of the recurrence (64-token
+ * chunks, 16-token sub-blocks) with fp32 accumulation and an fp32 master copy of
+ * the state.  Tensor-core operands: tf32 for the intra-chunk q.k and k.k products,
+ * fp16 for the inter-chunk products.  fp16 operands bound the magnitudes of v and
+ * of the state entries to below ~6e4; larger values overflow.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kda_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    KDA_DTYPE_NONE = 0, /* no state tensors */
+    KDA_DTYPE_BF16 = 1,
+    KDA_DTYPE_FP32 = 2
+} kda_dtype_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, bad size, misaligned pointer, bad dtype/state combination */
+    KDA_ERR_UNSUPPORTED = 2,      /* lower_bound outside [-5, 0], or scale not finite */
+    KDA_ERR_CUDA = 3,             /* a CUDA runtime call or the kernel launch failed */
+    KDA_ERR_TIMEOUT = 4           /* reserved for bounded device waits; not returned by kda_fwd */
+} kda_status_t;
+
+/*
+ * kda_fwd -- the KDA chunked forward pass (the call that flash_kda.fwd makes in
+ * the README mirror's "内核 API" section, in C form).
+ *
+ *   q, k, v, g     bf16 [B, T, H, 128], device, 16-byte aligned.
+ *   beta           bf16 [B, T, H], device, 2-byte aligned.
+ *   scale          output scale (finite).
+ *   out            bf16 [B, T, H, 128], device, 16-byte aligned; written for every token.
+ *   A_log          fp32 [H], device.   dt_bias  fp32 [H, 128], device, 16-byte aligned.
+ *   lower_bound    gate lower bound, must lie in [-5, 0].
+ *   initial_state  [N, H, 128, 128] of state_dtype, device, or NULL (zero initial state).
+ *   final_state    [N, H, 128, 128] of state_dtype, device, or NULL (not returned).
+ *   state_dtype    dtype of whichever state pointers are non-NULL (both share it); ignored
+ *                  when both are NULL.  States must be 16-byte aligned.
+ *   cu_seqlens     int64 [N + 1], device, or NULL.  With it, B = 1, T is the total token
+ *                  count and sequence n covers tokens [cu[n], cu[n+1]).  The contents must
+ *                  satisfy cu[0] = 0, cu[i] <= cu[i+1], cu[N] = T; they are device-resident
+ *                  and not checked (see kda_check_cu_seqlens).  Zero-length sequences are
+ *                  allowed: their final state equals the initial one.
+ *   N              number of sequences (>= 1): B without cu_seqlens.
+ *   T              tokens per sequence (without cu_seqlens) or in total (with it), >= 0.
+ *   H              number of heads, >= 1.
+ *   stream         CUDA stream to run on.
+ *
+ * When T == 0 (no tokens at all) q, k, v, g, beta and out may be NULL.
+ *
+ * Returns KDA_OK once the work is enqueued.  Argument errors are reported
+ * synchronously before anything is launched; the kernel itself never traps.
+ */
+kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                     float scale, void *out, const float *A_log, const float *dt_bias,
+                     float lower_bound, const void *initial_state, void *final_state,
+                     kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                     kda_stream_t stream);
+
+/*
+ * Host-side check of a cu_seqlens array (host pointer, N + 1 entries) against the
+ * contract above.  Returns KDA_OK or KDA_ERR_INVALID_ARGUMENT.  No CUDA calls.
+ */
+kda_status_t kda_check_cu_seqlens(const int64_t *host_cu_seqlens, int N, int64_t T);
+
+/* Static English description of a status code (never NULL). */
+const char *kda_status_string(kda_status_t status);
+
+/* Bytes of dynamic shared memory one CTA of the forward kernel uses (for diagnostics). */
+size_t kda_fwd_smem_bytes(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

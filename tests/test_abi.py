@@ -1,0 +1,88 @@
+"""CPU checks of the C ABI: the library builds and loads, exports what include/kda.h
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from gated_delta_rule_23_gb300 import _native
+from gated_delta_rule_23_gb300._native import (KDA_DTYPE_BF16, KDA_DTYPE_FP32, KDA_DTYPE_NONE, KDA_ERR_INVALID_ARGUMENT,
+                                               KDA_ERR_UNSUPPORTED, KDA_OK)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _native.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = _native.declared_functions()
+    assert {"kda_fwd", "kda_check_cu_seqlens", "kda_status_string", "kda_fwd_smem_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_smem_fits_one_cta_per_sm(lib):
+    assert 0 < lib.kda_fwd_smem_bytes() <= 232448
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.kda_status_string(s)
+    assert lib.kda_status_string(99) == b"unknown status"
+
+
+# fake, 256-byte aligned "device" addresses: kda_fwd must reject the call before touching them
+A = 1 << 20
+
+
+def call(lib, **kw):
+    args = dict(q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000, scale=0.1, out=A + 0x5000,
+                A_log=A + 0x6000, dt_bias=A + 0x7000, lower_bound=-5.0, init=None, fin=None,
+                state_dtype=KDA_DTYPE_NONE, cu=None, N=1, T=64, H=2, stream=None)
+    args.update(kw)
+    return lib.kda_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"], args["scale"], args["out"],
+                       args["A_log"], args["dt_bias"], args["lower_bound"], args["init"], args["fin"],
+                       args["state_dtype"], args["cu"], args["N"], args["T"], args["H"], args["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(k=None), dict(v=None), dict(g=None), dict(beta=None), dict(out=None),
+    dict(A_log=None), dict(dt_bias=None),
+    dict(N=0), dict(H=0), dict(T=-1), dict(N=1 << 20, H=1 << 12),
+    dict(q=A + 8), dict(out=A + 0x5002), dict(beta=A + 0x4001), dict(cu=A + 0x9004),
+    dict(init=A + 0x8000, state_dtype=KDA_DTYPE_NONE), dict(fin=A + 0x8000, state_dtype=7),
+    dict(init=A + 0x8008, state_dtype=KDA_DTYPE_FP32),
+])
+def test_invalid_arguments_rejected(lib, kw):
+    assert call(lib, **kw) == KDA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("lb", [-5.01, 0.5, float("nan"), float("-inf")])
+def test_lower_bound_outside_range_unsupported(lib, lb):
+    assert call(lib, lower_bound=lb) == KDA_ERR_UNSUPPORTED
+
+
+def test_nonfinite_scale_unsupported(lib):
+    assert call(lib, scale=float("inf")) == KDA_ERR_UNSUPPORTED
+
+
+def test_check_cu_seqlens(lib):
+    def chk(cu, N, T):
+        a = np.ascontiguousarray(cu, dtype=np.int64)
+        return lib.kda_check_cu_seqlens(a.ctypes.data_as(ctypes.c_void_p), N, T)
+    assert chk([0, 3, 3, 10], 3, 10) == KDA_OK
+    assert chk([0, 0], 1, 0) == KDA_OK
+    assert chk([1, 3, 10], 2, 10) == KDA_ERR_INVALID_ARGUMENT
+    assert chk([0, 5, 3, 10], 3, 10) == KDA_ERR_INVALID_ARGUMENT
+    assert chk([0, 3, 9], 2, 10) == KDA_ERR_INVALID_ARGUMENT
+    assert lib.kda_check_cu_seqlens(None, 1, 0) == KDA_ERR_INVALID_ARGUMENT
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    from gated_delta_rule_23_gb300 import kda_fwd
+    x = torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda_fwd(x, x, x, x, torch.zeros(1, 4, 1, dtype=torch.bfloat16), 1.0, x.clone(),
+                torch.zeros(1), torch.zeros(1, 128), -5.0)

@@ -1,0 +1,181 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
+inputs, element by element, at the five standard workloads and at edge cases.
+
+Tolerances (outputs rel-L2 <= 5e-3 and max-abs <= 3e-2, final states rel-L2 <= 5e-3,
+varlen indexing bit-exact) are in tests/gpu_util.py.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_23_gb300 import kda_fwd
+from gated_delta_rule_23_gb300.inputs import (STATE_BF16, STATE_FP32, STATE_NONE, bf16_bits, make_problem,
+                                              make_workload)
+from tests.gpu_util import assert_parity, rel_l2, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_run(p):
+    return oracle.kda_fwd_problem(p)
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_workload_parity(idx):
+    """All five standard workloads, every head and token, at full size."""
+    p = make_workload(idx)
+    out, fin = run_gpu(p)
+    o_ref, f_ref = oracle_run(p)
+    r = assert_parity(out, fin, o_ref, f_ref)
+    print(f"workload {idx}: {r}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 31, 63, 64, 65, 127, 128, 129, 200, 333])
+def test_lengths_across_chunk_and_subblock_edges(T):
+    p = make_problem(B=1, T=T, H=3, seed=100 + T)
+    out, fin = run_gpu(p)
+    assert_parity(out, fin, *oracle_run(p))
+
+
+@pytest.mark.parametrize("state", [STATE_NONE, STATE_BF16, STATE_FP32])
+@pytest.mark.parametrize("with_initial", [False, True])
+def test_state_dtypes_and_presence(state, with_initial):
+    p = make_problem(B=2, T=150, H=2, seed=7, state_dtype=state, with_initial=with_initial)
+    out, fin = run_gpu(p)
+    o_ref, f_ref = oracle_run(p)
+    assert_parity(out, fin, o_ref, f_ref)
+    if state == STATE_NONE:
+        assert fin is None
+
+
+def test_initial_state_without_final_state():
+    p = make_problem(B=1, T=100, H=2, seed=8, state_dtype=STATE_FP32, want_final=False)
+    out, fin = run_gpu(p)
+    assert fin is None
+    assert_parity(out, None, *oracle_run(p)[:1], None)
+
+
+def test_fixed_length_batch():
+    p = make_problem(B=3, T=130, H=2, seed=9)
+    out, fin = run_gpu(p)
+    assert_parity(out, fin, *oracle_run(p))
+
+
+def test_varlen_bitexact_against_separate_calls():
+    """One varlen call equals separate per-sequence calls bit for bit (cu_seqlens indexing)."""
+    lens = [5, 0, 64, 131, 1, 17]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    p = make_problem(B=1, T=int(cu[-1]), H=3, seed=10, cu_seqlens=cu)
+    out, fin = run_gpu(p)
+    assert_parity(out, fin, *oracle_run(p))
+    for n in range(len(lens)):
+        s = slice(int(cu[n]), int(cu[n + 1]))
+        pn = dataclasses.replace(p, q=p.q[:, s].copy(), k=p.k[:, s].copy(), v=p.v[:, s].copy(), g=p.g[:, s].copy(),
+                                 beta=p.beta[:, s].copy(), initial_state=p.initial_state[n:n + 1].copy(),
+                                 cu_seqlens=None)
+        o_n, f_n = run_gpu(pn)
+        assert np.array_equal(o_n, out[:, s]), n
+        assert np.array_equal(f_n[0], fin[n]), n
+    assert np.array_equal(fin[1], p.initial_state[1])    # zero-length: final = initial exactly
+
+
+def test_all_sequences_empty():
+    cu = np.zeros(4, dtype=np.int64)
+    p = make_problem(B=1, T=0, H=2, seed=11, cu_seqlens=cu)
+    out, fin = run_gpu(p)
+    assert out.size == 0 and np.array_equal(fin, p.initial_state)
+
+
+def test_guard_bands_untouched():
+    """Writes stay inside out and final_state: canaries around both are unchanged."""
+    p = make_problem(B=1, T=77, H=2, seed=12, cu_seqlens=np.array([0, 30, 77]))
+    dev = to_device(p)
+    pad = 4096
+    canary = -12345.0
+    out_buf = torch.full((pad * 2 + p.q.size,), canary, dtype=torch.bfloat16, device="cuda")
+    fin_buf = torch.full((pad * 2 + p.initial_state.size,), canary, dtype=torch.float32, device="cuda")
+    out = out_buf[pad:pad + p.q.size].view(p.q.shape)
+    fin = fin_buf[pad:pad + p.initial_state.size].view(p.initial_state.shape)
+    kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+            p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"])
+    torch.cuda.synchronize()
+    ob, fb = out_buf.float().cpu().numpy(), fin_buf.cpu().numpy()
+    assert np.all(ob[:pad] == canary) and np.all(ob[-pad:] == canary)
+    assert np.all(fb[:pad] == canary) and np.all(fb[-pad:] == canary)
+    assert_parity(out.float().cpu().numpy(), fin.cpu().numpy(), *oracle_run(p))
+
+
+@pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
+def test_in_place_state_update(state):
+    p = make_problem(B=2, T=90, H=2, seed=13, state_dtype=state)
+    out_sep, fin_sep = run_gpu(p)
+    out_inp, fin_inp = run_gpu(p, inplace=True)
+    assert np.array_equal(out_sep, out_inp) and np.array_equal(fin_sep, fin_inp)
+
+
+def test_no_write_no_decay_keeps_state_exactly():
+    """beta logit = -inf and lower_bound = 0: the state passes through unchanged (bit-exact)."""
+    p = make_problem(B=1, T=150, H=2, seed=14, lower_bound=0.0)
+    p.beta[:] = 0xFF80
+    out, fin = run_gpu(p)
+    assert np.array_equal(fin, p.initial_state)
+    assert_parity(out, fin, *oracle_run(p))
+
+
+def test_write_invariant_reads_back_v():
+    """beta = 1 and q = k: every output equals scale * v."""
+    p = make_problem(B=1, T=200, H=2, seed=15)
+    p.q[:] = p.k
+    p.beta[:] = bf16_bits(np.full(p.beta.shape, 100.0, np.float32))
+    out, fin = run_gpu(p)
+    o_ref, f_ref = oracle_run(p)
+    assert_parity(out, fin, o_ref, f_ref)
+
+
+@pytest.mark.parametrize("lb", [0.0, -0.5, -5.0])
+def test_gate_extremes(lb):
+    """Saturated gates at the lower bound (strongest decay the range argument allows) and none."""
+    p = make_problem(B=1, T=160, H=2, seed=16, lower_bound=lb)
+    p.A_log[:] = 12.0
+    out, fin = run_gpu(p)
+    assert_parity(out, fin, *oracle_run(p))
+
+
+def test_split_and_resume():
+    """Splitting at a token that is not a chunk boundary and chaining final -> initial state."""
+    p = make_problem(B=1, T=300, H=2, seed=17)
+    out, fin = run_gpu(p)
+    cut = 101
+    p1 = dataclasses.replace(p, q=p.q[:, :cut].copy(), k=p.k[:, :cut].copy(), v=p.v[:, :cut].copy(),
+                             g=p.g[:, :cut].copy(), beta=p.beta[:, :cut].copy())
+    o1, f1 = run_gpu(p1)
+    p2 = dataclasses.replace(p, q=p.q[:, cut:].copy(), k=p.k[:, cut:].copy(), v=p.v[:, cut:].copy(),
+                             g=p.g[:, cut:].copy(), beta=p.beta[:, cut:].copy(), initial_state=f1.astype(np.float32))
+    o2, f2 = run_gpu(p2)
+    o_ref, f_ref = oracle_run(p)
+    assert_parity(np.concatenate([o1, o2], axis=1), f2, o_ref, f_ref)
+    assert rel_l2(f2, fin) < 5e-3
+
+
+def test_repeat_calls_are_deterministic():
+    p = make_problem(B=1, T=257, H=4, seed=18, cu_seqlens=np.array([0, 100, 257]))
+    dev = to_device(p)
+    a = run_gpu(p, dev)
+    b = run_gpu(p, dev)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_side_stream():
+    p = make_problem(B=1, T=70, H=2, seed=19)
+    dev = to_device(p)
+    s = torch.cuda.Stream()
+    out = torch.empty_like(dev["q"])
+    fin = torch.empty((1, 2, 128, 128), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+            p.lower_bound, initial_state=dev["init"], final_state=fin, stream=s)
+    s.synchronize()
+    assert_parity(out.float().cpu().numpy(), fin.cpu().numpy(), *oracle_run(p))
