@@ -94,7 +94,7 @@ def test_guard_bands_untouched():
     p = make_problem(B=1, T=77, H=2, seed=12, cu_seqlens=np.array([0, 30, 77]))
     dev = to_device(p)
     pad = 4096
-    canary = -12345.0
+    canary = -12288.0          # exactly representable in bf16 and fp32
     out_buf = torch.full((pad * 2 + p.q.size,), canary, dtype=torch.bfloat16, device="cuda")
     fin_buf = torch.full((pad * 2 + p.initial_state.size,), canary, dtype=torch.float32, device="cuda")
     out = out_buf[pad:pad + p.q.size].view(p.q.shape)
