@@ -1,6 +1,6 @@
 // KDA chunked forward pass for sm_103a (GB300).
 //
-// One CTA owns one (sequence, head) pair and walks its tokens in 64-token
+// One CTA owns one (sequence, head) pair and walks its tokens in 32-token
 // chunks.  Per chunk it runs the token-parallel intra-chunk stage (gate, L2 norm,
 // decay factors, the strictly-lower beta*K*K^T and causal Q*K^T matrices, the
 // (I + A)^-1 inverse and the WY transform) and then the chunk recurrence on the
@@ -9,18 +9,22 @@
 // recurrence described in the guancyxx.cn FlashKDA article, section 2.2, but
 // fuses both into one launch so the intermediates never leave shared memory.
 //
-// Notation (per chunk, rows i = 0..63, channel c, state S in R^{K x V}):
+// Notation (per chunk, rows i = 0..31, channel c, state S in R^{K x V}):
 //   a_i    = lower_bound * sigmoid(exp(A_log) * (g_i + dt_bias))   (natural-log decay)
 //   alpha  = exp(a); G_i = sum_{s <= i} a_s; Gamma_i = exp(G_i)
 //   Akk[i][j] = b_i sum_c k^_ic k^_jc exp(G_ic - G_jc)  (j < i),  Aqk likewise with q^ (j <= i)
 //   Tm = (I + Akk)^-1, T' = Tm diag(b), W = T' (K^ . Gamma), U = T' V - W S
-//   O = scale (Q~ S + Aqk U), Q~ = Q^ . Gamma;  S <- Diag(Gamma_63) S + K~^T U,
-//   K~_j = k^_j . Gamma_63 / Gamma_j.
-// The decay factors are formed per 16-row sub-block (P, E, D below) so that no
-// factor leaves [2^-115.5, 2^115.5] when lower_bound >= -5 (7.22 binary orders of
-// magnitude per token at most, 16 tokens per sub-block): this is the numerical-range
-// argument for CHUNK = 16 in the FlashKDA article, section 2.1, applied per
-// sub-block inside a 64-token chunk.
+//   O = scale (Q~ S + Aqk U), Q~ = Q^ . Gamma;  S <- Diag(Gamma_31) S + K~^T U,
+//   K~_j = k^_j . Gamma_31 / Gamma_j.
+// The decay factors are formed per 16-row sub-block so that no factor leaves
+// [2^-115.5, 2^115.5] when lower_bound >= -5 (at most 7.22 binary orders of
+// magnitude per token, 16 tokens per sub-block): the numerical-range argument for
+// CHUNK = 16 in the FlashKDA article, section 2.1, applied per sub-block.  With
+// P_i / E_i the within-sub-block prefix (inclusive) / suffix (exclusive) products
+// of alpha and D_b the product over sub-block b:
+//   exp(G_i - G_j) = P_i E_j / D_b          (i, j in sub-block b, j <= i)
+//   exp(G_i - G_j) = P_i E_j                (i in sub-block 1, j in sub-block 0)
+//   Gamma_i = P_i (b(i) = 0) or D_0 P_i;    Gamma_31 / Gamma_j = E_j D_1 (b(j) = 0) or E_j.
 //
 // The inter-chunk stage is computed transposed: each warp owns 16 value columns of
 // the state (rows of S^T) and keeps S^T (fp32 master), U^T and O^T for them in
@@ -38,53 +42,64 @@
 namespace {
 
 constexpr int D = 128;        // K = V = 128
-constexpr int CH = 64;        // tokens per chunk
+constexpr int CH = 32;        // tokens per chunk
 constexpr int SB = 16;        // tokens per decay sub-block
 constexpr int NTHREADS = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- shared memory map
-// bf16/fp16 tiles use a 136-element (272-byte) row pitch and fp32 tiles a 132- or
-// 68-float pitch, which keeps ldmatrix rows and fragment loads free of bank conflicts.
-constexpr int PH = 136;                          // half-precision row pitch (elements)
-constexpr int PF = 132;                          // fp32 pitch of the 128-wide intra operands
-constexpr int PA = 68;                           // fp32 pitch of 64-wide matrices
-constexpr int PS = 72;                           // half pitch of 64-wide matrices
+// Half-precision [32][136] tiles (272-byte rows) hold q, k, g, v and the fp16 operands.
+// The q, k, g tiles and the fp16 operands written by the gate pass swizzle their
+// 16-byte chunks by ((row >> 3) & 3) << 1, which makes the gate pass (lanes spread
+// over four 8-row segments) and ldmatrix both free of bank conflicts.  fp32 tf32
+// operands use a 132-float pitch, conflict-free for the mma fragment loads.
+constexpr int PH = 136;                          // half row pitch (elements)
+constexpr int PF = 132;                          // fp32 pitch of 128-wide tf32 operands
+constexpr int PA = 36;                           // fp32 pitch of 32-wide matrices
+constexpr int PS = 40;                           // half pitch of 32-wide matrices
+constexpr int HT = CH * PH * 2;                  // 8704 B: one [32][136] half tile
 
-constexpr int RAW_TILE = CH * PH * 2;            // 17408 B
 constexpr int OFF_RAW_Q = 0;
-constexpr int OFF_RAW_K = OFF_RAW_Q + RAW_TILE;
-constexpr int OFF_RAW_G = OFF_RAW_K + RAW_TILE;
-constexpr int OFF_RAW_V = OFF_RAW_G + RAW_TILE;
-constexpr int OFF_RAW_B = OFF_RAW_V + RAW_TILE;  // beta logits, 64 bf16
+constexpr int OFF_RAW_K = OFF_RAW_Q + HT;
+constexpr int OFF_RAW_G = OFF_RAW_K + HT;
+constexpr int OFF_RAW_V = OFF_RAW_G + HT;
+constexpr int OFF_RAW_B = OFF_RAW_V + HT;        // beta logits, 32 bf16 (128 B reserved)
 constexpr int OFF_INTRA = OFF_RAW_B + 128;
-constexpr int INTRA_F32 = CH * PF * 4;           // 33792 B
-constexpr int OFF_LQ = OFF_INTRA;                // fp32 [64][132]  q^ . P
-constexpr int OFF_LK = OFF_LQ + INTRA_F32;       // fp32 [64][132]  k^ . P
-constexpr int OFF_EK = OFF_LK + INTRA_F32;       // fp32 [64][132]  k^ . E
-// after the Akk/Aqk products the same region holds:
-constexpr int OFF_AKK = OFF_INTRA;               // fp32 [64][68]
-constexpr int OFF_TM = OFF_AKK + CH * PA * 4;    // fp32 [64][68]
-constexpr int OFF_AQK = OFF_TM + CH * PA * 4;    // fp16 [64][72]
-constexpr int OFF_TP = OFF_AQK + CH * PS * 2;    // fp16 [64][72]  T' = Tm diag(b)
-constexpr int OFF_WN = OFF_TP + CH * PS * 2;     // fp16 [64][136] -W
-constexpr int OFF_OST = OFF_WN + RAW_TILE;       // bf16 [64][136] output staging / inverse scratch
-constexpr int INTRA_END = OFF_OST + RAW_TILE;
-constexpr int OFF_INTER = OFF_INTRA + 3 * INTRA_F32;
-constexpr int OFF_QT = OFF_INTER;                // fp16 [64][136] Q~
-constexpr int OFF_KT = OFF_QT + RAW_TILE;        // fp16 [64][136] K~
-constexpr int OFF_KG = OFF_KT + RAW_TILE;        // fp16 [64][136] K^ . Gamma
-constexpr int OFF_MISC = OFF_KG + RAW_TILE;
-constexpr int OFF_RQ = OFF_MISC;                 // fp32 [64] 1/|q|
-constexpr int OFF_RK = OFF_RQ + 256;             // fp32 [64] 1/|k|
-constexpr int OFF_BT = OFF_RK + 256;             // fp32 [64] b = sigmoid(beta), 0 past the end
-constexpr int OFF_DB = OFF_BT + 256;             // fp32 [4][128] sub-block decay D_b
-constexpr int OFF_GC = OFF_DB + 4 * D * 4;       // fp32 [128] chunk decay Gamma_63
-constexpr int OFF_SC = OFF_GC + D * 4;           // fp32 [10][128] sub-block pair scales
-constexpr int SMEM_BYTES = OFF_SC + 10 * D * 4;
+constexpr int F32T = CH * PF * 4;                // 16896 B
+constexpr int OFF_LQ = OFF_INTRA;                // fp32 [32][132]  q^ P          (tf32-rounded)
+constexpr int OFF_LK = OFF_LQ + F32T;            // fp32 [32][132]  k^ P
+constexpr int OFF_ED = OFF_LK + F32T;            // fp32 [32][132]  k^ E / D_b
+constexpr int OFF_EK = OFF_ED + F32T;            // fp32 [16][132]  k^ E  (sub-block 0 only)
+constexpr int INTRA_BYTES = 3 * F32T + F32T / 2;
+// after the Akk / Aqk products the same region holds:
+constexpr int OFF_AKK = OFF_INTRA;               // fp32 [32][36]
+constexpr int OFF_TM = OFF_AKK + CH * PA * 4;    // fp32 [32][36]  diagonal blocks of Tm
+constexpr int OFF_AQK = OFF_TM + CH * PA * 4;    // fp16 [32][40]
+constexpr int OFF_TP = OFF_AQK + CH * PS * 2;    // fp16 [32][40]  T' = Tm diag(b)
+constexpr int OFF_MT = OFF_TP + CH * PS * 2;     // fp32 [16][16]  inverse scratch
+constexpr int OFF_WN = OFF_MT + 16 * 16 * 4;     // fp16 [32][136] -W
+constexpr int OFF_OST = OFF_WN + HT;             // bf16 [32][136] output staging
+constexpr int INTRA_END = OFF_OST + HT;
+constexpr int OFF_INTER = OFF_INTRA + INTRA_BYTES;
+constexpr int OFF_QT = OFF_INTER;                // fp16 [32][136] Q~          (swizzled)
+constexpr int OFF_KT = OFF_QT + HT;              // fp16 [32][136] K~          (swizzled)
+constexpr int OFF_KG = OFF_KT + HT;              // fp16 [32][136] K^ . Gamma  (swizzled)
+constexpr int OFF_MISC = OFF_KG + HT;
+constexpr int OFF_RQ = OFF_MISC;                 // fp32 [32] 1/|q|
+constexpr int OFF_RK = OFF_RQ + 128;             // fp32 [32] 1/|k|
+constexpr int OFF_BT = OFF_RK + 128;             // fp32 [32] b = sigmoid(beta), 0 past the end
+constexpr int OFF_GC = OFF_BT + 128;             // fp32 [128] chunk decay Gamma_31
+constexpr int SMEM_BYTES = OFF_GC + D * 4;
 static_assert(INTRA_END <= OFF_INTER, "post-product overlay exceeds the intra region");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-static_assert(OFF_INTRA % 128 == 0 && OFF_INTER % 16 == 0 && OFF_MISC % 16 == 0, "alignment");
+static_assert(OFF_INTRA % 128 == 0 && OFF_INTER % 16 == 0 && OFF_MISC % 16 == 0 && OFF_WN % 16 == 0 &&
+              OFF_OST % 16 == 0 && OFF_TP % 16 == 0 && OFF_AQK % 16 == 0, "alignment");
+
+// byte offset of element (row, col) in a swizzled [32][136] half tile
+__host__ __device__ constexpr int swz(int row, int col)
+{
+    return row * PH * 2 + ((((col >> 3) ^ (((row >> 3) & 3) << 1))) << 4) + ((col & 7) << 1);
+}
 
 // ---------------------------------------------------------------- small device helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -170,19 +185,21 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
 
 // Stage rows [tok0, tok0 + len) of one [rows, H, 128] bf16 tensor (head h) into a
-// [64][136] tile; rows past len are zero-filled.
+// [32][136] tile (swizzled or plain); rows past len are zero-filled.  len >= 1.
+template <bool SWZ>
 __device__ __forceinline__ void load_tile_async(unsigned char *smem, int off, const __nv_bfloat16 *base,
                                                 int64_t tok0, int len, int H, int h)
 {
     const int tid = threadIdx.x;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int idx = tid + m * NTHREADS;   // 0..1023: 64 rows x 16 chunks of 16 bytes
+    for (int m = 0; m < 2; ++m) {
+        const int idx = tid + m * NTHREADS;   // 0..511: 32 rows x 16 chunks of 16 bytes
         const int r = idx >> 4, c16 = idx & 15;
-        const bool valid = r < len;   // len >= 1 whenever this is called
+        const bool valid = r < len;
         const int64_t row = tok0 + (valid ? r : 0);
         const __nv_bfloat16 *src = base + (row * H + h) * D + c16 * 8;
-        cp_async16(smem_u32(smem + off + r * PH * 2 + c16 * 16), src, valid);
+        const int dst = SWZ ? swz(r, c16 * 8) : r * PH * 2 + c16 * 16;
+        cp_async16(smem_u32(smem + off + dst), src, valid);
     }
 }
 
@@ -198,6 +215,8 @@ struct Params {
     int64_t T;
 };
 
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+
 // ---------------------------------------------------------------- the kernel
 template <int STATE, bool VARLEN>  // STATE: 0 none, 1 bf16, 2 fp32
 __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
@@ -205,6 +224,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;             // mma fragment coordinates
+    const int mi = lane >> 3, lr = lane & 7;             // ldmatrix lane roles
     const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int H = p.H;
 
@@ -220,12 +240,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     float *rq = reinterpret_cast<float *>(smem + OFF_RQ);
     float *rk = reinterpret_cast<float *>(smem + OFF_RK);
     float *bt = reinterpret_cast<float *>(smem + OFF_BT);
-    float *Db = reinterpret_cast<float *>(smem + OFF_DB);
     float *Gc = reinterpret_cast<float *>(smem + OFF_GC);
-    float *Sc = reinterpret_cast<float *>(smem + OFF_SC);
-    const __nv_bfloat16 *rawq = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_Q);
-    const __nv_bfloat16 *rawk = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_K);
-    const __nv_bfloat16 *rawg = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_G);
     __nv_bfloat16 *rawb = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_RAW_B);
 
     // -------- state: each warp owns value rows vr0..vr0+15 of S^T, all 128 key columns
@@ -257,18 +272,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         }
     }
 
+    // gate-pass lane roles: channel pair cp of this warp's 16 channels, 8-row segment sg
+    const int cp = lane & 7, sg = lane >> 3, blk = sg >> 1;
+    const int c0 = warp * 16 + 2 * cp;
     const float eA = expf(p.A_log[h]);
-    const float dtb = p.dt_bias[h * D + (tid & (D - 1))];
+    const float2 dtb = *reinterpret_cast<const float2 *>(p.dt_bias + h * D + c0);
     const int nchunks = (int)((len + CH - 1) / CH);
 
-    // prologue: stage chunk 0 (q, k, g, beta as one group, v as a second group)
+    // prologue: stage chunk 0 (q, k, g as one group, v as a second group)
     if (nchunks > 0) {
         const int L0 = (int)(len < CH ? len : CH);
-        load_tile_async(smem, OFF_RAW_Q, p.q, bos, L0, H, h);
-        load_tile_async(smem, OFF_RAW_K, p.k, bos, L0, H, h);
-        load_tile_async(smem, OFF_RAW_G, p.g, bos, L0, H, h);
+        load_tile_async<true>(smem, OFF_RAW_Q, p.q, bos, L0, H, h);
+        load_tile_async<true>(smem, OFF_RAW_K, p.k, bos, L0, H, h);
+        load_tile_async<true>(smem, OFF_RAW_G, p.g, bos, L0, H, h);
         cp_async_commit();
-        load_tile_async(smem, OFF_RAW_V, p.v, bos, L0, H, h);
+        load_tile_async<false>(smem, OFF_RAW_V, p.v, bos, L0, H, h);
         cp_async_commit();
         if (tid < CH)
             rawb[tid] = tid < L0 ? p.beta[(bos + tid) * H + h] : __float2bfloat16(0.f);
@@ -276,202 +294,168 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
 
     for (int ci = 0; ci < nchunks; ++ci) {
         const int64_t tok0 = bos + (int64_t)ci * CH;
-        const int L = (int)((len - (int64_t)ci * CH) < CH ? (len - (int64_t)ci * CH) : CH);
+        const int64_t rem = len - (int64_t)ci * CH;
+        const int L = (int)(rem < CH ? rem : CH);
         const bool has_next = ci + 1 < nchunks;
         const int64_t ntok0 = tok0 + CH;
-        const int Ln = has_next ? (int)((len - (int64_t)(ci + 1) * CH) < CH ? (len - (int64_t)(ci + 1) * CH) : CH) : 0;
+        const int Ln = has_next ? (int)((rem - CH) < CH ? (rem - CH) : CH) : 0;
 
         cp_async_wait<1>();   // q, k, g of this chunk have landed (v may still be in flight)
         __syncthreads();
 
-        // ---- S1a: row norms and beta (warp w: rows 8w..8w+7)
-        for (int rr = 0; rr < 8; ++rr) {
-            const int r = warp * 8 + rr;
-            const uint2 qa = *reinterpret_cast<const uint2 *>(rawq + r * PH + lane * 4);
-            const uint2 ka = *reinterpret_cast<const uint2 *>(rawk + r * PH + lane * 4);
-            float sq = 0.f, sk = 0.f;
-            {
-                float a = bf16_lo(qa.x), b = bf16_hi(qa.x), c = bf16_lo(qa.y), d = bf16_hi(qa.y);
-                sq = a * a + b * b + c * c + d * d;
-                a = bf16_lo(ka.x), b = bf16_hi(ka.x), c = bf16_lo(ka.y), d = bf16_hi(ka.y);
-                sk = a * a + b * b + c * c + d * d;
-            }
+        // ---- S1a: row norms (16 lanes per row, 8 channels per lane) and beta
+        {
+            const int half = lane >> 4, l16 = lane & 15;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            for (int it = 0; it < 2; ++it) {
+                const int r = warp * 4 + it * 2 + half;
+                const uint4 qa = *reinterpret_cast<const uint4 *>(smem + OFF_RAW_Q + swz(r, l16 * 8));
+                const uint4 ka = *reinterpret_cast<const uint4 *>(smem + OFF_RAW_K + swz(r, l16 * 8));
+                const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]), k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+                    sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+                    sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                }
+                if (l16 == 0) {
+                    rq[r] = rsqrtf(sq + 1e-6f);
+                    rk[r] = rsqrtf(sk + 1e-6f);
+                }
             }
-            if (lane == 0) {
-                rq[r] = rsqrtf(sq + 1e-6f);
-                rk[r] = rsqrtf(sk + 1e-6f);
-                bt[r] = r < L ? sigmoidf_fast(__bfloat162float(rawb[r])) : 0.f;
-            }
+            if (tid < CH)
+                bt[tid] = tid < L ? sigmoidf_fast(__bfloat162float(rawb[tid])) : 0.f;
         }
         __syncthreads();
 
-        // ---- S1b: gate, per-sub-block decay products, tf32-side operands (thread: channel c, half)
+        // ---- S1b: gate, sub-block decay products, all operands of this chunk (one pass)
         {
-            const int c = tid & (D - 1), half = tid >> 7;
+            uint32_t gqv[8], gkv[8];
+            float al0[8], al1[8];
+            float tot0 = 1.f, tot1 = 1.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = sg * 8 + i;
+                const uint32_t gg = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_G + swz(r, c0));
+                gqv[i] = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_Q + swz(r, c0));
+                gkv[i] = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_K + swz(r, c0));
+                const float z0 = eA * (bf16_lo(gg) + dtb.x), z1 = eA * (bf16_hi(gg) + dtb.y);
+                const bool live = r < L;
+                al0[i] = live ? ex2_approx(p.lb_log2e * sigmoidf_fast(z0)) : 1.f;
+                al1[i] = live ? ex2_approx(p.lb_log2e * sigmoidf_fast(z1)) : 1.f;
+                tot0 *= al0[i];
+                tot1 *= al1[i];
+            }
+            // the other 8-row segment of this sub-block (lane ^ 8) and the other sub-block (lane ^ 16)
+            const float ot0 = __shfl_xor_sync(0xffffffffu, tot0, 8), ot1 = __shfl_xor_sync(0xffffffffu, tot1, 8);
+            const float D0 = tot0 * ot0, D1 = tot1 * ot1;                     // this sub-block's decay
+            const float Do0 = __shfl_xor_sync(0xffffffffu, D0, 16), Do1 = __shfl_xor_sync(0xffffffffu, D1, 16);
+            const float pre0 = blk ? Do0 : 1.f, pre1 = blk ? Do1 : 1.f;       // Gamma at sub-block start
+            const float post0 = blk ? 1.f : Do0, post1 = blk ? 1.f : Do1;     // decay after sub-block end
+            const float iD0 = rcp_approx(D0), iD1 = rcp_approx(D1);
+            const bool odd = sg & 1;
+            float P0 = odd ? ot0 : 1.f, P1 = odd ? ot1 : 1.f;
+            float E0 = odd ? 1.f : ot0, E1 = odd ? 1.f : ot1;
             float *Lq = reinterpret_cast<float *>(smem + OFF_LQ);
             float *Lk = reinterpret_cast<float *>(smem + OFF_LK);
+            float *Ed = reinterpret_cast<float *>(smem + OFF_ED);
             float *Ek = reinterpret_cast<float *>(smem + OFF_EK);
 #pragma unroll
-            for (int sbk = 0; sbk < 2; ++sbk) {
-                const int blk = half * 2 + sbk, r0 = blk * SB;
-                float al[SB];
-#pragma unroll
-                for (int i = 0; i < SB; ++i) {
-                    const int r = r0 + i;
-                    const float z = eA * (__bfloat162float(rawg[r * PH + c]) + dtb);
-                    al[i] = r < L ? ex2_approx(p.lb_log2e * sigmoidf_fast(z)) : 1.f;
-                }
-                float P = 1.f;
-#pragma unroll
-                for (int i = 0; i < SB; ++i) {
-                    const int r = r0 + i;
-                    P *= al[i];
-                    const float qv = __bfloat162float(rawq[r * PH + c]) * rq[r];
-                    const float kv = __bfloat162float(rawk[r * PH + c]) * rk[r];
-                    Lq[r * PF + c] = qv * P;
-                    Lk[r * PF + c] = kv * P;
-                }
-                Db[blk * D + c] = P;
-                float E = 1.f;
-#pragma unroll
-                for (int i = SB - 1; i >= 0; --i) {
-                    const int r = r0 + i;
-                    const float kv = __bfloat162float(rawk[r * PH + c]) * rk[r];
-                    Ek[r * PF + c] = kv * E;
-                    E *= al[i];
-                }
+            for (int i = 0; i < 8; ++i) {
+                const int r = sg * 8 + i;
+                const float qn = rq[r], kn = rk[r];
+                const float q0 = bf16_lo(gqv[i]) * qn, q1 = bf16_hi(gqv[i]) * qn;
+                const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
+                P0 *= al0[i];
+                P1 *= al1[i];
+                *reinterpret_cast<float2 *>(Lq + r * PF + c0) = make_float2(tf32r(q0 * P0), tf32r(q1 * P1));
+                *reinterpret_cast<float2 *>(Lk + r * PF + c0) = make_float2(tf32r(k0 * P0), tf32r(k1 * P1));
+                *reinterpret_cast<uint32_t *>(smem + OFF_QT + swz(r, c0)) = pack_half2(q0 * P0 * pre0, q1 * P1 * pre1);
+                *reinterpret_cast<uint32_t *>(smem + OFF_KG + swz(r, c0)) = pack_half2(k0 * P0 * pre0, k1 * P1 * pre1);
             }
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                const int r = sg * 8 + i;
+                const float kn = rk[r];
+                const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
+                *reinterpret_cast<float2 *>(Ed + r * PF + c0) = make_float2(tf32r(k0 * E0 * iD0), tf32r(k1 * E1 * iD1));
+                if (blk == 0)
+                    *reinterpret_cast<float2 *>(Ek + r * PF + c0) = make_float2(tf32r(k0 * E0), tf32r(k1 * E1));
+                *reinterpret_cast<uint32_t *>(smem + OFF_KT + swz(r, c0)) = pack_half2(k0 * E0 * post0, k1 * E1 * post1);
+                E0 *= al0[i];
+                E1 *= al1[i];
+            }
+            if (sg == 0)
+                *reinterpret_cast<float2 *>(Gc + c0) = make_float2(D0 * Do0, D1 * Do1);
         }
         __syncthreads();
 
         // ---- raw q, k, g, beta are consumed: start staging the next chunk's
         if (has_next) {
-            load_tile_async(smem, OFF_RAW_Q, p.q, ntok0, Ln, H, h);
-            load_tile_async(smem, OFF_RAW_K, p.k, ntok0, Ln, H, h);
-            load_tile_async(smem, OFF_RAW_G, p.g, ntok0, Ln, H, h);
+            load_tile_async<true>(smem, OFF_RAW_Q, p.q, ntok0, Ln, H, h);
+            load_tile_async<true>(smem, OFF_RAW_K, p.k, ntok0, Ln, H, h);
+            load_tile_async<true>(smem, OFF_RAW_G, p.g, ntok0, Ln, H, h);
         }
         cp_async_commit();
         __nv_bfloat16 next_beta = __float2bfloat16(0.f);
         if (has_next && tid < Ln)
             next_beta = p.beta[(ntok0 + tid) * H + h];
 
-        // ---- S1c: chunk-start factors, pair scales, fp16 inter-chunk operands
-        {
-            const int c = tid & (D - 1), half = tid >> 7;
-            const float d0 = Db[c], d1 = Db[D + c], d2 = Db[2 * D + c], d3 = Db[3 * D + c];
-            const float pre[4] = {1.f, d0, d0 * d1, d0 * d1 * d2};
-            const float post[4] = {d1 * d2 * d3, d2 * d3, d3, 1.f};
-            if (half == 0) {
-                Gc[c] = d0 * d1 * d2 * d3;
-                // pair index pi(b1, b0) = b1 (b1 + 1) / 2 + b0
-                Sc[0 * D + c] = 1.f / d0;
-                Sc[1 * D + c] = 1.f;
-                Sc[2 * D + c] = 1.f / d1;
-                Sc[3 * D + c] = d1;
-                Sc[4 * D + c] = 1.f;
-            } else {
-                Sc[5 * D + c] = 1.f / d2;
-                Sc[6 * D + c] = d1 * d2;
-                Sc[7 * D + c] = d2;
-                Sc[8 * D + c] = 1.f;
-                Sc[9 * D + c] = 1.f / d3;
-            }
-            const float *Lq = reinterpret_cast<const float *>(smem + OFF_LQ);
-            const float *Lk = reinterpret_cast<const float *>(smem + OFF_LK);
-            const float *Ek = reinterpret_cast<const float *>(smem + OFF_EK);
-            __half *Qt = reinterpret_cast<__half *>(smem + OFF_QT);
-            __half *Kt = reinterpret_cast<__half *>(smem + OFF_KT);
-            __half *Kg = reinterpret_cast<__half *>(smem + OFF_KG);
-#pragma unroll 4
-            for (int i = 0; i < 32; ++i) {
-                const int r = half * 32 + i, b = r >> 4;
-                Qt[r * PH + c] = __float2half_rn(Lq[r * PF + c] * pre[b]);
-                Kg[r * PH + c] = __float2half_rn(Lk[r * PF + c] * pre[b]);
-                Kt[r * PH + c] = __float2half_rn(Ek[r * PF + c] * post[b]);
-            }
-        }
-        __syncthreads();
-
-        // ---- S2: Akk and Aqk on tf32 tensor cores (20 items: 10 sub-block pairs x {kk, qk})
-        float acc2[3][2][4];
-        {
-            const float *Lq = reinterpret_cast<const float *>(smem + OFF_LQ);
-            const float *Lk = reinterpret_cast<const float *>(smem + OFF_LK);
-            const float *Ek = reinterpret_cast<const float *>(smem + OFF_EK);
-#pragma unroll
-            for (int it = 0; it < 3; ++it) {
-                const int item = warp + it * 8;
+        // ---- S2: Akk and Aqk on tf32 tensor cores; items (pair, kind), pairs (0,0), (1,0), (1,1)
+        float acc2[2][4] = {};
+        const int item = warp;           // warps 0..5
+        const int pair = item >> 1, qk = item & 1;
+        const int rb1 = pair == 0 ? 0 : 16;                  // row block of the left factor
+        if (item < 6) {
+            const float *X = reinterpret_cast<const float *>(smem + (qk ? OFF_LQ : OFF_LK)) + (rb1 + gq) * PF + tq;
+            const float *Y = reinterpret_cast<const float *>(smem + (pair == 1 ? OFF_EK : OFF_ED)) +
+                             ((pair == 2 ? 16 : 0) + gq) * PF + tq;
+#pragma unroll 8
+            for (int ks = 0; ks < D / 8; ++ks) {
+                const int k0 = ks * 8;
+                const uint32_t a0 = __float_as_uint(X[k0]), a1 = __float_as_uint(X[8 * PF + k0]);
+                const uint32_t a2 = __float_as_uint(X[k0 + 4]), a3 = __float_as_uint(X[8 * PF + k0 + 4]);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        acc2[it][nt][e] = 0.f;
-                if (item < 20) {
-                    const int pi = item >> 1;
-                    const int b1 = pi >= 6 ? 3 : pi >= 3 ? 2 : pi >= 1 ? 1 : 0;
-                    const int b0 = pi - b1 * (b1 + 1) / 2;
-                    const float *X = (item & 1) ? Lq : Lk;
-                    const float *xa = X + (b1 * SB + gq) * PF + tq;
-                    const float *xb = Ek + (b0 * SB + gq) * PF + tq;
-                    const float *sc = Sc + pi * D + tq;
-#pragma unroll 4
-                    for (int ks = 0; ks < D / 8; ++ks) {
-                        const int k0 = ks * 8;
-                        const uint32_t a0 = to_tf32(xa[k0]);
-                        const uint32_t a1 = to_tf32(xa[8 * PF + k0]);
-                        const uint32_t a2 = to_tf32(xa[k0 + 4]);
-                        const uint32_t a3 = to_tf32(xa[8 * PF + k0 + 4]);
-                        const float s0 = sc[k0], s1 = sc[k0 + 4];
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            const uint32_t b0v = to_tf32(xb[nt * 8 * PF + k0] * s0);
-                            const uint32_t b1v = to_tf32(xb[nt * 8 * PF + k0 + 4] * s1);
-                            mma_tf32(acc2[it][nt], a0, a1, a2, a3, b0v, b1v);
-                        }
-                    }
-                }
+                    mma_tf32(acc2[nt], a0, a1, a2, a3, __float_as_uint(Y[nt * 8 * PF + k0]),
+                             __float_as_uint(Y[nt * 8 * PF + k0 + 4]));
             }
         }
         __syncthreads();   // the intra operands are dead; the region is reused below
-        {
+        if (item < 6) {
             float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
             __half *Aqk = reinterpret_cast<__half *>(smem + OFF_AQK);
+            const int cb0 = pair == 2 ? 16 : 0;
 #pragma unroll
-            for (int it = 0; it < 3; ++it) {
-                const int item = warp + it * 8;
-                if (item < 20) {
-                    const int pi = item >> 1;
-                    const int b1 = pi >= 6 ? 3 : pi >= 3 ? 2 : pi >= 1 ? 1 : 0;
-                    const int b0 = pi - b1 * (b1 + 1) / 2;
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int i = b1 * SB + gq + 8 * hh;
-                            const int j = b0 * SB + nt * 8 + 2 * tq;
-                            const float x0 = acc2[it][nt][2 * hh], x1 = acc2[it][nt][2 * hh + 1];
-                            if (item & 1) {
-                                Aqk[i * PS + j] = __float2half_rn(j <= i ? x0 : 0.f);
-                                Aqk[i * PS + j + 1] = __float2half_rn(j + 1 <= i ? x1 : 0.f);
-                            } else {
-                                const float bi = bt[i];
-                                Akk[i * PA + j] = j < i ? bi * x0 : 0.f;
-                                Akk[i * PA + j + 1] = j + 1 < i ? bi * x1 : 0.f;
-                            }
-                        }
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int i = rb1 + gq + 8 * hh, j = cb0 + nt * 8 + 2 * tq;
+                    const float x0 = acc2[nt][2 * hh], x1 = acc2[nt][2 * hh + 1];
+                    if (qk) {
+                        *reinterpret_cast<uint32_t *>(Aqk + i * PS + j) =
+                            pack_half2(j <= i ? x0 : 0.f, j + 1 <= i ? x1 : 0.f);
+                    } else {
+                        const float bi = bt[i];
+                        *reinterpret_cast<float2 *>(Akk + i * PA + j) =
+                            make_float2(j < i ? bi * x0 : 0.f, j + 1 < i ? bi * x1 : 0.f);
+                    }
                 }
-            }
         }
         __syncthreads();
 
-        // ---- S3: Tm = (I + Akk)^-1 in fp32; 16x16 diagonal blocks by forward substitution
+        // ---- S3: Tm = (I + Akk)^-1 (fp32) and T' = Tm diag(b) (fp16)
         float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
         float *Tm = reinterpret_cast<float *>(smem + OFF_TM);
-        if (warp < 4 && lane < 16) {
+        __half *Tp = reinterpret_cast<__half *>(smem + OFF_TP);
+        if (warp < 2 && lane < 16) {
+            // diagonal 16x16 blocks by forward substitution; lane = column
             const int b = warp, j = lane;
             float x[SB];
 #pragma unroll
@@ -482,62 +466,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                     s = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], s);
                 x[i] = i == j ? 1.f : (i < j ? 0.f : -s);
             }
+            const float bj = bt[b * SB + j];
 #pragma unroll
-            for (int i = 0; i < SB; ++i)
+            for (int i = 0; i < SB; ++i) {
                 Tm[(b * SB + i) * PA + b * SB + j] = x[i];
+                Tp[(b * SB + i) * PS + b * SB + j] = __float2half_rn(x[i] * bj);
+            }
+        } else if (warp >= 2 && warp < 4) {
+            // upper off-diagonal block of T' is zero
+            const int e = (warp - 2) * 32 + lane;            // 0..63: 16 rows x 4 groups of 4 columns
+            const int i = e >> 2, j4 = (e & 3) * 4;
+            *reinterpret_cast<uint2 *>(Tp + i * PS + 16 + j4) = make_uint2(0u, 0u);
         }
         __syncthreads();
-        // off-diagonal blocks, by distance d = b1 - b0:  Tm_{b1 b0} = -Tm_{b1 b1} sum_{m=b0}^{b1-1} A_{b1 m} Tm_{m b0}
         {
-            float *Mt = reinterpret_cast<float *>(smem + OFF_OST);
-            for (int d = 1; d < 4; ++d) {
-                const int nblk = 4 - d;
-                for (int e = tid; e < nblk * 256; e += NTHREADS) {
-                    const int b0 = e >> 8, b1 = b0 + d, i = (e >> 4) & 15, j = e & 15;
-                    float s = 0.f;
-                    for (int m = b0; m < b1; ++m)
+            // off-diagonal block: Tm_10 = -Tm_11 (A_10 Tm_00);  thread = (i, j)
+            const int i = tid >> 4, j = tid & 15;
+            float *Mt = reinterpret_cast<float *>(smem + OFF_MT);
+            float s = 0.f;
 #pragma unroll
-                        for (int l = 0; l < SB; ++l)
-                            s = fmaf(Akk[(b1 * SB + i) * PA + m * SB + l], Tm[(m * SB + l) * PA + b0 * SB + j], s);
-                    Mt[e] = s;
-                }
-                __syncthreads();
-                for (int e = tid; e < nblk * 256; e += NTHREADS) {
-                    const int b0 = e >> 8, b1 = b0 + d, i = (e >> 4) & 15, j = e & 15;
-                    float s = 0.f;
+            for (int l = 0; l < SB; ++l)
+                s = fmaf(Akk[(SB + i) * PA + l], Tm[l * PA + j], s);
+            Mt[i * 16 + j] = s;
+            __syncthreads();
+            s = 0.f;
 #pragma unroll
-                    for (int l = 0; l < SB; ++l)
-                        s = fmaf(Tm[(b1 * SB + i) * PA + b1 * SB + l], Mt[(b0 << 8) + l * 16 + j], s);
-                    Tm[(b1 * SB + i) * PA + b0 * SB + j] = -s;
-                }
-                __syncthreads();
-            }
+            for (int l = 0; l < SB; ++l)
+                s = fmaf(Tm[(SB + i) * PA + SB + l], Mt[l * 16 + j], s);
+            Tp[(SB + i) * PS + j] = __float2half_rn(-s * bt[j]);
         }
+        __syncthreads();
 
-        // ---- S4: T' = Tm diag(b) (fp16, lower triangle), then -W = -T' (K^ . Gamma)
-        {
-            __half *Tp = reinterpret_cast<__half *>(smem + OFF_TP);
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int e = tid + m * NTHREADS, r = e >> 6, c = e & 63;
-                Tp[r * PS + c] = __float2half_rn(c <= r ? Tm[r * PA + c] * bt[c] : 0.f);
-            }
-        }
-        __syncthreads();
+        // ---- S4: -W = -T' (K^ . Gamma); warp: key columns 16w..16w+15
         {
             const uint32_t tp_base = smem_u32(smem + OFF_TP);
             const uint32_t kg_base = smem_u32(smem + OFF_KG);
             __half *Wn = reinterpret_cast<__half *>(smem + OFF_WN);
-            const int mi = lane >> 3, lr = lane & 7;
 #pragma unroll
-            for (int rb = 0; rb < 4; ++rb) {
+            for (int rb = 0; rb < 2; ++rb) {
                 float acc[2][4] = {};
+#pragma unroll
                 for (int ks = 0; ks <= rb; ++ks) {
                     uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                    // A = T'[16rb.., 16ks..] stored [m][k]
                     ldsm_x4(tp_base + ((rb * 16 + lr + (mi & 1) * 8) * PS + ks * 16 + (mi >> 1) * 8) * 2, a0, a1, a2, a3);
-                    // B = Kg[16ks.., 16warp..] stored [k][n]
-                    ldsm_x4_t(kg_base + ((ks * 16 + lr + (mi & 1) * 8) * PH + warp * 16 + (mi >> 1) * 8) * 2, b0, b1, b2, b3);
+                    ldsm_x4_t(kg_base + swz(ks * 16 + lr + (mi & 1) * 8, warp * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
                     mma_f16(acc[0], a0, a1, a2, a3, b0, b1);
                     mma_f16(acc[1], a0, a1, a2, a3, b2, b3);
                 }
@@ -546,8 +518,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int i = rb * 16 + gq + 8 * hh, j = warp * 16 + nt * 8 + 2 * tq;
-                        *reinterpret_cast<uint32_t *>(Wn + i * PH + j) =
-                            pack_half2(-acc[nt][2 * hh], -acc[nt][2 * hh + 1]);
+                        *reinterpret_cast<uint32_t *>(Wn + i * PH + j) = pack_half2(-acc[nt][2 * hh], -acc[nt][2 * hh + 1]);
                     }
             }
         }
@@ -562,28 +533,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             const uint32_t qt_base = smem_u32(smem + OFF_QT);
             const uint32_t aq_base = smem_u32(smem + OFF_AQK);
             const uint32_t kt_base = smem_u32(smem + OFF_KT);
-            const int mi = lane >> 3, lr = lane & 7;
-            float accU[8][4], accO[8][4];
+            float accU[4][4], accO[4][4];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     accU[nt][e] = accO[nt][e] = 0.f;
 
-            // U^T = V^T T'^T  (k = t', blocks t' <= t only)
+            // U^T = V^T T'^T  (k = t', token blocks t' <= t only)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 2; ++ks) {
                 uint32_t a0, a1, a2, a3;
-                // A = V^T: element (m = v, k = t') read from V stored [t'][v]
                 ldsm_x4_t(v_base + ((ks * 16 + lr + (mi >> 1) * 8) * PH + vr0 + (mi & 1) * 8) * 2, a0, a1, a2, a3);
                 a0 = bf16x2_to_half2(a0);
                 a1 = bf16x2_to_half2(a1);
                 a2 = bf16x2_to_half2(a2);
                 a3 = bf16x2_to_half2(a3);
 #pragma unroll
-                for (int np = ks; np < 4; ++np) {
+                for (int np = ks; np < 2; ++np) {
                     uint32_t b0, b1, b2, b3;
-                    // B[k = t'][n = t] = T'[t][t'], stored [n][k]
                     ldsm_x4(tp_base + ((np * 16 + lr + (mi >> 1) * 8) * PS + ks * 16 + (mi & 1) * 8) * 2, b0, b1, b2, b3);
                     mma_f16(accU[2 * np], a0, a1, a2, a3, b0, b1);
                     mma_f16(accU[2 * np + 1], a0, a1, a2, a3, b2, b3);
@@ -597,38 +565,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 const uint32_t a2 = pack_half2(accS[2 * ks + 1][0], accS[2 * ks + 1][1]);
                 const uint32_t a3 = pack_half2(accS[2 * ks + 1][2], accS[2 * ks + 1][3]);
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
+                for (int np = 0; np < 2; ++np) {
                     uint32_t b0, b1, b2, b3;
-                    const uint32_t off = ((np * 16 + lr + (mi >> 1) * 8) * PH + ks * 16 + (mi & 1) * 8) * 2;
-                    ldsm_x4(wn_base + off, b0, b1, b2, b3);
+                    const int row = np * 16 + lr + (mi >> 1) * 8, col = ks * 16 + (mi & 1) * 8;
+                    ldsm_x4(wn_base + (row * PH + col) * 2, b0, b1, b2, b3);
                     mma_f16(accU[2 * np], a0, a1, a2, a3, b0, b1);
                     mma_f16(accU[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                    ldsm_x4(qt_base + off, b0, b1, b2, b3);
+                    ldsm_x4(qt_base + swz(row, col), b0, b1, b2, b3);
                     mma_f16(accO[2 * np], a0, a1, a2, a3, b0, b1);
                     mma_f16(accO[2 * np + 1], a0, a1, a2, a3, b2, b3);
                 }
             }
             // U^T as fp16 A fragments (k = token)
-            uint32_t ua[4][4];
+            uint32_t ua[2][4];
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 2; ++ks) {
                 ua[ks][0] = pack_half2(accU[2 * ks][0], accU[2 * ks][1]);
                 ua[ks][1] = pack_half2(accU[2 * ks][2], accU[2 * ks][3]);
                 ua[ks][2] = pack_half2(accU[2 * ks + 1][0], accU[2 * ks + 1][1]);
                 ua[ks][3] = pack_half2(accU[2 * ks + 1][2], accU[2 * ks + 1][3]);
             }
-            // O^T += U^T Aqk^T  (k = t', blocks t' <= t only)
+            // O^T += U^T Aqk^T  (token blocks t' <= t only)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-                for (int np = ks; np < 4; ++np) {
+                for (int np = ks; np < 2; ++np) {
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(aq_base + ((np * 16 + lr + (mi >> 1) * 8) * PS + ks * 16 + (mi & 1) * 8) * 2, b0, b1, b2, b3);
                     mma_f16(accO[2 * np], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b0, b1);
                     mma_f16(accO[2 * np + 1], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b2, b3);
                 }
             }
-            // S^T <- S^T Diag(Gamma_63) + U^T K~
+            // S^T <- S^T Diag(Gamma_31) + U^T K~
 #pragma unroll
             for (int nt = 0; nt < 16; ++nt) {
                 const float2 gm = *reinterpret_cast<const float2 *>(Gc + nt * 8 + 2 * tq);
@@ -638,12 +606,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 accS[nt][3] *= gm.y;
             }
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
                 for (int np = 0; np < 8; ++np) {
                     uint32_t b0, b1, b2, b3;
-                    // B[k = t][n = key] = K~[t][key], stored [k][n]
-                    ldsm_x4_t(kt_base + ((ks * 16 + lr + (mi & 1) * 8) * PH + np * 16 + (mi >> 1) * 8) * 2, b0, b1, b2, b3);
+                    ldsm_x4_t(kt_base + swz(ks * 16 + lr + (mi & 1) * 8, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
                     mma_f16(accS[2 * np], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b0, b1);
                     mma_f16(accS[2 * np + 1], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b2, b3);
                 }
@@ -651,7 +618,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             // O^T * scale -> bf16 staging tile [t][v]
             __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int vv = vr0 + gq + 8 * hh, t = nt * 8 + 2 * tq;
@@ -665,7 +632,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         {
             const unsigned char *Ost = smem + OFF_OST;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+            for (int m = 0; m < 2; ++m) {
                 const int idx = tid + m * NTHREADS, r = idx >> 4, c16 = idx & 15;
                 if (r < L)
                     *reinterpret_cast<uint4 *>(p.out + ((tok0 + r) * H + h) * D + c16 * 8) =
@@ -673,7 +640,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             }
         }
         if (has_next)
-            load_tile_async(smem, OFF_RAW_V, p.v, ntok0, Ln, H, h);
+            load_tile_async<false>(smem, OFF_RAW_V, p.v, ntok0, Ln, H, h);
         cp_async_commit();
         if (tid < CH)
             rawb[tid] = next_beta;
