@@ -14,6 +14,7 @@ collective on the data path); rank 0 prints the aggregate.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -239,7 +240,7 @@ def run_ours(args, p, idx, rank, world):
         step()
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device())
-    if rank == 0:
+    if rank == 0 and not args.kernel_only:
         sampler.start()
         time.sleep(0.3)
     if world > 1:
@@ -263,6 +264,11 @@ def run_ours(args, p, idx, rank, world):
     sampler.mark(t_host0, t_host1)
     sampler.stop()
     ms_step = ms_total / args.steps
+    if args.kernel_only:
+        if rank == 0:
+            print(json.dumps({"kernel_only": True, "ms_per_step": ms_step, "T": p.T, "H": p.H,
+                              "algorithmic_bytes_per_launch": algorithmic_bytes(p)}), flush=True)
+        return
 
     # end to end through the public API with host buffers (copies inside the timed region)
     has_init = p.initial_state is not None
@@ -327,6 +333,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, help="0-4; 2 = T=8192 H=96 fixed length")
+    ap.add_argument("--T", type=int, default=None,
+                    help="profiling aid: shorten a fixed-length workload to T tokens (not a bench line)")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="profiling aid: time only the device launches (no e2e, CPU baseline or clock sampling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
@@ -345,6 +355,11 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     p = make_workload(args.workload)
+    if args.T is not None:
+        if p.cu_seqlens is not None:
+            raise SystemExit("--T applies to fixed-length workloads only")
+        p = dataclasses.replace(p, q=p.q[:, :args.T].copy(), k=p.k[:, :args.T].copy(), v=p.v[:, :args.T].copy(),
+                                g=p.g[:, :args.T].copy(), beta=p.beta[:, :args.T].copy())
     run_ours(args, p, args.workload, rank, world)
     if world > 1:
         import torch.distributed as dist
