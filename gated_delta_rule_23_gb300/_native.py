@@ -66,6 +66,8 @@ def load() -> ctypes.CDLL:
         lib.kda_check_cu_seqlens.restype = I
         lib.kda_status_string.argtypes = [I]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_device_status.argtypes = [P]
+        lib.kda_device_status.restype = I
         lib.kda_fwd_smem_bytes.argtypes = []
         lib.kda_fwd_smem_bytes.restype = ctypes.c_size_t
         _lib = lib

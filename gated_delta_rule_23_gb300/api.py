@@ -83,6 +83,14 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         raise KDAError(rc)
 
 
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Synchronise `stream` and raise KDAError if a kernel gave up a bounded device wait."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _native.load().kda_device_status(s.cuda_stream)
+    if rc != KDA_OK:
+        raise KDAError(rc)
+
+
 class KDAHostRunner:
     """Runs kda_fwd on host (pinned) tensors: copies inputs in, computes, copies results out.
 

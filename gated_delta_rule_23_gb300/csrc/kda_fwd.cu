@@ -1,13 +1,14 @@
 // KDA chunked forward pass for sm_103a (GB300).
 //
-// One CTA owns one (sequence, head) pair and walks its tokens in 32-token
-// chunks.  Per chunk it runs the token-parallel intra-chunk stage (gate, L2 norm,
-// decay factors, the strictly-lower beta*K*K^T and causal Q*K^T matrices, the
-// (I + A)^-1 inverse and the WY transform) and then the chunk recurrence on the
-// state; this follows the split into an intra-chunk stage (gate activation -> L2
-// norm -> decay -> L / Mqk construction -> inversion) and a chunk-wise delta-rule
-// recurrence described in the guancyxx.cn FlashKDA article, section 2.2, but
-// fuses both into one launch so the intermediates never leave shared memory.
+// One CTA (16 warps) owns one (sequence, head) pair and walks its tokens in
+// 32-token chunks.  Per chunk it runs the token-parallel intra-chunk stage (gate,
+// L2 norm, decay factors, the strictly-lower beta*K*K^T and causal Q*K^T matrices,
+// the (I + A)^-1 inverse and the WY transform) on CUDA cores and mma.sync, and the
+// chunk recurrence on the 5th-generation tensor cores with the state resident in
+// tensor memory.  This follows the split into an intra-chunk stage (gate
+// activation -> L2 norm -> decay -> L / Mqk construction -> inversion) and a
+// chunk-wise delta-rule recurrence described in the guancyxx.cn FlashKDA article,
+// section 2.2, fused into one launch so the intermediates never leave the SM.
 //
 // Notation (per chunk, rows i = 0..31, channel c, state S in R^{K x V}):
 //   a_i    = lower_bound * sigmoid(exp(A_log) * (g_i + dt_bias))   (natural-log decay)
@@ -26,9 +27,12 @@
 //   exp(G_i - G_j) = P_i E_j                (i in sub-block 1, j in sub-block 0)
 //   Gamma_i = P_i (b(i) = 0) or D_0 P_i;    Gamma_31 / Gamma_j = E_j D_1 (b(j) = 0) or E_j.
 //
-// The inter-chunk stage is computed transposed: each warp owns 16 value columns of
-// the state (rows of S^T) and keeps S^T (fp32 master), U^T and O^T for them in
-// registers, since the recurrence never mixes value columns.
+// The recurrence is computed transposed, M = 128 value rows on the tensor-memory
+// lanes: S^T (fp32, 128 columns) is the A operand of kind::tf32 MMAs straight from
+// tensor memory, U^T (32 columns) likewise; B operands are tf32-rounded fp32 tiles
+// in shared memory (no-swizzle K-major core-matrix layout).  Per chunk:
+//   O^T = S^T Q~^T;  U^T = V^T T'^T - S^T W^T;  S^T *= Gamma_31 (threads);
+//   O^T += U^T Aqk^T;  S^T += U^T K~.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,25 +43,35 @@
 
 #include "kda.h"
 
+// Set when a bounded wait on the tensor cores expires (read by kda_device_status).
+__device__ unsigned int g_kda_device_error;
+
 namespace {
 
 constexpr int D = 128;        // K = V = 128
 constexpr int CH = 32;        // tokens per chunk
 constexpr int SB = 16;        // tokens per decay sub-block
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 512;
+constexpr int TMEM_COLS = 256;
+constexpr int TM_S = 0, TM_U = 128, TM_O = 160;  // tensor-memory columns of S^T, U^T, O^T
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr uint32_t WAIT_LIMIT = 1u << 24;        // try_wait polls before a wait is declared hung
 
 // ---------------------------------------------------------------- shared memory map
-// Half-precision [32][136] tiles (272-byte rows) hold q, k, g, v and the fp16 operands.
-// The q, k, g tiles and the fp16 operands written by the gate pass swizzle their
-// 16-byte chunks by ((row >> 3) & 3) << 1, which makes the gate pass (lanes spread
-// over four 8-row segments) and ldmatrix both free of bank conflicts.  fp32 tf32
-// operands use a 132-float pitch, conflict-free for the mma fragment loads.
-constexpr int PH = 136;                          // half row pitch (elements)
-constexpr int PF = 132;                          // fp32 pitch of 128-wide tf32 operands
+// Half-precision [32][136] tiles (272-byte rows).  The q, k, g tiles and K^.Gamma swizzle
+// their 16-byte chunks by (row >> 3) & 3, which makes the gate pass (lanes spread over
+// eight 4-row segments) and ldmatrix free of bank conflicts.
+constexpr int PH = 136;
+constexpr int PF = 132;                          // fp32 pitch of 128-wide tf32 mma.sync operands
 constexpr int PA = 36;                           // fp32 pitch of 32-wide matrices
 constexpr int PS = 40;                           // half pitch of 32-wide matrices
-constexpr int HT = CH * PH * 2;                  // 8704 B: one [32][136] half tile
+constexpr int HT = CH * PH * 2;                  // 8704 B
+// tcgen05 operand tiles: element (row r, k) of a K-major tile sits at
+// (r / 8) * SBO + (k / 4) * LBO + (r % 8) * 16 + (k % 4) * 4 (fp32, 8x16-byte core matrices).
+constexpr int QT_LBO = 144, QT_SBO = 4640;       // Q~   [32 t][128 k]  (padded: conflict-free gate-pass stores)
+constexpr int KT_LBO = 144, KT_SBO = 1152;       // K~^T [128 k][32 t]
+constexpr int W_LBO = 128, W_SBO = 4096;         // -W   [32 t][128 k]
+constexpr int SQ_LBO = 128, SQ_SBO = 1024;       // Aqk, T' [32 t][32 t'];  V^T [128 v][32 t']
 
 constexpr int OFF_RAW_Q = 0;
 constexpr int OFF_RAW_K = OFF_RAW_Q + HT;
@@ -73,32 +87,40 @@ constexpr int OFF_EK = OFF_ED + F32T;            // fp32 [16][132]  k^ E  (sub-b
 constexpr int INTRA_BYTES = 3 * F32T + F32T / 2;
 // after the Akk / Aqk products the same region holds:
 constexpr int OFF_AKK = OFF_INTRA;               // fp32 [32][36]
-constexpr int OFF_TM = OFF_AKK + CH * PA * 4;    // fp32 [32][36]  diagonal blocks of Tm
-constexpr int OFF_AQK = OFF_TM + CH * PA * 4;    // fp16 [32][40]
-constexpr int OFF_TP = OFF_AQK + CH * PS * 2;    // fp16 [32][40]  T' = Tm diag(b)
-constexpr int OFF_MT = OFF_TP + CH * PS * 2;     // fp32 [16][16]  inverse scratch
-constexpr int OFF_WN = OFF_MT + 16 * 16 * 4;     // fp16 [32][136] -W
-constexpr int OFF_OST = OFF_WN + HT;             // bf16 [32][136] output staging
+constexpr int OFF_TMD = OFF_AKK + CH * PA * 4;   // fp32 [32][36]  diagonal blocks of Tm
+constexpr int OFF_TPH = OFF_TMD + CH * PA * 4;   // fp16 [32][40]  T' for the W product
+constexpr int OFF_MT = OFF_TPH + CH * PS * 2;    // fp32 [16][16]  inverse scratch
+constexpr int OFF_OST = OFF_MT + 16 * 16 * 4;    // bf16 [32][136] output staging
 constexpr int INTRA_END = OFF_OST + HT;
-constexpr int OFF_INTER = OFF_INTRA + INTRA_BYTES;
-constexpr int OFF_QT = OFF_INTER;                // fp16 [32][136] Q~          (swizzled)
-constexpr int OFF_KT = OFF_QT + HT;              // fp16 [32][136] K~          (swizzled)
-constexpr int OFF_KG = OFF_KT + HT;              // fp16 [32][136] K^ . Gamma  (swizzled)
+constexpr int OFF_QT = OFF_INTRA + INTRA_BYTES;  // tcgen05 B tiles from here on
+constexpr int OFF_KT = OFF_QT + 4 * QT_SBO;
+constexpr int OFF_W = OFF_KT + 16 * KT_SBO;
+constexpr int OFF_AQ = OFF_W + 4 * W_SBO;
+constexpr int OFF_TP = OFF_AQ + 4 * SQ_SBO;
+constexpr int OFF_VT = OFF_TP + 4 * SQ_SBO;
+constexpr int OFF_KG = OFF_VT + 16 * SQ_SBO;     // fp16 [32][136] K^ . Gamma (swizzled)
 constexpr int OFF_MISC = OFF_KG + HT;
 constexpr int OFF_RQ = OFF_MISC;                 // fp32 [32] 1/|q|
 constexpr int OFF_RK = OFF_RQ + 128;             // fp32 [32] 1/|k|
 constexpr int OFF_BT = OFF_RK + 128;             // fp32 [32] b = sigmoid(beta), 0 past the end
 constexpr int OFF_GC = OFF_BT + 128;             // fp32 [128] chunk decay Gamma_31
-constexpr int SMEM_BYTES = OFF_GC + D * 4;
-static_assert(INTRA_END <= OFF_INTER, "post-product overlay exceeds the intra region");
+constexpr int OFF_BAR = OFF_GC + D * 4;          // 2 mbarriers + tensor-memory base address
+constexpr int SMEM_BYTES = OFF_BAR + 32;
+static_assert(INTRA_END <= OFF_QT, "post-product overlay exceeds the intra region");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-static_assert(OFF_INTRA % 128 == 0 && OFF_INTER % 16 == 0 && OFF_MISC % 16 == 0 && OFF_WN % 16 == 0 &&
-              OFF_OST % 16 == 0 && OFF_TP % 16 == 0 && OFF_AQK % 16 == 0, "alignment");
+static_assert(OFF_INTRA % 128 == 0 && OFF_QT % 16 == 0 && OFF_KT % 16 == 0 && OFF_W % 16 == 0 &&
+              OFF_AQ % 16 == 0 && OFF_TP % 16 == 0 && OFF_VT % 16 == 0 && OFF_KG % 16 == 0 &&
+              OFF_MISC % 16 == 0 && OFF_OST % 16 == 0 && OFF_TPH % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
 // byte offset of element (row, col) in a swizzled [32][136] half tile
 __host__ __device__ constexpr int swz(int row, int col)
 {
-    return row * PH * 2 + ((((col >> 3) ^ (((row >> 3) & 3) << 1))) << 4) + ((col & 7) << 1);
+    return row * PH * 2 + (((col >> 3) ^ ((row >> 3) & 3)) << 4) + ((col & 7) << 1);
+}
+// byte offset of fp32 element (r, k) in a K-major tcgen05 tile
+__host__ __device__ constexpr int kmaj(int r, int k, int lbo, int sbo)
+{
+    return (r >> 3) * sbo + (k >> 2) * lbo + ((r & 7) << 4) + ((k & 3) << 2);
 }
 
 // ---------------------------------------------------------------- small device helpers
@@ -135,8 +157,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_half2(uint32_t u) { return pack_half2(bf16_lo(u), bf16_hi(u)); }
-
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
     uint32_t y;
@@ -147,12 +167,6 @@ __device__ __forceinline__ uint32_t to_tf32(float x)
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
@@ -176,6 +190,88 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- tcgen05 helpers
+// Shared-memory matrix descriptor: start address, leading (K-direction) and stride
+// (M/N-direction) byte offsets between 8x16-byte core matrices, no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor: fp32 accumulator, tf32 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, int acc)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}"
+                 ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void umma_commit(uint32_t mbar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&u)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+                   "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
+                   "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]),
+                   "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]),
+                   "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&u)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                   "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]),
+                   "r"(u[15]), "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]),
+                   "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]),
+                   "r"(u[31]));
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&u)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait for an mbarrier phase; returns false if the wait gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
+{
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t &r0, uint32_t &r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
 {
     const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
@@ -190,10 +286,11 @@ template <bool SWZ>
 __device__ __forceinline__ void load_tile_async(unsigned char *smem, int off, const __nv_bfloat16 *base,
                                                 int64_t tok0, int len, int H, int h)
 {
+    static_assert((CH * 16) % NTHREADS == 0, "tile load split");
     const int tid = threadIdx.x;
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int idx = tid + m * NTHREADS;   // 0..511: 32 rows x 16 chunks of 16 bytes
+    for (int m = 0; m < CH * 16 / NTHREADS; ++m) {
+        const int idx = tid + m * NTHREADS;   // 32 rows x 16 chunks of 16 bytes
         const int r = idx >> 4, c16 = idx & 15;
         const bool valid = r < len;
         const int64_t row = tok0 + (valid ? r : 0);
@@ -223,7 +320,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, tq = lane & 3;             // mma fragment coordinates
+    const int gq = lane >> 2, tq = lane & 3;             // mma.sync fragment coordinates
     const int mi = lane >> 3, lr = lane & 7;             // ldmatrix lane roles
     const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int H = p.H;
@@ -242,42 +339,75 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     float *bt = reinterpret_cast<float *>(smem + OFF_BT);
     float *Gc = reinterpret_cast<float *>(smem + OFF_GC);
     __nv_bfloat16 *rawb = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_RAW_B);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 16);
+    const uint32_t mbarA = smem_u32(smem + OFF_BAR), mbarB = smem_u32(smem + OFF_BAR + 8);
+    const uint32_t s_qt = smem_u32(smem + OFF_QT), s_kt = smem_u32(smem + OFF_KT), s_w = smem_u32(smem + OFF_W);
+    const uint32_t s_aq = smem_u32(smem + OFF_AQ), s_tp = smem_u32(smem + OFF_TP), s_vt = smem_u32(smem + OFF_VT);
 
-    // -------- state: each warp owns value rows vr0..vr0+15 of S^T, all 128 key columns
-    const int vr0 = warp * 16;
-    float accS[16][4];
-    {
-        const size_t sbase = ((size_t)n * H + h) * D * D;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int kc = nt * 8 + 2 * tq;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int vv = vr0 + gq + 8 * hh;
-                float x0 = 0.f, x1 = 0.f;
-                if (STATE == 2 && p.init) {
-                    const float2 s = *reinterpret_cast<const float2 *>(
-                        static_cast<const float *>(p.init) + sbase + (size_t)vv * D + kc);
-                    x0 = s.x;
-                    x1 = s.y;
-                } else if (STATE == 1 && p.init) {
-                    const uint32_t s = *reinterpret_cast<const uint32_t *>(
-                        static_cast<const __nv_bfloat16 *>(p.init) + sbase + (size_t)vv * D + kc);
-                    x0 = bf16_lo(s);
-                    x1 = bf16_hi(s);
-                }
-                accS[nt][2 * hh] = x0;
-                accS[nt][2 * hh + 1] = x1;
-            }
-        }
+    // -------- tensor memory, barriers, constant-zero tile parts
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
     }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarA));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarB));
+    }
+    // the Aqk and T' tiles are written lower-block-triangular only; their upper blocks stay zero
+    static_assert(OFF_TP == OFF_AQ + 4 * SQ_SBO && 8 * SQ_SBO == NTHREADS * 16, "zero fill");
+    reinterpret_cast<uint4 *>(smem + OFF_AQ)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    // tensor-memory lanes a warp may touch: quarter q4; this thread's value row and column group
+    const int q4 = warp & 3, cg = warp >> 2;
+    const int vrow = q4 * 32 + lane;
+    const uint32_t trow = tbase + ((uint32_t)(q4 * 32) << 16);
+    const size_t srow = ((size_t)n * H + h) * D * D + (size_t)vrow * D + cg * 32;
 
-    // gate-pass lane roles: channel pair cp of this warp's 16 channels, 8-row segment sg
-    const int cp = lane & 7, sg = lane >> 3, blk = sg >> 1;
-    const int c0 = warp * 16 + 2 * cp;
+    // -------- initial state -> S^T in tensor memory (row v, columns k)
+    {
+        uint32_t u[32];
+        if (STATE == 2 && p.init) {
+            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + srow);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 x = src[e];
+                u[4 * e] = __float_as_uint(x.x);
+                u[4 * e + 1] = __float_as_uint(x.y);
+                u[4 * e + 2] = __float_as_uint(x.z);
+                u[4 * e + 3] = __float_as_uint(x.w);
+            }
+        } else if (STATE == 1 && p.init) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.init) + srow);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint4 x = src[e];
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    u[8 * e + 2 * f] = w4[f] << 16;
+                    u[8 * e + 2 * f + 1] = w4[f] & 0xffff0000u;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                u[e] = 0u;
+        }
+        tmem_st32(trow + TM_S + cg * 32, u);
+    }
+    tc_fence_before();
+
+    // gate-pass lane roles: channel pair cp of this warp's 8 channels, 4-row segment sg
+    const int cp = lane & 3, sg = lane >> 2, blk = sg >> 2, si = sg & 3;
+    const int c0 = warp * 8 + 2 * cp;
     const float eA = expf(p.A_log[h]);
     const float2 dtb = *reinterpret_cast<const float2 *>(p.dt_bias + h * D + c0);
     const int nchunks = (int)((len + CH - 1) / CH);
+    bool hung = false;
 
     // prologue: stage chunk 0 (q, k, g as one group, v as a second group)
     if (nchunks > 0) {
@@ -299,6 +429,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         const bool has_next = ci + 1 < nchunks;
         const int64_t ntok0 = tok0 + CH;
         const int Ln = has_next ? (int)((rem - CH) < CH ? (rem - CH) : CH) : 0;
+        const uint32_t parity = ci & 1;
 
         cp_async_wait<1>();   // q, k, g of this chunk have landed (v may still be in flight)
         __syncthreads();
@@ -306,42 +437,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         // ---- S1a: row norms (16 lanes per row, 8 channels per lane) and beta
         {
             const int half = lane >> 4, l16 = lane & 15;
+            const int r = warp * 2 + half;
+            const uint4 qa = *reinterpret_cast<const uint4 *>(smem + OFF_RAW_Q + swz(r, l16 * 8));
+            const uint4 ka = *reinterpret_cast<const uint4 *>(smem + OFF_RAW_K + swz(r, l16 * 8));
+            const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+            float sq = 0.f, sk = 0.f;
 #pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int r = warp * 4 + it * 2 + half;
-                const uint4 qa = *reinterpret_cast<const uint4 *>(smem + OFF_RAW_Q + swz(r, l16 * 8));
-                const uint4 ka = *reinterpret_cast<const uint4 *>(smem + OFF_RAW_K + swz(r, l16 * 8));
-                const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
-                float sq = 0.f, sk = 0.f;
+            for (int e = 0; e < 4; ++e) {
+                const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]), k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+                sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+                sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]), k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
-                    sq = fmaf(q0, q0, fmaf(q1, q1, sq));
-                    sk = fmaf(k0, k0, fmaf(k1, k1, sk));
-                }
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                }
-                if (l16 == 0) {
-                    rq[r] = rsqrtf(sq + 1e-6f);
-                    rk[r] = rsqrtf(sk + 1e-6f);
-                }
+            for (int o = 8; o > 0; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            if (l16 == 0) {
+                rq[r] = rsqrtf(sq + 1e-6f);
+                rk[r] = rsqrtf(sk + 1e-6f);
             }
             if (tid < CH)
                 bt[tid] = tid < L ? sigmoidf_fast(__bfloat162float(rawb[tid])) : 0.f;
         }
         __syncthreads();
 
-        // ---- S1b: gate, sub-block decay products, all operands of this chunk (one pass)
+        // ---- S1b: gate, sub-block decay products and every operand of this chunk (one pass)
         {
-            uint32_t gqv[8], gkv[8];
-            float al0[8], al1[8];
+            uint32_t gqv[4], gkv[4];
+            float al0[4], al1[4];
             float tot0 = 1.f, tot1 = 1.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = sg * 8 + i;
+            for (int i = 0; i < 4; ++i) {
+                const int r = sg * 4 + i;
                 const uint32_t gg = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_G + swz(r, c0));
                 gqv[i] = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_Q + swz(r, c0));
                 gkv[i] = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_K + swz(r, c0));
@@ -352,23 +480,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 tot0 *= al0[i];
                 tot1 *= al1[i];
             }
-            // the other 8-row segment of this sub-block (lane ^ 8) and the other sub-block (lane ^ 16)
-            const float ot0 = __shfl_xor_sync(0xffffffffu, tot0, 8), ot1 = __shfl_xor_sync(0xffffffffu, tot1, 8);
-            const float D0 = tot0 * ot0, D1 = tot1 * ot1;                     // this sub-block's decay
-            const float Do0 = __shfl_xor_sync(0xffffffffu, D0, 16), Do1 = __shfl_xor_sync(0xffffffffu, D1, 16);
+            // scans over the four 4-row segments of this sub-block (lane bits 2-3), per channel
+            const unsigned FULL = 0xffffffffu;
+            float x0 = tot0, x1 = tot1, y0, y1;
+            y0 = __shfl_up_sync(FULL, x0, 4);
+            y1 = __shfl_up_sync(FULL, x1, 4);
+            if (si >= 1) { x0 *= y0; x1 *= y1; }
+            y0 = __shfl_up_sync(FULL, x0, 8);
+            y1 = __shfl_up_sync(FULL, x1, 8);
+            if (si >= 2) { x0 *= y0; x1 *= y1; }                         // inclusive prefix
+            float ex0 = __shfl_up_sync(FULL, x0, 4), ex1 = __shfl_up_sync(FULL, x1, 4);
+            if (si == 0) { ex0 = 1.f; ex1 = 1.f; }                       // exclusive prefix
+            const float D0 = __shfl_sync(FULL, x0, lane | 12), D1 = __shfl_sync(FULL, x1, lane | 12);
+            float z0 = tot0, z1 = tot1, w0, w1;
+            w0 = __shfl_down_sync(FULL, z0, 4);
+            w1 = __shfl_down_sync(FULL, z1, 4);
+            if (si <= 2) { z0 *= w0; z1 *= w1; }
+            w0 = __shfl_down_sync(FULL, z0, 8);
+            w1 = __shfl_down_sync(FULL, z1, 8);
+            if (si <= 1) { z0 *= w0; z1 *= w1; }                         // inclusive suffix
+            float es0 = __shfl_down_sync(FULL, z0, 4), es1 = __shfl_down_sync(FULL, z1, 4);
+            if (si == 3) { es0 = 1.f; es1 = 1.f; }                       // exclusive suffix
+            const float Do0 = __shfl_xor_sync(FULL, D0, 16), Do1 = __shfl_xor_sync(FULL, D1, 16);
             const float pre0 = blk ? Do0 : 1.f, pre1 = blk ? Do1 : 1.f;       // Gamma at sub-block start
             const float post0 = blk ? 1.f : Do0, post1 = blk ? 1.f : Do1;     // decay after sub-block end
             const float iD0 = rcp_approx(D0), iD1 = rcp_approx(D1);
-            const bool odd = sg & 1;
-            float P0 = odd ? ot0 : 1.f, P1 = odd ? ot1 : 1.f;
-            float E0 = odd ? 1.f : ot0, E1 = odd ? 1.f : ot1;
             float *Lq = reinterpret_cast<float *>(smem + OFF_LQ);
             float *Lk = reinterpret_cast<float *>(smem + OFF_LK);
             float *Ed = reinterpret_cast<float *>(smem + OFF_ED);
             float *Ek = reinterpret_cast<float *>(smem + OFF_EK);
+            float P0 = ex0, P1 = ex1;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = sg * 8 + i;
+            for (int i = 0; i < 4; ++i) {
+                const int r = sg * 4 + i;
                 const float qn = rq[r], kn = rk[r];
                 const float q0 = bf16_lo(gqv[i]) * qn, q1 = bf16_hi(gqv[i]) * qn;
                 const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
@@ -376,24 +520,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 P1 *= al1[i];
                 *reinterpret_cast<float2 *>(Lq + r * PF + c0) = make_float2(tf32r(q0 * P0), tf32r(q1 * P1));
                 *reinterpret_cast<float2 *>(Lk + r * PF + c0) = make_float2(tf32r(k0 * P0), tf32r(k1 * P1));
-                *reinterpret_cast<uint32_t *>(smem + OFF_QT + swz(r, c0)) = pack_half2(q0 * P0 * pre0, q1 * P1 * pre1);
+                *reinterpret_cast<float2 *>(smem + OFF_QT + kmaj(r, c0, QT_LBO, QT_SBO)) =
+                    make_float2(tf32r(q0 * P0 * pre0), tf32r(q1 * P1 * pre1));
                 *reinterpret_cast<uint32_t *>(smem + OFF_KG + swz(r, c0)) = pack_half2(k0 * P0 * pre0, k1 * P1 * pre1);
             }
+            float E0 = es0, E1 = es1;
+            float kt0[4], kt1[4];
 #pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                const int r = sg * 8 + i;
+            for (int i = 3; i >= 0; --i) {
+                const int r = sg * 4 + i;
                 const float kn = rk[r];
                 const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
                 *reinterpret_cast<float2 *>(Ed + r * PF + c0) = make_float2(tf32r(k0 * E0 * iD0), tf32r(k1 * E1 * iD1));
                 if (blk == 0)
                     *reinterpret_cast<float2 *>(Ek + r * PF + c0) = make_float2(tf32r(k0 * E0), tf32r(k1 * E1));
-                *reinterpret_cast<uint32_t *>(smem + OFF_KT + swz(r, c0)) = pack_half2(k0 * E0 * post0, k1 * E1 * post1);
+                kt0[i] = tf32r(k0 * E0 * post0);
+                kt1[i] = tf32r(k1 * E1 * post1);
                 E0 *= al0[i];
                 E1 *= al1[i];
             }
+            *reinterpret_cast<float4 *>(smem + OFF_KT + kmaj(c0, sg * 4, KT_LBO, KT_SBO)) =
+                make_float4(kt0[0], kt0[1], kt0[2], kt0[3]);
+            *reinterpret_cast<float4 *>(smem + OFF_KT + kmaj(c0 + 1, sg * 4, KT_LBO, KT_SBO)) =
+                make_float4(kt1[0], kt1[1], kt1[2], kt1[3]);
             if (sg == 0)
                 *reinterpret_cast<float2 *>(Gc + c0) = make_float2(D0 * Do0, D1 * Do1);
         }
+        fence_async_smem();
         __syncthreads();
 
         // ---- raw q, k, g, beta are consumed: start staging the next chunk's
@@ -407,53 +560,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         if (has_next && tid < Ln)
             next_beta = p.beta[(ntok0 + tid) * H + h];
 
-        // ---- S2: Akk and Aqk on tf32 tensor cores; items (pair, kind), pairs (0,0), (1,0), (1,1)
-        float acc2[2][4] = {};
-        const int item = warp;           // warps 0..5
-        const int pair = item >> 1, qk = item & 1;
-        const int rb1 = pair == 0 ? 0 : 16;                  // row block of the left factor
-        if (item < 6) {
+        // ---- tensor cores: O^T = S^T Q~^T (runs while the threads build the remaining operands)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < D / 8; ++s)
+                mma_tf32_ts(tbase + TM_O, tbase + TM_S + 8 * s, umma_desc(s_qt + s * 2 * QT_LBO, QT_LBO, QT_SBO),
+                            idesc_tf32(128, 32), s > 0);
+        }
+
+        // ---- S2: Akk and Aqk on tf32 mma.sync; items (pair, kind, n-tile) on warps 0..11
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        const int pair = warp >> 2, qk = (warp >> 1) & 1, ntl = warp & 1;
+        const int rb1 = pair == 0 ? 0 : 16, cb0 = pair == 2 ? 16 : 0;
+        if (warp < 12) {
             const float *X = reinterpret_cast<const float *>(smem + (qk ? OFF_LQ : OFF_LK)) + (rb1 + gq) * PF + tq;
             const float *Y = reinterpret_cast<const float *>(smem + (pair == 1 ? OFF_EK : OFF_ED)) +
-                             ((pair == 2 ? 16 : 0) + gq) * PF + tq;
+                             (cb0 + ntl * 8 + gq) * PF + tq;
 #pragma unroll 8
             for (int ks = 0; ks < D / 8; ++ks) {
                 const int k0 = ks * 8;
-                const uint32_t a0 = __float_as_uint(X[k0]), a1 = __float_as_uint(X[8 * PF + k0]);
-                const uint32_t a2 = __float_as_uint(X[k0 + 4]), a3 = __float_as_uint(X[8 * PF + k0 + 4]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-                    mma_tf32(acc2[nt], a0, a1, a2, a3, __float_as_uint(Y[nt * 8 * PF + k0]),
-                             __float_as_uint(Y[nt * 8 * PF + k0 + 4]));
+                mma_tf32(acc2, __float_as_uint(X[k0]), __float_as_uint(X[8 * PF + k0]), __float_as_uint(X[k0 + 4]),
+                         __float_as_uint(X[8 * PF + k0 + 4]), __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
             }
         }
         __syncthreads();   // the intra operands are dead; the region is reused below
-        if (item < 6) {
+        if (warp < 12) {
             float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
-            __half *Aqk = reinterpret_cast<__half *>(smem + OFF_AQK);
-            const int cb0 = pair == 2 ? 16 : 0;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int i = rb1 + gq + 8 * hh, j = cb0 + nt * 8 + 2 * tq;
-                    const float x0 = acc2[nt][2 * hh], x1 = acc2[nt][2 * hh + 1];
-                    if (qk) {
-                        *reinterpret_cast<uint32_t *>(Aqk + i * PS + j) =
-                            pack_half2(j <= i ? x0 : 0.f, j + 1 <= i ? x1 : 0.f);
-                    } else {
-                        const float bi = bt[i];
-                        *reinterpret_cast<float2 *>(Akk + i * PA + j) =
-                            make_float2(j < i ? bi * x0 : 0.f, j + 1 < i ? bi * x1 : 0.f);
-                    }
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = rb1 + gq + 8 * hh, j = cb0 + ntl * 8 + 2 * tq;
+                const float x0 = acc2[2 * hh], x1 = acc2[2 * hh + 1];
+                if (qk) {
+                    *reinterpret_cast<float2 *>(smem + OFF_AQ + kmaj(i, j, SQ_LBO, SQ_SBO)) =
+                        make_float2(tf32r(j <= i ? x0 : 0.f), tf32r(j + 1 <= i ? x1 : 0.f));
+                } else {
+                    const float bi = bt[i];
+                    *reinterpret_cast<float2 *>(Akk + i * PA + j) =
+                        make_float2(j < i ? bi * x0 : 0.f, j + 1 < i ? bi * x1 : 0.f);
                 }
+            }
         }
         __syncthreads();
 
-        // ---- S3: Tm = (I + Akk)^-1 (fp32) and T' = Tm diag(b) (fp16)
+        // ---- S3: Tm = (I + Akk)^-1 (fp32); T' = Tm diag(b) as fp16 (for -W) and as a tf32 tile
         float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
-        float *Tm = reinterpret_cast<float *>(smem + OFF_TM);
-        __half *Tp = reinterpret_cast<__half *>(smem + OFF_TP);
+        float *Tmd = reinterpret_cast<float *>(smem + OFF_TMD);
+        __half *Tph = reinterpret_cast<__half *>(smem + OFF_TPH);
         if (warp < 2 && lane < 16) {
             // diagonal 16x16 blocks by forward substitution; lane = column
             const int b = warp, j = lane;
@@ -469,175 +622,148 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             const float bj = bt[b * SB + j];
 #pragma unroll
             for (int i = 0; i < SB; ++i) {
-                Tm[(b * SB + i) * PA + b * SB + j] = x[i];
-                Tp[(b * SB + i) * PS + b * SB + j] = __float2half_rn(x[i] * bj);
+                const int r = b * SB + i, c = b * SB + j;
+                Tmd[r * PA + c] = x[i];
+                Tph[r * PS + c] = __float2half_rn(x[i] * bj);
+                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(r, c, SQ_LBO, SQ_SBO)) = tf32r(x[i] * bj);
             }
-        } else if (warp >= 2 && warp < 4) {
-            // upper off-diagonal block of T' is zero
-            const int e = (warp - 2) * 32 + lane;            // 0..63: 16 rows x 4 groups of 4 columns
-            const int i = e >> 2, j4 = (e & 3) * 4;
-            *reinterpret_cast<uint2 *>(Tp + i * PS + 16 + j4) = make_uint2(0u, 0u);
         }
         __syncthreads();
         {
-            // off-diagonal block: Tm_10 = -Tm_11 (A_10 Tm_00);  thread = (i, j)
-            const int i = tid >> 4, j = tid & 15;
+            // off-diagonal block: Tm_10 = -Tm_11 (A_10 Tm_00);  threads 0..255 = (i, j)
+            const int i = (tid >> 4) & 15, j = tid & 15;
             float *Mt = reinterpret_cast<float *>(smem + OFF_MT);
-            float s = 0.f;
+            if (tid < 256) {
+                float s = 0.f;
 #pragma unroll
-            for (int l = 0; l < SB; ++l)
-                s = fmaf(Akk[(SB + i) * PA + l], Tm[l * PA + j], s);
-            Mt[i * 16 + j] = s;
+                for (int l = 0; l < SB; ++l)
+                    s = fmaf(Akk[(SB + i) * PA + l], Tmd[l * PA + j], s);
+                Mt[i * 16 + j] = s;
+            }
             __syncthreads();
-            s = 0.f;
+            if (tid < 256) {
+                float s = 0.f;
 #pragma unroll
-            for (int l = 0; l < SB; ++l)
-                s = fmaf(Tm[(SB + i) * PA + SB + l], Mt[l * 16 + j], s);
-            Tp[(SB + i) * PS + j] = __float2half_rn(-s * bt[j]);
+                for (int l = 0; l < SB; ++l)
+                    s = fmaf(Tmd[(SB + i) * PA + SB + l], Mt[l * 16 + j], s);
+                const float tv = -s * bt[j];
+                Tph[(SB + i) * PS + j] = __float2half_rn(tv);
+                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(SB + i, j, SQ_LBO, SQ_SBO)) = tf32r(tv);
+            }
         }
         __syncthreads();
 
-        // ---- S4: -W = -T' (K^ . Gamma); warp: key columns 16w..16w+15
+        // ---- S4: -W = -T' (K^ . Gamma) on mma.sync; warp: key columns 8w..8w+7
         {
-            const uint32_t tp_base = smem_u32(smem + OFF_TP);
-            const uint32_t kg_base = smem_u32(smem + OFF_KG);
-            __half *Wn = reinterpret_cast<__half *>(smem + OFF_WN);
+            const uint32_t tph = smem_u32(smem + OFF_TPH), kg = smem_u32(smem + OFF_KG);
 #pragma unroll
             for (int rb = 0; rb < 2; ++rb) {
-                float acc[2][4] = {};
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks <= rb; ++ks) {
-                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                    ldsm_x4(tp_base + ((rb * 16 + lr + (mi & 1) * 8) * PS + ks * 16 + (mi >> 1) * 8) * 2, a0, a1, a2, a3);
-                    ldsm_x4_t(kg_base + swz(ks * 16 + lr + (mi & 1) * 8, warp * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
-                    mma_f16(acc[0], a0, a1, a2, a3, b0, b1);
-                    mma_f16(acc[1], a0, a1, a2, a3, b2, b3);
+                    uint32_t a0, a1, a2, a3, b0, b1;
+                    ldsm_x4(tph + ((rb * 16 + lr + (mi & 1) * 8) * PS + ks * 16 + (mi >> 1) * 8) * 2, a0, a1, a2, a3);
+                    ldsm_x2_t(kg + swz(ks * 16 + (lane & 15), warp * 8), b0, b1);
+                    mma_f16(acc, a0, a1, a2, a3, b0, b1);
                 }
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int i = rb * 16 + gq + 8 * hh, j = warp * 16 + nt * 8 + 2 * tq;
-                        *reinterpret_cast<uint32_t *>(Wn + i * PH + j) = pack_half2(-acc[nt][2 * hh], -acc[nt][2 * hh + 1]);
-                    }
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = rb * 16 + gq + 8 * hh, kc = warp * 8 + 2 * tq;
+                    *reinterpret_cast<float2 *>(smem + OFF_W + kmaj(t, kc, W_LBO, W_SBO)) =
+                        make_float2(tf32r(-acc[2 * hh]), tf32r(-acc[2 * hh + 1]));
+                }
             }
         }
         cp_async_wait<1>();   // v of this chunk (the next chunk's q, k, g may stay in flight)
         __syncthreads();
+        // ---- V^T as a tf32 tile (A operand): thread task (value row v, token quad)
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int e = tid + m * NTHREADS, vv = e & 127, qd = e >> 7;
+            const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_V);
+            float4 f;
+            f.x = tf32r(__bfloat162float(rv[(4 * qd + 0) * PH + vv]));
+            f.y = tf32r(__bfloat162float(rv[(4 * qd + 1) * PH + vv]));
+            f.z = tf32r(__bfloat162float(rv[(4 * qd + 2) * PH + vv]));
+            f.w = tf32r(__bfloat162float(rv[(4 * qd + 3) * PH + vv]));
+            *reinterpret_cast<float4 *>(smem + OFF_VT + kmaj(vv, 4 * qd, SQ_LBO, SQ_SBO)) = f;
+        }
+        fence_async_smem();
+        __syncthreads();
 
-        // ---- S5: chunk recurrence, transposed, per warp: value rows vr0..vr0+15
+        // ---- tensor cores: U^T = V^T T'^T + S^T (-W)^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < CH / 8; ++s)
+                mma_tf32_ss(tbase + TM_U, umma_desc(s_vt + s * 2 * SQ_LBO, SQ_LBO, SQ_SBO),
+                            umma_desc(s_tp + s * 2 * SQ_LBO, SQ_LBO, SQ_SBO), idesc_tf32(128, 32), s > 0);
+#pragma unroll
+            for (int s = 0; s < D / 8; ++s)
+                mma_tf32_ts(tbase + TM_U, tbase + TM_S + 8 * s, umma_desc(s_w + s * 2 * W_LBO, W_LBO, W_SBO),
+                            idesc_tf32(128, 32), 1);
+            umma_commit(mbarA);
+        }
+        hung = !mbar_wait(mbarA, parity);
+        if (__syncthreads_or(hung)) {
+            hung = true;
+            break;
+        }
+        tc_fence_after();
+        // ---- S^T <- S^T Diag(Gamma_31): this thread's row, columns 32cg..32cg+31
         {
-            const uint32_t v_base = smem_u32(smem + OFF_RAW_V);
-            const uint32_t tp_base = smem_u32(smem + OFF_TP);
-            const uint32_t wn_base = smem_u32(smem + OFF_WN);
-            const uint32_t qt_base = smem_u32(smem + OFF_QT);
-            const uint32_t aq_base = smem_u32(smem + OFF_AQK);
-            const uint32_t kt_base = smem_u32(smem + OFF_KT);
-            float accU[4][4], accO[4][4];
+            uint32_t u[32];
+            tmem_ld32(trow + TM_S + cg * 32, u);
+            const float4 *g4 = reinterpret_cast<const float4 *>(Gc + cg * 32);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    accU[nt][e] = accO[nt][e] = 0.f;
-
-            // U^T = V^T T'^T  (k = t', token blocks t' <= t only)
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(v_base + ((ks * 16 + lr + (mi >> 1) * 8) * PH + vr0 + (mi & 1) * 8) * 2, a0, a1, a2, a3);
-                a0 = bf16x2_to_half2(a0);
-                a1 = bf16x2_to_half2(a1);
-                a2 = bf16x2_to_half2(a2);
-                a3 = bf16x2_to_half2(a3);
-#pragma unroll
-                for (int np = ks; np < 2; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(tp_base + ((np * 16 + lr + (mi >> 1) * 8) * PS + ks * 16 + (mi & 1) * 8) * 2, b0, b1, b2, b3);
-                    mma_f16(accU[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_f16(accU[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                }
+            for (int e = 0; e < 8; ++e) {
+                const float4 gm = g4[e];
+                u[4 * e] = __float_as_uint(__uint_as_float(u[4 * e]) * gm.x);
+                u[4 * e + 1] = __float_as_uint(__uint_as_float(u[4 * e + 1]) * gm.y);
+                u[4 * e + 2] = __float_as_uint(__uint_as_float(u[4 * e + 2]) * gm.z);
+                u[4 * e + 3] = __float_as_uint(__uint_as_float(u[4 * e + 3]) * gm.w);
             }
-            // U^T += S^T (-W)^T,  O^T = S^T Q~^T   (k = key channel)
+            tmem_st32(trow + TM_S + cg * 32, u);
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- tensor cores: O^T += U^T Aqk^T;  S^T += U^T K~
+        if (tid == 0) {
+            tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t a0 = pack_half2(accS[2 * ks][0], accS[2 * ks][1]);
-                const uint32_t a1 = pack_half2(accS[2 * ks][2], accS[2 * ks][3]);
-                const uint32_t a2 = pack_half2(accS[2 * ks + 1][0], accS[2 * ks + 1][1]);
-                const uint32_t a3 = pack_half2(accS[2 * ks + 1][2], accS[2 * ks + 1][3]);
+            for (int s = 0; s < CH / 8; ++s)
+                mma_tf32_ts(tbase + TM_O, tbase + TM_U + 8 * s, umma_desc(s_aq + s * 2 * SQ_LBO, SQ_LBO, SQ_SBO),
+                            idesc_tf32(128, 32), 1);
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int row = np * 16 + lr + (mi >> 1) * 8, col = ks * 16 + (mi & 1) * 8;
-                    ldsm_x4(wn_base + (row * PH + col) * 2, b0, b1, b2, b3);
-                    mma_f16(accU[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_f16(accU[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                    ldsm_x4(qt_base + swz(row, col), b0, b1, b2, b3);
-                    mma_f16(accO[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_f16(accO[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-            // U^T as fp16 A fragments (k = token)
-            uint32_t ua[2][4];
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                ua[ks][0] = pack_half2(accU[2 * ks][0], accU[2 * ks][1]);
-                ua[ks][1] = pack_half2(accU[2 * ks][2], accU[2 * ks][3]);
-                ua[ks][2] = pack_half2(accU[2 * ks + 1][0], accU[2 * ks + 1][1]);
-                ua[ks][3] = pack_half2(accU[2 * ks + 1][2], accU[2 * ks + 1][3]);
-            }
-            // O^T += U^T Aqk^T  (token blocks t' <= t only)
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-                for (int np = ks; np < 2; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(aq_base + ((np * 16 + lr + (mi >> 1) * 8) * PS + ks * 16 + (mi & 1) * 8) * 2, b0, b1, b2, b3);
-                    mma_f16(accO[2 * np], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b0, b1);
-                    mma_f16(accO[2 * np + 1], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b2, b3);
-                }
-            }
-            // S^T <- S^T Diag(Gamma_31) + U^T K~
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                const float2 gm = *reinterpret_cast<const float2 *>(Gc + nt * 8 + 2 * tq);
-                accS[nt][0] *= gm.x;
-                accS[nt][1] *= gm.y;
-                accS[nt][2] *= gm.x;
-                accS[nt][3] *= gm.y;
-            }
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-                for (int np = 0; np < 8; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(kt_base + swz(ks * 16 + lr + (mi & 1) * 8, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
-                    mma_f16(accS[2 * np], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b0, b1);
-                    mma_f16(accS[2 * np + 1], ua[ks][0], ua[ks][1], ua[ks][2], ua[ks][3], b2, b3);
-                }
-            }
-            // O^T * scale -> bf16 staging tile [t][v]
+            for (int s = 0; s < CH / 8; ++s)
+                mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_kt + s * 2 * KT_LBO, KT_LBO, KT_SBO),
+                            idesc_tf32(128, 128), 1);
+            umma_commit(mbarB);
+        }
+        hung = !mbar_wait(mbarB, parity);
+        if (__syncthreads_or(hung)) {
+            hung = true;
+            break;
+        }
+        tc_fence_after();
+        // ---- O^T * scale -> bf16 staging tile [t][v]: this thread's row, tokens 8cg..8cg+7
+        {
+            uint32_t o[8];
+            tmem_ld8(trow + TM_O + cg * 8, o);
             __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int vv = vr0 + gq + 8 * hh, t = nt * 8 + 2 * tq;
-                    Ost[t * PH + vv] = __float2bfloat16_rn(accO[nt][2 * hh] * p.scale);
-                    Ost[(t + 1) * PH + vv] = __float2bfloat16_rn(accO[nt][2 * hh + 1] * p.scale);
-                }
+            for (int j = 0; j < 8; ++j)
+                Ost[(cg * 8 + j) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[j]) * p.scale);
         }
+        tc_fence_before();
         __syncthreads();
 
         // ---- write this chunk's outputs; stage the next chunk's v and beta
         {
-            const unsigned char *Ost = smem + OFF_OST;
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int idx = tid + m * NTHREADS, r = idx >> 4, c16 = idx & 15;
-                if (r < L)
-                    *reinterpret_cast<uint4 *>(p.out + ((tok0 + r) * H + h) * D + c16 * 8) =
-                        *reinterpret_cast<const uint4 *>(Ost + r * PH * 2 + c16 * 16);
-            }
+            const int r = tid >> 4, c16 = tid & 15;
+            if (r < L)
+                *reinterpret_cast<uint4 *>(p.out + ((tok0 + r) * H + h) * D + c16 * 8) =
+                    *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
         }
         if (has_next)
             load_tile_async<false>(smem, OFF_RAW_V, p.v, ntok0, Ln, H, h);
@@ -646,26 +772,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             rawb[tid] = next_beta;
     }
     cp_async_wait<0>();
+    __syncthreads();
 
-    // -------- final state
-    if (STATE != 0 && p.fin) {
-        const size_t sbase = ((size_t)n * H + h) * D * D;
+    // -------- final state, tensor memory release
+    if (hung) {
+        // give any tensor-core work still in flight a bounded chance to finish before releasing
+        mbar_wait(mbarA, 0);
+        mbar_wait(mbarB, 0);
+        if (tid == 0)
+            atomicOr(&g_kda_device_error, 1u);
+    } else if (STATE != 0 && p.fin) {
+        tc_fence_after();
+        uint32_t u[32];
+        tmem_ld32(trow + TM_S + cg * 32, u);
+        if (STATE == 2) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.fin) + srow);
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int kc = nt * 8 + 2 * tq;
+            for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                     __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
+        } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.fin) + srow);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int vv = vr0 + gq + 8 * hh;
-                if (STATE == 2) {
-                    *reinterpret_cast<float2 *>(static_cast<float *>(p.fin) + sbase + (size_t)vv * D + kc) =
-                        make_float2(accS[nt][2 * hh], accS[nt][2 * hh + 1]);
-                } else {
-                    __nv_bfloat162 s = __floats2bfloat162_rn(accS[nt][2 * hh], accS[nt][2 * hh + 1]);
-                    *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.fin) + sbase +
-                                                        (size_t)vv * D + kc) = s;
+            for (int e = 0; e < 4; ++e) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(u[8 * e + 2 * f]),
+                                                              __uint_as_float(u[8 * e + 2 * f + 1]));
+                    w4[f] = *reinterpret_cast<uint32_t *>(&b2);
                 }
+                dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS));
     }
 }
 
@@ -777,3 +922,15 @@ extern "C" const char *kda_status_string(kda_status_t s)
 }
 
 extern "C" size_t kda_fwd_smem_bytes(void) { return SMEM_BYTES; }
+
+extern "C" kda_status_t kda_device_status(kda_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    unsigned int flag = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&flag, g_kda_device_error, sizeof flag) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (flag && cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof zero) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return flag ? KDA_ERR_TIMEOUT : KDA_OK;
+}

@@ -34,11 +34,11 @@
  * final_state (in-place update).  Calls on different streams may run concurrently
  * if their output buffers do not overlap.
  *
- * Numerics: the kernel evaluates the chunked form of the recurrence (64-token
- * chunks, 16-token sub-blocks) with fp32 accumulation and an fp32 master copy of
- * the state.  Tensor-core operands: tf32 for the intra-chunk q.k and k.k products,
- * fp16 for the inter-chunk products.  fp16 operands bound the magnitudes of v and
- * of the state entries to below ~6e4; larger values overflow.
+ * Numerics: the kernel evaluates the chunked form of the recurrence (32-token
+ * chunks, 16-token decay sub-blocks) with fp32 accumulation; the state is held in
+ * fp32 (tensor memory) for the whole call.  Tensor-core operands are tf32 (fp32
+ * range) except the small T'.(K^ . Gamma) product, whose operands are bounded by 1
+ * in magnitude for any input and use fp16.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -63,7 +63,7 @@ typedef enum {
     KDA_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, bad size, misaligned pointer, bad dtype/state combination */
     KDA_ERR_UNSUPPORTED = 2,      /* lower_bound outside [-5, 0], or scale not finite */
     KDA_ERR_CUDA = 3,             /* a CUDA runtime call or the kernel launch failed */
-    KDA_ERR_TIMEOUT = 4           /* reserved for bounded device waits; not returned by kda_fwd */
+    KDA_ERR_TIMEOUT = 4           /* a bounded device wait expired (reported by kda_device_status) */
 } kda_status_t;
 
 /*
@@ -109,6 +109,14 @@ kda_status_t kda_check_cu_seqlens(const int64_t *host_cu_seqlens, int N, int64_t
 
 /* Static English description of a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);
+
+/*
+ * Waits for `stream`, then reports whether any kda_fwd kernel on this device gave
+ * up a bounded wait on the tensor cores since the last call (KDA_ERR_TIMEOUT; the
+ * outputs of that call are not valid), and clears the report.  KDA_ERR_CUDA if the
+ * stream or the query failed.  The kernel never spins without a limit and never traps.
+ */
+kda_status_t kda_device_status(kda_stream_t stream);
 
 /* Bytes of dynamic shared memory one CTA of the forward kernel uses (for diagnostics). */
 size_t kda_fwd_smem_bytes(void);

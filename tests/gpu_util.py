@@ -3,7 +3,7 @@ path through the C ABI, and compare with the oracle under the parity tolerances.
 import numpy as np
 import torch
 
-from gated_delta_rule_23_gb300 import kda_fwd
+from gated_delta_rule_23_gb300 import device_status, kda_fwd
 from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, bf16_to_f32
 
 # Parity bar: outputs rel-L2 <= 5e-3 and max-abs <= 3e-2; final states rel-L2 <= 5e-3.
@@ -43,7 +43,7 @@ def run_gpu(p, dev=None, inplace=False):
             fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device=dev["q"].device)
     kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
             p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"])
-    torch.cuda.synchronize()
+    device_status()            # synchronises; raises if a bounded device wait expired
     return out.float().cpu().numpy(), (None if fin is None else fin.float().cpu().numpy())
 
 

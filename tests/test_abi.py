@@ -17,7 +17,8 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = _native.declared_functions()
-    assert {"kda_fwd", "kda_check_cu_seqlens", "kda_status_string", "kda_fwd_smem_bytes"} <= set(names)
+    assert {"kda_fwd", "kda_check_cu_seqlens", "kda_status_string", "kda_fwd_smem_bytes",
+            "kda_device_status"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
