@@ -29,10 +29,13 @@
 //
 // The recurrence is computed transposed, M = 128 value rows on the tensor-memory
 // lanes: S^T (fp32, 128 columns) is the A operand of kind::tf32 MMAs straight from
-// tensor memory, U^T (32 columns) likewise; B operands are tf32-rounded fp32 tiles
-// in shared memory (no-swizzle K-major core-matrix layout).  Per chunk:
-//   O^T = S^T Q~^T;  U^T = V^T T'^T - S^T W^T;  S^T *= Gamma_31 (threads);
-//   O^T += U^T Aqk^T;  S^T += U^T K~.
+// tensor memory, as are Y^T and U^T; B operands are tf32-rounded fp32 tiles in
+// shared memory (no-swizzle K-major core-matrix layout).  Per chunk, using
+// U = T' (V - (K^ . Gamma) S):
+//   [O^T | X^T] = S^T [Q~ ; K^.Gamma]^T        (issued right after the gate pass;
+//                                               overlaps the Akk/Aqk products and the inverse)
+//   Y^T = V^T - X^T (threads);  U^T = Y^T T'^T;  S^T *= Gamma_31 (threads);
+//   [S^T | O^T] += U^T [K~^T ; Aqk]^T.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -53,7 +56,10 @@ constexpr int CH = 32;        // tokens per chunk
 constexpr int SB = 16;        // tokens per decay sub-block
 constexpr int NTHREADS = 512;
 constexpr int TMEM_COLS = 256;
-constexpr int TM_S = 0, TM_U = 128, TM_O = 160;  // tensor-memory columns of S^T, U^T, O^T
+// tensor-memory columns: S^T | O^T | X^T | Y^T | U^T (O^T follows S^T and X^T follows O^T so
+// that the merged MMAs write one contiguous accumulator)
+constexpr int TM_S = 0, TM_O = 128, TM_X = 160, TM_Y = 192, TM_U = 224;
+constexpr int MMA_TID = 384;                     // issuing thread: warp 12 has no Akk/Aqk item
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;        // try_wait polls before a wait is declared hung
 
@@ -64,14 +70,12 @@ constexpr uint32_t WAIT_LIMIT = 1u << 24;        // try_wait polls before a wait
 constexpr int PH = 136;
 constexpr int PF = 132;                          // fp32 pitch of 128-wide tf32 mma.sync operands
 constexpr int PA = 36;                           // fp32 pitch of 32-wide matrices
-constexpr int PS = 40;                           // half pitch of 32-wide matrices
 constexpr int HT = CH * PH * 2;                  // 8704 B
 // tcgen05 operand tiles: element (row r, k) of a K-major tile sits at
 // (r / 8) * SBO + (k / 4) * LBO + (r % 8) * 16 + (k % 4) * 4 (fp32, 8x16-byte core matrices).
-constexpr int QT_LBO = 144, QT_SBO = 4640;       // Q~   [32 t][128 k]  (padded: conflict-free gate-pass stores)
-constexpr int KT_LBO = 144, KT_SBO = 1152;       // K~^T [128 k][32 t]
-constexpr int W_LBO = 128, W_SBO = 4096;         // -W   [32 t][128 k]
-constexpr int SQ_LBO = 128, SQ_SBO = 1024;       // Aqk, T' [32 t][32 t'];  V^T [128 v][32 t']
+constexpr int QX_LBO = 144, QX_SBO = 4640;       // [Q~ ; K^.Gamma] [64 t][128 k]  (padded: conflict-free stores)
+constexpr int SO_LBO = 144, SO_SBO = 1152;       // [K~^T ; Aqk]    [160][32 t]
+constexpr int TP_LBO = 128, TP_SBO = 1024;       // T'              [32 t][32 t']
 
 constexpr int OFF_RAW_Q = 0;
 constexpr int OFF_RAW_K = OFF_RAW_Q + HT;
@@ -88,29 +92,23 @@ constexpr int INTRA_BYTES = 3 * F32T + F32T / 2;
 // after the Akk / Aqk products the same region holds:
 constexpr int OFF_AKK = OFF_INTRA;               // fp32 [32][36]
 constexpr int OFF_TMD = OFF_AKK + CH * PA * 4;   // fp32 [32][36]  diagonal blocks of Tm
-constexpr int OFF_TPH = OFF_TMD + CH * PA * 4;   // fp16 [32][40]  T' for the W product
-constexpr int OFF_MT = OFF_TPH + CH * PS * 2;    // fp32 [16][16]  inverse scratch
+constexpr int OFF_MT = OFF_TMD + CH * PA * 4;    // fp32 [16][16]  inverse scratch
 constexpr int OFF_OST = OFF_MT + 16 * 16 * 4;    // bf16 [32][136] output staging
 constexpr int INTRA_END = OFF_OST + HT;
-constexpr int OFF_QT = OFF_INTRA + INTRA_BYTES;  // tcgen05 B tiles from here on
-constexpr int OFF_KT = OFF_QT + 4 * QT_SBO;
-constexpr int OFF_W = OFF_KT + 16 * KT_SBO;
-constexpr int OFF_AQ = OFF_W + 4 * W_SBO;
-constexpr int OFF_TP = OFF_AQ + 4 * SQ_SBO;
-constexpr int OFF_VT = OFF_TP + 4 * SQ_SBO;
-constexpr int OFF_KG = OFF_VT + 16 * SQ_SBO;     // fp16 [32][136] K^ . Gamma (swizzled)
-constexpr int OFF_MISC = OFF_KG + HT;
+constexpr int OFF_QX = OFF_INTRA + INTRA_BYTES;  // tcgen05 B tiles from here on
+constexpr int OFF_SO = OFF_QX + 8 * QX_SBO;
+constexpr int OFF_TP = OFF_SO + 20 * SO_SBO;
+constexpr int OFF_MISC = OFF_TP + 4 * TP_SBO;
 constexpr int OFF_RQ = OFF_MISC;                 // fp32 [32] 1/|q|
 constexpr int OFF_RK = OFF_RQ + 128;             // fp32 [32] 1/|k|
 constexpr int OFF_BT = OFF_RK + 128;             // fp32 [32] b = sigmoid(beta), 0 past the end
 constexpr int OFF_GC = OFF_BT + 128;             // fp32 [128] chunk decay Gamma_31
-constexpr int OFF_BAR = OFF_GC + D * 4;          // 2 mbarriers + tensor-memory base address
+constexpr int OFF_BAR = OFF_GC + D * 4;          // 3 mbarriers + tensor-memory base address
 constexpr int SMEM_BYTES = OFF_BAR + 32;
-static_assert(INTRA_END <= OFF_QT, "post-product overlay exceeds the intra region");
+static_assert(INTRA_END <= OFF_QX, "post-product overlay exceeds the intra region");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-static_assert(OFF_INTRA % 128 == 0 && OFF_QT % 16 == 0 && OFF_KT % 16 == 0 && OFF_W % 16 == 0 &&
-              OFF_AQ % 16 == 0 && OFF_TP % 16 == 0 && OFF_VT % 16 == 0 && OFF_KG % 16 == 0 &&
-              OFF_MISC % 16 == 0 && OFF_OST % 16 == 0 && OFF_TPH % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+static_assert(OFF_INTRA % 128 == 0 && OFF_QX % 16 == 0 && OFF_SO % 16 == 0 && OFF_TP % 16 == 0 &&
+              OFF_MISC % 16 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
 // byte offset of element (row, col) in a swizzled [32][136] half tile
 __host__ __device__ constexpr int swz(int row, int col)
@@ -151,33 +149,11 @@ __device__ __forceinline__ float sigmoidf_fast(float z)
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
-{
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
     uint32_t y;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-
-// D += A * B, m16n8k16, fp16 operands, fp32 accumulators
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                       uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // D += A * B, m16n8k8, tf32 operands, fp32 accumulators
@@ -208,12 +184,6 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_
     asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                  " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}"
                  ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int acc)
-{
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                 " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}"
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void umma_commit(uint32_t mbar)
 {
@@ -254,6 +224,13 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&u)[8])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&u)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]));
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Bounded wait for an mbarrier phase; returns false if the wait gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
 {
@@ -265,11 +242,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
             return true;
     }
     return false;
-}
-
-__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t &r0, uint32_t &r1)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
@@ -321,7 +293,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;             // mma.sync fragment coordinates
-    const int mi = lane >> 3, lr = lane & 7;             // ldmatrix lane roles
     const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int H = p.H;
 
@@ -339,10 +310,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     float *bt = reinterpret_cast<float *>(smem + OFF_BT);
     float *Gc = reinterpret_cast<float *>(smem + OFF_GC);
     __nv_bfloat16 *rawb = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_RAW_B);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 16);
-    const uint32_t mbarA = smem_u32(smem + OFF_BAR), mbarB = smem_u32(smem + OFF_BAR + 8);
-    const uint32_t s_qt = smem_u32(smem + OFF_QT), s_kt = smem_u32(smem + OFF_KT), s_w = smem_u32(smem + OFF_W);
-    const uint32_t s_aq = smem_u32(smem + OFF_AQ), s_tp = smem_u32(smem + OFF_TP), s_vt = smem_u32(smem + OFF_VT);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 24);
+    const uint32_t mbarX = smem_u32(smem + OFF_BAR), mbarU = smem_u32(smem + OFF_BAR + 8);
+    const uint32_t mbarB = smem_u32(smem + OFF_BAR + 16);
+    const uint32_t s_qx = smem_u32(smem + OFF_QX), s_so = smem_u32(smem + OFF_SO), s_tp = smem_u32(smem + OFF_TP);
 
     // -------- tensor memory, barriers, constant-zero tile parts
     if (warp == 0) {
@@ -352,12 +323,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         tc_fence_before();
     }
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarA));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarX));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarU));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarB));
     }
-    // the Aqk and T' tiles are written lower-block-triangular only; their upper blocks stay zero
-    static_assert(OFF_TP == OFF_AQ + 4 * SQ_SBO && 8 * SQ_SBO == NTHREADS * 16, "zero fill");
-    reinterpret_cast<uint4 *>(smem + OFF_AQ)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    // Aqk (rows 128..159 of the [K~^T ; Aqk] tile) and T' are written block-lower-triangular
+    // only; their upper blocks stay zero.
+    for (int e = tid; e < 12 * SO_SBO / 16; e += NTHREADS)          // rows 64..159 of that tile
+        reinterpret_cast<uint4 *>(smem + OFF_SO + 8 * SO_SBO)[e] = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = tid; e < 4 * TP_SBO / 16; e += NTHREADS)
+        reinterpret_cast<uint4 *>(smem + OFF_TP)[e] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
@@ -518,11 +493,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
                 P0 *= al0[i];
                 P1 *= al1[i];
-                *reinterpret_cast<float2 *>(Lq + r * PF + c0) = make_float2(tf32r(q0 * P0), tf32r(q1 * P1));
-                *reinterpret_cast<float2 *>(Lk + r * PF + c0) = make_float2(tf32r(k0 * P0), tf32r(k1 * P1));
-                *reinterpret_cast<float2 *>(smem + OFF_QT + kmaj(r, c0, QT_LBO, QT_SBO)) =
-                    make_float2(tf32r(q0 * P0 * pre0), tf32r(q1 * P1 * pre1));
-                *reinterpret_cast<uint32_t *>(smem + OFF_KG + swz(r, c0)) = pack_half2(k0 * P0 * pre0, k1 * P1 * pre1);
+                const float qp0 = q0 * P0, qp1 = q1 * P1, kp0 = k0 * P0, kp1 = k1 * P1;
+                *reinterpret_cast<float2 *>(Lq + r * PF + c0) = make_float2(tf32r(qp0), tf32r(qp1));
+                *reinterpret_cast<float2 *>(Lk + r * PF + c0) = make_float2(tf32r(kp0), tf32r(kp1));
+                *reinterpret_cast<float2 *>(smem + OFF_QX + kmaj(r, c0, QX_LBO, QX_SBO)) =
+                    make_float2(tf32r(qp0 * pre0), tf32r(qp1 * pre1));
+                *reinterpret_cast<float2 *>(smem + OFF_QX + kmaj(CH + r, c0, QX_LBO, QX_SBO)) =
+                    make_float2(tf32r(kp0 * pre0), tf32r(kp1 * pre1));
             }
             float E0 = es0, E1 = es1;
             float kt0[4], kt1[4];
@@ -531,17 +508,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 const int r = sg * 4 + i;
                 const float kn = rk[r];
                 const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
-                *reinterpret_cast<float2 *>(Ed + r * PF + c0) = make_float2(tf32r(k0 * E0 * iD0), tf32r(k1 * E1 * iD1));
+                const float ke0 = k0 * E0, ke1 = k1 * E1;
+                *reinterpret_cast<float2 *>(Ed + r * PF + c0) = make_float2(tf32r(ke0 * iD0), tf32r(ke1 * iD1));
                 if (blk == 0)
-                    *reinterpret_cast<float2 *>(Ek + r * PF + c0) = make_float2(tf32r(k0 * E0), tf32r(k1 * E1));
-                kt0[i] = tf32r(k0 * E0 * post0);
-                kt1[i] = tf32r(k1 * E1 * post1);
+                    *reinterpret_cast<float2 *>(Ek + r * PF + c0) = make_float2(tf32r(ke0), tf32r(ke1));
+                kt0[i] = tf32r(ke0 * post0);
+                kt1[i] = tf32r(ke1 * post1);
                 E0 *= al0[i];
                 E1 *= al1[i];
             }
-            *reinterpret_cast<float4 *>(smem + OFF_KT + kmaj(c0, sg * 4, KT_LBO, KT_SBO)) =
+            *reinterpret_cast<float4 *>(smem + OFF_SO + kmaj(c0, sg * 4, SO_LBO, SO_SBO)) =
                 make_float4(kt0[0], kt0[1], kt0[2], kt0[3]);
-            *reinterpret_cast<float4 *>(smem + OFF_KT + kmaj(c0 + 1, sg * 4, KT_LBO, KT_SBO)) =
+            *reinterpret_cast<float4 *>(smem + OFF_SO + kmaj(c0 + 1, sg * 4, SO_LBO, SO_SBO)) =
                 make_float4(kt1[0], kt1[1], kt1[2], kt1[3]);
             if (sg == 0)
                 *reinterpret_cast<float2 *>(Gc + c0) = make_float2(D0 * Do0, D1 * Do1);
@@ -560,29 +538,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         if (has_next && tid < Ln)
             next_beta = p.beta[(ntok0 + tid) * H + h];
 
-        // ---- tensor cores: O^T = S^T Q~^T (runs while the threads build the remaining operands)
-        if (tid == 0) {
+        // ---- tensor cores: [O^T | X^T] = S^T [Q~ ; K^.Gamma]^T (overlaps the products and the inverse)
+        if (tid == MMA_TID) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < D / 8; ++s)
-                mma_tf32_ts(tbase + TM_O, tbase + TM_S + 8 * s, umma_desc(s_qt + s * 2 * QT_LBO, QT_LBO, QT_SBO),
-                            idesc_tf32(128, 32), s > 0);
+                mma_tf32_ts(tbase + TM_O, tbase + TM_S + 8 * s, umma_desc(s_qx + s * 2 * QX_LBO, QX_LBO, QX_SBO),
+                            idesc_tf32(128, 2 * CH), s > 0);
+            umma_commit(mbarX);
         }
 
         // ---- S2: Akk and Aqk on tf32 mma.sync; items (pair, kind, n-tile) on warps 0..11
-        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc2b[4] = {0.f, 0.f, 0.f, 0.f};
         const int pair = warp >> 2, qk = (warp >> 1) & 1, ntl = warp & 1;
         const int rb1 = pair == 0 ? 0 : 16, cb0 = pair == 2 ? 16 : 0;
         if (warp < 12) {
             const float *X = reinterpret_cast<const float *>(smem + (qk ? OFF_LQ : OFF_LK)) + (rb1 + gq) * PF + tq;
             const float *Y = reinterpret_cast<const float *>(smem + (pair == 1 ? OFF_EK : OFF_ED)) +
                              (cb0 + ntl * 8 + gq) * PF + tq;
-#pragma unroll 8
-            for (int ks = 0; ks < D / 8; ++ks) {
-                const int k0 = ks * 8;
+#pragma unroll 4
+            for (int ks = 0; ks < D / 8; ks += 2) {
+                const int k0 = ks * 8, k1 = k0 + 8;
                 mma_tf32(acc2, __float_as_uint(X[k0]), __float_as_uint(X[8 * PF + k0]), __float_as_uint(X[k0 + 4]),
                          __float_as_uint(X[8 * PF + k0 + 4]), __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
+                mma_tf32(acc2b, __float_as_uint(X[k1]), __float_as_uint(X[8 * PF + k1]), __float_as_uint(X[k1 + 4]),
+                         __float_as_uint(X[8 * PF + k1 + 4]), __float_as_uint(Y[k1]), __float_as_uint(Y[k1 + 4]));
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc2[e] += acc2b[e];
         }
         __syncthreads();   // the intra operands are dead; the region is reused below
         if (warp < 12) {
@@ -592,7 +576,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 const int i = rb1 + gq + 8 * hh, j = cb0 + ntl * 8 + 2 * tq;
                 const float x0 = acc2[2 * hh], x1 = acc2[2 * hh + 1];
                 if (qk) {
-                    *reinterpret_cast<float2 *>(smem + OFF_AQ + kmaj(i, j, SQ_LBO, SQ_SBO)) =
+                    *reinterpret_cast<float2 *>(smem + OFF_SO + kmaj(D + i, j, SO_LBO, SO_SBO)) =
                         make_float2(tf32r(j <= i ? x0 : 0.f), tf32r(j + 1 <= i ? x1 : 0.f));
                 } else {
                     const float bi = bt[i];
@@ -603,29 +587,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         }
         __syncthreads();
 
-        // ---- S3: Tm = (I + Akk)^-1 (fp32); T' = Tm diag(b) as fp16 (for -W) and as a tf32 tile
+        // ---- S3: Tm = (I + Akk)^-1 (fp32) and the tf32 tile of T' = Tm diag(b)
         float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
         float *Tmd = reinterpret_cast<float *>(smem + OFF_TMD);
-        __half *Tph = reinterpret_cast<__half *>(smem + OFF_TPH);
         if (warp < 2 && lane < 16) {
-            // diagonal 16x16 blocks by forward substitution; lane = column
+            // diagonal 16x16 blocks, column j per lane, right-looking forward substitution
             const int b = warp, j = lane;
-            float x[SB];
+            float x[SB], acc[SB];
 #pragma unroll
-            for (int i = 0; i < SB; ++i) {
-                float s = 0.f;
+            for (int i = 0; i < SB; ++i)
+                acc[i] = 0.f;
 #pragma unroll
-                for (int l = 0; l < i; ++l)
-                    s = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], s);
-                x[i] = i == j ? 1.f : (i < j ? 0.f : -s);
+            for (int l = 0; l < SB; ++l) {
+                x[l] = l == j ? 1.f : (l < j ? 0.f : -acc[l]);
+#pragma unroll
+                for (int i = l + 1; i < SB; ++i)
+                    acc[i] = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], acc[i]);
             }
             const float bj = bt[b * SB + j];
 #pragma unroll
             for (int i = 0; i < SB; ++i) {
                 const int r = b * SB + i, c = b * SB + j;
                 Tmd[r * PA + c] = x[i];
-                Tph[r * PS + c] = __float2half_rn(x[i] * bj);
-                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(r, c, SQ_LBO, SQ_SBO)) = tf32r(x[i] * bj);
+                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(r, c, TP_LBO, TP_SBO)) = tf32r(x[i] * bj);
             }
         }
         __syncthreads();
@@ -634,77 +618,57 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             const int i = (tid >> 4) & 15, j = tid & 15;
             float *Mt = reinterpret_cast<float *>(smem + OFF_MT);
             if (tid < 256) {
-                float s = 0.f;
+                float s = 0.f, s2 = 0.f;
 #pragma unroll
-                for (int l = 0; l < SB; ++l)
+                for (int l = 0; l < SB; l += 2) {
                     s = fmaf(Akk[(SB + i) * PA + l], Tmd[l * PA + j], s);
-                Mt[i * 16 + j] = s;
+                    s2 = fmaf(Akk[(SB + i) * PA + l + 1], Tmd[(l + 1) * PA + j], s2);
+                }
+                Mt[i * 16 + j] = s + s2;
             }
             __syncthreads();
             if (tid < 256) {
-                float s = 0.f;
+                float s = 0.f, s2 = 0.f;
 #pragma unroll
-                for (int l = 0; l < SB; ++l)
+                for (int l = 0; l < SB; l += 2) {
                     s = fmaf(Tmd[(SB + i) * PA + SB + l], Mt[l * 16 + j], s);
-                const float tv = -s * bt[j];
-                Tph[(SB + i) * PS + j] = __float2half_rn(tv);
-                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(SB + i, j, SQ_LBO, SQ_SBO)) = tf32r(tv);
-            }
-        }
-        __syncthreads();
-
-        // ---- S4: -W = -T' (K^ . Gamma) on mma.sync; warp: key columns 8w..8w+7
-        {
-            const uint32_t tph = smem_u32(smem + OFF_TPH), kg = smem_u32(smem + OFF_KG);
-#pragma unroll
-            for (int rb = 0; rb < 2; ++rb) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks <= rb; ++ks) {
-                    uint32_t a0, a1, a2, a3, b0, b1;
-                    ldsm_x4(tph + ((rb * 16 + lr + (mi & 1) * 8) * PS + ks * 16 + (mi >> 1) * 8) * 2, a0, a1, a2, a3);
-                    ldsm_x2_t(kg + swz(ks * 16 + (lane & 15), warp * 8), b0, b1);
-                    mma_f16(acc, a0, a1, a2, a3, b0, b1);
+                    s2 = fmaf(Tmd[(SB + i) * PA + SB + l + 1], Mt[(l + 1) * 16 + j], s2);
                 }
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = rb * 16 + gq + 8 * hh, kc = warp * 8 + 2 * tq;
-                    *reinterpret_cast<float2 *>(smem + OFF_W + kmaj(t, kc, W_LBO, W_SBO)) =
-                        make_float2(tf32r(-acc[2 * hh]), tf32r(-acc[2 * hh + 1]));
-                }
+                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(SB + i, j, TP_LBO, TP_SBO)) = tf32r(-(s + s2) * bt[j]);
             }
-        }
-        cp_async_wait<1>();   // v of this chunk (the next chunk's q, k, g may stay in flight)
-        __syncthreads();
-        // ---- V^T as a tf32 tile (A operand): thread task (value row v, token quad)
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int e = tid + m * NTHREADS, vv = e & 127, qd = e >> 7;
-            const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_V);
-            float4 f;
-            f.x = tf32r(__bfloat162float(rv[(4 * qd + 0) * PH + vv]));
-            f.y = tf32r(__bfloat162float(rv[(4 * qd + 1) * PH + vv]));
-            f.z = tf32r(__bfloat162float(rv[(4 * qd + 2) * PH + vv]));
-            f.w = tf32r(__bfloat162float(rv[(4 * qd + 3) * PH + vv]));
-            *reinterpret_cast<float4 *>(smem + OFF_VT + kmaj(vv, 4 * qd, SQ_LBO, SQ_SBO)) = f;
         }
         fence_async_smem();
+        cp_async_wait<1>();   // v of this chunk (the next chunk's q, k, g may stay in flight)
         __syncthreads();
 
-        // ---- tensor cores: U^T = V^T T'^T + S^T (-W)^T
-        if (tid == 0) {
+        // ---- Y^T = V^T - X^T into tensor memory: this thread's value row, tokens 8cg..8cg+7
+        hung = !mbar_wait(mbarX, parity);
+        if (__syncthreads_or(hung)) {
+            hung = true;
+            break;
+        }
+        tc_fence_after();
+        {
+            uint32_t xv[8];
+            tmem_ld8(trow + TM_X + cg * 8, xv);
+            const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_V);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                xv[jj] = __float_as_uint(__bfloat162float(rv[(cg * 8 + jj) * PH + vrow]) - __uint_as_float(xv[jj]));
+            tmem_st8(trow + TM_Y + cg * 8, xv);
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- tensor cores: U^T = Y^T T'^T
+        if (tid == MMA_TID) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < CH / 8; ++s)
-                mma_tf32_ss(tbase + TM_U, umma_desc(s_vt + s * 2 * SQ_LBO, SQ_LBO, SQ_SBO),
-                            umma_desc(s_tp + s * 2 * SQ_LBO, SQ_LBO, SQ_SBO), idesc_tf32(128, 32), s > 0);
-#pragma unroll
-            for (int s = 0; s < D / 8; ++s)
-                mma_tf32_ts(tbase + TM_U, tbase + TM_S + 8 * s, umma_desc(s_w + s * 2 * W_LBO, W_LBO, W_SBO),
-                            idesc_tf32(128, 32), 1);
-            umma_commit(mbarA);
+                mma_tf32_ts(tbase + TM_U, tbase + TM_Y + 8 * s, umma_desc(s_tp + s * 2 * TP_LBO, TP_LBO, TP_SBO),
+                            idesc_tf32(128, CH), s > 0);
+            umma_commit(mbarU);
         }
-        hung = !mbar_wait(mbarA, parity);
+        hung = !mbar_wait(mbarU, parity);
         if (__syncthreads_or(hung)) {
             hung = true;
             break;
@@ -727,17 +691,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         }
         tc_fence_before();
         __syncthreads();
-        // ---- tensor cores: O^T += U^T Aqk^T;  S^T += U^T K~
-        if (tid == 0) {
+        // ---- tensor cores: [S^T | O^T] += U^T [K~^T ; Aqk]^T
+        if (tid == MMA_TID) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < CH / 8; ++s)
-                mma_tf32_ts(tbase + TM_O, tbase + TM_U + 8 * s, umma_desc(s_aq + s * 2 * SQ_LBO, SQ_LBO, SQ_SBO),
-                            idesc_tf32(128, 32), 1);
-#pragma unroll
-            for (int s = 0; s < CH / 8; ++s)
-                mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_kt + s * 2 * KT_LBO, KT_LBO, KT_SBO),
-                            idesc_tf32(128, 128), 1);
+                mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_so + s * 2 * SO_LBO, SO_LBO, SO_SBO),
+                            idesc_tf32(128, D + CH), 1);
             umma_commit(mbarB);
         }
         hung = !mbar_wait(mbarB, parity);
@@ -752,8 +712,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             tmem_ld8(trow + TM_O + cg * 8, o);
             __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                Ost[(cg * 8 + j) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[j]) * p.scale);
+            for (int jj = 0; jj < 8; ++jj)
+                Ost[(cg * 8 + jj) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
         }
         tc_fence_before();
         __syncthreads();
@@ -777,7 +737,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     // -------- final state, tensor memory release
     if (hung) {
         // give any tensor-core work still in flight a bounded chance to finish before releasing
-        mbar_wait(mbarA, 0);
+        mbar_wait(mbarX, 0);
+        mbar_wait(mbarU, 0);
         mbar_wait(mbarB, 0);
         if (tid == 0)
             atomicOr(&g_kda_device_error, 1u);
