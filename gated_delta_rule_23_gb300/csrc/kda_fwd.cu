@@ -68,7 +68,7 @@ constexpr uint32_t WAIT_LIMIT = 1u << 24;        // try_wait polls before a wait
 // their 16-byte chunks by (row >> 3) & 3, which makes the gate pass (lanes spread over
 // eight 4-row segments) and ldmatrix free of bank conflicts.
 constexpr int PH = 136;
-constexpr int PF = 132;                          // fp32 pitch of 128-wide tf32 mma.sync operands
+constexpr int PF = 134;                          // fp32 pitch of 128-wide tf32 mma.sync operands
 constexpr int PA = 36;                           // fp32 pitch of 32-wide matrices
 constexpr int HT = CH * PH * 2;                  // 8704 B
 // tcgen05 operand tiles: element (row r, k) of a K-major tile sits at
@@ -83,27 +83,27 @@ constexpr int OFF_RAW_G = OFF_RAW_K + HT;
 constexpr int OFF_RAW_V = OFF_RAW_G + HT;
 constexpr int OFF_RAW_B = OFF_RAW_V + HT;        // beta logits, 32 bf16 (128 B reserved)
 constexpr int OFF_INTRA = OFF_RAW_B + 128;
-constexpr int F32T = CH * PF * 4;                // 16896 B
-constexpr int OFF_LQ = OFF_INTRA;                // fp32 [32][132]  q^ P          (tf32-rounded)
-constexpr int OFF_LK = OFF_LQ + F32T;            // fp32 [32][132]  k^ P
-constexpr int OFF_ED = OFF_LK + F32T;            // fp32 [32][132]  k^ E / D_b
-constexpr int OFF_EK = OFF_ED + F32T;            // fp32 [16][132]  k^ E  (sub-block 0 only)
-constexpr int INTRA_BYTES = 3 * F32T + F32T / 2;
+constexpr int F32H = SB * PF * 4;                // 8576 B: 16 rows of 128 fp32
+constexpr int OFF_LQ = OFF_INTRA;                // fp32 [16][134]  q^ P, rows 16..31 (sub-block 1)
+constexpr int OFF_LK = OFF_LQ + F32H;            // fp32 [16][134]  k^ P, rows 16..31
+constexpr int OFF_ED = OFF_LK + F32H;            // fp32 [32][134]  k^ E / D_b
+constexpr int INTRA_BYTES = 4 * F32H;
 // after the Akk / Aqk products the same region holds:
 constexpr int OFF_AKK = OFF_INTRA;               // fp32 [32][36]
 constexpr int OFF_TMD = OFF_AKK + CH * PA * 4;   // fp32 [32][36]  diagonal blocks of Tm
 constexpr int OFF_MT = OFF_TMD + CH * PA * 4;    // fp32 [16][16]  inverse scratch
-constexpr int OFF_OST = OFF_MT + 16 * 16 * 4;    // bf16 [32][136] output staging
-constexpr int INTRA_END = OFF_OST + HT;
+constexpr int INTRA_END = OFF_MT + 16 * 16 * 4;
 constexpr int OFF_QX = OFF_INTRA + INTRA_BYTES;  // tcgen05 B tiles from here on
-constexpr int OFF_SO = OFF_QX + 8 * QX_SBO;
-constexpr int OFF_TP = OFF_SO + 20 * SO_SBO;
-constexpr int OFF_MISC = OFF_TP + 4 * TP_SBO;
+constexpr int SO_BYTES = 20 * SO_SBO;
+constexpr int OFF_SO = OFF_QX + 8 * QX_SBO;      // two buffers: the update of chunk c reads one while
+constexpr int OFF_TP = OFF_SO + 2 * SO_BYTES;    // the gate pass of chunk c+1 writes the other
+constexpr int OFF_OST = OFF_TP + 4 * TP_SBO;     // bf16 [32][136] output staging
+constexpr int OFF_MISC = OFF_OST + HT;
 constexpr int OFF_RQ = OFF_MISC;                 // fp32 [32] 1/|q|
 constexpr int OFF_RK = OFF_RQ + 128;             // fp32 [32] 1/|k|
 constexpr int OFF_BT = OFF_RK + 128;             // fp32 [32] b = sigmoid(beta), 0 past the end
 constexpr int OFF_GC = OFF_BT + 128;             // fp32 [128] chunk decay Gamma_31
-constexpr int OFF_BAR = OFF_GC + D * 4;          // 3 mbarriers + tensor-memory base address
+constexpr int OFF_BAR = OFF_GC + D * 4;          // 3 mbarriers, tensor-memory base address, hang flag
 constexpr int SMEM_BYTES = OFF_BAR + 32;
 static_assert(INTRA_END <= OFF_QX, "post-product overlay exceeds the intra region");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     float *Gc = reinterpret_cast<float *>(smem + OFF_GC);
     __nv_bfloat16 *rawb = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_RAW_B);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + 24);
+    volatile uint32_t *hang_flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_BAR + 28);
     const uint32_t mbarX = smem_u32(smem + OFF_BAR), mbarU = smem_u32(smem + OFF_BAR + 8);
     const uint32_t mbarB = smem_u32(smem + OFF_BAR + 16);
     const uint32_t s_qx = smem_u32(smem + OFF_QX), s_so = smem_u32(smem + OFF_SO), s_tp = smem_u32(smem + OFF_TP);
@@ -326,11 +327,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarX));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarU));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbarB));
+        *hang_flag = 0u;
     }
-    // Aqk (rows 128..159 of the [K~^T ; Aqk] tile) and T' are written block-lower-triangular
+    // Aqk (rows 128..159 of both [K~^T ; Aqk] tiles) and T' are written block-lower-triangular
     // only; their upper blocks stay zero.
-    for (int e = tid; e < 12 * SO_SBO / 16; e += NTHREADS)          // rows 64..159 of that tile
-        reinterpret_cast<uint4 *>(smem + OFF_SO + 8 * SO_SBO)[e] = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = tid; e < 2 * 4 * SO_SBO / 16; e += NTHREADS) {
+        const int b = e / (4 * SO_SBO / 16), o = e % (4 * SO_SBO / 16);
+        reinterpret_cast<uint4 *>(smem + OFF_SO + b * SO_BYTES + 16 * SO_SBO)[o] = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int e = tid; e < 4 * TP_SBO / 16; e += NTHREADS)
         reinterpret_cast<uint4 *>(smem + OFF_TP)[e] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
@@ -397,6 +401,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             rawb[tid] = tid < L0 ? p.beta[(bos + tid) * H + h] : __float2bfloat16(0.f);
     }
 
+    // Read O^T of the previous chunk (its final update may still be running) into the staging tile.
+    auto read_out_previous = [&](uint32_t prev_parity) -> bool {
+        const bool ok = mbar_wait(mbarB, prev_parity) && *hang_flag == 0u;
+        if (__syncthreads_or(!ok))
+            return false;
+        tc_fence_after();
+        uint32_t o[8];
+        tmem_ld8(trow + TM_O + cg * 8, o);
+        __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            Ost[(cg * 8 + jj) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
+        tc_fence_before();
+        return true;
+    };
+    auto store_previous = [&](int64_t ptok0, int pL) {
+        const int r = tid >> 4, c16 = tid & 15;
+        if (r < pL)
+            *reinterpret_cast<uint4 *>(p.out + ((ptok0 + r) * H + h) * D + c16 * 8) =
+                *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
+    };
+
+    int64_t prev_tok0 = 0;
+    int prev_L = 0;
     for (int ci = 0; ci < nchunks; ++ci) {
         const int64_t tok0 = bos + (int64_t)ci * CH;
         const int64_t rem = len - (int64_t)ci * CH;
@@ -405,6 +433,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         const int64_t ntok0 = tok0 + CH;
         const int Ln = has_next ? (int)((rem - CH) < CH ? (rem - CH) : CH) : 0;
         const uint32_t parity = ci & 1;
+        const int sob = ci & 1;                                 // [K~^T ; Aqk] buffer of this chunk
+        unsigned char *so = smem + OFF_SO + sob * SO_BYTES;
 
         cp_async_wait<1>();   // q, k, g of this chunk have landed (v may still be in flight)
         __syncthreads();
@@ -435,12 +465,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             if (tid < CH)
                 bt[tid] = tid < L ? sigmoidf_fast(__bfloat162float(rawb[tid])) : 0.f;
         }
+        // ---- the previous chunk's output: wait for its last update, read O^T out of tensor memory
+        if (ci > 0) {
+            if (!read_out_previous((ci - 1) & 1)) {
+                hung = true;
+                break;
+            }
+        }
         __syncthreads();
 
         // ---- S1b: gate, sub-block decay products and every operand of this chunk (one pass)
         {
             uint32_t gqv[4], gkv[4];
-            float al0[4], al1[4];
+            float al0[4], al1[4], qn[4], kn[4];
             float tot0 = 1.f, tot1 = 1.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -448,6 +485,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 const uint32_t gg = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_G + swz(r, c0));
                 gqv[i] = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_Q + swz(r, c0));
                 gkv[i] = *reinterpret_cast<const uint32_t *>(smem + OFF_RAW_K + swz(r, c0));
+                qn[i] = rq[r];
+                kn[i] = rk[r];
                 const float z0 = eA * (bf16_lo(gg) + dtb.x), z1 = eA * (bf16_hi(gg) + dtb.y);
                 const bool live = r < L;
                 al0[i] = live ? ex2_approx(p.lb_log2e * sigmoidf_fast(z0)) : 1.f;
@@ -483,51 +522,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             float *Lq = reinterpret_cast<float *>(smem + OFF_LQ);
             float *Lk = reinterpret_cast<float *>(smem + OFF_LK);
             float *Ed = reinterpret_cast<float *>(smem + OFF_ED);
-            float *Ek = reinterpret_cast<float *>(smem + OFF_EK);
             float P0 = ex0, P1 = ex1;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = sg * 4 + i;
-                const float qn = rq[r], kn = rk[r];
-                const float q0 = bf16_lo(gqv[i]) * qn, q1 = bf16_hi(gqv[i]) * qn;
-                const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
+                const float q0 = bf16_lo(gqv[i]) * qn[i], q1 = bf16_hi(gqv[i]) * qn[i];
+                const float k0 = bf16_lo(gkv[i]) * kn[i], k1 = bf16_hi(gkv[i]) * kn[i];
                 P0 *= al0[i];
                 P1 *= al1[i];
                 const float qp0 = q0 * P0, qp1 = q1 * P1, kp0 = k0 * P0, kp1 = k1 * P1;
-                *reinterpret_cast<float2 *>(Lq + r * PF + c0) = make_float2(tf32r(qp0), tf32r(qp1));
-                *reinterpret_cast<float2 *>(Lk + r * PF + c0) = make_float2(tf32r(kp0), tf32r(kp1));
+                // chunk-start reference: Q~ = q^ Gamma and K^.Gamma (also the sub-block-0 product operands)
                 *reinterpret_cast<float2 *>(smem + OFF_QX + kmaj(r, c0, QX_LBO, QX_SBO)) =
                     make_float2(tf32r(qp0 * pre0), tf32r(qp1 * pre1));
                 *reinterpret_cast<float2 *>(smem + OFF_QX + kmaj(CH + r, c0, QX_LBO, QX_SBO)) =
                     make_float2(tf32r(kp0 * pre0), tf32r(kp1 * pre1));
+                if (blk) {   // sub-block-1 reference for the (1,1) products
+                    *reinterpret_cast<float2 *>(Lq + (r - SB) * PF + c0) = make_float2(tf32r(qp0), tf32r(qp1));
+                    *reinterpret_cast<float2 *>(Lk + (r - SB) * PF + c0) = make_float2(tf32r(kp0), tf32r(kp1));
+                }
             }
             float E0 = es0, E1 = es1;
             float kt0[4], kt1[4];
 #pragma unroll
             for (int i = 3; i >= 0; --i) {
                 const int r = sg * 4 + i;
-                const float kn = rk[r];
-                const float k0 = bf16_lo(gkv[i]) * kn, k1 = bf16_hi(gkv[i]) * kn;
-                const float ke0 = k0 * E0, ke1 = k1 * E1;
+                const float ke0 = bf16_lo(gkv[i]) * kn[i] * E0, ke1 = bf16_hi(gkv[i]) * kn[i] * E1;
                 *reinterpret_cast<float2 *>(Ed + r * PF + c0) = make_float2(tf32r(ke0 * iD0), tf32r(ke1 * iD1));
-                if (blk == 0)
-                    *reinterpret_cast<float2 *>(Ek + r * PF + c0) = make_float2(tf32r(ke0), tf32r(ke1));
                 kt0[i] = tf32r(ke0 * post0);
                 kt1[i] = tf32r(ke1 * post1);
                 E0 *= al0[i];
                 E1 *= al1[i];
             }
-            *reinterpret_cast<float4 *>(smem + OFF_SO + kmaj(c0, sg * 4, SO_LBO, SO_SBO)) =
-                make_float4(kt0[0], kt0[1], kt0[2], kt0[3]);
-            *reinterpret_cast<float4 *>(smem + OFF_SO + kmaj(c0 + 1, sg * 4, SO_LBO, SO_SBO)) =
-                make_float4(kt1[0], kt1[1], kt1[2], kt1[3]);
+            *reinterpret_cast<float4 *>(so + kmaj(c0, sg * 4, SO_LBO, SO_SBO)) = make_float4(kt0[0], kt0[1], kt0[2], kt0[3]);
+            *reinterpret_cast<float4 *>(so + kmaj(c0 + 1, sg * 4, SO_LBO, SO_SBO)) = make_float4(kt1[0], kt1[1], kt1[2], kt1[3]);
             if (sg == 0)
                 *reinterpret_cast<float2 *>(Gc + c0) = make_float2(D0 * Do0, D1 * Do1);
         }
         fence_async_smem();
         __syncthreads();
 
-        // ---- raw q, k, g, beta are consumed: start staging the next chunk's
+        // ---- the previous chunk's output to HBM; raw q, k, g, beta are consumed: stage the next chunk's
+        if (ci > 0)
+            store_previous(prev_tok0, prev_L);
         if (has_next) {
             load_tile_async<true>(smem, OFF_RAW_Q, p.q, ntok0, Ln, H, h);
             load_tile_async<true>(smem, OFF_RAW_K, p.k, ntok0, Ln, H, h);
@@ -548,21 +584,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             umma_commit(mbarX);
         }
 
-        // ---- S2: Akk and Aqk on tf32 mma.sync; items (pair, kind, n-tile) on warps 0..11
+        // ---- S2: Akk and Aqk on tf32 mma.sync; items (pair, kind, n-tile) on warps 0..11.
+        // pair 0 = (0,0), 1 = (1,0): left factor from the chunk-start tile, right factor k^ E / D_0;
+        // pair 2 = (1,1): left factor q^ P / k^ P of sub-block 1, right factor k^ E / D_1.
         float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc2b[4] = {0.f, 0.f, 0.f, 0.f};
         const int pair = warp >> 2, qk = (warp >> 1) & 1, ntl = warp & 1;
         const int rb1 = pair == 0 ? 0 : 16, cb0 = pair == 2 ? 16 : 0;
         if (warp < 12) {
-            const float *X = reinterpret_cast<const float *>(smem + (qk ? OFF_LQ : OFF_LK)) + (rb1 + gq) * PF + tq;
-            const float *Y = reinterpret_cast<const float *>(smem + (pair == 1 ? OFF_EK : OFF_ED)) +
-                             (cb0 + ntl * 8 + gq) * PF + tq;
+            const float *Y = reinterpret_cast<const float *>(smem + OFF_ED) + (cb0 + ntl * 8 + gq) * PF + tq;
+            if (pair < 2) {
+                const unsigned char *X = smem + OFF_QX + kmaj((qk ? 0 : CH) + rb1 + gq, tq, QX_LBO, QX_SBO);
 #pragma unroll 4
-            for (int ks = 0; ks < D / 8; ks += 2) {
-                const int k0 = ks * 8, k1 = k0 + 8;
-                mma_tf32(acc2, __float_as_uint(X[k0]), __float_as_uint(X[8 * PF + k0]), __float_as_uint(X[k0 + 4]),
-                         __float_as_uint(X[8 * PF + k0 + 4]), __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
-                mma_tf32(acc2b, __float_as_uint(X[k1]), __float_as_uint(X[8 * PF + k1]), __float_as_uint(X[k1 + 4]),
-                         __float_as_uint(X[8 * PF + k1 + 4]), __float_as_uint(Y[k1]), __float_as_uint(Y[k1 + 4]));
+                for (int ks = 0; ks < D / 8; ks += 2) {
+                    const unsigned char *x0 = X + ks * 2 * QX_LBO, *x1 = x0 + 2 * QX_LBO;
+                    const int k0 = ks * 8, k1 = k0 + 8;
+                    mma_tf32(acc2, *reinterpret_cast<const uint32_t *>(x0), *reinterpret_cast<const uint32_t *>(x0 + QX_SBO),
+                             *reinterpret_cast<const uint32_t *>(x0 + QX_LBO),
+                             *reinterpret_cast<const uint32_t *>(x0 + QX_SBO + QX_LBO),
+                             __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
+                    mma_tf32(acc2b, *reinterpret_cast<const uint32_t *>(x1), *reinterpret_cast<const uint32_t *>(x1 + QX_SBO),
+                             *reinterpret_cast<const uint32_t *>(x1 + QX_LBO),
+                             *reinterpret_cast<const uint32_t *>(x1 + QX_SBO + QX_LBO),
+                             __float_as_uint(Y[k1]), __float_as_uint(Y[k1 + 4]));
+                }
+            } else {
+                const float *X = reinterpret_cast<const float *>(smem + (qk ? OFF_LQ : OFF_LK)) + gq * PF + tq;
+#pragma unroll 4
+                for (int ks = 0; ks < D / 8; ks += 2) {
+                    const int k0 = ks * 8, k1 = k0 + 8;
+                    mma_tf32(acc2, __float_as_uint(X[k0]), __float_as_uint(X[8 * PF + k0]), __float_as_uint(X[k0 + 4]),
+                             __float_as_uint(X[8 * PF + k0 + 4]), __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
+                    mma_tf32(acc2b, __float_as_uint(X[k1]), __float_as_uint(X[8 * PF + k1]), __float_as_uint(X[k1 + 4]),
+                             __float_as_uint(X[8 * PF + k1 + 4]), __float_as_uint(Y[k1]), __float_as_uint(Y[k1 + 4]));
+                }
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -576,7 +630,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 const int i = rb1 + gq + 8 * hh, j = cb0 + ntl * 8 + 2 * tq;
                 const float x0 = acc2[2 * hh], x1 = acc2[2 * hh + 1];
                 if (qk) {
-                    *reinterpret_cast<float2 *>(smem + OFF_SO + kmaj(D + i, j, SO_LBO, SO_SBO)) =
+                    *reinterpret_cast<float2 *>(so + kmaj(D + i, j, SO_LBO, SO_SBO)) =
                         make_float2(tf32r(j <= i ? x0 : 0.f), tf32r(j + 1 <= i ? x1 : 0.f));
                 } else {
                     const float bi = bt[i];
@@ -641,7 +695,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         cp_async_wait<1>();   // v of this chunk (the next chunk's q, k, g may stay in flight)
         __syncthreads();
 
-        // ---- Y^T = V^T - X^T into tensor memory: this thread's value row, tokens 8cg..8cg+7
+        // ---- Y^T = V^T - X^T into tensor memory, and S^T <- S^T Diag(Gamma_31)
         hung = !mbar_wait(mbarX, parity);
         if (__syncthreads_or(hung)) {
             hung = true;
@@ -656,26 +710,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             for (int jj = 0; jj < 8; ++jj)
                 xv[jj] = __float_as_uint(__bfloat162float(rv[(cg * 8 + jj) * PH + vrow]) - __uint_as_float(xv[jj]));
             tmem_st8(trow + TM_Y + cg * 8, xv);
-        }
-        tc_fence_before();
-        __syncthreads();
-        // ---- tensor cores: U^T = Y^T T'^T
-        if (tid == MMA_TID) {
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < CH / 8; ++s)
-                mma_tf32_ts(tbase + TM_U, tbase + TM_Y + 8 * s, umma_desc(s_tp + s * 2 * TP_LBO, TP_LBO, TP_SBO),
-                            idesc_tf32(128, CH), s > 0);
-            umma_commit(mbarU);
-        }
-        hung = !mbar_wait(mbarU, parity);
-        if (__syncthreads_or(hung)) {
-            hung = true;
-            break;
-        }
-        tc_fence_after();
-        // ---- S^T <- S^T Diag(Gamma_31): this thread's row, columns 32cg..32cg+31
-        {
             uint32_t u[32];
             tmem_ld32(trow + TM_S + cg * 32, u);
             const float4 *g4 = reinterpret_cast<const float4 *>(Gc + cg * 32);
@@ -691,48 +725,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         }
         tc_fence_before();
         __syncthreads();
-        // ---- tensor cores: [S^T | O^T] += U^T [K~^T ; Aqk]^T
+        // ---- tensor cores: U^T = Y^T T'^T, then [S^T | O^T] += U^T [K~^T ; Aqk]^T (completes while the
+        //      next chunk's gate pass runs; its output is read out there)
         if (tid == MMA_TID) {
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < CH / 8; ++s)
-                mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_so + s * 2 * SO_LBO, SO_LBO, SO_SBO),
-                            idesc_tf32(128, D + CH), 1);
-            umma_commit(mbarB);
-        }
-        hung = !mbar_wait(mbarB, parity);
-        if (__syncthreads_or(hung)) {
-            hung = true;
-            break;
-        }
-        tc_fence_after();
-        // ---- O^T * scale -> bf16 staging tile [t][v]: this thread's row, tokens 8cg..8cg+7
-        {
-            uint32_t o[8];
-            tmem_ld8(trow + TM_O + cg * 8, o);
-            __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
+                mma_tf32_ts(tbase + TM_U, tbase + TM_Y + 8 * s, umma_desc(s_tp + s * 2 * TP_LBO, TP_LBO, TP_SBO),
+                            idesc_tf32(128, CH), s > 0);
+            umma_commit(mbarU);
+            if (mbar_wait(mbarU, parity)) {
+                tc_fence_after();
+                const uint32_t s_sob = s_so + sob * SO_BYTES;
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                Ost[(cg * 8 + jj) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
+                for (int s = 0; s < CH / 8; ++s)
+                    mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_sob + s * 2 * SO_LBO, SO_LBO, SO_SBO),
+                                idesc_tf32(128, D + CH), 1);
+                umma_commit(mbarB);
+            } else {
+                *hang_flag = 1u;
+            }
         }
-        tc_fence_before();
-        __syncthreads();
 
-        // ---- write this chunk's outputs; stage the next chunk's v and beta
-        {
-            const int r = tid >> 4, c16 = tid & 15;
-            if (r < L)
-                *reinterpret_cast<uint4 *>(p.out + ((tok0 + r) * H + h) * D + c16 * 8) =
-                    *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
-        }
+        // ---- stage the next chunk's v and beta
         if (has_next)
             load_tile_async<false>(smem, OFF_RAW_V, p.v, ntok0, Ln, H, h);
         cp_async_commit();
         if (tid < CH)
             rawb[tid] = next_beta;
+        prev_tok0 = tok0;
+        prev_L = L;
     }
     cp_async_wait<0>();
     __syncthreads();
+    // the last chunk's output
+    if (!hung && nchunks > 0) {
+        if (read_out_previous((nchunks - 1) & 1)) {
+            __syncthreads();
+            store_previous(prev_tok0, prev_L);
+        } else {
+            hung = true;
+        }
+    }
 
     // -------- final state, tensor memory release
     if (hung) {
