@@ -97,8 +97,8 @@ constexpr int OFF_QX = OFF_INTRA + INTRA_BYTES;  // tcgen05 B tiles from here on
 constexpr int SO_BYTES = 20 * SO_SBO;
 constexpr int OFF_SO = OFF_QX + 8 * QX_SBO;      // two buffers: the update of chunk c reads one while
 constexpr int OFF_TP = OFF_SO + 2 * SO_BYTES;    // the gate pass of chunk c+1 writes the other
-constexpr int OFF_OST = OFF_TP + 4 * TP_SBO;     // bf16 [32][136] output staging
-constexpr int OFF_MISC = OFF_OST + HT;
+constexpr int OFF_RED = OFF_TP + 4 * TP_SBO;     // fp32 [3 pairs][2 kinds][32 lanes][8] K-half partials
+constexpr int OFF_MISC = OFF_RED + 3 * 2 * 32 * 8 * 4;
 constexpr int OFF_RQ = OFF_MISC;                 // fp32 [32] 1/|q|
 constexpr int OFF_RK = OFF_RQ + 128;             // fp32 [32] 1/|k|
 constexpr int OFF_BT = OFF_RK + 128;             // fp32 [32] b = sigmoid(beta), 0 past the end
@@ -108,7 +108,7 @@ constexpr int SMEM_BYTES = OFF_BAR + 32;
 static_assert(INTRA_END <= OFF_QX, "post-product overlay exceeds the intra region");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(OFF_INTRA % 128 == 0 && OFF_QX % 16 == 0 && OFF_SO % 16 == 0 && OFF_TP % 16 == 0 &&
-              OFF_MISC % 16 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+              OFF_MISC % 16 == 0 && OFF_RED % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
 // byte offset of element (row, col) in a swizzled [32][136] half tile
 __host__ __device__ constexpr int swz(int row, int col)
@@ -401,26 +401,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             rawb[tid] = tid < L0 ? p.beta[(bos + tid) * H + h] : __float2bfloat16(0.f);
     }
 
-    // Read O^T of the previous chunk (its final update may still be running) into the staging tile.
-    auto read_out_previous = [&](uint32_t prev_parity) -> bool {
+    // Output of the previous chunk: wait for its last update, then each thread writes its value
+    // row for tokens 8cg..8cg+7 straight from tensor memory (a warp stores 64 contiguous bytes).
+    auto write_out_previous = [&](uint32_t prev_parity, int64_t ptok0, int pL) -> bool {
         const bool ok = mbar_wait(mbarB, prev_parity) && *hang_flag == 0u;
         if (__syncthreads_or(!ok))
             return false;
         tc_fence_after();
         uint32_t o[8];
         tmem_ld8(trow + TM_O + cg * 8, o);
-        __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            Ost[(cg * 8 + jj) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
+        for (int jj = 0; jj < 8; ++jj) {
+            const int t = cg * 8 + jj;
+            if (t < pL)
+                p.out[((ptok0 + t) * H + h) * D + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
+        }
         tc_fence_before();
         return true;
-    };
-    auto store_previous = [&](int64_t ptok0, int pL) {
-        const int r = tid >> 4, c16 = tid & 15;
-        if (r < pL)
-            *reinterpret_cast<uint4 *>(p.out + ((ptok0 + r) * H + h) * D + c16 * 8) =
-                *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
     };
 
     int64_t prev_tok0 = 0;
@@ -464,13 +461,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             }
             if (tid < CH)
                 bt[tid] = tid < L ? sigmoidf_fast(__bfloat162float(rawb[tid])) : 0.f;
-        }
-        // ---- the previous chunk's output: wait for its last update, read O^T out of tensor memory
-        if (ci > 0) {
-            if (!read_out_previous((ci - 1) & 1)) {
-                hung = true;
-                break;
-            }
         }
         __syncthreads();
 
@@ -559,11 +549,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 *reinterpret_cast<float2 *>(Gc + c0) = make_float2(D0 * Do0, D1 * Do1);
         }
         fence_async_smem();
+        // ---- the previous chunk's output (its final update ran during this gate pass)
+        if (ci > 0 && !write_out_previous((ci - 1) & 1, prev_tok0, prev_L)) {
+            hung = true;
+            break;
+        }
         __syncthreads();
 
-        // ---- the previous chunk's output to HBM; raw q, k, g, beta are consumed: stage the next chunk's
-        if (ci > 0)
-            store_previous(prev_tok0, prev_L);
+        // ---- raw q, k, g, beta are consumed: stage the next chunk's
         if (has_next) {
             load_tile_async<true>(smem, OFF_RAW_Q, p.q, ntok0, Ln, H, h);
             load_tile_async<true>(smem, OFF_RAW_K, p.k, ntok0, Ln, H, h);
@@ -584,60 +577,71 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             umma_commit(mbarX);
         }
 
-        // ---- S2: Akk and Aqk on tf32 mma.sync; items (pair, kind, n-tile) on warps 0..11.
+        // ---- S2: Akk and Aqk on tf32 mma.sync; warp = (pair, K half, kind), both n-tiles of the pair.
         // pair 0 = (0,0), 1 = (1,0): left factor from the chunk-start tile, right factor k^ E / D_0;
         // pair 2 = (1,1): left factor q^ P / k^ P of sub-block 1, right factor k^ E / D_1.
-        float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc2b[4] = {0.f, 0.f, 0.f, 0.f};
-        const int pair = warp >> 2, qk = (warp >> 1) & 1, ntl = warp & 1;
+        const int pair = warp >> 2, khalf = (warp >> 1) & 1, qk = warp & 1;
         const int rb1 = pair == 0 ? 0 : 16, cb0 = pair == 2 ? 16 : 0;
+        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if (warp < 12) {
-            const float *Y = reinterpret_cast<const float *>(smem + OFF_ED) + (cb0 + ntl * 8 + gq) * PF + tq;
+            const float *Y = reinterpret_cast<const float *>(smem + OFF_ED) + (cb0 + gq) * PF + tq;
+            const int ks0 = khalf * 8;
             if (pair < 2) {
                 const unsigned char *X = smem + OFF_QX + kmaj((qk ? 0 : CH) + rb1 + gq, tq, QX_LBO, QX_SBO);
-#pragma unroll 4
-                for (int ks = 0; ks < D / 8; ks += 2) {
-                    const unsigned char *x0 = X + ks * 2 * QX_LBO, *x1 = x0 + 2 * QX_LBO;
-                    const int k0 = ks * 8, k1 = k0 + 8;
-                    mma_tf32(acc2, *reinterpret_cast<const uint32_t *>(x0), *reinterpret_cast<const uint32_t *>(x0 + QX_SBO),
-                             *reinterpret_cast<const uint32_t *>(x0 + QX_LBO),
-                             *reinterpret_cast<const uint32_t *>(x0 + QX_SBO + QX_LBO),
-                             __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
-                    mma_tf32(acc2b, *reinterpret_cast<const uint32_t *>(x1), *reinterpret_cast<const uint32_t *>(x1 + QX_SBO),
-                             *reinterpret_cast<const uint32_t *>(x1 + QX_LBO),
-                             *reinterpret_cast<const uint32_t *>(x1 + QX_SBO + QX_LBO),
-                             __float_as_uint(Y[k1]), __float_as_uint(Y[k1 + 4]));
+#pragma unroll
+                for (int ks = ks0; ks < ks0 + 8; ++ks) {
+                    const unsigned char *x0 = X + ks * 2 * QX_LBO;
+                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(x0);
+                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(x0 + QX_SBO);
+                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(x0 + QX_LBO);
+                    const uint32_t a3 = *reinterpret_cast<const uint32_t *>(x0 + QX_SBO + QX_LBO);
+                    const int k0 = ks * 8;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        mma_tf32(acc2[nt], a0, a1, a2, a3, __float_as_uint(Y[nt * 8 * PF + k0]),
+                                 __float_as_uint(Y[nt * 8 * PF + k0 + 4]));
                 }
             } else {
                 const float *X = reinterpret_cast<const float *>(smem + (qk ? OFF_LQ : OFF_LK)) + gq * PF + tq;
-#pragma unroll 4
-                for (int ks = 0; ks < D / 8; ks += 2) {
-                    const int k0 = ks * 8, k1 = k0 + 8;
-                    mma_tf32(acc2, __float_as_uint(X[k0]), __float_as_uint(X[8 * PF + k0]), __float_as_uint(X[k0 + 4]),
-                             __float_as_uint(X[8 * PF + k0 + 4]), __float_as_uint(Y[k0]), __float_as_uint(Y[k0 + 4]));
-                    mma_tf32(acc2b, __float_as_uint(X[k1]), __float_as_uint(X[8 * PF + k1]), __float_as_uint(X[k1 + 4]),
-                             __float_as_uint(X[8 * PF + k1 + 4]), __float_as_uint(Y[k1]), __float_as_uint(Y[k1 + 4]));
+#pragma unroll
+                for (int ks = ks0; ks < ks0 + 8; ++ks) {
+                    const int k0 = ks * 8;
+                    const uint32_t a0 = __float_as_uint(X[k0]), a1 = __float_as_uint(X[8 * PF + k0]);
+                    const uint32_t a2 = __float_as_uint(X[k0 + 4]), a3 = __float_as_uint(X[8 * PF + k0 + 4]);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        mma_tf32(acc2[nt], a0, a1, a2, a3, __float_as_uint(Y[nt * 8 * PF + k0]),
+                                 __float_as_uint(Y[nt * 8 * PF + k0 + 4]));
                 }
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc2[e] += acc2b[e];
+            if (khalf) {
+                float4 *red = reinterpret_cast<float4 *>(smem + OFF_RED) + ((pair * 2 + qk) * 32 + lane) * 2;
+                red[0] = make_float4(acc2[0][0], acc2[0][1], acc2[0][2], acc2[0][3]);
+                red[1] = make_float4(acc2[1][0], acc2[1][1], acc2[1][2], acc2[1][3]);
+            }
         }
         __syncthreads();   // the intra operands are dead; the region is reused below
-        if (warp < 12) {
+        if (warp < 12 && !khalf) {
+            const float4 *red = reinterpret_cast<const float4 *>(smem + OFF_RED) + ((pair * 2 + qk) * 32 + lane) * 2;
+            const float4 r0 = red[0], r1 = red[1];
+            acc2[0][0] += r0.x; acc2[0][1] += r0.y; acc2[0][2] += r0.z; acc2[0][3] += r0.w;
+            acc2[1][0] += r1.x; acc2[1][1] += r1.y; acc2[1][2] += r1.z; acc2[1][3] += r1.w;
             float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = rb1 + gq + 8 * hh, j = cb0 + ntl * 8 + 2 * tq;
-                const float x0 = acc2[2 * hh], x1 = acc2[2 * hh + 1];
-                if (qk) {
-                    *reinterpret_cast<float2 *>(so + kmaj(D + i, j, SO_LBO, SO_SBO)) =
-                        make_float2(tf32r(j <= i ? x0 : 0.f), tf32r(j + 1 <= i ? x1 : 0.f));
-                } else {
-                    const float bi = bt[i];
-                    *reinterpret_cast<float2 *>(Akk + i * PA + j) =
-                        make_float2(j < i ? bi * x0 : 0.f, j + 1 < i ? bi * x1 : 0.f);
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int i = rb1 + gq + 8 * hh, j = cb0 + nt * 8 + 2 * tq;
+                    const float x0 = acc2[nt][2 * hh], x1 = acc2[nt][2 * hh + 1];
+                    if (qk) {
+                        *reinterpret_cast<float2 *>(so + kmaj(D + i, j, SO_LBO, SO_SBO)) =
+                            make_float2(tf32r(j <= i ? x0 : 0.f), tf32r(j + 1 <= i ? x1 : 0.f));
+                    } else {
+                        const float bi = bt[i];
+                        *reinterpret_cast<float2 *>(Akk + i * PA + j) =
+                            make_float2(j < i ? bi * x0 : 0.f, j + 1 < i ? bi * x1 : 0.f);
+                    }
                 }
-            }
         }
         __syncthreads();
 
@@ -759,14 +763,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     cp_async_wait<0>();
     __syncthreads();
     // the last chunk's output
-    if (!hung && nchunks > 0) {
-        if (read_out_previous((nchunks - 1) & 1)) {
-            __syncthreads();
-            store_previous(prev_tok0, prev_L);
-        } else {
-            hung = true;
-        }
-    }
+    if (!hung && nchunks > 0 && !write_out_previous((nchunks - 1) & 1, prev_tok0, prev_L))
+        hung = true;
 
     // -------- final state, tensor memory release
     if (hung) {
