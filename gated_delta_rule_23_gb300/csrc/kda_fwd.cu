@@ -98,7 +98,8 @@ constexpr int SO_BYTES = 20 * SO_SBO;
 constexpr int OFF_SO = OFF_QX + 8 * QX_SBO;      // two buffers: the update of chunk c reads one while
 constexpr int OFF_TP = OFF_SO + 2 * SO_BYTES;    // the gate pass of chunk c+1 writes the other
 constexpr int OFF_RED = OFF_TP + 4 * TP_SBO;     // fp32 [3 pairs][2 kinds][32 lanes][8] K-half partials
-constexpr int OFF_MISC = OFF_RED + 3 * 2 * 32 * 8 * 4;
+constexpr int OFF_OST = OFF_RED + 3 * 2 * 32 * 8 * 4;   // bf16 [32][136] output staging
+constexpr int OFF_MISC = OFF_OST + HT;
 constexpr int OFF_RQ = OFF_MISC;                 // fp32 [32] 1/|q|
 constexpr int OFF_RK = OFF_RQ + 128;             // fp32 [32] 1/|k|
 constexpr int OFF_BT = OFF_RK + 128;             // fp32 [32] b = sigmoid(beta), 0 past the end
@@ -108,7 +109,7 @@ constexpr int SMEM_BYTES = OFF_BAR + 32;
 static_assert(INTRA_END <= OFF_QX, "post-product overlay exceeds the intra region");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(OFF_INTRA % 128 == 0 && OFF_QX % 16 == 0 && OFF_SO % 16 == 0 && OFF_TP % 16 == 0 &&
-              OFF_MISC % 16 == 0 && OFF_RED % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+              OFF_MISC % 16 == 0 && OFF_RED % 16 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
 // byte offset of element (row, col) in a swizzled [32][136] half tile
 __host__ __device__ constexpr int swz(int row, int col)
@@ -401,23 +402,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             rawb[tid] = tid < L0 ? p.beta[(bos + tid) * H + h] : __float2bfloat16(0.f);
     }
 
-    // Output of the previous chunk: wait for its last update, then each thread writes its value
-    // row for tokens 8cg..8cg+7 straight from tensor memory (a warp stores 64 contiguous bytes).
-    auto write_out_previous = [&](uint32_t prev_parity, int64_t ptok0, int pL) -> bool {
+    // Output of the previous chunk: wait for its last update and move O^T from tensor memory to the
+    // bf16 staging tile [t][v] (this thread: its value row, tokens 8cg..8cg+7); after the next
+    // barrier store_previous writes it to HBM with 16-byte coalesced stores.
+    auto read_out_previous = [&](uint32_t prev_parity) -> bool {
         const bool ok = mbar_wait(mbarB, prev_parity) && *hang_flag == 0u;
         if (__syncthreads_or(!ok))
             return false;
         tc_fence_after();
         uint32_t o[8];
         tmem_ld8(trow + TM_O + cg * 8, o);
+        __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const int t = cg * 8 + jj;
-            if (t < pL)
-                p.out[((ptok0 + t) * H + h) * D + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
-        }
+        for (int jj = 0; jj < 8; ++jj)
+            Ost[(cg * 8 + jj) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
         tc_fence_before();
         return true;
+    };
+    auto store_previous = [&](int64_t ptok0, int pL) {
+        const int r = tid >> 4, c16 = tid & 15;
+        if (r < pL)
+            *reinterpret_cast<uint4 *>(p.out + ((ptok0 + r) * H + h) * D + c16 * 8) =
+                *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
     };
 
     int64_t prev_tok0 = 0;
@@ -550,13 +556,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         }
         fence_async_smem();
         // ---- the previous chunk's output (its final update ran during this gate pass)
-        if (ci > 0 && !write_out_previous((ci - 1) & 1, prev_tok0, prev_L)) {
+        if (ci > 0 && !read_out_previous((ci - 1) & 1)) {
             hung = true;
             break;
         }
         __syncthreads();
 
-        // ---- raw q, k, g, beta are consumed: stage the next chunk's
+        // ---- the previous chunk's output to HBM; raw q, k, g, beta are consumed: stage the next chunk's
+        if (ci > 0)
+            store_previous(prev_tok0, prev_L);
         if (has_next) {
             load_tile_async<true>(smem, OFF_RAW_Q, p.q, ntok0, Ln, H, h);
             load_tile_async<true>(smem, OFF_RAW_K, p.k, ntok0, Ln, H, h);
@@ -763,8 +771,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     cp_async_wait<0>();
     __syncthreads();
     // the last chunk's output
-    if (!hung && nchunks > 0 && !write_out_previous((nchunks - 1) & 1, prev_tok0, prev_L))
-        hung = true;
+    if (!hung && nchunks > 0) {
+        if (read_out_previous((nchunks - 1) & 1)) {
+            __syncthreads();
+            store_previous(prev_tok0, prev_L);
+        } else {
+            hung = true;
+        }
+    }
 
     // -------- final state, tensor memory release
     if (hung) {
