@@ -62,6 +62,7 @@ constexpr int TM_S = 0, TM_O = 128, TM_X = 160, TM_Y = 192, TM_U = 224;
 constexpr int MMA_TID = 384;                     // issuing thread: warp 12 has no Akk/Aqk item
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;        // try_wait polls before a wait is declared hung
+constexpr int LPT_MAX_SEQS = 256;                // longest-first ordering of varlen sequences up to this count
 
 // ---------------------------------------------------------------- shared memory map
 // Half-precision [32][136] tiles (272-byte rows).  The q, k, g tiles and K^.Gamma swizzle
@@ -107,6 +108,7 @@ constexpr int OFF_GC = OFF_BT + 128;             // fp32 [128] chunk decay Gamma
 constexpr int OFF_BAR = OFF_GC + D * 4;          // 3 mbarriers, tensor-memory base address, hang flag
 constexpr int SMEM_BYTES = OFF_BAR + 32;
 static_assert(INTRA_END <= OFF_QX, "post-product overlay exceeds the intra region");
+static_assert((LPT_MAX_SEQS + 1) * 8 + LPT_MAX_SEQS * 4 <= OFF_INTRA, "varlen scheduler scratch");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 static_assert(OFF_INTRA % 128 == 0 && OFF_QX % 16 == 0 && OFF_SO % 16 == 0 && OFF_TP % 16 == 0 &&
               OFF_MISC % 16 == 0 && OFF_RED % 16 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
@@ -294,8 +296,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;             // mma.sync fragment coordinates
-    const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
     const int H = p.H;
+    const int h = blockIdx.x % H;
+    int n = blockIdx.x / H;
+    if (VARLEN && p.N > 1 && p.N <= LPT_MAX_SEQS) {
+        // Varlen scheduler: blocks are dispatched in index order, so block b takes the (b / H)-th
+        // longest sequence (ties by index) and the longest sequences start first.
+        int64_t *cu_s = reinterpret_cast<int64_t *>(smem + OFF_RAW_Q);   // scratch before the first tile load
+        int *order = reinterpret_cast<int *>(smem + OFF_RAW_Q + (LPT_MAX_SEQS + 1) * 8);
+        for (int s = tid; s <= p.N; s += NTHREADS)
+            cu_s[s] = p.cu[s];
+        __syncthreads();
+        for (int s = tid; s < p.N; s += NTHREADS) {
+            const int64_t ls = cu_s[s + 1] - cu_s[s];
+            int rank = 0;
+            for (int m = 0; m < p.N; ++m) {
+                const int64_t lm = cu_s[m + 1] - cu_s[m];
+                rank += (lm > ls) || (lm == ls && m < s);
+            }
+            order[rank] = s;
+        }
+        __syncthreads();
+        n = order[blockIdx.x / H];
+        __syncthreads();   // the scratch is overwritten by the first tile loads
+    }
 
     int64_t bos, len;
     if (VARLEN) {
