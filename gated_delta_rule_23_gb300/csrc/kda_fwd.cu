@@ -59,11 +59,10 @@ constexpr int TMEM_COLS = 256;
 // tensor-memory columns: S^T | O^T | X^T | Y^T | U^T (O^T follows S^T and X^T follows O^T so
 // that the merged MMAs write one contiguous accumulator)
 constexpr int TM_S = 0, TM_O = 128, TM_X = 160, TM_Y = 192, TM_U = 224;
-constexpr int MMA_TID = 384;                     // issuing thread: first thread of warp 12
-// Warp roles besides the all-warp stages: warps 0..11 compute Akk/Aqk while warps 12..15 move the
-// previous chunk's output out of tensor memory and issue the early MMA group; warps 0..7 invert
-// (I + Akk) while warps 8..15 (which also stage v) form Y^T and decay S^T in tensor memory.
-constexpr int BAR_OUT = 1, BAR_INV = 2, BAR_TM = 3;   // named barriers of those warp groups
+constexpr int MMA_TID = 384;                     // issuing thread: warp 12 has no Akk/Aqk item
+// An issuing thread blocks while the tensor-core queue drains, so between the early MMA group and
+// the end of the inverse the other warps synchronise on a named barrier without warp 12.
+constexpr int BAR_NO_MMA = 1, NO_MMA_THREADS = NTHREADS - 32;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;        // try_wait polls before a wait is declared hung
 constexpr int LPT_MAX_SEQS = 256;                // longest-first ordering of varlen sequences up to this count
@@ -231,6 +230,13 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&u)[8])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&u)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]));
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Bounded wait for an mbarrier phase; returns false if the wait gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
 {
@@ -275,20 +281,6 @@ __device__ __forceinline__ void load_tile_async(unsigned char *smem, int off, co
 __device__ __forceinline__ void named_bar(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// v tile [32][136] (plain layout), staged by the 256 threads of warps 8..15 only (so that those
-// warps can wait for it without a CTA-wide barrier); rows past len are zero-filled.  len >= 1.
-__device__ __forceinline__ void load_v_async(unsigned char *smem, int off, const __nv_bfloat16 *base, int64_t tok0,
-                                             int len, int H, int h, int t256)
-{
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int idx = t256 + m * 256, r = idx >> 4, c16 = idx & 15;
-        const bool valid = r < len;
-        const int64_t row = tok0 + (valid ? r : 0);
-        cp_async16(smem_u32(smem + off + r * PH * 2 + c16 * 16), base + (row * H + h) * D + c16 * 8, valid);
-    }
 }
 
 struct Params {
@@ -436,8 +428,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         load_tile_async<true>(smem, OFF_RAW_K, p.k, bos, L0, H, h);
         load_tile_async<true>(smem, OFF_RAW_G, p.g, bos, L0, H, h);
         cp_async_commit();
-        if (warp >= 8)
-            load_v_async(smem, OFF_RAW_V, p.v, bos, L0, H, h, tid - 256);
+        load_tile_async<false>(smem, OFF_RAW_V, p.v, bos, L0, H, h);
         cp_async_commit();
         if (tid < CH)
             rawb[tid] = tid < L0 ? p.beta[(bos + tid) * H + h] : __float2bfloat16(0.f);
@@ -465,6 +456,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         if (r < pL)
             *reinterpret_cast<uint4 *>(p.out + ((ptok0 + r) * H + h) * D + c16 * 8) =
                 *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
+    };
+
+    // [S^T | O^T] += U^T [K~^T ; Aqk]^T for chunk c, issued once U^T of that chunk is done; the issuing
+    // thread calls this one stage later (after the next chunk's norms) so that it never blocks a barrier.
+    auto issue_update = [&](int c) {
+        if (mbar_wait(mbarU, c & 1) && *hang_flag == 0u) {
+            tc_fence_after();
+            const uint32_t s_sob = s_so + (c & 1) * SO_BYTES;
+#pragma unroll
+            for (int s = 0; s < CH / 8; ++s)
+                mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_sob + s * 2 * SO_LBO, SO_LBO, SO_SBO),
+                            idesc_tf32(128, D + CH), 1);
+            umma_commit(mbarB);
+        } else {
+            *hang_flag = 1u;
+        }
     };
 
     int64_t prev_tok0 = 0;
@@ -509,6 +516,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
             if (tid < CH)
                 bt[tid] = tid < L ? sigmoidf_fast(__bfloat162float(rawb[tid])) : 0.f;
         }
+        if (ci > 0 && tid == MMA_TID)
+            issue_update(ci - 1);
         __syncthreads();
 
         // ---- S1b: gate, sub-block decay products and every operand of this chunk (one pass)
@@ -596,9 +605,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 *reinterpret_cast<float2 *>(Gc + c0) = make_float2(D0 * Do0, D1 * Do1);
         }
         fence_async_smem();
+        // ---- the previous chunk's output (its final update ran during this gate pass)
+        if (ci > 0 && !read_out_previous((ci - 1) & 1)) {
+            hung = true;
+            break;
+        }
         __syncthreads();
 
-        // ---- raw q, k, g, beta are consumed: stage the next chunk's
+        // ---- the previous chunk's output to HBM; raw q, k, g, beta are consumed: stage the next chunk's
+        if (ci > 0)
+            store_previous(prev_tok0, prev_L);
         if (has_next) {
             load_tile_async<true>(smem, OFF_RAW_Q, p.q, ntok0, Ln, H, h);
             load_tile_async<true>(smem, OFF_RAW_K, p.k, ntok0, Ln, H, h);
@@ -609,41 +625,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
         if (has_next && tid < Ln)
             next_beta = p.beta[(ntok0 + tid) * H + h];
 
-        // ---- warps 12..15: the previous chunk's output (its last update ran during this gate pass), then
-        //      the tensor cores' [O^T | X^T] = S^T [Q~ ; K^.Gamma]^T, which overlaps the products and the inverse
-        if (warp >= 12) {
-            if (ci > 0) {
-                if (mbar_wait(mbarB, (ci - 1) & 1) && *hang_flag == 0u) {
-                    tc_fence_after();
-                    uint32_t o[32];
-                    tmem_ld32(trow + TM_O, o);
-                    __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(smem + OFF_OST);
+        // ---- tensor cores: [O^T | X^T] = S^T [Q~ ; K^.Gamma]^T (overlaps the products and the inverse)
+        if (tid == MMA_TID) {
+            tc_fence_after();
 #pragma unroll
-                    for (int jj = 0; jj < CH; ++jj)
-                        Ost[jj * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[jj]) * p.scale);
-                } else {
-                    *hang_flag = 1u;
-                }
-            }
-            tc_fence_before();
-            named_bar(BAR_OUT, 128);
-            if (ci > 0 && *hang_flag == 0u) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int idx = (tid - 384) + m * 128, r = idx >> 4, c16 = idx & 15;
-                    if (r < prev_L)
-                        *reinterpret_cast<uint4 *>(p.out + ((prev_tok0 + r) * H + h) * D + c16 * 8) =
-                            *reinterpret_cast<const uint4 *>(smem + OFF_OST + r * PH * 2 + c16 * 16);
-                }
-            }
-            if (tid == MMA_TID && *hang_flag == 0u) {
-                tc_fence_after();
-#pragma unroll
-                for (int s = 0; s < D / 8; ++s)
-                    mma_tf32_ts(tbase + TM_O, tbase + TM_S + 8 * s, umma_desc(s_qx + s * 2 * QX_LBO, QX_LBO, QX_SBO),
-                                idesc_tf32(128, 2 * CH), s > 0);
-                umma_commit(mbarX);
-            }
+            for (int s = 0; s < D / 8; ++s)
+                mma_tf32_ts(tbase + TM_O, tbase + TM_S + 8 * s, umma_desc(s_qx + s * 2 * QX_LBO, QX_LBO, QX_SBO),
+                            idesc_tf32(128, 2 * CH), s > 0);
+            umma_commit(mbarX);
         }
 
         // ---- S2: Akk and Aqk on tf32 mma.sync; warp = (pair, K half, kind), both n-tiles of the pair.
@@ -689,7 +678,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 red[1] = make_float4(acc2[1][0], acc2[1][1], acc2[1][2], acc2[1][3]);
             }
         }
-        __syncthreads();   // the intra operands are dead; the region is reused below
+        if (warp != MMA_TID / 32)
+            named_bar(BAR_NO_MMA, NO_MMA_THREADS);   // the intra operands are dead; the region is reused below
         if (warp < 12 && !khalf) {
             const float4 *red = reinterpret_cast<const float4 *>(smem + OFF_RED) + ((pair * 2 + qk) * 32 + lane) * 2;
             const float4 r0 = red[0], r1 = red[1];
@@ -712,98 +702,95 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                     }
                 }
         }
-        __syncthreads();
+        if (warp != MMA_TID / 32)
+            named_bar(BAR_NO_MMA, NO_MMA_THREADS);
 
-        // ---- warps 0..7: Tm = (I + Akk)^-1 (fp32) and the tf32 tile of T' = Tm diag(b);
-        //      warps 8..15 meanwhile: Y^T = V^T - X^T and S^T <- S^T Diag(Gamma_31) in tensor memory
+        // ---- S3: Tm = (I + Akk)^-1 (fp32) and the tf32 tile of T' = Tm diag(b)
         float *Akk = reinterpret_cast<float *>(smem + OFF_AKK);
         float *Tmd = reinterpret_cast<float *>(smem + OFF_TMD);
-        if (warp < 8) {
-            if (warp < 2 && lane < 16) {
-                // diagonal 16x16 blocks, column j per lane, right-looking forward substitution
-                const int b = warp, j = lane;
-                float x[SB], acc[SB];
+        if (warp < 2 && lane < 16) {
+            // diagonal 16x16 blocks, column j per lane, right-looking forward substitution
+            const int b = warp, j = lane;
+            float x[SB], acc[SB];
 #pragma unroll
-                for (int i = 0; i < SB; ++i)
-                    acc[i] = 0.f;
+            for (int i = 0; i < SB; ++i)
+                acc[i] = 0.f;
 #pragma unroll
-                for (int l = 0; l < SB; ++l) {
-                    x[l] = l == j ? 1.f : (l < j ? 0.f : -acc[l]);
+            for (int l = 0; l < SB; ++l) {
+                x[l] = l == j ? 1.f : (l < j ? 0.f : -acc[l]);
 #pragma unroll
-                    for (int i = l + 1; i < SB; ++i)
-                        acc[i] = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], acc[i]);
-                }
-                const float bj = bt[b * SB + j];
-#pragma unroll
-                for (int i = 0; i < SB; ++i) {
-                    const int r = b * SB + i, c = b * SB + j;
-                    Tmd[r * PA + c] = x[i];
-                    *reinterpret_cast<float *>(smem + OFF_TP + kmaj(r, c, TP_LBO, TP_SBO)) = tf32r(x[i] * bj);
-                }
+                for (int i = l + 1; i < SB; ++i)
+                    acc[i] = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], acc[i]);
             }
-            named_bar(BAR_INV, 256);
-            // off-diagonal block: Tm_10 = -Tm_11 (A_10 Tm_00);  thread = (i, j)
-            const int i = tid >> 4, j = tid & 15;
-            float *Mt = reinterpret_cast<float *>(smem + OFF_MT);
-            {
-                float s0 = 0.f, s1 = 0.f;
+            const float bj = bt[b * SB + j];
 #pragma unroll
-                for (int l = 0; l < SB; l += 2) {
-                    s0 = fmaf(Akk[(SB + i) * PA + l], Tmd[l * PA + j], s0);
-                    s1 = fmaf(Akk[(SB + i) * PA + l + 1], Tmd[(l + 1) * PA + j], s1);
-                }
-                Mt[i * 16 + j] = s0 + s1;
+            for (int i = 0; i < SB; ++i) {
+                const int r = b * SB + i, c = b * SB + j;
+                Tmd[r * PA + c] = x[i];
+                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(r, c, TP_LBO, TP_SBO)) = tf32r(x[i] * bj);
             }
-            named_bar(BAR_INV, 256);
-            {
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int l = 0; l < SB; l += 2) {
-                    s0 = fmaf(Tmd[(SB + i) * PA + SB + l], Mt[l * 16 + j], s0);
-                    s1 = fmaf(Tmd[(SB + i) * PA + SB + l + 1], Mt[(l + 1) * 16 + j], s1);
-                }
-                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(SB + i, j, TP_LBO, TP_SBO)) = tf32r(-(s0 + s1) * bt[j]);
-            }
-            fence_async_smem();
-        } else {
-            cp_async_wait<1>();   // this thread's v copies of this chunk (the next q, k, g may stay in flight)
-            named_bar(BAR_TM, 256);
-            if (mbar_wait(mbarX, parity) && *hang_flag == 0u) {
-                tc_fence_after();
-                const int grp = (warp >> 2) - 2;   // 0: Y^T and state columns 0..63; 1: state columns 64..127
-                uint32_t u[32];
-                if (grp == 0) {
-                    tmem_ld32(trow + TM_X, u);
-                    const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_V);
-#pragma unroll
-                    for (int jj = 0; jj < CH; ++jj)
-                        u[jj] = __float_as_uint(__bfloat162float(rv[jj * PH + vrow]) - __uint_as_float(u[jj]));
-                    tmem_st32(trow + TM_Y, u);
-                }
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const int col = grp * 64 + part * 32;
-                    tmem_ld32(trow + TM_S + col, u);
-                    const float4 *g4 = reinterpret_cast<const float4 *>(Gc + col);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 gm = g4[e];
-                        u[4 * e] = __float_as_uint(__uint_as_float(u[4 * e]) * gm.x);
-                        u[4 * e + 1] = __float_as_uint(__uint_as_float(u[4 * e + 1]) * gm.y);
-                        u[4 * e + 2] = __float_as_uint(__uint_as_float(u[4 * e + 2]) * gm.z);
-                        u[4 * e + 3] = __float_as_uint(__uint_as_float(u[4 * e + 3]) * gm.w);
-                    }
-                    tmem_st32(trow + TM_S + col, u);
-                }
-            } else {
-                *hang_flag = 1u;
-            }
-            tc_fence_before();
         }
-        if (__syncthreads_or(*hang_flag != 0u)) {
+        if (warp != MMA_TID / 32)
+            named_bar(BAR_NO_MMA, NO_MMA_THREADS);
+        {
+            // off-diagonal block: Tm_10 = -Tm_11 (A_10 Tm_00);  threads 0..255 = (i, j)
+            const int i = (tid >> 4) & 15, j = tid & 15;
+            float *Mt = reinterpret_cast<float *>(smem + OFF_MT);
+            if (tid < 256) {
+                float s = 0.f, s2 = 0.f;
+#pragma unroll
+                for (int l = 0; l < SB; l += 2) {
+                    s = fmaf(Akk[(SB + i) * PA + l], Tmd[l * PA + j], s);
+                    s2 = fmaf(Akk[(SB + i) * PA + l + 1], Tmd[(l + 1) * PA + j], s2);
+                }
+                Mt[i * 16 + j] = s + s2;
+            }
+            if (warp != MMA_TID / 32)
+                named_bar(BAR_NO_MMA, NO_MMA_THREADS);
+            if (tid < 256) {
+                float s = 0.f, s2 = 0.f;
+#pragma unroll
+                for (int l = 0; l < SB; l += 2) {
+                    s = fmaf(Tmd[(SB + i) * PA + SB + l], Mt[l * 16 + j], s);
+                    s2 = fmaf(Tmd[(SB + i) * PA + SB + l + 1], Mt[(l + 1) * 16 + j], s2);
+                }
+                *reinterpret_cast<float *>(smem + OFF_TP + kmaj(SB + i, j, TP_LBO, TP_SBO)) = tf32r(-(s + s2) * bt[j]);
+            }
+        }
+        fence_async_smem();
+        cp_async_wait<1>();   // v of this chunk (the next chunk's q, k, g may stay in flight)
+        __syncthreads();
+
+        // ---- Y^T = V^T - X^T into tensor memory, and S^T <- S^T Diag(Gamma_31)
+        hung = !mbar_wait(mbarX, parity);
+        if (__syncthreads_or(hung)) {
             hung = true;
             break;
         }
+        tc_fence_after();
+        {
+            uint32_t xv[8];
+            tmem_ld8(trow + TM_X + cg * 8, xv);
+            const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_RAW_V);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                xv[jj] = __float_as_uint(__bfloat162float(rv[(cg * 8 + jj) * PH + vrow]) - __uint_as_float(xv[jj]));
+            tmem_st8(trow + TM_Y + cg * 8, xv);
+            uint32_t u[32];
+            tmem_ld32(trow + TM_S + cg * 32, u);
+            const float4 *g4 = reinterpret_cast<const float4 *>(Gc + cg * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 gm = g4[e];
+                u[4 * e] = __float_as_uint(__uint_as_float(u[4 * e]) * gm.x);
+                u[4 * e + 1] = __float_as_uint(__uint_as_float(u[4 * e + 1]) * gm.y);
+                u[4 * e + 2] = __float_as_uint(__uint_as_float(u[4 * e + 2]) * gm.z);
+                u[4 * e + 3] = __float_as_uint(__uint_as_float(u[4 * e + 3]) * gm.w);
+            }
+            tmem_st32(trow + TM_S + cg * 32, u);
+        }
+        tc_fence_before();
+        __syncthreads();
         // ---- tensor cores: U^T = Y^T T'^T, then [S^T | O^T] += U^T [K~^T ; Aqk]^T (completes while the
         //      next chunk's gate pass runs; its output is read out there)
         if (tid == MMA_TID) {
@@ -813,28 +800,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) kda_fwd_kernel(const Params p)
                 mma_tf32_ts(tbase + TM_U, tbase + TM_Y + 8 * s, umma_desc(s_tp + s * 2 * TP_LBO, TP_LBO, TP_SBO),
                             idesc_tf32(128, CH), s > 0);
             umma_commit(mbarU);
-            if (mbar_wait(mbarU, parity)) {
-                tc_fence_after();
-                const uint32_t s_sob = s_so + sob * SO_BYTES;
-#pragma unroll
-                for (int s = 0; s < CH / 8; ++s)
-                    mma_tf32_ts(tbase + TM_S, tbase + TM_U + 8 * s, umma_desc(s_sob + s * 2 * SO_LBO, SO_LBO, SO_SBO),
-                                idesc_tf32(128, D + CH), 1);
-                umma_commit(mbarB);
-            } else {
-                *hang_flag = 1u;
-            }
         }
 
         // ---- stage the next chunk's v and beta
-        if (has_next && warp >= 8)
-            load_v_async(smem, OFF_RAW_V, p.v, ntok0, Ln, H, h, tid - 256);
+        if (has_next)
+            load_tile_async<false>(smem, OFF_RAW_V, p.v, ntok0, Ln, H, h);
         cp_async_commit();
         if (tid < CH)
             rawb[tid] = next_beta;
         prev_tok0 = tok0;
         prev_L = L;
     }
+    if (!hung && nchunks > 0 && tid == MMA_TID)
+        issue_update(nchunks - 1);
     cp_async_wait<0>();
     __syncthreads();
     // the last chunk's output
