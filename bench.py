@@ -35,7 +35,7 @@ from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, WORKLOADS, 
 
 METRIC = "KDA fwd ms & tokens·heads/s at T=8192 H=96; % of HBM/tensor roofline"
 UNIT = "tokens·heads/s"
-KERNEL_SRC = os.path.join(ROOT, "gated_delta_rule_23_gb300", "csrc", "kda_fwd.cu")
+KERNEL_DIR = os.path.join(ROOT, "gated_delta_rule_23_gb300", "csrc")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kda_fwd_kernel_T8192_H96_bf16state.md")
 # FlashKDA on GB200, H=96 fixed length, T=8192: 1.01 ms (guancyxx.cn FlashKDA article, section 三,
 # GB200 table) -> tokens*heads per second.  Another machine: context, not the target.
@@ -64,8 +64,13 @@ def algorithmic_bytes(p):
 
 
 def kernel_source_hash():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of every CUDA source of the library (the profile summary is valid only for these)."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(KERNEL_DIR)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(KERNEL_DIR, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(p):

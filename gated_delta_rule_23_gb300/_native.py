@@ -17,8 +17,9 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
-SOURCES = [os.path.join(CSRC, "kda_fwd.cu")]
-HEADERS = [os.path.join(INCLUDE, "kda.h")]
+UNITS = ["kda_api", "kda_prep", "kda_recur"]
+SOURCES = [os.path.join(CSRC, u + ".cu") for u in UNITS]
+HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh"), os.path.join(CSRC, "kda_internal.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -38,18 +39,32 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/*.cu into _build/libkda.so (sm_103a, -O3, -lineinfo)."""
+    """Compile csrc/*.cu (sm_103a, -O3, -lineinfo), one process per unit, and link _build/libkda.so."""
     with _lock:
         if not force and not _stale():
             return LIB_PATH
         os.makedirs(BUILD_DIR, exist_ok=True)
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-               "-I" + INCLUDE, "-o", tmp, *SOURCES]
+        tag = f".tmp{os.getpid()}"
+        common = [nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
         if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB_PATH)
+            common.append("-Xptxas=-v")
+        objs, procs = [], []
+        for u, src in zip(UNITS, SOURCES):
+            obj = os.path.join(BUILD_DIR, u + tag + ".o")
+            objs.append(obj)
+            procs.append(subprocess.Popen(common + ["-c", "-o", obj, src]))
+        codes = [pr.wait() for pr in procs]
+        try:
+            for src, rc in zip(SOURCES, codes):
+                if rc != 0:
+                    raise subprocess.CalledProcessError(rc, f"nvcc {src}")
+            tmp = LIB_PATH + tag
+            subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", "-o", tmp, *objs], check=True)
+            os.replace(tmp, LIB_PATH)
+        finally:
+            for o in objs:
+                if os.path.exists(o):
+                    os.remove(o)
         return LIB_PATH
 
 
@@ -62,6 +77,12 @@ def load() -> ctypes.CDLL:
         P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
         lib.kda_fwd.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P]
         lib.kda_fwd.restype = I
+        lib.kda_fwd_ws.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t, P]
+        lib.kda_fwd_ws.restype = I
+        lib.kda_fwd_workspace_size.argtypes = [I, I64, I, I]
+        lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.kda_workspace_trim.argtypes = []
+        lib.kda_workspace_trim.restype = I
         lib.kda_check_cu_seqlens.argtypes = [P, I, I64]
         lib.kda_check_cu_seqlens.restype = I
         lib.kda_status_string.argtypes = [I]

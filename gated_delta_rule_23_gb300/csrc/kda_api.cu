@@ -1,0 +1,300 @@
+// C ABI of the KDA forward library (include/kda.h): argument checks, workspace layout and the
+// launch sequence  [plan (varlen only)] -> prep -> recurrence  on the caller's stream.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kda.h"
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int PLAN_THREADS = 1024;
+constexpr int LPT_MAX_SEQS = 2048;   // longest-first ordering of varlen sequences up to this count
+
+// Varlen plan, one CTA: chunk_off[n] = sum_{m < n} ceil(len_m / 64) (exclusive scan, [N + 1]),
+// and, when order != nullptr, order[rank] = sequence with that rank by length (longest first,
+// ties by index), so that the recurrence CTAs that start first take the longest sequences.
+__global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *cu, int N, int64_t *chunk_off,
+                                                              int *order)
+{
+    __shared__ int64_t wsum[PLAN_THREADS / 32];
+    __shared__ int64_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0)
+        carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += PLAN_THREADS) {
+        const int n = base + tid;
+        const int64_t cnt = n < N ? (cu[n + 1] - cu[n] + CH - 1) / CH : 0;
+        int64_t x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        if (lane == 31)
+            wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int64_t w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o)
+                    w += y;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const int64_t excl = carry + (warp > 0 ? wsum[warp - 1] : 0) + x - cnt;
+        if (n < N)
+            chunk_off[n] = excl;
+        __syncthreads();
+        if (tid == PLAN_THREADS - 1)
+            carry = excl + cnt;
+        __syncthreads();
+    }
+    if (tid == 0)
+        chunk_off[N] = carry;
+    if (order) {
+        for (int s = tid; s < N; s += PLAN_THREADS) {
+            const int64_t ls = cu[s + 1] - cu[s];
+            int rank = 0;
+            for (int m = 0; m < N; ++m) {
+                const int64_t lm = cu[m + 1] - cu[m];
+                rank += (lm > ls) || (lm == ls && m < s);
+            }
+            order[rank] = s;
+        }
+    }
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// workspace: [chunk_off: (N + 1) int64][order: N int32] (varlen only), then the operand slots
+size_t header_bytes(int N, bool varlen) { return varlen ? round_up((size_t)(N + 1) * 8 + (size_t)N * 4, 256) : 0; }
+
+int64_t max_chunks(int N, int64_t T, bool varlen)
+{
+    // varlen: sum_n ceil(len_n / 64) <= (T + 63 N) / 64
+    return varlen ? (T + (int64_t)(CH - 1) * N) / CH : (int64_t)N * ((T + CH - 1) / CH);
+}
+
+size_t workspace_bytes(int N, int64_t T, int H, bool varlen)
+{
+    return header_bytes(N, varlen) + (size_t)max_chunks(N, T, varlen) * (size_t)H * SLOT_BYTES;
+}
+
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[64] = {};
+
+// A memory pool owned by this library (one per device) that keeps what it has reserved, so
+// repeated calls reuse the same workspace memory without a device synchronisation.
+cudaError_t get_pool(int dev, cudaMemPool_t *out)
+{
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        cudaError_t err = cudaMemPoolCreate(&pool, &props);
+        if (err != cudaSuccess)
+            return err;
+        uint64_t keep = UINT64_MAX;
+        err = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (err != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return err;
+        }
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+
+kda_status_t check_args(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                        const void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                        const void *initial_state, const void *final_state, kda_dtype_t state_dtype,
+                        const int64_t *cu_seqlens, int N, int64_t T, int H)
+{
+    if (N < 1 || H < 1 || T < 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    // with no tokens at all the token tensors may be empty (NULL)
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!A_log || !dt_bias)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)N * H > INT32_MAX || T > ((int64_t)1 << 40))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(out, 16) ||
+        !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 16) || !aligned(cu_seqlens, 8))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (initial_state || final_state) {
+        if (state_dtype != KDA_DTYPE_BF16 && state_dtype != KDA_DTYPE_FP32)
+            return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned(initial_state, 16) || !aligned(final_state, 16))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if (!(lower_bound >= -5.0f && lower_bound <= 0.0f))
+        return KDA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale))
+        return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                 void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
+                 void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                 unsigned char *ws, cudaStream_t stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    Problem p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.g = static_cast<const __nv_bfloat16 *>(g);
+    p.beta = static_cast<const __nv_bfloat16 *>(beta);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.init = initial_state;
+    p.fin = final_state;
+    p.cu = cu_seqlens;
+    p.scale = scale;
+    p.lb_log2e = lower_bound * LOG2E;
+    p.N = N;
+    p.H = H;
+    p.T = T;
+    p.nch_fixed = (T + CH - 1) / CH;
+    p.chunk_off = nullptr;
+    p.order = nullptr;
+    p.slots = ws + header_bytes(N, varlen);
+    cudaError_t err = cudaSuccess;
+    if (varlen) {
+        int64_t *chunk_off = reinterpret_cast<int64_t *>(ws);
+        int *order = N > 1 && N <= LPT_MAX_SEQS ? reinterpret_cast<int *>(ws + (size_t)(N + 1) * 8) : nullptr;
+        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, chunk_off, order);
+        err = cudaGetLastError();
+        p.chunk_off = chunk_off;
+        p.order = order;
+    }
+    if (err == cudaSuccess)
+        err = launch_prep(p, max_chunks(N, T, varlen), stream);
+    const int st = (initial_state || final_state) ? (state_dtype == KDA_DTYPE_FP32 ? 2 : 1) : 0;
+    if (err == cudaSuccess)
+        err = launch_recur(p, st, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen)
+{
+    if (N < 1 || H < 1 || T < 0)
+        return 0;
+    return workspace_bytes(N, T, H, varlen != 0);
+}
+
+extern "C" kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                   float scale, void *out, const float *A_log, const float *dt_bias,
+                                   float lower_bound, const void *initial_state, void *final_state,
+                                   kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                                   void *workspace, size_t workspace_bytes_, kda_stream_t stream)
+{
+    kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s != KDA_OK)
+        return s;
+    const size_t need = workspace_bytes(N, T, H, cu_seqlens != nullptr);
+    if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes_ < need))
+        return KDA_ERR_INVALID_ARGUMENT;
+    return run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
+               cu_seqlens, N, T, H, static_cast<unsigned char *>(workspace), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                float scale, void *out, const float *A_log, const float *dt_bias,
+                                float lower_bound, const void *initial_state, void *final_state,
+                                kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                                kda_stream_t stream)
+{
+    kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s != KDA_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t need = workspace_bytes(N, T, H, cu_seqlens != nullptr);
+    void *ws = nullptr;
+    if (need > 0) {
+        int dev = 0;
+        cudaMemPool_t pool;
+        if (cudaGetDevice(&dev) != cudaSuccess || get_pool(dev, &pool) != cudaSuccess ||
+            cudaMallocFromPoolAsync(&ws, need, pool, st) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    s = run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
+            cu_seqlens, N, T, H, static_cast<unsigned char *>(ws), st);
+    if (ws && cudaFreeAsync(ws, st) != cudaSuccess && s == KDA_OK)
+        s = KDA_ERR_CUDA;
+    return s;
+}
+
+extern "C" kda_status_t kda_workspace_trim(void)
+{
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    for (cudaMemPool_t pool : g_pools)
+        if (pool && cudaMemPoolTrimTo(pool, 0) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+extern "C" kda_status_t kda_check_cu_seqlens(const int64_t *cu, int N, int64_t T)
+{
+    if (!cu || N < 1 || T < 0 || cu[0] != 0 || cu[N] != T)
+        return KDA_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < N; ++i)
+        if (cu[i + 1] < cu[i])
+            return KDA_ERR_INVALID_ARGUMENT;
+    return KDA_OK;
+}
+
+extern "C" const char *kda_status_string(kda_status_t s)
+{
+    switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported argument value";
+    case KDA_ERR_CUDA: return "CUDA error";
+    case KDA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+extern "C" size_t kda_fwd_smem_bytes(void)
+{
+    const size_t a = prep_smem_bytes(), b = recur_smem_bytes();
+    return a > b ? a : b;
+}
+
+extern "C" kda_status_t kda_device_status(kda_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    unsigned int flag = 0, flag2 = 0;
+    if (read_and_clear_device_error(&flag) != cudaSuccess || prep_read_and_clear_error(&flag2) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return (flag | flag2) ? KDA_ERR_TIMEOUT : KDA_OK;
+}

@@ -1,0 +1,622 @@
+// KDA prep kernel: the token-parallel intra-chunk stage, one CTA per (64-token chunk, head).
+//
+// This is the first of the two stages the guancyxx.cn FlashKDA article (section 2.2) splits
+// the forward pass into: gate activation -> L2 norm -> cumulative decay -> the L / Mqk
+// matrices -> their inversion, run for every chunk at once, independent of the state.  The
+// CTA writes the chunk's state-free operands of the recurrence into its workspace slot
+// (layout in kda_device.cuh), in fp16, ready for the tensor cores of the recurrence kernel:
+//   W = T' (K^ . Gamma),  Q~ = Q^ . Gamma,  Aqk,  K~ = K^ . Gamma_C / Gamma,  U0 = T' V,  Gamma_C
+// with T' = (I + Akk)^-1 diag(b).  The recurrence kernel then only evaluates
+//   U = U0 - W S,   O = scale (Q~ S + Aqk U),   S <- Diag(Gamma_C) S + K~^T U.
+//
+// Decay factors.  Per key channel c, a_t = lower_bound * sigmoid(exp(A_log) (g_t + dt_bias)),
+// alpha_t = exp(a_t) and Gamma_t = prod_{s <= t} alpha_s (chunk-relative).  The chunk is cut
+// into four 16-token sub-blocks b with inclusive prefix P_t, exclusive suffix E_t and total D_b
+// of alpha inside the sub-block; pre_b / post_b are the products of D over the earlier / later
+// sub-blocks, so Gamma_t = pre_b P_t and Gamma_C / Gamma_t = E_t post_b.
+// The intra-chunk products need Gamma_i / Gamma_j (j <= i).  Each 32-token half h is anchored
+// at the end of its first sub-block (token m_0 = 15, m_1 = 47): row i of half h uses
+//   left  factor Gamma_i / Gamma_{m_h}   (1 / E_i on sub-blocks 0 and 2, P_i on 1 and 3)
+//   right factor Gamma_{m_h} / Gamma_j   (E_j, E_j D_1 D_2, E_j D_2 or 1 / P_j by sub-block)
+// and Gamma_i / Gamma_j is their product.  Inside a half every factor lies within 16 tokens of
+// its anchor, so it stays in [2^-115.5, 2^115.5] when lower_bound >= -5 (at most 7.22 binary
+// orders of decay per token): the CHUNK = 16 range argument of the article (section 2.1),
+// applied around each anchor.  Right factors of the second half's anchor for columns in the
+// first half only shrink (a value below fp32 range stands for a contribution below 2^-41).
+// With both halves' rows stacked, Akk and Aqk of the whole chunk are ONE tf32 tensor-core
+// product: [k^ L ; q^ L] (128 rows) times [k^ R] (96 columns), K = 128.
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+// Set when a bounded wait on the tensor cores expires in the prep kernel.
+__device__ unsigned int g_kda_prep_error;
+
+namespace kda {
+namespace {
+
+constexpr int PREP_THREADS = 256;
+constexpr int TMEM_COLS = 128;          // Akk / Aqk accumulators: 128 lanes x 96 columns
+// tf32 operand tiles of the Akk / Aqk product for one half of the channels (the gate pass runs in
+// two passes of 64 channels; the tensor cores accumulate both).  No-swizzle K-major core-matrix
+// layout, element (row r, compact channel kk) at (r / 8) * OPS_SBO + (kk / 4) * OPS_LBO
+// + (r % 8) * 16 + (kk % 4) * 4; the padded strides make the gate pass's 16-byte stores
+// conflict-light.  Rows of A: [k^ L_0 (tokens 0..31) ; q^ L_0 ; k^ L_1 (tokens 32..63) ; q^ L_1];
+// rows of B: [k^ R_0 (tokens 0..31) ; k^ R_1 (tokens 0..63)].
+constexpr int OPS_LBO = 160, OPS_SBO = 2576;
+constexpr int OPS_A = 0;
+constexpr int OPS_B = 16 * OPS_SBO;                 // 41216
+constexpr int OPS_BYTES = OPS_B + 12 * OPS_SBO;     // 72128
+// shared memory map (bytes)
+constexpr int OFF_OPS = 0;
+constexpr int OFF_PART = OFF_OPS;                   // fp32 [8 warps][2][64] sums of squares (before the gate pass)
+// reused once the Akk / Aqk product has completed:
+constexpr int PA = 68;                              // fp32 pitch of 64-wide matrices
+constexpr int OFF_AKK = OFF_OPS;                    // fp32 [64][68] b_i Akk (strictly lower)
+constexpr int OFF_TM = OFF_AKK + CH * PA * 4;       // fp32 [64][68] (I + Akk)^-1
+constexpr int OFF_TP = OFF_TM + CH * PA * 4;        // fp16 [64 t][64 j] T' (swizzled)
+constexpr int OFF_ZW = OFF_TP + CH * CH * 2;        // fp32 [8 warps][16][8] off-diagonal partial products
+static_assert(OFF_ZW + 8 * 16 * 8 * 4 <= OPS_BYTES, "post-product overlay");
+constexpr int OFF_KG = 72192;                       // fp16 [64 j][128 c] K^ . Gamma (swizzled)
+constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizzled)
+constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 [64] 1 / |q|
+constexpr int OFF_RK = OFF_RQ + 256;                // fp32 [64] 1 / |k|
+constexpr int OFF_BT = OFF_RK + 256;                // fp32 [64] b = sigmoid(beta), 0 past the end
+constexpr int OFF_MISC = OFF_BT + 256;              // mbarrier, tensor-memory base
+constexpr int PREP_SMEM = OFF_MISC + 16;
+static_assert(OFF_KG >= OPS_BYTES && OFF_KG % 128 == 0, "shared memory map");
+static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two CTAs per SM");
+
+__host__ __device__ constexpr int ops_off(int r, int kgrp) { return (r >> 3) * OPS_SBO + kgrp * OPS_LBO + ((r & 7) << 4); }
+// byte offset of a 16-bit element in a [64][128] / [64][64] tile; 16-byte chunks XOR-swizzled
+// by row (conflict-free ldmatrix)
+__device__ __forceinline__ int h128(int r, int c) { return r * 256 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
+__device__ __forceinline__ int h64(int r, int c) { return r * 128 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
+
+template <bool VARLEN>
+__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem p)
+{
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H;
+    const int64_t item = blockIdx.x;
+    const int h = (int)(item % H);
+    const int64_t gc = item / H;
+
+    // -------- this CTA's chunk: first token tok0 and L valid tokens
+    int64_t tok0, rem;
+    if (VARLEN) {
+        if (gc >= p.chunk_off[p.N])
+            return;
+        int lo = 0, hi = p.N - 1;   // the last sequence whose first chunk is <= gc
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.chunk_off[mid] <= gc)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int64_t c = gc - p.chunk_off[lo];
+        tok0 = p.cu[lo] + c * CH;
+        rem = p.cu[lo + 1] - tok0;
+    } else {
+        const int64_t n = gc / p.nch_fixed, c = gc % p.nch_fixed;
+        tok0 = n * p.T + c * CH;
+        rem = p.T - c * CH;
+    }
+    const int L = (int)(rem < CH ? rem : CH);
+    unsigned char *slot = p.slots + (size_t)item * SLOT_BYTES;
+
+    float *rq = reinterpret_cast<float *>(sm + OFF_RQ);
+    float *rk = reinterpret_cast<float *>(sm + OFF_RK);
+    float *bt = reinterpret_cast<float *>(sm + OFF_BT);
+    const uint32_t mbarA = smem_u32(sm + OFF_MISC);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 8);
+    bool hung = false;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        mbar_init(mbarA, 1);
+        mbar_fence_init();
+    }
+
+    // -------- phase 0: v rows (bf16) staged for the WY products; this thread's q, k, g
+#pragma unroll
+    for (int m = 0; m < (CH * 16) / PREP_THREADS; ++m) {
+        const int idx = tid + m * PREP_THREADS, r = idx >> 4, c16 = idx & 15;
+        const bool valid = r < L;
+        const __nv_bfloat16 *src = p.v + ((size_t)(tok0 + (valid ? r : 0)) * H + h) * D + c16 * 8;
+        cp_async16(smem_u32(sm + OFF_V + h128(r, c16 * 8)), src, valid);
+    }
+    cp_async_commit();
+    // lane roles: channel group cgrp (8 channels), run (4 consecutive tokens); sub-block = run / 4
+    const int cgrp = lane >> 4, run = lane & 15, sblk = run >> 2, s4 = run & 3;
+    const int c0 = warp * 16 + cgrp * 8;
+    const int kgrp = warp * 2 + cgrp;   // this thread's 4-channel group in each pass's compact K
+    uint4 qv[4], kv[4], gv[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = 4 * run + r;
+        if (t < L) {
+            const size_t off = ((size_t)(tok0 + t) * H + h) * D + c0;
+            qv[r] = ldg_nc16(p.q + off);
+            kv[r] = ldg_nc16(p.k + off);
+            gv[r] = ldg_nc16(p.g + off);
+        } else {
+            qv[r] = kv[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (tid < CH)
+        bt[tid] = tid < L ? sigmoid_fast(__bfloat162float(p.beta[(tok0 + tid) * H + h])) : 0.f;
+    const float eA = expf(p.A_log[h]);
+    float dtb[8];
+    {
+        const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0);
+        const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0 + 4);
+        dtb[0] = d0.x; dtb[1] = d0.y; dtb[2] = d0.z; dtb[3] = d0.w;
+        dtb[4] = d1.x; dtb[5] = d1.y; dtb[6] = d1.z; dtb[7] = d1.w;
+    }
+
+    // -------- phase 1: row norms of q and k
+    {
+        float *part = reinterpret_cast<float *>(sm + OFF_PART);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t qw[4] = {qv[r].x, qv[r].y, qv[r].z, qv[r].w};
+            const uint32_t kw[4] = {kv[r].x, kv[r].y, kv[r].z, kv[r].w};
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]), k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+                sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+                sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+            }
+            sq += __shfl_xor_sync(0xffffffffu, sq, 16);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 16);
+            if (cgrp == 0) {
+                part[(warp * 2) * CH + 4 * run + r] = sq;
+                part[(warp * 2 + 1) * CH + 4 * run + r] = sk;
+            }
+        }
+        __syncthreads();
+        if (tid < 2 * CH) {
+            const int t = tid & (CH - 1), which = tid >> 6;
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                s += part[(w * 2 + which) * CH + t];
+            (which ? rk : rq)[t] = rsqrtf(s + 1e-6f);
+        }
+        __syncthreads();
+    }
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t s_ops = smem_u32(sm + OFF_OPS);
+
+    // -------- phase 2: gate, decay factors and every per-token operand (two passes of 4 channels;
+    //          each pass fills one half of the channels of the Akk / Aqk operands, then the tensor
+    //          cores accumulate that half)
+    {
+        float rqt[4], rkt[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            rqt[r] = rq[4 * run + r];
+            rkt[r] = rk[4 * run + r];
+        }
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+            // alpha, inclusive prefix pf and exclusive suffix ef inside the 4-token run
+            float pf[4][4], ef[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t gw[2] = {hc ? gv[r].z : gv[r].x, hc ? gv[r].w : gv[r].y};
+                const bool valid = 4 * run + r < L;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float gval = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+                    const float sig = sigmoid_fast(eA * (gval + dtb[4 * hc + i]));
+                    ef[r][i] = valid ? ex2_approx(p.lb_log2e * sig) : 1.f;   // alpha (no decay past the end)
+                }
+            }
+            float X[4], Y[4], pre[4], post[4], gcv[4], f1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pf[0][i] = ef[0][i];
+#pragma unroll
+                for (int r = 1; r < 4; ++r)
+                    pf[r][i] = pf[r - 1][i] * ef[r][i];
+                float acc = 1.f;
+#pragma unroll
+                for (int r = 3; r >= 0; --r) {
+                    const float a = ef[r][i];
+                    ef[r][i] = acc;
+                    acc *= a;
+                }
+                const float Rt = acc;   // product over the run
+                // runs of one sub-block: lanes differing in bits 0..1
+                float inc = Rt, sinc = Rt, t1;
+                t1 = __shfl_up_sync(0xffffffffu, inc, 1, 4);
+                if (s4 >= 1) inc *= t1;
+                t1 = __shfl_up_sync(0xffffffffu, inc, 2, 4);
+                if (s4 >= 2) inc *= t1;
+                t1 = __shfl_down_sync(0xffffffffu, sinc, 1, 4);
+                if (s4 <= 2) sinc *= t1;
+                t1 = __shfl_down_sync(0xffffffffu, sinc, 2, 4);
+                if (s4 <= 1) sinc *= t1;
+                X[i] = __shfl_up_sync(0xffffffffu, inc, 1, 4);
+                if (s4 == 0) X[i] = 1.f;
+                Y[i] = __shfl_down_sync(0xffffffffu, sinc, 1, 4);
+                if (s4 == 3) Y[i] = 1.f;
+                const float Db = __shfl_sync(0xffffffffu, inc, (lane & ~3) | 3);
+                // sub-blocks: lanes differing in bits 2..3
+                float inc2 = Db, sinc2 = Db;
+                t1 = __shfl_up_sync(0xffffffffu, inc2, 4, 16);
+                if (sblk >= 1) inc2 *= t1;
+                t1 = __shfl_up_sync(0xffffffffu, inc2, 8, 16);
+                if (sblk >= 2) inc2 *= t1;
+                t1 = __shfl_down_sync(0xffffffffu, sinc2, 4, 16);
+                if (sblk <= 2) sinc2 *= t1;
+                t1 = __shfl_down_sync(0xffffffffu, sinc2, 8, 16);
+                if (sblk <= 1) sinc2 *= t1;
+                pre[i] = __shfl_up_sync(0xffffffffu, inc2, 4, 16);
+                if (sblk == 0) pre[i] = 1.f;
+                post[i] = __shfl_down_sync(0xffffffffu, sinc2, 4, 16);
+                if (sblk == 3) post[i] = 1.f;
+                gcv[i] = inc2;   // on the last sub-block: the whole chunk's decay
+                const float D1 = __shfl_sync(0xffffffffu, Db, (lane & ~12) | 4);
+                const float D2 = __shfl_sync(0xffffffffu, Db, (lane & ~12) | 8);
+                f1[i] = sblk == 0 ? D1 * D2 : (sblk == 1 ? D2 : 1.f);   // right factor, second anchor
+            }
+            const int cb = c0 + 4 * hc;
+            if (run == 15)
+                *reinterpret_cast<float4 *>(slot + SLOT_GC + cb * 4) = make_float4(gcv[0], gcv[1], gcv[2], gcv[3]);
+            // the previous pass's tensor-core product has read the operand tiles
+            if (hc == 1 && !mbar_wait(mbarA, 0))
+                hung = true;
+            uint32_t ktw[4][2];   // K~ for (channel i, tokens r = 0,1 / 2,3) as fp16 pairs
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * run + r;
+                const uint32_t qw[2] = {hc ? qv[r].z : qv[r].x, hc ? qv[r].w : qv[r].y};
+                const uint32_t kw[2] = {hc ? kv[r].z : kv[r].x, hc ? kv[r].w : kv[r].y};
+                float lq[4], lk[4], r0[4], r1[4], qt[4], kg[4], kt[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float qh = ((i & 1) ? bf16_hi(qw[i >> 1]) : bf16_lo(qw[i >> 1])) * rqt[r];
+                    const float kh = ((i & 1) ? bf16_hi(kw[i >> 1]) : bf16_lo(kw[i >> 1])) * rkt[r];
+                    const float P = X[i] * pf[r][i], E = ef[r][i] * Y[i];
+                    const bool even = (sblk & 1) == 0;
+                    const float rc = rcp_approx(even ? E : P);
+                    const float Lf = even ? rc : P;
+                    lq[i] = tf32r(qh * Lf);
+                    lk[i] = tf32r(kh * Lf);
+                    r1[i] = tf32r(kh * (sblk == 3 ? rc : E * f1[i]));
+                    r0[i] = tf32r(kh * (sblk == 0 ? E : rc));
+                    const float G = pre[i] * P;
+                    qt[i] = qh * G;
+                    kg[i] = kh * G;
+                    kt[i] = kh * (E * post[i]);
+                }
+                const int ra = (t >> 5) * 64 + (t & 31);
+                *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_A + ops_off(ra, kgrp)) =
+                    make_float4(lk[0], lk[1], lk[2], lk[3]);
+                *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_A + ops_off(ra + 32, kgrp)) =
+                    make_float4(lq[0], lq[1], lq[2], lq[3]);
+                *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_B + ops_off(32 + t, kgrp)) =
+                    make_float4(r1[0], r1[1], r1[2], r1[3]);
+                if (t < 32)
+                    *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_B + ops_off(t, kgrp)) =
+                        make_float4(r0[0], r0[1], r0[2], r0[3]);
+                *reinterpret_cast<uint2 *>(sm + OFF_KG + h128(t, cb)) =
+                    make_uint2(pack_half2(kg[0], kg[1]), pack_half2(kg[2], kg[3]));
+                *reinterpret_cast<uint2 *>(slot + qw_off(CH + t, cb)) =
+                    make_uint2(pack_half2(qt[0], qt[1]), pack_half2(qt[2], qt[3]));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const __half hv = __float2half_rn(kt[i]);
+                    const uint32_t bits = *reinterpret_cast<const uint16_t *>(&hv);
+                    if (r & 1)
+                        ktw[i][r >> 1] |= bits << 16;
+                    else
+                        ktw[i][r >> 1] = bits;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint2 *>(slot + ka_off(CH + cb + i, 4 * run)) = make_uint2(ktw[i][0], ktw[i][1]);
+            // this half of the channels: [Akk | Aqk] (+)= A B^T on the tensor cores
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_tf32_ss(tbase, umma_desc(s_ops + OPS_A + s * 2 * OPS_LBO, OPS_LBO, OPS_SBO),
+                                umma_desc(s_ops + OPS_B + s * 2 * OPS_LBO, OPS_LBO, OPS_SBO), idesc_tf32(128, 96),
+                                hc > 0 || s > 0);
+                umma_commit(mbarA);
+            }
+        }
+    }
+
+    // -------- phase 3: Akk / Aqk out of tensor memory.  Lanes 0..31 / 32..63: Akk / Aqk rows 0..31
+    //          (columns 0..31 = tokens 0..31); lanes 64..95 / 96..127: rows 32..63 (columns 32..95 =
+    //          tokens 0..63).  Aqk (causal) goes to the slot, b_i Akk (strictly lower) to shared memory.
+    if (!mbar_wait(mbarA, 1))
+        hung = true;
+    tc_fence_after();
+    {
+        const int q4 = warp & 3, hw = warp >> 2;
+        const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
+        float *Akk = reinterpret_cast<float *>(sm + OFF_AKK);
+        if (q4 < 2) {
+            const int i = lane, j0 = 16 * hw;
+            uint32_t u[16];
+            tmem_ld16(tl + j0, u);
+            if (q4 == 0) {
+                const float bi = bt[i];
+#pragma unroll
+                for (int e = 0; e < 16; e += 4) {
+                    float x[4];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        x[f] = j0 + e + f < i ? bi * __uint_as_float(u[e + f]) : 0.f;
+                    *reinterpret_cast<float4 *>(Akk + i * PA + j0 + e) = make_float4(x[0], x[1], x[2], x[3]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; e += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const int j = j0 + e + 2 * f;
+                        w[f] = pack_half2(j <= i ? __uint_as_float(u[e + 2 * f]) : 0.f,
+                                          j + 1 <= i ? __uint_as_float(u[e + 2 * f + 1]) : 0.f);
+                    }
+                    *reinterpret_cast<uint4 *>(slot + ka_off(i, j0 + e)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                // columns 32..63 of rows 0..31 are zero
+                *reinterpret_cast<uint4 *>(slot + ka_off(i, 32 + j0)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(slot + ka_off(i, 40 + j0)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        } else {
+            const int i = 32 + lane, j0 = 32 * hw;
+            uint32_t u[32];
+            tmem_ld32(tl + 32 + j0, u);
+            if (q4 == 2) {
+                const float bi = bt[i];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    float x[4];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        x[f] = j0 + e + f < i ? bi * __uint_as_float(u[e + f]) : 0.f;
+                    *reinterpret_cast<float4 *>(Akk + i * PA + j0 + e) = make_float4(x[0], x[1], x[2], x[3]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const int j = j0 + e + 2 * f;
+                        w[f] = pack_half2(j <= i ? __uint_as_float(u[e + 2 * f]) : 0.f,
+                                          j + 1 <= i ? __uint_as_float(u[e + 2 * f + 1]) : 0.f);
+                    }
+                    *reinterpret_cast<uint4 *>(slot + ka_off(i, j0 + e)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // -------- phase 4: Tm = (I + Akk)^-1, blocked by 16-token sub-blocks: fp32 forward
+    //          substitution on the diagonal blocks, then Tm_{bi,bj} = -Tm_{bi,bi} sum_m A_{bi,m} Tm_{m,bj}
+    //          by distance bi - bj on fp16 mma.sync (fp32 accumulation)
+    {
+        const float *Akk = reinterpret_cast<const float *>(sm + OFF_AKK);
+        float *Tm = reinterpret_cast<float *>(sm + OFF_TM);
+        if (warp < NSB && lane < SB) {
+            const int b = warp, j = lane;
+            float x[SB], acc[SB];
+#pragma unroll
+            for (int i = 0; i < SB; ++i)
+                acc[i] = 0.f;
+#pragma unroll
+            for (int l = 0; l < SB; ++l) {
+                x[l] = l == j ? 1.f : (l < j ? 0.f : -acc[l]);
+#pragma unroll
+                for (int i = l + 1; i < SB; ++i)
+                    acc[i] = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], acc[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < SB; ++i)
+                Tm[(b * SB + i) * PA + b * SB + j] = x[i];
+        }
+        __syncthreads();
+        const int gq = lane >> 2, t4 = lane & 3;
+        float *Zw = reinterpret_cast<float *>(sm + OFF_ZW) + warp * 128;   // [16][8]
+#pragma unroll 1
+        for (int dist = 1; dist < NSB; ++dist) {
+            if (warp < 2 * (NSB - dist)) {
+                const int bj = warp >> 1, nt = warp & 1, bi = bj + dist;
+                const int ra = bi * SB + gq, cn = bj * SB + nt * 8 + gq;
+                float z[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int m = bj; m < bi; ++m) {
+                    const int ka = m * SB + 2 * t4;
+                    const float2 a0 = *reinterpret_cast<const float2 *>(Akk + ra * PA + ka);
+                    const float2 a1 = *reinterpret_cast<const float2 *>(Akk + (ra + 8) * PA + ka);
+                    const float2 a2 = *reinterpret_cast<const float2 *>(Akk + ra * PA + ka + 8);
+                    const float2 a3 = *reinterpret_cast<const float2 *>(Akk + (ra + 8) * PA + ka + 8);
+                    const uint32_t af[4] = {pack_half2(a0.x, a0.y), pack_half2(a1.x, a1.y), pack_half2(a2.x, a2.y),
+                                            pack_half2(a3.x, a3.y)};
+                    const uint32_t b0 = pack_half2(Tm[ka * PA + cn], Tm[(ka + 1) * PA + cn]);
+                    const uint32_t b1 = pack_half2(Tm[(ka + 8) * PA + cn], Tm[(ka + 9) * PA + cn]);
+                    mma_f16(z, af, b0, b1);
+                }
+                // Z (16 x 8) through this warp's scratch into the B-operand layout
+                Zw[gq * 8 + 2 * t4] = z[0];
+                Zw[gq * 8 + 2 * t4 + 1] = z[1];
+                Zw[(gq + 8) * 8 + 2 * t4] = z[2];
+                Zw[(gq + 8) * 8 + 2 * t4 + 1] = z[3];
+                __syncwarp();
+                const int kd = bi * SB + 2 * t4;
+                const float2 d0 = *reinterpret_cast<const float2 *>(Tm + ra * PA + kd);
+                const float2 d1 = *reinterpret_cast<const float2 *>(Tm + (ra + 8) * PA + kd);
+                const float2 d2 = *reinterpret_cast<const float2 *>(Tm + ra * PA + kd + 8);
+                const float2 d3 = *reinterpret_cast<const float2 *>(Tm + (ra + 8) * PA + kd + 8);
+                const uint32_t df[4] = {pack_half2(d0.x, d0.y), pack_half2(d1.x, d1.y), pack_half2(d2.x, d2.y),
+                                        pack_half2(d3.x, d3.y)};
+                const uint32_t zb0 = pack_half2(Zw[(2 * t4) * 8 + gq], Zw[(2 * t4 + 1) * 8 + gq]);
+                const uint32_t zb1 = pack_half2(Zw[(2 * t4 + 8) * 8 + gq], Zw[(2 * t4 + 9) * 8 + gq]);
+                float tt[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16(tt, df, zb0, zb1);
+                const int cc = bj * SB + nt * 8 + 2 * t4;
+                *reinterpret_cast<float2 *>(Tm + ra * PA + cc) = make_float2(-tt[0], -tt[1]);
+                *reinterpret_cast<float2 *>(Tm + (ra + 8) * PA + cc) = make_float2(-tt[2], -tt[3]);
+            }
+            __syncthreads();
+        }
+        // T' = Tm diag(b), fp16 [t][j]; blocks above the diagonal are zero
+#pragma unroll
+        for (int m = 0; m < (CH * CH / 8) / PREP_THREADS; ++m) {
+            const int idx = tid + m * PREP_THREADS, r = idx >> 3, c = (idx & 7) * 8;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int ca = c + 2 * e, cbb = ca + 1;
+                const float x0 = (ca >> 4) <= (r >> 4) ? Tm[r * PA + ca] * bt[ca] : 0.f;
+                const float x1 = (cbb >> 4) <= (r >> 4) ? Tm[r * PA + cbb] * bt[cbb] : 0.f;
+                w[e] = pack_half2(x0, x1);
+            }
+            *reinterpret_cast<uint4 *>(sm + OFF_TP + h64(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // -------- phase 5: W = T' (K^.Gamma) and U0^T = V^T T'^T (fp16 mma.sync), to the slot
+    {
+        const uint32_t s_tp = smem_u32(sm + OFF_TP), s_kg = smem_u32(sm + OFF_KG), s_v = smem_u32(sm + OFF_V);
+        const int gq = lane >> 2, t4 = lane & 3;
+        const int lr = lane & 7, lsel = lane >> 3;   // ldmatrix: row within a matrix, matrix index
+        // W: rows t of m-tile (warp & 3), channels of n-tiles 8 (warp >> 2) .. + 7
+        {
+            const int mt = warp & 3, nt0 = (warp >> 2) * 8;
+            float acc[8][4];
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+                acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < CH / 16; ++ks) {
+                uint32_t af[4];
+                ldsm_x4(s_tp + h64(mt * 16 + (lsel & 1) * 8 + lr, ks * 16 + (lsel >> 1) * 8), af);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bf[4];
+                    const int nt = nt0 + 2 * np + (lsel >> 1);
+                    ldsm_x4_t(s_kg + h128(ks * 16 + (lsel & 1) * 8 + lr, nt * 8), bf);
+                    mma_f16(acc[2 * np], af, bf[0], bf[1]);
+                    mma_f16(acc[2 * np + 1], af, bf[2], bf[3]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = mt * 16 + gq + 8 * hh, c = (nt0 + a) * 8 + 2 * t4;
+                    *reinterpret_cast<uint32_t *>(slot + qw_off(t, c)) = pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
+                }
+        }
+        // U0^T: value rows 16 warp .. + 15, all 64 tokens
+        {
+            float acc[8][4];
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+                acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < CH / 16; ++ks) {
+                uint32_t af[4];
+                // A = V^T: matrices (v 0-7, j 0-7), (v 8-15, j 0-7), (v 0-7, j 8-15), (v 8-15, j 8-15)
+                ldsm_x4_t(s_v + h128(ks * 16 + (lsel >> 1) * 8 + lr, warp * 16 + (lsel & 1) * 8), af);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    af[e] = bf16x2_to_half2(af[e]);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bf[4];
+                    // B = T'^T: matrices (t-tile 2np, j 0-7), (2np, j 8-15), (2np+1, j 0-7), (2np+1, j 8-15)
+                    ldsm_x4(s_tp + h64((2 * np + (lsel >> 1)) * 8 + lr, ks * 16 + (lsel & 1) * 8), bf);
+                    mma_f16(acc[2 * np], af, bf[0], bf[1]);
+                    mma_f16(acc[2 * np + 1], af, bf[2], bf[3]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int vr = warp * 16 + gq + 8 * hh, t = a * 8 + 2 * t4;
+                    *reinterpret_cast<uint32_t *>(slot + u0_off(vr, t)) = pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
+                }
+        }
+    }
+
+    // -------- release tensor memory; report a bounded wait that gave up
+    if (hung && lane == 0)
+        atomicOr(&g_kda_prep_error, 1u);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS));
+    }
+}
+
+template <bool VARLEN>
+cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
+{
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev >= 64 || !configured[dev]) {
+        err = cudaFuncSetAttribute(kda_prep_kernel<VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+        if (err != cudaSuccess)
+            return err;
+        if (dev < 64)
+            configured[dev] = true;
+    }
+    kda_prep_kernel<VARLEN><<<(unsigned)items, PREP_THREADS, PREP_SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t stream)
+{
+    const int64_t items = max_chunks * p.H;
+    if (items <= 0)
+        return cudaSuccess;
+    if (items > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    return p.cu ? launch_prep_t<true>(p, items, stream) : launch_prep_t<false>(p, items, stream);
+}
+
+size_t prep_smem_bytes() { return PREP_SMEM; }
+
+cudaError_t prep_read_and_clear_error(unsigned int *flag)
+{
+    unsigned int zero = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(flag, g_kda_prep_error, sizeof *flag);
+    if (err == cudaSuccess && *flag)
+        err = cudaMemcpyToSymbol(g_kda_prep_error, &zero, sizeof zero);
+    return err;
+}
+
+}  // namespace kda

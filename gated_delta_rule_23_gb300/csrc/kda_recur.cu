@@ -1,0 +1,364 @@
+// KDA recurrence kernel: the head-parallel chunk-wise delta-rule recurrence (the second stage
+// of the guancyxx.cn FlashKDA article, section 2.2), one CTA per (sequence, head).
+//
+// Per 64-token chunk, with the operands the prep kernel left in the chunk's slot:
+//   U = U0 - W S,   O = scale (Q~ S + Aqk U),   S <- Diag(Gamma_C) S + K~^T U.
+// Everything runs transposed on the 5th-generation tensor cores with the value dimension on the
+// 128 tensor-memory lanes (M = 128) and fp32 accumulators:
+//   [X^T | O'^T] = S^T [W ; Q~]^T               (A = S^T as fp16 in tensor memory, K = 128)
+//   U^T = U0^T - X^T                            (threads; fp16 into tensor memory)
+//   [O^T | S^T] += U^T [Aqk ; K~^T]^T           (A = U^T, K = 64; S^T decayed beforehand)
+// The fp32 master state S^T never leaves tensor memory; an fp16 copy of it is the A operand of
+// the first product.  The slot of chunk c + 1 is bulk-copied into shared memory while chunk c
+// runs.
+//
+// Tensor-memory columns: X^T 0..63 | O^T 64..127 | S^T 128..255 | fp16 S^T 256..319 |
+// fp16 U^T 320..351 (512 allocated).
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+// Set when a bounded wait on the tensor cores or a bulk copy expires (read by kda_device_status).
+__device__ unsigned int g_kda_device_error;
+
+namespace kda {
+namespace {
+
+constexpr int RT = 256;                     // threads: warp w reads lanes 32 (w % 4) .. + 31
+constexpr int TMEM_COLS = 512;
+constexpr int TM_X = 0, TM_O = 64, TM_S = 128, TM_S16 = 256, TM_U16 = 320;
+constexpr int PH = 136;                     // bf16 pitch of the output staging tile
+constexpr int OFF_BUF0 = 0;
+constexpr int OFF_BUF1 = SLOT_BYTES;
+constexpr int OFF_OST = 2 * SLOT_BYTES;     // bf16 [64 t][136] output staging
+constexpr int OFF_BAR = OFF_OST + CH * PH * 2;
+constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load0, load1, product X|O, update; tmem slot; flag
+static_assert(RECUR_SMEM <= 232448, "shared memory budget");
+static_assert(OFF_BUF1 % 128 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+
+template <int STATE, bool VARLEN>  // STATE: 0 none, 1 bf16, 2 fp32
+__global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
+{
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H;
+    const int h = blockIdx.x % H;
+    int n = blockIdx.x / H;
+    if (VARLEN && p.order)
+        n = p.order[n];   // longest sequences first
+    int64_t bos, len, slot0;
+    if (VARLEN) {
+        bos = p.cu[n];
+        len = p.cu[n + 1] - bos;
+        slot0 = p.chunk_off[n];
+    } else {
+        bos = (int64_t)n * p.T;
+        len = p.T;
+        slot0 = (int64_t)n * p.nch_fixed;
+    }
+    const int nch = (int)((len + CH - 1) / CH);
+
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 32);
+    volatile uint32_t *hang_flag = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 36);
+    const uint32_t mbarL0 = smem_u32(sm + OFF_BAR), mbarL1 = smem_u32(sm + OFF_BAR + 8);
+    const uint32_t mbarQ = smem_u32(sm + OFF_BAR + 16), mbarB = smem_u32(sm + OFF_BAR + 24);
+    auto slot_ptr = [&](int c) -> const unsigned char * {
+        return p.slots + (size_t)((slot0 + c) * H + h) * SLOT_BYTES;
+    };
+    auto issue_load = [&](int c) {   // one thread: the whole slot of chunk c into buffer c % 2
+        const uint32_t mb = (c & 1) ? mbarL1 : mbarL0;
+        mbar_expect_tx(mb, SLOT_BYTES);
+        bulk_g2s(smem_u32(sm + ((c & 1) ? OFF_BUF1 : OFF_BUF0)), slot_ptr(c), SLOT_BYTES, mb);
+    };
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        mbar_init(mbarL0, 1);
+        mbar_init(mbarL1, 1);
+        mbar_init(mbarQ, 1);
+        mbar_init(mbarB, 1);
+        *hang_flag = 0u;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    int loads_issued = 0;
+    if (tid == 0) {
+        if (nch > 0) issue_load(0);
+        if (nch > 1) issue_load(1);
+    }
+    loads_issued = nch < 2 ? nch : 2;
+
+    const int q4 = warp & 3, half = warp >> 2;
+    const int vrow = q4 * 32 + lane;
+    const uint32_t trow = tbase + ((uint32_t)(q4 * 32) << 16);
+    const size_t srow = ((size_t)n * H + h) * D * D + (size_t)vrow * D + half * 64;
+
+    // -------- initial state -> S^T (row v, key columns 64 half .. + 63)
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        uint32_t u[32];
+        if (STATE == 2 && p.init) {
+            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + srow + 32 * part);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 x = src[e];
+                u[4 * e] = __float_as_uint(x.x);
+                u[4 * e + 1] = __float_as_uint(x.y);
+                u[4 * e + 2] = __float_as_uint(x.z);
+                u[4 * e + 3] = __float_as_uint(x.w);
+            }
+        } else if (STATE == 1 && p.init) {
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.init) + srow + 32 * part);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint4 x = src[e];
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    u[8 * e + 2 * f] = w4[f] << 16;
+                    u[8 * e + 2 * f + 1] = w4[f] & 0xffff0000u;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                u[e] = 0u;
+        }
+        tmem_st32(trow + TM_S + half * 64 + 32 * part, u);
+    }
+    tc_fence_before();
+
+    __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST);
+    // O^T of the chunk just updated -> bf16 staging tile [t][v] (this thread: tokens 32 half .. + 31)
+    auto read_out = [&]() {
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + half * 32, o);
+#pragma unroll
+        for (int m = 0; m < 32; ++m)
+            Ost[(half * 32 + m) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[m]) * p.scale);
+    };
+    auto store_out = [&](int64_t ptok0, int pL) {
+#pragma unroll
+        for (int m = 0; m < (CH * 16) / RT; ++m) {
+            const int idx = tid + m * RT, r = idx >> 4, c16 = idx & 15;
+            if (r < pL)
+                *reinterpret_cast<uint4 *>(p.out + ((ptok0 + r) * H + h) * D + c16 * 8) =
+                    *reinterpret_cast<const uint4 *>(sm + OFF_OST + r * PH * 2 + c16 * 16);
+        }
+    };
+
+    bool hung = false;
+    int nq = 0, nb = 0;   // commits issued on mbarQ / mbarB (same count in every thread)
+    int64_t prev_tok0 = 0;
+    int prev_L = 0;
+    int c = 0;
+    for (; c < nch; ++c) {
+        const int buf = c & 1;
+        const unsigned char *sb = sm + (buf ? OFF_BUF1 : OFF_BUF0);
+        const uint32_t s_buf = smem_u32(sb);
+        const int64_t tok0 = bos + (int64_t)c * CH;
+        const int64_t rem = len - (int64_t)c * CH;
+        const int L = (int)(rem < CH ? rem : CH);
+
+        // the previous update is complete and this chunk's slot has landed
+        bool ok = true;
+        if (c > 0)
+            ok = mbar_wait(mbarB, (c - 1) & 1);
+        ok = ok && mbar_wait(buf ? mbarL1 : mbarL0, (c >> 1) & 1);
+        if (__syncthreads_or(!ok)) {
+            hung = true;
+            break;
+        }
+        tc_fence_after();
+        if (tid == 0 && c >= 1 && c + 1 < nch) {
+            fence_async_smem();   // the other buffer's last readers finished before the barrier above
+            issue_load(c + 1);
+        }
+        if (c >= 1 && c + 1 < nch)
+            ++loads_issued;
+
+        // ---- P1: fp16 copy of S^T (A operand), S^T <- S^T Diag(Gamma_C), previous output read-out
+        {
+            const float *gam = reinterpret_cast<const float *>(sb + SLOT_GC) + half * 64;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                uint32_t u[32], hv[16];
+                tmem_ld32(trow + TM_S + half * 64 + 32 * part, u);
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    hv[m] = pack_half2(__uint_as_float(u[2 * m]), __uint_as_float(u[2 * m + 1]));
+                tmem_st16(trow + TM_S16 + half * 32 + 16 * part, hv);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[32 * part + e]);
+                tmem_st32(trow + TM_S + half * 64 + 32 * part, u);
+            }
+            if (c > 0)
+                read_out();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s)
+                mma_f16_ts(tbase + TM_X, tbase + TM_S16 + 8 * s,
+                           umma_desc(s_buf + SLOT_QW + s * 2 * CORE_LBO, CORE_LBO, QW_SBO), idesc_f16(128, 128), s > 0);
+            umma_commit(mbarQ);
+        }
+        ++nq;
+        if (c > 0)
+            store_out(prev_tok0, prev_L);
+
+        // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
+        ok = mbar_wait(mbarQ, c & 1);
+        if (__syncthreads_or(!ok)) {
+            hung = true;
+            break;
+        }
+        tc_fence_after();
+        {
+            uint32_t x[32], hv[16];
+            tmem_ld32(trow + TM_X + half * 32, x);
+            const unsigned char *u0row = sb + SLOT_U0 + vrow * (CH * 2);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(u0row + (((half * 4 + m) ^ (vrow & 7)) << 4));
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
+                    hv[4 * m + e] = pack_half2(f.x - __uint_as_float(x[8 * m + 2 * e]),
+                                               f.y - __uint_as_float(x[8 * m + 2 * e + 1]));
+                }
+            }
+            tmem_st16(trow + TM_U16 + half * 16, hv);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < CH / 16; ++s)
+                mma_f16_ts(tbase + TM_O, tbase + TM_U16 + 8 * s,
+                           umma_desc(s_buf + SLOT_KA + s * 2 * CORE_LBO, CORE_LBO, KA_SBO), idesc_f16(128, 64 + D), 1);
+            umma_commit(mbarB);
+        }
+        ++nb;
+        prev_tok0 = tok0;
+        prev_L = L;
+    }
+
+    if (!hung && nch > 0) {
+        const bool ok = mbar_wait(mbarB, (nch - 1) & 1);
+        if (__syncthreads_or(!ok)) {
+            hung = true;
+        } else {
+            tc_fence_after();
+            read_out();
+            __syncthreads();
+            store_out(prev_tok0, prev_L);
+        }
+    }
+
+    // -------- final state, release
+    if (hung) {
+        // let tensor-core work and bulk copies still in flight finish (bounded) before leaving
+        if (tid == 0) {
+            if (nq > 0)
+                mbar_wait(mbarQ, (nq - 1) & 1);
+            if (nb > 0)
+                mbar_wait(mbarB, (nb - 1) & 1);
+            for (int k = c; k < loads_issued; ++k)
+                mbar_wait((k & 1) ? mbarL1 : mbarL0, (k >> 1) & 1);
+            atomicOr(&g_kda_device_error, 1u);
+        }
+    } else if (STATE != 0 && p.fin) {
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            uint32_t u[32];
+            tmem_ld32(trow + TM_S + half * 64 + 32 * part, u);
+            if (STATE == 2) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.fin) + srow + 32 * part);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                         __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.fin) + srow + 32 * part);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(u[8 * e + 2 * f]),
+                                                                  __uint_as_float(u[8 * e + 2 * f + 1]));
+                        w4[f] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS));
+    }
+}
+
+template <int STATE, bool VARLEN>
+cudaError_t launch_recur_t(const Problem &p, int grid, cudaStream_t stream)
+{
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev >= 64 || !configured[dev]) {
+        err = cudaFuncSetAttribute(kda_recur_kernel<STATE, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   RECUR_SMEM);
+        if (err != cudaSuccess)
+            return err;
+        if (dev < 64)
+            configured[dev] = true;
+    }
+    kda_recur_kernel<STATE, VARLEN><<<grid, RT, RECUR_SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream)
+{
+    const int grid = p.N * p.H;
+    if (p.cu)
+        return state_kind == 2 ? launch_recur_t<2, true>(p, grid, stream)
+             : state_kind == 1 ? launch_recur_t<1, true>(p, grid, stream)
+                               : launch_recur_t<0, true>(p, grid, stream);
+    return state_kind == 2 ? launch_recur_t<2, false>(p, grid, stream)
+         : state_kind == 1 ? launch_recur_t<1, false>(p, grid, stream)
+                           : launch_recur_t<0, false>(p, grid, stream);
+}
+
+size_t recur_smem_bytes() { return RECUR_SMEM; }
+
+cudaError_t read_and_clear_device_error(unsigned int *flag)
+{
+    unsigned int zero = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(flag, g_kda_device_error, sizeof *flag);
+    if (err == cudaSuccess && *flag)
+        err = cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof zero);
+    return err;
+}
+
+}  // namespace kda

@@ -28,17 +28,24 @@
  *   cu_seqlens      : int64 [N + 1], cumulative sequence lengths (varlen mode)
  *
  * Ownership: the caller allocates and owns every buffer, including out and
- * final_state.  The library allocates no memory and keeps no state beyond a
- * per-device "attributes set" flag.  Calls are asynchronous on `stream`; results
- * are valid once the stream has been synchronised.  initial_state may equal
- * final_state (in-place update).  Calls on different streams may run concurrently
- * if their output buffers do not overlap.
+ * final_state.  kda_fwd takes its scratch workspace (the per-chunk operands passed from
+ * the prep kernel to the recurrence kernel, kda_fwd_workspace_size bytes) from a
+ * stream-ordered memory pool that the library owns, one per device, and returns it on
+ * the same stream; the pool keeps the memory for later calls until kda_workspace_trim.
+ * kda_fwd_ws takes a caller-owned workspace instead.  Calls are asynchronous on
+ * `stream`; results are valid once the stream has been synchronised.  initial_state may
+ * equal final_state (in-place update).  Calls on different streams may run
+ * concurrently if their output buffers (and kda_fwd_ws workspaces) do not overlap.
  *
- * Numerics: the kernel evaluates the chunked form of the recurrence (32-token
- * chunks, 16-token decay sub-blocks) with fp32 accumulation; the state is held in
- * fp32 (tensor memory) for the whole call.  Tensor-core operands are tf32 (fp32
- * range) except the small T'.(K^ . Gamma) product, whose operands are bounded by 1
- * in magnitude for any input and use fp16.
+ * Numerics: the chunked form of the recurrence (64-token chunks, 16-token decay
+ * sub-blocks).  A prep kernel computes, for every chunk in parallel, the gate, the L2
+ * norms, the decay factors, the strictly-lower beta K K^T and causal Q K^T matrices
+ * (tf32 tensor-core products of factors in fp32 range), the (I + A)^-1 inverse (fp32)
+ * and the WY products, and stores the recurrence operands in fp16 (each bounded by 1 in
+ * magnitude except T' V and T' (K^ . Gamma), which are delta-rule residuals of the
+ * inputs).  A recurrence kernel then runs the chunk-to-chunk state update on the tensor
+ * cores with fp16 operands and fp32 accumulation; the state itself stays fp32 for the
+ * whole call.  States and outputs therefore need |values| well below 6.5e4.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -102,6 +109,31 @@ kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g,
                      kda_stream_t stream);
 
 /*
+ * Bytes of workspace kda_fwd_ws needs for this problem size (an upper bound that depends
+ * only on N, T, H and whether cu_seqlens is given: varlen != 0).  0 for invalid sizes.
+ */
+size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen);
+
+/*
+ * kda_fwd_ws -- kda_fwd with a caller-owned device workspace of at least
+ * kda_fwd_workspace_size(N, T, H, cu_seqlens != NULL) bytes, 256-byte aligned (it may be
+ * NULL when that size is 0).  The workspace must not be used by anything else until the
+ * call has completed on `stream`.  Same arguments, results and errors as kda_fwd, plus
+ * KDA_ERR_INVALID_ARGUMENT for a missing, misaligned or too small workspace.
+ */
+kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                        float scale, void *out, const float *A_log, const float *dt_bias,
+                        float lower_bound, const void *initial_state, void *final_state,
+                        kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                        void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * Returns the workspace memory kda_fwd's pools hold but no call is using to the driver.
+ * KDA_ERR_CUDA if a pool could not be trimmed.
+ */
+kda_status_t kda_workspace_trim(void);
+
+/*
  * Host-side check of a cu_seqlens array (host pointer, N + 1 entries) against the
  * contract above.  Returns KDA_OK or KDA_ERR_INVALID_ARGUMENT.  No CUDA calls.
  */
@@ -118,7 +150,7 @@ const char *kda_status_string(kda_status_t status);
  */
 kda_status_t kda_device_status(kda_stream_t stream);
 
-/* Bytes of dynamic shared memory one CTA of the forward kernel uses (for diagnostics). */
+/* Largest dynamic shared memory one CTA of the forward kernels uses (for diagnostics). */
 size_t kda_fwd_smem_bytes(void);
 
 #ifdef __cplusplus

@@ -17,8 +17,8 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = _native.declared_functions()
-    assert {"kda_fwd", "kda_check_cu_seqlens", "kda_status_string", "kda_fwd_smem_bytes",
-            "kda_device_status"} <= set(names)
+    assert {"kda_fwd", "kda_fwd_ws", "kda_fwd_workspace_size", "kda_workspace_trim", "kda_check_cu_seqlens",
+            "kda_status_string", "kda_fwd_smem_bytes", "kda_device_status"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -53,7 +53,7 @@ def call(lib, **kw):
     dict(N=0), dict(H=0), dict(T=-1), dict(N=1 << 20, H=1 << 12),
     dict(q=A + 8), dict(out=A + 0x5002), dict(beta=A + 0x4001), dict(cu=A + 0x9004),
     dict(init=A + 0x8000, state_dtype=KDA_DTYPE_NONE), dict(fin=A + 0x8000, state_dtype=7),
-    dict(init=A + 0x8008, state_dtype=KDA_DTYPE_FP32),
+    dict(init=A + 0x8008, state_dtype=KDA_DTYPE_FP32), dict(dt_bias=A + 0x7004),
 ])
 def test_invalid_arguments_rejected(lib, kw):
     assert call(lib, **kw) == KDA_ERR_INVALID_ARGUMENT
@@ -87,3 +87,23 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         kda_fwd(x, x, x, x, torch.zeros(1, 4, 1, dtype=torch.bfloat16), 1.0, x.clone(),
                 torch.zeros(1), torch.zeros(1, 128), -5.0)
+
+
+def test_workspace_size(lib):
+    slot = 74240   # fp16 operands of one (64-token chunk, head)
+    assert lib.kda_fwd_workspace_size(1, 8192, 96, 0) == 128 * 96 * slot
+    assert lib.kda_fwd_workspace_size(2, 65, 3, 0) == 2 * 2 * 3 * slot
+    assert lib.kda_fwd_workspace_size(1, 0, 4, 0) == 0
+    # varlen: a header (chunk offsets, order), then at most (T + 63 N) / 64 chunks
+    hdr = -(-(9 * 8 + 8 * 4) // 256) * 256
+    assert lib.kda_fwd_workspace_size(8, 8192, 96, 1) == hdr + (8192 + 63 * 8) // 64 * 96 * slot
+    assert lib.kda_fwd_workspace_size(0, 10, 1, 0) == 0
+
+
+def test_ws_entry_rejects_missing_workspace(lib):
+    args = [A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 0.1, A + 0x5000, A + 0x6000, A + 0x7000, -5.0,
+            None, None, KDA_DTYPE_NONE, None, 1, 64, 2]
+    need = lib.kda_fwd_workspace_size(1, 64, 2, 0)
+    assert lib.kda_fwd_ws(*args, None, need, None) == KDA_ERR_INVALID_ARGUMENT
+    assert lib.kda_fwd_ws(*args, A + 0x100000, need - 16, None) == KDA_ERR_INVALID_ARGUMENT
+    assert lib.kda_fwd_ws(*args, A + 0x100010, need, None) == KDA_ERR_INVALID_ARGUMENT   # not 256-byte aligned
