@@ -3,8 +3,9 @@
 
 Default workload: fixed-length prefill, B = 1, T = 8192, H = 96, K = V = 128, bf16
 initial and final state (the H = 96 fixed-length row of the FlashKDA benchmark
-tables).  One step = one kda_fwd launch over the whole workload.  Inputs (1.0 GB)
-exceed the 129 MB L2, so no flush is needed between steps.
+tables).  One step = one kda_fwd call over the whole workload: the prep kernel (all chunks
+in parallel) and the recurrence kernel (plus a one-CTA plan kernel with cu_seqlens).
+Inputs (1.0 GB) exceed the 129 MB L2, so no flush is needed between steps.
 
 Prints one JSON line.  `--impl reference` times the fp64 CPU oracle instead (the
 reference arm for this method: a deliberately plain program on the host cores).
@@ -36,7 +37,8 @@ from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, WORKLOADS, 
 METRIC = "KDA fwd ms & tokens·heads/s at T=8192 H=96; % of HBM/tensor roofline"
 UNIT = "tokens·heads/s"
 KERNEL_DIR = os.path.join(ROOT, "gated_delta_rule_23_gb300", "csrc")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kda_fwd_kernel_T8192_H96_bf16state.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kda_prep_recur_T8192_H96_bf16state.md")
+SLOT_BYTES_PER_CHUNK_HEAD = 74240   # fp16 operands the prep kernel hands to the recurrence kernel per (64-token chunk, head)
 # FlashKDA on GB200, H=96 fixed length, T=8192: 1.01 ms (guancyxx.cn FlashKDA article, section 三,
 # GB200 table) -> tokens*heads per second.  Another machine: context, not the target.
 PAGES_GB200_TOKHEADS_PER_S = 8192 * 96 / 1.01e-3
@@ -63,6 +65,19 @@ def algorithmic_bytes(p):
     return b
 
 
+def kernel_bytes(p):
+    """HBM bytes each kernel must move in this design (the workspace slots count here, not in the path)."""
+    th = p.token_heads()
+    es = {STATE_BF16: 2, STATE_FP32: 4}.get(p.state_dtype, 0)
+    per_state = p.N * p.H * 128 * 128 * es
+    states = per_state * ((p.initial_state is not None) + bool(p.want_final and es))
+    lengths = p.seq_lengths()
+    slots = int(sum((int(n) + 63) // 64 for n in lengths)) * p.H * SLOT_BYTES_PER_CHUNK_HEAD
+    prep = th * (4 * 128 * 2 + 2) + slots + p.H * (4 + 128 * 4)
+    recur = slots + th * 128 * 2 + states
+    return {"kda_prep_kernel": prep, "kda_recur_kernel": recur}
+
+
 def kernel_source_hash():
     """Hash of every CUDA source of the library (the profile summary is valid only for these)."""
     h = hashlib.sha256()
@@ -73,14 +88,14 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(p):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel."""
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if taken on the current sources."""
     try:
         text = open(PROFILE_SUMMARY).read()
     except OSError:
         return None
     m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+    m_tr = re.search(kernel + r" traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
     if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
         return None
     return float(m_tr.group(1))
@@ -269,10 +284,30 @@ def run_ours(args, p, idx, rank, world):
     sampler.mark(t_host0, t_host1)
     sampler.stop()
     ms_step = ms_total / args.steps
+
+    # per-kernel breakdown: the same calls through kda_fwd_ws_profiled, which records events at the
+    # kernel boundaries on the launching stream
+    from gated_delta_rule_23_gb300 import workspace_size
+    ws = torch.empty(workspace_size(p.N, p.T, p.H, p.cu_seqlens is not None), dtype=torch.uint8, device="cuda")
+    n_prof = max(3, min(args.steps, 100))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_prof)]
+    for trio in evs:
+        for e in trio:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for trio in evs:
+        kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+                p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], stream=stream,
+                workspace=ws, stage_events=trio)
+    torch.cuda.synchronize()
+    kernel_ms = {"kda_prep_kernel": statistics.mean(t[0].elapsed_time(t[1]) for t in evs),
+                 "kda_recur_kernel": statistics.mean(t[1].elapsed_time(t[2]) for t in evs)}
+    del ws
     if args.kernel_only:
         if rank == 0:
             print(json.dumps({"kernel_only": True, "ms_per_step": ms_step, "T": p.T, "H": p.H,
-                              "algorithmic_bytes_per_launch": algorithmic_bytes(p)}), flush=True)
+                              "algorithmic_bytes_per_launch": algorithmic_bytes(p), "kernel_ms": kernel_ms}),
+                  flush=True)
         return
 
     # end to end through the public API with host buffers (copies inside the timed region)
@@ -308,8 +343,14 @@ def run_ours(args, p, idx, rank, world):
     th = p.token_heads() * world
     hbm, tc, peak_src = peaks()
     abytes = algorithmic_bytes(p)
-    achieved = abytes / (ms_step * 1e-3) / 1e9
-    traffic = measured_traffic(p)
+    kbytes = kernel_bytes(p)
+    kernels = {}
+    for name, kms in kernel_ms.items():
+        ach = kbytes[name] / (kms * 1e-3) / 1e9
+        kernels[name] = {"ms": kms, "bytes_per_launch": kbytes[name], "achieved": ach, "frac": ach / hbm,
+                         "traffic": measured_traffic(name)}
+    dom = max(kernel_ms, key=kernel_ms.get)
+    achieved = kernels[dom]["achieved"]
     line = {
         "metric": METRIC, "value": th / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -317,16 +358,20 @@ def run_ours(args, p, idx, rank, world):
         "dtype": "bf16", "precision": "bf16 inputs/outputs; tf32 and fp16 tensor-core operands; fp32 accumulation "
                                       "and fp32 state master",
         "data": "synthetic", "config": workload_config(p, idx),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
-                     "algorithmic_bytes_per_launch": abytes, "kernel": "kda_fwd_kernel",
-                     "roofline_ms": abytes / (hbm * 1e9) * 1e3},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": kernels[dom]["traffic"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                     "kernel_bytes_per_launch": kbytes[dom], "kernels": kernels,
+                     "path": {"algorithmic_bytes_per_launch": abytes, "ms": ms_step,
+                              "achieved": abytes / (ms_step * 1e-3) / 1e9,
+                              "frac": abytes / (ms_step * 1e-3) / 1e9 / hbm,
+                              "roofline_ms": abytes / (hbm * 1e9) * 1e3}},
         "cpu_baseline": cpu_baseline(p, idx),
         "e2e": {"value": th / world / (e2e_ms * 1e-3) * world, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": runner.h2d_bytes(p.cu_seqlens is not None),
                 "d2h_bytes_per_step": runner.d2h_bytes()},
         "clocks": sampler.summary(),
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (3 if p.cu_seqlens is not None else 2),
     }
     print(json.dumps(line), flush=True)
 

@@ -4,6 +4,6 @@ The computation lives in libkda.so (csrc/kda_fwd.cu, C ABI in include/kda.h);
 this package builds and loads it and marshals arguments.  There is no CPU path.
 """
 from ._native import KDAError, build, load  # noqa: F401
-from .api import KDAHostRunner, device_status, kda_fwd  # noqa: F401
+from .api import KDAHostRunner, device_status, kda_fwd, workspace_size  # noqa: F401
 
-__all__ = ["kda_fwd", "device_status", "KDAHostRunner", "KDAError", "build", "load"]
+__all__ = ["kda_fwd", "workspace_size", "device_status", "KDAHostRunner", "KDAError", "build", "load"]

@@ -79,6 +79,9 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd.restype = I
         lib.kda_fwd_ws.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t, P]
         lib.kda_fwd_ws.restype = I
+        lib.kda_fwd_ws_profiled.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t,
+                                             P, P]
+        lib.kda_fwd_ws_profiled.restype = I
         lib.kda_fwd_workspace_size.argtypes = [I, I64, I, I]
         lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_workspace_trim.argtypes = []

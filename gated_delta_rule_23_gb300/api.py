@@ -7,6 +7,7 @@ libkda.so.  PyTorch is used only to hold device memory and to name the stream.
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional
 
 import torch
@@ -35,13 +36,18 @@ def _ptr(t: Optional[torch.Tensor]):
 def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
             scale: float, out: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, lower_bound: float,
             initial_state: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
-            cu_seqlens: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> None:
+            cu_seqlens: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+            workspace: Optional[torch.Tensor] = None, stage_events=None) -> None:
     """KDA chunked forward on CUDA tensors; writes ``out`` and ``final_state`` in place.
 
     q, k, v, g: bf16 [B, T, H, 128]; beta: bf16 [B, T, H]; out: bf16 [B, T, H, 128];
     A_log: fp32 [H]; dt_bias: fp32 [H, 128]; states: bf16 or fp32 [N, H, 128, 128] (same dtype
     when both are given); cu_seqlens: int64 [N + 1] with B = 1.  Runs asynchronously on
-    ``stream`` (default: the current stream).
+    ``stream`` (default: the current stream).  ``workspace``: optional uint8 CUDA tensor of at
+    least ``workspace_size(...)`` bytes (kda_fwd_ws); without it the library's pool provides one.
+    ``stage_events``: optional three recorded-once torch.cuda.Event objects marking the start of
+    the prep kernel, the prep/recurrence boundary and the end (kda_fwd_ws_profiled; needs
+    ``workspace``).
     """
     lib = _native.load()
     if q.dim() != 4 or q.shape[-1] != D:
@@ -75,12 +81,30 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         _check(t, name, sd, (N, H, D, D), dev)
     state_dtype = KDA_DTYPE_NONE if sd is None else (KDA_DTYPE_BF16 if sd == torch.bfloat16 else KDA_DTYPE_FP32)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log), _ptr(dt_bias),
+            float(lower_bound), _ptr(initial_state), _ptr(final_state), state_dtype, _ptr(cu_seqlens), int(N),
+            int(T), int(H))
+    if workspace is not None:
+        if workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+        wsz = workspace.numel()
+    elif stage_events is not None:
+        raise ValueError("stage_events needs a workspace")
     with torch.cuda.device(dev):
-        rc = lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log),
-                         _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _ptr(final_state), state_dtype,
-                         _ptr(cu_seqlens), int(N), int(T), int(H), s.cuda_stream)
+        if workspace is None:
+            rc = lib.kda_fwd(*args, s.cuda_stream)
+        elif stage_events is None:
+            rc = lib.kda_fwd_ws(*args, _ptr(workspace), wsz, s.cuda_stream)
+        else:
+            ev = (ctypes.c_void_p * 3)(*[e.cuda_event if e is not None else None for e in stage_events])
+            rc = lib.kda_fwd_ws_profiled(*args, _ptr(workspace), wsz, ev, s.cuda_stream)
     if rc != KDA_OK:
         raise KDAError(rc)
+
+
+def workspace_size(N: int, T: int, H: int, varlen: bool) -> int:
+    """Bytes of workspace kda_fwd needs for N sequences, T tokens, H heads (kda_fwd_workspace_size)."""
+    return int(_native.load().kda_fwd_workspace_size(int(N), int(T), int(H), int(bool(varlen))))
 
 
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> None:

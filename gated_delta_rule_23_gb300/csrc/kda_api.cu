@@ -155,9 +155,13 @@ kda_status_t check_args(const void *q, const void *k, const void *v, const void 
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                  void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream)
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr)
 {
     const bool varlen = cu_seqlens != nullptr;
+    auto mark = [&](int i) -> cudaError_t {
+        return stage_events && stage_events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream)
+                                               : cudaSuccess;
+    };
     Problem p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(k);
@@ -189,10 +193,16 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
         p.order = order;
     }
     if (err == cudaSuccess)
+        err = mark(0);
+    if (err == cudaSuccess)
         err = launch_prep(p, max_chunks(N, T, varlen), stream);
+    if (err == cudaSuccess)
+        err = mark(1);
     const int st = (initial_state || final_state) ? (state_dtype == KDA_DTYPE_FP32 ? 2 : 1) : 0;
     if (err == cudaSuccess)
         err = launch_recur(p, st, stream);
+    if (err == cudaSuccess)
+        err = mark(2);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -223,6 +233,25 @@ extern "C" kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, 
         return KDA_ERR_INVALID_ARGUMENT;
     return run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
                cu_seqlens, N, T, H, static_cast<unsigned char *>(workspace), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, const void *g,
+                                            const void *beta, float scale, void *out, const float *A_log,
+                                            const float *dt_bias, float lower_bound, const void *initial_state,
+                                            void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens,
+                                            int N, int64_t T, int H, void *workspace, size_t workspace_bytes_,
+                                            void *const *stage_events, kda_stream_t stream)
+{
+    kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s != KDA_OK)
+        return s;
+    const size_t need = workspace_bytes(N, T, H, cu_seqlens != nullptr);
+    if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes_ < need))
+        return KDA_ERR_INVALID_ARGUMENT;
+    return run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
+               cu_seqlens, N, T, H, static_cast<unsigned char *>(workspace), reinterpret_cast<cudaStream_t>(stream),
+               stage_events);
 }
 
 extern "C" kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,

@@ -128,6 +128,20 @@ kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void 
                         void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_fwd_ws_profiled -- kda_fwd_ws that also records CUDA events on `stream` at the stage
+ * boundaries, for timing the two kernels separately: stage_events[0] right before the prep
+ * kernel (after the varlen plan), [1] between the prep and recurrence kernels, [2] after the
+ * recurrence kernel.  stage_events points to 3 cudaEvent_t handles (any may be NULL).  The
+ * computation and its results are exactly those of kda_fwd_ws.
+ */
+kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                 float scale, void *out, const float *A_log, const float *dt_bias,
+                                 float lower_bound, const void *initial_state, void *final_state,
+                                 kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                                 void *workspace, size_t workspace_bytes, void *const *stage_events,
+                                 kda_stream_t stream);
+
+/*
  * Returns the workspace memory kda_fwd's pools hold but no call is using to the driver.
  * KDA_ERR_CUDA if a pool could not be trimmed.
  */

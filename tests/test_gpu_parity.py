@@ -179,3 +179,46 @@ def test_side_stream():
             p.lower_bound, initial_state=dev["init"], final_state=fin, stream=s)
     s.synchronize()
     assert_parity(out.float().cpu().numpy(), fin.cpu().numpy(), *oracle_run(p))
+
+
+def _call(p, dev, out, fin, **kw):
+    kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+            p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], **kw)
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_caller_workspace_matches_pool_workspace(varlen):
+    """kda_fwd_ws (caller-owned workspace, reused twice) and kda_fwd_ws_profiled give the same bits as kda_fwd."""
+    from gated_delta_rule_23_gb300 import workspace_size
+    cu = np.array([0, 90, 90, 300, 333]) if varlen else None
+    p = make_problem(B=1, T=333, H=3, seed=21, cu_seqlens=cu)
+    dev = to_device(p)
+    nbytes = workspace_size(p.N, p.T, p.H, varlen)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    results = []
+    for kw in ({}, {"workspace": ws}, {"workspace": ws},
+               {"workspace": ws, "stage_events": [torch.cuda.Event(enable_timing=True) for _ in range(3)]}):
+        if "stage_events" in kw:
+            for e in kw["stage_events"]:
+                e.record()   # creates the event handles
+        out = torch.empty_like(dev["q"])
+        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda")
+        _call(p, dev, out, fin, **kw)
+        torch.cuda.synchronize()
+        results.append((out.float().cpu().numpy(), fin.float().cpu().numpy()))
+        if "stage_events" in kw:
+            e0, e1, e2 = kw["stage_events"]
+            assert e0.elapsed_time(e1) >= 0 and e1.elapsed_time(e2) >= 0
+    for o, f in results[1:]:
+        assert np.array_equal(o, results[0][0]) and np.array_equal(f, results[0][1])
+    assert_parity(results[0][0], results[0][1], *oracle_run(p))
+
+
+def test_workspace_too_small_rejected():
+    from gated_delta_rule_23_gb300 import KDAError, workspace_size
+    p = make_problem(B=1, T=130, H=2, seed=22)
+    dev = to_device(p)
+    ws = torch.empty(workspace_size(p.N, p.T, p.H, False) - 256, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["q"])
+    with pytest.raises(KDAError):
+        _call(p, dev, out, None, workspace=ws)
