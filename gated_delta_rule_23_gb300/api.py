@@ -37,7 +37,7 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             scale: float, out: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, lower_bound: float,
             initial_state: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
             cu_seqlens: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-            workspace: Optional[torch.Tensor] = None, stage_events=None) -> None:
+            workspace: Optional[torch.Tensor] = None, stage_events=None, noalloc: bool = False) -> None:
     """KDA chunked forward on CUDA tensors; writes ``out`` and ``final_state`` in place.
 
     q, k, v, g: bf16 [B, T, H, 128]; beta: bf16 [B, T, H]; out: bf16 [B, T, H, 128];
@@ -47,7 +47,7 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     least ``workspace_size(...)`` bytes (kda_fwd_ws); without it the library's pool provides one.
     ``stage_events``: optional three recorded-once torch.cuda.Event objects marking the start of
     the prep kernel, the prep/recurrence boundary and the end (kda_fwd_ws_profiled; needs
-    ``workspace``).
+    ``workspace``).  ``noalloc``: use the library's static workspace (kda_fwd_noalloc).
     """
     lib = _native.load()
     if q.dim() != 4 or q.shape[-1] != D:
@@ -90,8 +90,12 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         wsz = workspace.numel()
     elif stage_events is not None:
         raise ValueError("stage_events needs a workspace")
+    if noalloc and (workspace is not None or stage_events is not None):
+        raise ValueError("noalloc takes no workspace or stage events")
     with torch.cuda.device(dev):
-        if workspace is None:
+        if noalloc:
+            rc = lib.kda_fwd_noalloc(*args, s.cuda_stream)
+        elif workspace is None:
             rc = lib.kda_fwd(*args, s.cuda_stream)
         elif stage_events is None:
             rc = lib.kda_fwd_ws(*args, _ptr(workspace), wsz, s.cuda_stream)

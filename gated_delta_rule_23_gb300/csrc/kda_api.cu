@@ -86,10 +86,14 @@ int64_t max_chunks(int N, int64_t T, bool varlen)
     return varlen ? (T + (int64_t)(CH - 1) * N) / CH : (int64_t)N * ((T + CH - 1) / CH);
 }
 
+}  // namespace
+
 size_t workspace_bytes(int N, int64_t T, int H, bool varlen)
 {
     return header_bytes(N, varlen) + (size_t)max_chunks(N, T, varlen) * (size_t)H * SLOT_BYTES;
 }
+
+namespace {
 
 std::mutex g_pool_mu;
 cudaMemPool_t g_pools[64] = {};
@@ -121,6 +125,8 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out)
     *out = g_pools[dev];
     return cudaSuccess;
 }
+
+}  // namespace
 
 kda_status_t check_args(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                         const void *out, const float *A_log, const float *dt_bias, float lower_bound,
@@ -155,7 +161,7 @@ kda_status_t check_args(const void *q, const void *k, const void *v, const void 
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                  void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr)
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events)
 {
     const bool varlen = cu_seqlens != nullptr;
     auto mark = [&](int i) -> cudaError_t {
@@ -206,7 +212,6 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-}  // namespace
 }  // namespace kda
 
 using namespace kda;

@@ -6,7 +6,22 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "kda.h"
+
 namespace kda {
+
+// Host-side argument checks of kda_fwd (no CUDA calls).
+kda_status_t check_args(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                        const void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                        const void *initial_state, const void *final_state, kda_dtype_t state_dtype,
+                        const int64_t *cu_seqlens, int N, int64_t T, int H);
+// Workspace bytes of one call (kda_fwd_workspace_size).
+size_t workspace_bytes(int N, int64_t T, int H, bool varlen);
+// The launch sequence on `stream` with workspace `ws` (checked arguments).
+kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                 void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
+                 void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr);
 
 struct Problem;
 

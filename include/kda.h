@@ -141,6 +141,26 @@ kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, co
                                  void *workspace, size_t workspace_bytes, void *const *stage_events,
                                  kda_stream_t stream);
 
+/* Capacity of the static workspace of kda_fwd_noalloc (256 MiB per device). */
+#define KDA_NOALLOC_SCRATCH_BYTES 268435456
+
+/*
+ * kda_fwd_noalloc -- kda_fwd whose workspace is a fixed device array of
+ * KDA_NOALLOC_SCRATCH_BYTES inside the library (one per device, created with the library's
+ * module on that device): the call allocates no memory at all.  The FlashKDA pages have no
+ * counterpart of this entry point; it exists for callers that must not allocate inside the
+ * call (for instance while capturing a CUDA graph without allocation nodes).  Because the
+ * array is shared, calls on one device must be ordered (the same stream, or serialised by the
+ * caller).  Same arguments, results and errors as kda_fwd, plus KDA_ERR_UNSUPPORTED when
+ * kda_fwd_workspace_size(N, T, H, cu_seqlens != NULL) exceeds KDA_NOALLOC_SCRATCH_BYTES
+ * (reported before any CUDA call).
+ */
+kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                             float scale, void *out, const float *A_log, const float *dt_bias,
+                             float lower_bound, const void *initial_state, void *final_state,
+                             kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                             kda_stream_t stream);
+
 /*
  * Returns the workspace memory kda_fwd's pools hold but no call is using to the driver.
  * KDA_ERR_CUDA if a pool could not be trimmed.

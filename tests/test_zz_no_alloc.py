@@ -1,0 +1,45 @@
+"""kda_fwd_noalloc: the forward pass with the library's static device workspace.
+
+CPU: the entry point is exported and rejects a problem whose workspace exceeds the static
+array before any CUDA call.  GPU: two calls give the same bits as kda_fwd (library pool
+workspace) on fixed-length and varlen problems.
+"""
+import numpy as np
+import pytest
+
+from gated_delta_rule_23_gb300 import _native
+from gated_delta_rule_23_gb300._native import KDA_DTYPE_NONE, KDA_ERR_UNSUPPORTED
+
+SCRATCH = 268435456   # KDA_NOALLOC_SCRATCH_BYTES
+
+
+def test_oversize_rejected_before_any_cuda_call():
+    lib = _native.load()
+    A = 1 << 20   # fake, aligned device addresses: the call must fail on the size check
+    args = [A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 0.1, A + 0x5000, A + 0x6000, A + 0x7000, -5.0,
+            None, None, KDA_DTYPE_NONE, None]
+    assert lib.kda_fwd_workspace_size(1, 8192, 96, 0) > SCRATCH
+    assert lib.kda_fwd_noalloc(*args, 1, 8192, 96, None) == KDA_ERR_UNSUPPORTED
+    assert lib.kda_fwd_workspace_size(1, 1024, 96, 0) <= SCRATCH
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cu", [None, np.array([0, 90, 90, 300, 333])])
+def test_noalloc_matches_kda_fwd(cu):
+    import torch
+    from gated_delta_rule_23_gb300 import kda_fwd
+    from gated_delta_rule_23_gb300.inputs import make_problem
+    from tests.gpu_util import to_device
+    p = make_problem(B=1, T=333, H=3, seed=31, cu_seqlens=cu)
+    dev = to_device(p)
+    res = {}
+    for noalloc in (False, True, True):
+        out = torch.empty_like(dev["q"])
+        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda")
+        kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+                p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], noalloc=noalloc)
+        torch.cuda.synchronize()
+        res.setdefault(noalloc, []).append((out.float().cpu().numpy(), fin.float().cpu().numpy()))
+    ref = res[False][0]
+    for o, f in res[True]:
+        assert np.array_equal(o, ref[0]) and np.array_equal(f, ref[1])
