@@ -55,7 +55,11 @@ constexpr int OFF_AKK = OFF_OPS;                    // fp32 [64][68] b_i Akk (st
 constexpr int OFF_TM = OFF_AKK + CH * PA * 4;       // fp32 [64][68] (I + Akk)^-1
 constexpr int OFF_TP = OFF_TM + CH * PA * 4;        // fp16 [64 t][64 j] T' (swizzled)
 constexpr int OFF_ZW = OFF_TP + CH * CH * 2;        // fp32 [8 warps][16][8] off-diagonal partial products
-static_assert(OFF_ZW + 8 * 16 * 8 * 4 <= OPS_BYTES, "post-product overlay");
+constexpr int OFF_AQS = OFF_ZW + 8 * 16 * 8 * 4;  // Aqk rows of the slot (KA rows 0..63), staged for a bulk copy
+static_assert(OFF_AQS + 64 * CH * 2 <= OPS_BYTES, "post-product overlay");
+// after T' is formed, the W and U0^T parts of the slot are staged over Akk / Tm for bulk copies
+constexpr int OFF_WS = OFF_AKK, OFF_US = OFF_AKK + 64 * D * 2;
+static_assert(OFF_US + D * CH * 2 <= OFF_TP, "W / U0 staging overlaps T'");
 constexpr int OFF_KG = 72192;                       // fp16 [64 j][128 c] K^ . Gamma (swizzled)
 constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizzled)
 constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 [64] 1 / |q|
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
             rqt[r] = rq[4 * run + r];
             rkt[r] = rk[4 * run + r];
         }
+        uint32_t qkeep[4][2];   // Q~ of the first pass (4 tokens x 4 channels, fp16 pairs)
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
             // alpha, inclusive prefix pf and exclusive suffix ef inside the 4-token run
@@ -313,8 +318,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                         make_float4(r0[0], r0[1], r0[2], r0[3]);
                 *reinterpret_cast<uint2 *>(sm + OFF_KG + h128(t, cb)) =
                     make_uint2(pack_half2(kg[0], kg[1]), pack_half2(kg[2], kg[3]));
-                *reinterpret_cast<uint2 *>(slot + qw_off(CH + t, cb)) =
-                    make_uint2(pack_half2(qt[0], qt[1]), pack_half2(qt[2], qt[3]));
+                // Q~: the first pass keeps its 4 channels, the second stores all 8 as one 16-byte row piece
+                if (hc == 0) {
+                    qkeep[r][0] = pack_half2(qt[0], qt[1]);
+                    qkeep[r][1] = pack_half2(qt[2], qt[3]);
+                } else {
+                    *reinterpret_cast<uint4 *>(slot + qw_off(CH + t, c0)) =
+                        make_uint4(qkeep[r][0], qkeep[r][1], pack_half2(qt[0], qt[1]), pack_half2(qt[2], qt[3]));
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const __half hv = __float2half_rn(kt[i]);
@@ -325,9 +336,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                         ktw[i][r >> 1] = bits;
                 }
             }
+            // K~ (slot rows = key channel, 8 tokens per 16-byte core row): the lanes of runs 2m and 2m + 1
+            // swap halves so that each stores two full rows (even run: channels 0, 2; odd run: 1, 3)
+            {
+                const bool ev = (run & 1) == 0;
+                uint32_t ra_[2], rb_[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<uint2 *>(slot + ka_off(CH + cb + i, 4 * run)) = make_uint2(ktw[i][0], ktw[i][1]);
+                for (int w = 0; w < 2; ++w) {
+                    ra_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[1][w] : ktw[0][w], 1);
+                    rb_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[3][w] : ktw[2][w], 1);
+                }
+                const int j8 = 8 * (run >> 1);
+                if (ev) {
+                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb, j8)) = make_uint4(ktw[0][0], ktw[0][1], ra_[0], ra_[1]);
+                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb + 2, j8)) =
+                        make_uint4(ktw[2][0], ktw[2][1], rb_[0], rb_[1]);
+                } else {
+                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb + 1, j8)) =
+                        make_uint4(ra_[0], ra_[1], ktw[1][0], ktw[1][1]);
+                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb + 3, j8)) =
+                        make_uint4(rb_[0], rb_[1], ktw[3][0], ktw[3][1]);
+                }
+            }
             // this half of the channels: [Akk | Aqk] (+)= A B^T on the tensor cores
             fence_async_smem();
             __syncthreads();
@@ -377,11 +407,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                         w[f] = pack_half2(j <= i ? __uint_as_float(u[e + 2 * f]) : 0.f,
                                           j + 1 <= i ? __uint_as_float(u[e + 2 * f + 1]) : 0.f);
                     }
-                    *reinterpret_cast<uint4 *>(slot + ka_off(i, j0 + e)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_AQS + ka_off(i, j0 + e) - SLOT_KA) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 // columns 32..63 of rows 0..31 are zero
-                *reinterpret_cast<uint4 *>(slot + ka_off(i, 32 + j0)) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(slot + ka_off(i, 40 + j0)) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sm + OFF_AQS + ka_off(i, 32 + j0) - SLOT_KA) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sm + OFF_AQS + ka_off(i, 40 + j0) - SLOT_KA) = make_uint4(0u, 0u, 0u, 0u);
             }
         } else {
             const int i = 32 + lane, j0 = 32 * hw;
@@ -407,13 +437,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                         w[f] = pack_half2(j <= i ? __uint_as_float(u[e + 2 * f]) : 0.f,
                                           j + 1 <= i ? __uint_as_float(u[e + 2 * f + 1]) : 0.f);
                     }
-                    *reinterpret_cast<uint4 *>(slot + ka_off(i, j0 + e)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_AQS + ka_off(i, j0 + e) - SLOT_KA) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         }
     }
     tc_fence_before();
+    fence_async_smem();
     __syncthreads();
+    if (tid == 0) {   // Aqk rows of the slot: one bulk copy
+        bulk_s2g(slot + SLOT_KA, smem_u32(sm + OFF_AQS), 64 * CH * 2);
+        bulk_commit();
+    }
 
     // -------- phase 4: Tm = (I + Akk)^-1, blocked by 16-token sub-blocks: fp32 forward
     //          substitution on the diagonal blocks, then Tm_{bi,bj} = -Tm_{bi,bi} sum_m A_{bi,m} Tm_{m,bj}
@@ -530,7 +565,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int t = mt * 16 + gq + 8 * hh, c = (nt0 + a) * 8 + 2 * t4;
-                    *reinterpret_cast<uint32_t *>(slot + qw_off(t, c)) = pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_WS + qw_off(t, c)) = pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
                 }
         }
         // U0^T: value rows 16 warp .. + 15, all 64 tokens
@@ -561,9 +596,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int vr = warp * 16 + gq + 8 * hh, t = a * 8 + 2 * t4;
-                    *reinterpret_cast<uint32_t *>(slot + u0_off(vr, t)) = pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
+                    *reinterpret_cast<uint32_t *>(sm + OFF_US + u0_off(vr, t) - SLOT_U0) =
+                        pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
                 }
         }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {   // W rows (QW rows 0..63) and U0^T of the slot: bulk copies; all copies complete before exit
+        bulk_s2g(slot + SLOT_QW, smem_u32(sm + OFF_WS), 64 * D * 2);
+        bulk_s2g(slot + SLOT_U0, smem_u32(sm + OFF_US), D * CH * 2);
+        bulk_commit();
+        bulk_wait_all();
     }
 
     // -------- release tensor memory; report a bounded wait that gave up
