@@ -211,11 +211,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
             rqt[r] = rq[4 * run + r];
             rkt[r] = rk[4 * run + r];
         }
+        // gate constants: sigmoid(eA (g + dt)) = 1 / (1 + 2^(g gz + gd))
+        const float gz = -eA * LOG2E;
+        float gd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            gd[i] = gz * dtb[i];
         uint32_t qkeep[4][2];   // Q~ of the first pass (4 tokens x 4 channels, fp16 pairs)
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
-            // alpha, inclusive prefix pf and exclusive suffix ef inside the 4-token run
-            float pf[4][4], ef[4][4];
+            // alpha and its inclusive prefix pf inside the 4-token run
+            float pf[4][4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const uint32_t gw[2] = {hc ? gv[r].z : gv[r].x, hc ? gv[r].w : gv[r].y};
@@ -223,40 +229,33 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float gval = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-                    const float sig = sigmoid_fast(eA * (gval + dtb[4 * hc + i]));
-                    ef[r][i] = valid ? ex2_approx(p.lb_log2e * sig) : 1.f;   // alpha (no decay past the end)
+                    // sigmoid(eA (g + dt)) = 1 / (1 + 2^(g gz + gd))
+                    const float sig = rcp_approx(1.f + ex2_approx(fmaf(gval, gz, gd[4 * hc + i])));
+                    const float a = valid ? ex2_approx(p.lb_log2e * sig) : 1.f;   // alpha (no decay past the end)
+                    pf[r][i] = r == 0 ? a : pf[r - 1][i] * a;
                 }
             }
-            float X[4], Y[4], pre[4], post[4], gcv[4], f1[4];
+            // per channel: pf *= X (the earlier runs of the sub-block) so that pf = P; Dv = D_b, the
+            // sub-block product; pre / post over the earlier / later sub-blocks; f1, the extra right
+            // factor of the second anchor.  The exclusive suffix is E = D_b / P.
+            float Dv[4], iD[4], pre[4], post[4], gcv[4], f1[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                pf[0][i] = ef[0][i];
-#pragma unroll
-                for (int r = 1; r < 4; ++r)
-                    pf[r][i] = pf[r - 1][i] * ef[r][i];
-                float acc = 1.f;
-#pragma unroll
-                for (int r = 3; r >= 0; --r) {
-                    const float a = ef[r][i];
-                    ef[r][i] = acc;
-                    acc *= a;
-                }
-                const float Rt = acc;   // product over the run
+                const float Rt = pf[3][i];   // product over the run
                 // runs of one sub-block: lanes differing in bits 0..1
-                float inc = Rt, sinc = Rt, t1;
+                float inc = Rt, t1;
                 t1 = __shfl_up_sync(0xffffffffu, inc, 1, 4);
                 if (s4 >= 1) inc *= t1;
                 t1 = __shfl_up_sync(0xffffffffu, inc, 2, 4);
                 if (s4 >= 2) inc *= t1;
-                t1 = __shfl_down_sync(0xffffffffu, sinc, 1, 4);
-                if (s4 <= 2) sinc *= t1;
-                t1 = __shfl_down_sync(0xffffffffu, sinc, 2, 4);
-                if (s4 <= 1) sinc *= t1;
-                X[i] = __shfl_up_sync(0xffffffffu, inc, 1, 4);
-                if (s4 == 0) X[i] = 1.f;
-                Y[i] = __shfl_down_sync(0xffffffffu, sinc, 1, 4);
-                if (s4 == 3) Y[i] = 1.f;
+                float X = __shfl_up_sync(0xffffffffu, inc, 1, 4);
+                if (s4 == 0) X = 1.f;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    pf[r][i] *= X;
                 const float Db = __shfl_sync(0xffffffffu, inc, (lane & ~3) | 3);
+                Dv[i] = Db;
+                iD[i] = rcp_approx(Db);
                 // sub-blocks: lanes differing in bits 2..3
                 float inc2 = Db, sinc2 = Db;
                 t1 = __shfl_up_sync(0xffffffffu, inc2, 4, 16);
@@ -274,7 +273,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 gcv[i] = inc2;   // on the last sub-block: the whole chunk's decay
                 const float D1 = __shfl_sync(0xffffffffu, Db, (lane & ~12) | 4);
                 const float D2 = __shfl_sync(0xffffffffu, Db, (lane & ~12) | 8);
-                f1[i] = sblk == 0 ? D1 * D2 : (sblk == 1 ? D2 : 1.f);   // right factor, second anchor
+                f1[i] = sblk == 0 ? D1 * D2 : (sblk == 1 ? D2 : 1.f);
             }
             const int cb = c0 + 4 * hc;
             if (run == 15)
@@ -293,10 +292,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 for (int i = 0; i < 4; ++i) {
                     const float qh = ((i & 1) ? bf16_hi(qw[i >> 1]) : bf16_lo(qw[i >> 1])) * rqt[r];
                     const float kh = ((i & 1) ? bf16_hi(kw[i >> 1]) : bf16_lo(kw[i >> 1])) * rkt[r];
-                    const float P = X[i] * pf[r][i], E = ef[r][i] * Y[i];
+                    const float P = pf[r][i], rc = rcp_approx(P), E = Dv[i] * rc;   // rc = 1 / P
                     const bool even = (sblk & 1) == 0;
-                    const float rc = rcp_approx(even ? E : P);
-                    const float Lf = even ? rc : P;
+                    const float Lf = even ? P * iD[i] : P;                         // 1 / E or P
                     lq[i] = tf32r(qh * Lf);
                     lk[i] = tf32r(kh * Lf);
                     r1[i] = tf32r(kh * (sblk == 3 ? rc : E * f1[i]));
