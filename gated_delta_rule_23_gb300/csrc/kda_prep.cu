@@ -538,33 +538,37 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         const uint32_t s_tp = smem_u32(sm + OFF_TP), s_kg = smem_u32(sm + OFF_KG), s_v = smem_u32(sm + OFF_V);
         const int gq = lane >> 2, t4 = lane & 3;
         const int lr = lane & 7, lsel = lane >> 3;   // ldmatrix: row within a matrix, matrix index
-        // W: rows t of m-tile (warp & 3), channels of n-tiles 8 (warp >> 2) .. + 7
+        // W: channels of n-tiles 2 warp, 2 warp + 1, all rows t.  T' is block lower triangular, so
+        // m-tile mt needs k-steps 0..mt only.
         {
-            const int mt = warp & 3, nt0 = (warp >> 2) * 8;
-            float acc[8][4];
+            float acc[4][2][4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
-                acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+                    acc[m][a][0] = acc[m][a][1] = acc[m][a][2] = acc[m][a][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < CH / 16; ++ks) {
-                uint32_t af[4];
-                ldsm_x4(s_tp + h64(mt * 16 + (lsel & 1) * 8 + lr, ks * 16 + (lsel >> 1) * 8), af);
+                uint32_t bf[4];   // K^.Gamma rows j of k-step ks, the warp's two n-tiles
+                ldsm_x4_t(s_kg + h128(ks * 16 + (lsel & 1) * 8 + lr, (2 * warp + (lsel >> 1)) * 8), bf);
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t bf[4];
-                    const int nt = nt0 + 2 * np + (lsel >> 1);
-                    ldsm_x4_t(s_kg + h128(ks * 16 + (lsel & 1) * 8 + lr, nt * 8), bf);
-                    mma_f16(acc[2 * np], af, bf[0], bf[1]);
-                    mma_f16(acc[2 * np + 1], af, bf[2], bf[3]);
+                for (int mt = ks; mt < 4; ++mt) {
+                    uint32_t af[4];
+                    ldsm_x4(s_tp + h64(mt * 16 + (lsel & 1) * 8 + lr, ks * 16 + (lsel >> 1) * 8), af);
+                    mma_f16(acc[mt][0], af, bf[0], bf[1]);
+                    mma_f16(acc[mt][1], af, bf[2], bf[3]);
                 }
             }
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = mt * 16 + gq + 8 * hh, c = (nt0 + a) * 8 + 2 * t4;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_WS + qw_off(t, c)) = pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
-                }
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int t = mt * 16 + gq + 8 * hh, c = (2 * warp + a) * 8 + 2 * t4;
+                        *reinterpret_cast<uint32_t *>(sm + OFF_WS + qw_off(t, c)) =
+                            pack_half2(acc[mt][a][2 * hh], acc[mt][a][2 * hh + 1]);
+                    }
         }
         // U0^T: value rows 16 warp .. + 15, all 64 tokens
         {
@@ -581,7 +585,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 for (int e = 0; e < 4; ++e)
                     af[e] = bf16x2_to_half2(af[e]);
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
+                for (int np = ks; np < 4; ++np) {   // T'^T rows j of k-step ks are zero for tokens t < 16 ks
                     uint32_t bf[4];
                     // B = T'^T: matrices (t-tile 2np, j 0-7), (2np, j 8-15), (2np+1, j 0-7), (2np+1, j 8-15)
                     ldsm_x4(s_tp + h64((2 * np + (lsel >> 1)) * 8 + lr, ks * 16 + (lsel & 1) * 8), bf);
