@@ -92,7 +92,10 @@ __device__ __forceinline__ uint32_t to_tf32(float x)
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+// Round to tf32 (10 explicit mantissa bits), to nearest with ties away from zero, on the integer
+// pipe: adding half a tf32 ulp to the magnitude bits and truncating is that rounding for finite
+// values (a carry into the exponent is the correct round-up).
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 {
     const __half2 h = __floats2half2_rn(lo, hi);

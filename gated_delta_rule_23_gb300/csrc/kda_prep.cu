@@ -141,6 +141,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     const int cgrp = lane >> 4, run = lane & 15, sblk = run >> 2, s4 = run & 3;
     const int c0 = warp * 16 + cgrp * 8;
     const int kgrp = warp * 2 + cgrp;   // this thread's 4-channel group in each pass's compact K
+    // every global load of this phase is issued before any of them is used
+    const __nv_bfloat16 bval = tid < L ? p.beta[(tok0 + (tid < L ? tid : 0)) * H + h] : __float2bfloat16(0.f);
+    const float alog = p.A_log[h];
+    const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0);
+    const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0 + 4);
     uint4 qv[4], kv[4], gv[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -155,15 +160,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         }
     }
     if (tid < CH)
-        bt[tid] = tid < L ? sigmoid_fast(__bfloat162float(p.beta[(tok0 + tid) * H + h])) : 0.f;
-    const float eA = expf(p.A_log[h]);
-    float dtb[8];
-    {
-        const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0);
-        const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0 + 4);
-        dtb[0] = d0.x; dtb[1] = d0.y; dtb[2] = d0.z; dtb[3] = d0.w;
-        dtb[4] = d1.x; dtb[5] = d1.y; dtb[6] = d1.z; dtb[7] = d1.w;
-    }
+        bt[tid] = tid < L ? sigmoid_fast(__bfloat162float(bval)) : 0.f;
+    const float eA = expf(alog);
+    const float dtb[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 
     // -------- phase 1: row norms of q and k
     {
