@@ -128,15 +128,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         mbar_fence_init();
     }
 
-    // -------- phase 0: v rows (bf16) staged for the WY products; this thread's q, k, g
-#pragma unroll
-    for (int m = 0; m < (CH * 16) / PREP_THREADS; ++m) {
-        const int idx = tid + m * PREP_THREADS, r = idx >> 4, c16 = idx & 15;
-        const bool valid = r < L;
-        const __nv_bfloat16 *src = p.v + ((size_t)(tok0 + (valid ? r : 0)) * H + h) * D + c16 * 8;
-        cp_async16(smem_u32(sm + OFF_V + h128(r, c16 * 8)), src, valid);
-    }
-    cp_async_commit();
+    // -------- phase 0: this thread's q, k, g and the chunk's beta / gate parameters
     // lane roles: channel group cgrp (8 channels), run (4 consecutive tokens); sub-block = run / 4
     const int cgrp = lane >> 4, run = lane & 15, sblk = run >> 2, s4 = run & 3;
     const int c0 = warp * 16 + cgrp * 8;
@@ -370,6 +362,16 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         }
     }
 
+    // v rows (bf16) for the WY products: requested after the gate pass so that they do not compete
+    // with q, k, g; the readout and the inverse hide their latency
+#pragma unroll
+    for (int m = 0; m < (CH * 16) / PREP_THREADS; ++m) {
+        const int idx = tid + m * PREP_THREADS, r = idx >> 4, c16 = idx & 15;
+        const bool valid = r < L;
+        const __nv_bfloat16 *src = p.v + ((size_t)(tok0 + (valid ? r : 0)) * H + h) * D + c16 * 8;
+        cp_async16(smem_u32(sm + OFF_V + h128(r, c16 * 8)), src, valid);
+    }
+    cp_async_commit();
     // -------- phase 3: Akk / Aqk out of tensor memory.  Lanes 0..31 / 32..63: Akk / Aqk rows 0..31
     //          (columns 0..31 = tokens 0..31); lanes 64..95 / 96..127: rows 32..63 (columns 32..95 =
     //          tokens 0..63).  Aqk (causal) goes to the slot, b_i Akk (strictly lower) to shared memory.
