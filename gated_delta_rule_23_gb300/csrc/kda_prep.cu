@@ -606,11 +606,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     }
     fence_async_smem();
     __syncthreads();
-    if (tid == 0) {   // W rows (QW rows 0..63) and U0^T of the slot: bulk copies; all copies complete before exit
+    if (tid == 0) {
+        // W rows (QW rows 0..63) and U0^T of the slot: bulk copies.  The CTA may leave once every copy
+        // has read its shared-memory source; the writes complete before the kernel does.
         bulk_s2g(slot + SLOT_QW, smem_u32(sm + OFF_WS), 64 * D * 2);
         bulk_s2g(slot + SLOT_U0, smem_u32(sm + OFF_US), D * CH * 2);
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read_all();
     }
 
     // -------- release tensor memory; report a bounded wait that gave up
