@@ -37,7 +37,8 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             scale: float, out: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, lower_bound: float,
             initial_state: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
             cu_seqlens: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-            workspace: Optional[torch.Tensor] = None, stage_events=None, noalloc: bool = False) -> None:
+            workspace: Optional[torch.Tensor] = None, stage_events=None, noalloc: bool = False,
+            recurrent: bool = False) -> None:
     """KDA chunked forward on CUDA tensors; writes ``out`` and ``final_state`` in place.
 
     q, k, v, g: bf16 [B, T, H, 128]; beta: bf16 [B, T, H]; out: bf16 [B, T, H, 128];
@@ -48,6 +49,8 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     ``stage_events``: optional three recorded-once torch.cuda.Event objects marking the start of
     the prep kernel, the prep/recurrence boundary and the end (kda_fwd_ws_profiled; needs
     ``workspace``).  ``noalloc``: use the library's static workspace (kda_fwd_noalloc).
+    ``recurrent``: evaluate token by token (kda_fwd_recurrent; decode and short sequences, no
+    workspace).
     """
     lib = _native.load()
     if q.dim() != 4 or q.shape[-1] != D:
@@ -90,10 +93,14 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         wsz = workspace.numel()
     elif stage_events is not None:
         raise ValueError("stage_events needs a workspace")
-    if noalloc and (workspace is not None or stage_events is not None):
-        raise ValueError("noalloc takes no workspace or stage events")
+    if (noalloc or recurrent) and (workspace is not None or stage_events is not None):
+        raise ValueError("noalloc and recurrent take no workspace or stage events")
+    if noalloc and recurrent:
+        raise ValueError("noalloc and recurrent are exclusive")
     with torch.cuda.device(dev):
-        if noalloc:
+        if recurrent:
+            rc = lib.kda_fwd_recurrent(*args, s.cuda_stream)
+        elif noalloc:
             rc = lib.kda_fwd_noalloc(*args, s.cuda_stream)
         elif workspace is None:
             rc = lib.kda_fwd(*args, s.cuda_stream)
@@ -104,6 +111,12 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             rc = lib.kda_fwd_ws_profiled(*args, _ptr(workspace), wsz, ev, s.cuda_stream)
     if rc != KDA_OK:
         raise KDAError(rc)
+
+
+def kda_fwd_recurrent(*args, **kwargs) -> None:
+    """kda_fwd evaluated token by token (the C entry point kda_fwd_recurrent): same arguments
+    as kda_fwd without ``workspace``, ``stage_events`` and ``noalloc``."""
+    kda_fwd(*args, recurrent=True, **kwargs)
 
 
 def workspace_size(N: int, T: int, H: int, varlen: bool) -> int:

@@ -158,16 +158,13 @@ kda_status_t check_args(const void *q, const void *k, const void *v, const void 
     return KDA_OK;
 }
 
-kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
-                 void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
-                 void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream, void *const *stage_events)
+namespace {
+
+// The kernels' view of one call (pointers and sizes; the workspace fields are set by the caller).
+Problem make_problem(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                     void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
+                     void *final_state, const int64_t *cu_seqlens, int N, int64_t T, int H)
 {
-    const bool varlen = cu_seqlens != nullptr;
-    auto mark = [&](int i) -> cudaError_t {
-        return stage_events && stage_events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream)
-                                               : cudaSuccess;
-    };
     Problem p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.k = static_cast<const __nv_bfloat16 *>(k);
@@ -188,6 +185,29 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
     p.nch_fixed = (T + CH - 1) / CH;
     p.chunk_off = nullptr;
     p.order = nullptr;
+    p.slots = nullptr;
+    return p;
+}
+
+int state_kind(const void *initial_state, const void *final_state, kda_dtype_t state_dtype)
+{
+    return (initial_state || final_state) ? (state_dtype == KDA_DTYPE_FP32 ? 2 : 1) : 0;
+}
+
+}  // namespace
+
+kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                 void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
+                 void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    auto mark = [&](int i) -> cudaError_t {
+        return stage_events && stage_events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream)
+                                               : cudaSuccess;
+    };
+    Problem p = make_problem(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
+                             cu_seqlens, N, T, H);
     p.slots = ws + header_bytes(N, varlen);
     cudaError_t err = cudaSuccess;
     if (varlen) {
@@ -204,7 +224,7 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
         err = launch_prep(p, max_chunks(N, T, varlen), stream);
     if (err == cudaSuccess)
         err = mark(1);
-    const int st = (initial_state || final_state) ? (state_dtype == KDA_DTYPE_FP32 ? 2 : 1) : 0;
+    const int st = state_kind(initial_state, final_state, state_dtype);
     if (err == cudaSuccess)
         err = launch_recur(p, st, stream);
     if (err == cudaSuccess)
@@ -284,6 +304,26 @@ extern "C" kda_status_t kda_fwd(const void *q, const void *k, const void *v, con
     if (ws && cudaFreeAsync(ws, st) != cudaSuccess && s == KDA_OK)
         s = KDA_ERR_CUDA;
     return s;
+}
+
+extern "C" kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, const void *g,
+                                          const void *beta, float scale, void *out, const float *A_log,
+                                          const float *dt_bias, float lower_bound, const void *initial_state,
+                                          void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens,
+                                          int N, int64_t T, int H, kda_stream_t stream)
+{
+    kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s != KDA_OK)
+        return s;
+    if (T > INT32_MAX)
+        return KDA_ERR_UNSUPPORTED;
+    const Problem p = make_problem(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                   final_state, cu_seqlens, N, T, H);
+    return launch_recurrent(p, state_kind(initial_state, final_state, state_dtype),
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
 }
 
 extern "C" kda_status_t kda_workspace_trim(void)

@@ -68,7 +68,7 @@ typedef enum {
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, bad size, misaligned pointer, bad dtype/state combination */
-    KDA_ERR_UNSUPPORTED = 2,      /* lower_bound outside [-5, 0], or scale not finite */
+    KDA_ERR_UNSUPPORTED = 2,      /* lower_bound outside [-5, 0], scale not finite, or a size limit of the entry point */
     KDA_ERR_CUDA = 3,             /* a CUDA runtime call or the kernel launch failed */
     KDA_ERR_TIMEOUT = 4           /* a bounded device wait expired (reported by kda_device_status) */
 } kda_status_t;
@@ -160,6 +160,24 @@ kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v, const 
                              float lower_bound, const void *initial_state, void *final_state,
                              kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
                              kda_stream_t stream);
+
+/*
+ * kda_fwd_recurrent -- the same operation as kda_fwd, evaluated token by token: the
+ * per-token update of the guancyxx.cn FlashKDA article, section 一 (the recurrent form
+ * that the chunked form of section 2.2 reorganises), one CTA per (sequence, head, half of
+ * the values) with the state in fp32 registers.  Meant for decode steps (one or a few
+ * tokens per sequence) and short prefills, where it moves only the state and the tokens
+ * (no per-chunk operands, no workspace, no allocation); its cost grows linearly with the
+ * longest sequence, so long sequences belong to kda_fwd.  Same arguments, layouts,
+ * ownership (including in-place initial_state == final_state) and errors as kda_fwd, plus
+ * KDA_ERR_UNSUPPORTED when T >= 2^31.  Results agree with kda_fwd's within the parity
+ * tolerances, not bit for bit: this path keeps every operand in fp32.
+ */
+kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                               float scale, void *out, const float *A_log, const float *dt_bias,
+                               float lower_bound, const void *initial_state, void *final_state,
+                               kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                               kda_stream_t stream);
 
 /*
  * Returns the workspace memory kda_fwd's pools hold but no call is using to the driver.

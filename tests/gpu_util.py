@@ -31,8 +31,9 @@ def to_device(p, device="cuda"):
     return d
 
 
-def run_gpu(p, dev=None, inplace=False):
-    """Run the CUDA path on problem p; returns (out float32 [B,T,H,128], final float32 or None)."""
+def run_gpu(p, dev=None, inplace=False, recurrent=False):
+    """Run the CUDA path on problem p (the chunked entry point, or the token-recurrent one);
+    returns (out float32 [B,T,H,128], final float32 or None)."""
     dev = dev or to_device(p)
     out = torch.empty_like(dev["q"])
     fin = None
@@ -42,7 +43,7 @@ def run_gpu(p, dev=None, inplace=False):
         else:
             fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device=dev["q"].device)
     kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
-            p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"])
+            p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], recurrent=recurrent)
     device_status()            # synchronises; raises if a bounded device wait expired
     return out.float().cpu().numpy(), (None if fin is None else fin.float().cpu().numpy())
 

@@ -18,7 +18,7 @@ def lib():
 def test_exports_every_declared_function(lib):
     names = _native.declared_functions()
     assert {"kda_fwd", "kda_fwd_ws", "kda_fwd_workspace_size", "kda_workspace_trim", "kda_check_cu_seqlens",
-            "kda_status_string", "kda_fwd_smem_bytes", "kda_device_status"} <= set(names)
+            "kda_status_string", "kda_fwd_smem_bytes", "kda_device_status", "kda_fwd_recurrent"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -37,12 +37,12 @@ def test_status_strings(lib):
 A = 1 << 20
 
 
-def call(lib, **kw):
+def call(lib, entry="kda_fwd", **kw):
     args = dict(q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000, scale=0.1, out=A + 0x5000,
                 A_log=A + 0x6000, dt_bias=A + 0x7000, lower_bound=-5.0, init=None, fin=None,
                 state_dtype=KDA_DTYPE_NONE, cu=None, N=1, T=64, H=2, stream=None)
     args.update(kw)
-    return lib.kda_fwd(args["q"], args["k"], args["v"], args["g"], args["beta"], args["scale"], args["out"],
+    return getattr(lib, entry)(args["q"], args["k"], args["v"], args["g"], args["beta"], args["scale"], args["out"],
                        args["A_log"], args["dt_bias"], args["lower_bound"], args["init"], args["fin"],
                        args["state_dtype"], args["cu"], args["N"], args["T"], args["H"], args["stream"])
 
@@ -55,17 +55,25 @@ def call(lib, **kw):
     dict(init=A + 0x8000, state_dtype=KDA_DTYPE_NONE), dict(fin=A + 0x8000, state_dtype=7),
     dict(init=A + 0x8008, state_dtype=KDA_DTYPE_FP32), dict(dt_bias=A + 0x7004),
 ])
-def test_invalid_arguments_rejected(lib, kw):
-    assert call(lib, **kw) == KDA_ERR_INVALID_ARGUMENT
+@pytest.mark.parametrize("entry", ["kda_fwd", "kda_fwd_recurrent"])
+def test_invalid_arguments_rejected(lib, kw, entry):
+    assert call(lib, entry, **kw) == KDA_ERR_INVALID_ARGUMENT
 
 
 @pytest.mark.parametrize("lb", [-5.01, 0.5, float("nan"), float("-inf")])
-def test_lower_bound_outside_range_unsupported(lib, lb):
-    assert call(lib, lower_bound=lb) == KDA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("entry", ["kda_fwd", "kda_fwd_recurrent"])
+def test_lower_bound_outside_range_unsupported(lib, lb, entry):
+    assert call(lib, entry, lower_bound=lb) == KDA_ERR_UNSUPPORTED
 
 
-def test_nonfinite_scale_unsupported(lib):
-    assert call(lib, scale=float("inf")) == KDA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("entry", ["kda_fwd", "kda_fwd_recurrent"])
+def test_nonfinite_scale_unsupported(lib, entry):
+    assert call(lib, entry, scale=float("inf")) == KDA_ERR_UNSUPPORTED
+
+
+def test_recurrent_entry_limits_tokens(lib):
+    """The token-recurrent entry point takes at most 2^31 - 1 tokens per call."""
+    assert call(lib, "kda_fwd_recurrent", T=1 << 31) == KDA_ERR_UNSUPPORTED
 
 
 def test_check_cu_seqlens(lib):
