@@ -316,7 +316,7 @@ extern "C" kda_status_t kda_fwd_recurrent(const void *q, const void *k, const vo
                                 final_state, state_dtype, cu_seqlens, N, T, H);
     if (s != KDA_OK)
         return s;
-    if (T > INT32_MAX)
+    if (T > INT32_MAX || 2 * (int64_t)N * H > INT32_MAX)
         return KDA_ERR_UNSUPPORTED;
     const Problem p = make_problem(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                                    final_state, cu_seqlens, N, T, H);
@@ -367,8 +367,9 @@ extern "C" kda_status_t kda_device_status(kda_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KDA_ERR_CUDA;
-    unsigned int flag = 0, flag2 = 0;
-    if (read_and_clear_device_error(&flag) != cudaSuccess || prep_read_and_clear_error(&flag2) != cudaSuccess)
+    unsigned int flag = 0, flag2 = 0, flag3 = 0;
+    if (read_and_clear_device_error(&flag) != cudaSuccess || prep_read_and_clear_error(&flag2) != cudaSuccess ||
+        recurrent_read_and_clear_error(&flag3) != cudaSuccess)
         return KDA_ERR_CUDA;
-    return (flag | flag2) ? KDA_ERR_TIMEOUT : KDA_OK;
+    return (flag | flag2 | flag3) ? KDA_ERR_TIMEOUT : KDA_OK;
 }

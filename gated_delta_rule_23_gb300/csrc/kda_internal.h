@@ -29,7 +29,7 @@ struct Problem;
 cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t stream);
 // Recurrence kernel over N x H (sequence, head) pairs; state_kind 0 none, 1 bf16, 2 fp32.
 cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream);
-// Token-recurrent kernel over N x H x 2 (sequence, head, value half); no workspace.
+// Token-recurrent kernel, persistent over the N x H x 2 (sequence, head, value half) items; no workspace.
 cudaError_t launch_recurrent(const Problem &p, int state_kind, cudaStream_t stream);
 size_t recurrent_smem_bytes();
 size_t prep_smem_bytes();
@@ -37,5 +37,6 @@ size_t recur_smem_bytes();
 // Read the device-side "bounded wait expired" words of the recurrence / prep kernels and clear them.
 cudaError_t read_and_clear_device_error(unsigned int *flag);
 cudaError_t prep_read_and_clear_error(unsigned int *flag);
+cudaError_t recurrent_read_and_clear_error(unsigned int *flag);
 
 }  // namespace kda

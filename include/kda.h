@@ -164,14 +164,16 @@ kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v, const 
 /*
  * kda_fwd_recurrent -- the same operation as kda_fwd, evaluated token by token: the
  * per-token update of the guancyxx.cn FlashKDA article, section 一 (the recurrent form
- * that the chunked form of section 2.2 reorganises), one CTA per (sequence, head, half of
- * the values) with the state in fp32 registers.  Meant for decode steps (one or a few
- * tokens per sequence) and short prefills, where it moves only the state and the tokens
- * (no per-chunk operands, no workspace, no allocation); its cost grows linearly with the
- * longest sequence, so long sequences belong to kda_fwd.  Same arguments, layouts,
- * ownership (including in-place initial_state == final_state) and errors as kda_fwd, plus
- * KDA_ERR_UNSUPPORTED when T >= 2^31.  Results agree with kda_fwd's within the parity
- * tolerances, not bit for bit: this path keeps every operand in fp32.
+ * that the chunked form of section 2.2 reorganises).  A persistent grid walks the
+ * (sequence, head, half of the values) items; each CTA holds an item's 64 state columns
+ * in fp32 registers while the next items' states and tokens stream in.  Meant for decode
+ * steps (one or a few tokens per sequence) and short prefills, where it moves only the
+ * state and the tokens (no per-chunk operands, no workspace, no allocation); its cost
+ * grows linearly with the longest sequence, so long sequences belong to kda_fwd.  Same
+ * arguments, layouts, ownership (including in-place initial_state == final_state) and
+ * errors as kda_fwd, plus KDA_ERR_UNSUPPORTED when T >= 2^31 or 2 N H >= 2^31.  Results agree with
+ * kda_fwd's within the parity tolerances, not bit for bit: this path keeps every operand
+ * in fp32.
  */
 kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, const void *g, const void *beta,
                                float scale, void *out, const float *A_log, const float *dt_bias,
@@ -195,10 +197,11 @@ kda_status_t kda_check_cu_seqlens(const int64_t *host_cu_seqlens, int N, int64_t
 const char *kda_status_string(kda_status_t status);
 
 /*
- * Waits for `stream`, then reports whether any kda_fwd kernel on this device gave
- * up a bounded wait on the tensor cores since the last call (KDA_ERR_TIMEOUT; the
- * outputs of that call are not valid), and clears the report.  KDA_ERR_CUDA if the
- * stream or the query failed.  The kernel never spins without a limit and never traps.
+ * Waits for `stream`, then reports whether any kernel of this library on this device
+ * (kda_fwd and its variants, kda_fwd_recurrent) gave up a bounded wait on the tensor
+ * cores or on a bulk copy since the last call (KDA_ERR_TIMEOUT; the outputs of that call
+ * are not valid), and clears the report.  KDA_ERR_CUDA if the stream or the query failed.
+ * The kernels never spin without a limit and never trap.
  */
 kda_status_t kda_device_status(kda_stream_t stream);
 

@@ -72,8 +72,9 @@ def test_nonfinite_scale_unsupported(lib, entry):
 
 
 def test_recurrent_entry_limits_tokens(lib):
-    """The token-recurrent entry point takes at most 2^31 - 1 tokens per call."""
+    """The token-recurrent entry point takes fewer than 2^31 tokens and 2^30 (sequence, head) pairs."""
     assert call(lib, "kda_fwd_recurrent", T=1 << 31) == KDA_ERR_UNSUPPORTED
+    assert call(lib, "kda_fwd_recurrent", N=1 << 15, H=1 << 15) == KDA_ERR_UNSUPPORTED
 
 
 def test_check_cu_seqlens(lib):

@@ -60,18 +60,35 @@ def test_in_place_decode_matches_separate_buffers(state):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_decode_chain_equals_one_call():
-    """T one-token calls chaining an fp32 state give the bits of one T-token call."""
-    T = 21
-    p = make_problem(B=2, T=T, H=3, seed=304)
-    out_all, fin_all = run_rec(p)
+def chain(p, seg):
+    """Run p as consecutive calls of `seg` tokens, each starting from the last call's fp32 state."""
     state = p.initial_state
     outs = []
-    for t in range(T):
-        o, state = run_rec(token_slice(p, slice(t, t + 1), initial_state=state.astype(np.float32)))
+    for t0 in range(0, p.q.shape[1], seg):
+        o, state = run_rec(token_slice(p, slice(t0, t0 + seg), initial_state=state.astype(np.float32)))
         outs.append(o)
-    assert np.array_equal(np.concatenate(outs, axis=1), out_all)
-    assert np.array_equal(state, fin_all)
+    return np.concatenate(outs, axis=1), state
+
+
+def test_chain_of_stage_aligned_calls_equals_one_call():
+    """The kernel works in stages of 8 tokens from each sequence's start: calls of 8 tokens chaining an
+    fp32 state give the bits of one call over all the tokens."""
+    p = make_problem(B=2, T=24, H=3, seed=304)
+    out_all, fin_all = run_rec(p)
+    out_c, fin_c = chain(p, 8)
+    assert np.array_equal(out_c, out_all)
+    assert np.array_equal(fin_c, fin_all)
+
+
+def test_decode_chain_matches_one_call():
+    """One-token decode calls chaining an fp32 state agree with one call to fp32 rounding (the decay is
+    applied per token instead of per stage) and both meet the oracle."""
+    p = make_problem(B=2, T=21, H=3, seed=314)
+    out_all, fin_all = run_rec(p)
+    out_c, fin_c = chain(p, 1)
+    assert rel_l2(out_c, out_all) < 1e-5 and rel_l2(fin_c, fin_all) < 1e-5
+    o_ref, f_ref = oracle_run(p)
+    assert_parity(out_c, fin_c, o_ref, f_ref)
 
 
 def test_varlen_bitexact_against_separate_calls():
