@@ -37,7 +37,11 @@ from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, WORKLOADS, 
 METRIC = "KDA fwd ms & tokens·heads/s at T=8192 H=96; % of HBM/tensor roofline"
 UNIT = "tokens·heads/s"
 KERNEL_DIR = os.path.join(ROOT, "gated_delta_rule_23_gb300", "csrc")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kda_prep_recur_T8192_H96_bf16state.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+# device sources each kernel is compiled from (a profile summary is valid only for these)
+KERNEL_SOURCES = {"kda_prep_kernel": ["kda_device.cuh", "kda_prep.cu"],
+                  "kda_recur_kernel": ["kda_device.cuh", "kda_recur.cu"],
+                  "kda_recurrent_kernel": ["kda_device.cuh", "kda_recurrent.cu"]}
 SLOT_BYTES_PER_CHUNK_HEAD = 74240   # fp16 operands the prep kernel hands to the recurrence kernel per (64-token chunk, head)
 # FlashKDA on GB200, H=96 fixed length, T=8192: 1.01 ms (guancyxx.cn FlashKDA article, section 三,
 # GB200 table) -> tokens*heads per second.  Another machine: context, not the target.
@@ -78,27 +82,28 @@ def kernel_bytes(p):
     return {"kda_prep_kernel": prep, "kda_recur_kernel": recur}
 
 
-def kernel_source_hash():
-    """Hash of every CUDA source of the library (the profile summary is valid only for these)."""
+def kernel_source_hash(kernel):
+    """Hash of the device sources `kernel` is built from."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(KERNEL_DIR)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(KERNEL_DIR, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(KERNEL_DIR, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if taken on the current sources."""
-    try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
-        return None
-    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(kernel + r" traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
-        return None
-    return float(m_tr.group(1))
+    """DRAM bytes per launch of `kernel` from a committed ncu summary under profiles/, if it was taken
+    on the kernel's current sources."""
+    want = kernel_source_hash(kernel)
+    for name in sorted(os.listdir(PROFILE_DIR)):
+        if not name.endswith(".md"):
+            continue
+        text = open(os.path.join(PROFILE_DIR, name)).read()
+        m_src = re.search(kernel + r" source_sha256_16:\s*([0-9a-f]+)", text)
+        m_tr = re.search(kernel + r" traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+        if m_src and m_tr and m_src.group(1) == want:
+            return float(m_tr.group(1))
+    return None
 
 
 def peaks():
@@ -241,6 +246,53 @@ def run_reference(args, p, idx, rank):
     }), flush=True)
 
 
+DECODE_N, DECODE_H = 256, 96
+
+
+def measure_decode(stream, steps=50, warmup=5):
+    """One decode step (T = 1) for 256 sequences at 96 heads with an fp32 state updated in place,
+    through the token-recurrent entry point and, for comparison, through the chunked one.  The
+    state (1.6 GB) is larger than L2, so no flush is needed between steps."""
+    import torch
+    from gated_delta_rule_23_gb300 import kda_fwd, kda_fwd_recurrent
+    from gated_delta_rule_23_gb300.inputs import make_problem
+    from tests.gpu_util import to_device
+
+    p = make_problem(B=DECODE_N, T=1, H=DECODE_H, seed=77)
+    dev = to_device(p)
+    out = torch.empty_like(dev["q"])
+    st = dev["init"]
+    args = (dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+            p.lower_bound)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_rec = timed(lambda: kda_fwd_recurrent(*args, initial_state=st, final_state=st, stream=stream))
+    ms_chk = timed(lambda: kda_fwd(*args, initial_state=st, final_state=st, stream=stream))
+    th = DECODE_N * DECODE_H
+    state_bytes = 2 * th * 128 * 128 * 4
+    token_bytes = th * (4 * 128 * 2 + 2 + 128 * 2)
+    hbm = peaks()[0]
+    ach = (state_bytes + token_bytes) / (ms_rec * 1e-3) / 1e9
+    return {"entry": "kda_fwd_recurrent", "workload": f"decode step: N={DECODE_N} sequences x T=1, H={DECODE_H}, "
+                                                      "fp32 state in place",
+            "ms": ms_rec, "value": th / (ms_rec * 1e-3), "unit": "tokens*heads/s",
+            "bytes_per_step": state_bytes + token_bytes,
+            "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel", "achieved": ach, "peak": hbm,
+                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic("kda_recurrent_kernel")},
+            "chunked_entry_ms": ms_chk, "steps": steps, "warmup": warmup}
+
+
 def run_ours(args, p, idx, rank, world):
     import torch
     import torch.distributed as dist
@@ -372,6 +424,7 @@ def run_ours(args, p, idx, rank, world):
                 "d2h_bytes_per_step": runner.d2h_bytes()},
         "clocks": sampler.summary(),
         "gpu_launches": args.steps * (3 if p.cu_seqlens is not None else 2),
+        "decode": measure_decode(stream) if world == 1 else None,
     }
     print(json.dumps(line), flush=True)
 
@@ -387,6 +440,9 @@ def main():
                     help="profiling aid: shorten a fixed-length workload to T tokens (not a bench line)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="profiling aid: time only the device launches (no e2e, CPU baseline or clock sampling)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode step (token-recurrent entry point, N=256 x T=1, H=96) and print "
+                         "its measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
@@ -404,6 +460,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.decode_only:
+        if rank == 0:
+            print(json.dumps(measure_decode(torch.cuda.current_stream(), steps=args.steps, warmup=args.warmup)),
+                  flush=True)
+        return
     p = make_workload(args.workload)
     if args.T is not None:
         if p.cu_seqlens is not None:
