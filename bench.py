@@ -246,6 +246,25 @@ def run_reference(args, p, idx, rank):
     }), flush=True)
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: every rank passes its own measured milliseconds and gets the maximum
+    (a barrier plus an all-reduce; NCCL on the GPU, gloo in the CPU tests)."""
+    if world == 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    dist.barrier()
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank, world, ms):
+    """Whole-job throughput of `world` replicas: the units all ranks processed over the slowest rank's
+    time in milliseconds."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 DECODE_N, DECODE_H = 256, 96
 
 
@@ -326,13 +345,7 @@ def run_ours(args, p, idx, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
-    if world > 1:
-        dist.barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     sampler.mark(t_host0, t_host1)
     sampler.stop()
     ms_step = ms_total / args.steps
@@ -388,11 +401,11 @@ def run_ours(args, p, idx, rank, world):
         e2e_step()
     f1.record(runner.stream)
     runner.stream.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / n_e2e
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, "cuda")
 
     if rank != 0:
         return
-    th = p.token_heads() * world
+    th = p.token_heads() * world   # replicas: every rank processes the whole workload
     hbm, tc, peak_src = peaks()
     abytes = algorithmic_bytes(p)
     kbytes = kernel_bytes(p)
@@ -404,7 +417,8 @@ def run_ours(args, p, idx, rank, world):
     dom = max(kernel_ms, key=kernel_ms.get)
     achieved = kernels[dom]["achieved"]
     line = {
-        "metric": METRIC, "value": th / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": aggregate_throughput(p.token_heads(), world, ms_step), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (th / world) / (ms_step * 1e-3) / PAGES_GB200_TOKHEADS_PER_S,
         "dtype": "bf16", "precision": "bf16 inputs/outputs; tf32 and fp16 tensor-core operands; fp32 accumulation "
@@ -419,7 +433,7 @@ def run_ours(args, p, idx, rank, world):
                               "frac": abytes / (ms_step * 1e-3) / 1e9 / hbm,
                               "roofline_ms": abytes / (hbm * 1e9) * 1e3}},
         "cpu_baseline": cpu_baseline(p, idx),
-        "e2e": {"value": th / world / (e2e_ms * 1e-3) * world, "unit": UNIT, "ms_per_step": e2e_ms,
+        "e2e": {"value": aggregate_throughput(p.token_heads(), world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": runner.h2d_bytes(p.cu_seqlens is not None),
                 "d2h_bytes_per_step": runner.d2h_bytes()},
         "clocks": sampler.summary(),
