@@ -186,6 +186,7 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.chunk_off = nullptr;
     p.order = nullptr;
     p.slots = nullptr;
+    p.prep_pf = 0;
     return p;
 }
 

@@ -64,6 +64,7 @@ struct Problem {
     int N, H;
     int64_t T;
     int64_t nch_fixed;        // chunks per sequence without cu_seqlens
+    int prep_pf;              // prep: a CTA prefetches into L2 the rows of item blockIdx.x + prep_pf (0: off)
 };
 
 // ---------------------------------------------------------------- small helpers

@@ -35,6 +35,14 @@ namespace kda {
 namespace {
 
 constexpr int PREP_THREADS = 256;
+#ifndef KDA_PREP_PF_BETA
+#define KDA_PREP_PF_BETA 1
+#endif
+#ifndef KDA_PREP_PF_QUARTER_WAVES
+#define KDA_PREP_PF_QUARTER_WAVES 3
+#endif
+// L2 prefetch distance in quarters of a wave of resident CTAs (0: off)
+constexpr int PREP_PF_QUARTER_WAVES = KDA_PREP_PF_QUARTER_WAVES;
 constexpr int TMEM_COLS = 128;          // Akk / Aqk accumulators: 128 lanes x 96 columns
 // tf32 operand tiles of the Akk / Aqk product for one half of the channels (the gate pass runs in
 // two passes of 64 channels; the tensor cores accumulate both).  No-swizzle K-major core-matrix
@@ -76,21 +84,13 @@ __host__ __device__ constexpr int ops_off(int r, int kgrp) { return (r >> 3) * O
 __device__ __forceinline__ int h128(int r, int c) { return r * 256 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
 __device__ __forceinline__ int h64(int r, int c) { return r * 128 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
 
-template <bool VARLEN>
-__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem p)
-{
-    extern __shared__ __align__(128) unsigned char sm[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int H = p.H;
-    const int64_t item = blockIdx.x;
-    const int h = (int)(item % H);
-    const int64_t gc = item / H;
+__device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 
-    // -------- this CTA's chunk: first token tok0 and L valid tokens
-    int64_t tok0, rem;
+// first token and valid length of chunk gc (a global chunk index over all sequences)
+template <bool VARLEN>
+__device__ __forceinline__ void chunk_tokens(const Problem &p, int64_t gc, int64_t &tok0, int64_t &rem)
+{
     if (VARLEN) {
-        if (gc >= p.chunk_off[p.N])
-            return;
         int lo = 0, hi = p.N - 1;   // the last sequence whose first chunk is <= gc
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -107,6 +107,23 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         tok0 = n * p.T + c * CH;
         rem = p.T - c * CH;
     }
+}
+
+template <bool VARLEN>
+__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem p)
+{
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = p.H;
+    const int64_t item = blockIdx.x;
+    const int h = (int)(item % H);
+    const int64_t gc = item / H;
+
+    // -------- this CTA's chunk: first token tok0 and L valid tokens
+    if (VARLEN && gc >= p.chunk_off[p.N])
+        return;
+    int64_t tok0, rem;
+    chunk_tokens<VARLEN>(p, gc, tok0, rem);
     const int L = (int)(rem < CH ? rem : CH);
     unsigned char *slot = p.slots + (size_t)item * SLOT_BYTES;
 
@@ -149,6 +166,32 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
             gv[r] = ldg_nc16(p.g + off);
         } else {
             qv[r] = kv[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    // rows of the item that starts about prep_pf / resident CTAs waves later: q, k, g and v
+    // into L2 (two 128-byte lines per token and tensor), so that its first loads hit L2
+    if (p.prep_pf > 0 && item + p.prep_pf < (int64_t)gridDim.x) {
+        const int64_t pit = item + p.prep_pf, pgc = pit / H;
+        const int ph = (int)(pit % H);
+        if (!VARLEN || pgc < p.chunk_off[p.N]) {
+            int64_t ptok0, prem;
+            chunk_tokens<VARLEN>(p, pgc, ptok0, prem);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int li = tid + m * PREP_THREADS, which = li >> 7, t = (li >> 1) & (CH - 1);
+                if (t < prem) {
+                    const __nv_bfloat16 *base = which == 0 ? p.q : which == 1 ? p.k : which == 2 ? p.g : p.v;
+                    prefetch_l2(base + ((size_t)(ptok0 + t) * H + ph) * D + (li & 1) * 64);
+                }
+            }
+#if KDA_PREP_PF_BETA
+            // beta of the chunk for every head (contiguous, shared by the chunk's CTAs): by its first head
+            if (ph == 0) {
+                const int64_t nb = (prem < CH ? prem : CH) * H * 2;   // bytes
+                for (int64_t o = (int64_t)tid * 128; o < nb; o += (int64_t)PREP_THREADS * 128)
+                    prefetch_l2(reinterpret_cast<const unsigned char *>(p.beta + (size_t)ptok0 * H) + o);
+            }
+#endif
         }
     }
     if (tid < CH)
@@ -641,7 +684,18 @@ cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
         if (dev < 64)
             configured[dev] = true;
     }
-    kda_prep_kernel<VARLEN><<<(unsigned)items, PREP_THREADS, PREP_SMEM, stream>>>(p);
+    static int sms[64] = {};
+    int nsm = dev < 64 ? sms[dev] : 0;
+    if (nsm == 0) {
+        err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess)
+            return err;
+        if (dev < 64)
+            sms[dev] = nsm;
+    }
+    Problem q = p;
+    q.prep_pf = PREP_PF_QUARTER_WAVES * 2 * nsm / 4;   // two resident CTAs per SM
+    kda_prep_kernel<VARLEN><<<(unsigned)items, PREP_THREADS, PREP_SMEM, stream>>>(q);
     return cudaGetLastError();
 }
 
