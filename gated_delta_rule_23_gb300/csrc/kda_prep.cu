@@ -57,6 +57,10 @@ constexpr int OPS_BYTES = OPS_B + 12 * OPS_SBO;     // 72128
 // shared memory map (bytes)
 constexpr int OFF_OPS = 0;
 constexpr int OFF_PART = OFF_OPS;                   // fp32 [8 warps][2][64] sums of squares (before the gate pass)
+// q, k, g of the chunk as loaded (bf16 [64 t][128 c] each, 16-byte chunks XOR-swizzled by t / 4), read into
+// registers before the gate pass overwrites the region
+constexpr int OFF_STG = OFF_PART + 8 * 2 * CH * 4;   // 4096
+static_assert(OFF_STG + 3 * CH * D * 2 <= OPS_BYTES, "staging inside the operand tiles");
 // reused once the Akk / Aqk product has completed:
 constexpr int PA = 68;                              // fp32 pitch of 64-wide matrices
 constexpr int OFF_AKK = OFF_OPS;                    // fp32 [64][68] b_i Akk (strictly lower)
@@ -83,12 +87,16 @@ __host__ __device__ constexpr int ops_off(int r, int kgrp) { return (r >> 3) * O
 // by row (conflict-free ldmatrix)
 __device__ __forceinline__ int h128(int r, int c) { return r * 256 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
 __device__ __forceinline__ int h64(int r, int c) { return r * 128 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
+// byte offset of 16-byte chunk c16 of token row t in the q / k / g staging tiles: swizzled by t / 4, so
+// that the 8 runs a quarter-warp reads (rows 4 run + r) fall on 8 different bank groups
+__device__ __forceinline__ int stg_off(int t, int c16) { return t * 256 + ((c16 ^ ((t >> 2) & 7)) << 4); }
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 
-// first token and valid length of chunk gc (a global chunk index over all sequences)
+// first token and valid length of chunk gc (a global chunk index over all sequences; the launch
+// keeps every item index, and so gc, below 2^31, so the divisions are 32-bit)
 template <bool VARLEN>
-__device__ __forceinline__ void chunk_tokens(const Problem &p, int64_t gc, int64_t &tok0, int64_t &rem)
+__device__ __forceinline__ void chunk_tokens(const Problem &p, uint32_t gc, int64_t &tok0, int64_t &rem)
 {
     if (VARLEN) {
         int lo = 0, hi = p.N - 1;   // the last sequence whose first chunk is <= gc
@@ -99,13 +107,13 @@ __device__ __forceinline__ void chunk_tokens(const Problem &p, int64_t gc, int64
             else
                 hi = mid - 1;
         }
-        const int64_t c = gc - p.chunk_off[lo];
+        const int64_t c = (int64_t)gc - p.chunk_off[lo];
         tok0 = p.cu[lo] + c * CH;
         rem = p.cu[lo + 1] - tok0;
     } else {
-        const int64_t n = gc / p.nch_fixed, c = gc % p.nch_fixed;
-        tok0 = n * p.T + c * CH;
-        rem = p.T - c * CH;
+        const uint32_t nch = (uint32_t)p.nch_fixed, n = gc / nch, c = gc - n * nch;
+        tok0 = (int64_t)n * p.T + (int64_t)c * CH;
+        rem = p.T - (int64_t)c * CH;
     }
 }
 
@@ -115,12 +123,12 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
-    const int64_t item = blockIdx.x;
-    const int h = (int)(item % H);
-    const int64_t gc = item / H;
+    const uint32_t item = blockIdx.x;
+    const uint32_t gc = item / (uint32_t)H;
+    const int h = (int)(item - gc * (uint32_t)H);
 
     // -------- this CTA's chunk: first token tok0 and L valid tokens
-    if (VARLEN && gc >= p.chunk_off[p.N])
+    if (VARLEN && (int64_t)gc >= p.chunk_off[p.N])
         return;
     int64_t tok0, rem;
     chunk_tokens<VARLEN>(p, gc, tok0, rem);
@@ -134,46 +142,42 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 8);
     bool hung = false;
 
+    // -------- phase 0: the chunk's q, k, g rows into the staging tiles (cp.async, 512 contiguous bytes per
+    // warp instruction; rows past the end zero-filled), the beta and gate parameters into registers
+#pragma unroll
+    for (int m = 0; m < (3 * CH * 16) / PREP_THREADS; ++m) {
+        const int idx = tid + m * PREP_THREADS, which = idx >> 10, t = (idx >> 4) & (CH - 1), c16 = idx & 15;
+        const __nv_bfloat16 *base = which == 0 ? p.q : which == 1 ? p.k : p.g;
+        const bool valid = t < L;
+        cp_async16(smem_u32(sm + OFF_STG + which * (CH * D * 2) + stg_off(t, c16)),
+                   base + ((size_t)(tok0 + (valid ? t : 0)) * H + h) * D + c16 * 8, valid);
+    }
+    cp_async_commit();
+    // lane roles: channel group cgrp (8 channels), run (4 consecutive tokens); sub-block = run / 4
+    const int cgrp = lane >> 4, run = lane & 15, sblk = run >> 2, s4 = run & 3;
+    const int c0 = warp * 16 + cgrp * 8;
+    const int kgrp = warp * 2 + cgrp;   // this thread's 4-channel group in each pass's compact K
+    const __nv_bfloat16 bval = tid < L ? p.beta[(tok0 + (tid < L ? tid : 0)) * H + h] : __float2bfloat16(0.f);
+    const float alog = p.A_log[h];
+    const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0);
+    const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0 + 4);
+
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
         tc_fence_before();
     }
-    if (tid == 0) {
+    if (tid == 32) {
         mbar_init(mbarA, 1);
         mbar_fence_init();
     }
-
-    // -------- phase 0: this thread's q, k, g and the chunk's beta / gate parameters
-    // lane roles: channel group cgrp (8 channels), run (4 consecutive tokens); sub-block = run / 4
-    const int cgrp = lane >> 4, run = lane & 15, sblk = run >> 2, s4 = run & 3;
-    const int c0 = warp * 16 + cgrp * 8;
-    const int kgrp = warp * 2 + cgrp;   // this thread's 4-channel group in each pass's compact K
-    // every global load of this phase is issued before any of them is used
-    const __nv_bfloat16 bval = tid < L ? p.beta[(tok0 + (tid < L ? tid : 0)) * H + h] : __float2bfloat16(0.f);
-    const float alog = p.A_log[h];
-    const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0);
-    const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0 + 4);
-    uint4 qv[4], kv[4], gv[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int t = 4 * run + r;
-        if (t < L) {
-            const size_t off = ((size_t)(tok0 + t) * H + h) * D + c0;
-            qv[r] = ldg_nc16(p.q + off);
-            kv[r] = ldg_nc16(p.k + off);
-            gv[r] = ldg_nc16(p.g + off);
-        } else {
-            qv[r] = kv[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
     // rows of the item that starts about prep_pf / resident CTAs waves later: q, k, g and v
     // into L2 (two 128-byte lines per token and tensor), so that its first loads hit L2
-    if (p.prep_pf > 0 && item + p.prep_pf < (int64_t)gridDim.x) {
-        const int64_t pit = item + p.prep_pf, pgc = pit / H;
-        const int ph = (int)(pit % H);
-        if (!VARLEN || pgc < p.chunk_off[p.N]) {
+    if (p.prep_pf > 0 && item + (uint32_t)p.prep_pf < gridDim.x) {
+        const uint32_t pit = item + (uint32_t)p.prep_pf, pgc = pit / (uint32_t)H;
+        const int ph = (int)(pit - pgc * (uint32_t)H);
+        if (!VARLEN || (int64_t)pgc < p.chunk_off[p.N]) {
             int64_t ptok0, prem;
             chunk_tokens<VARLEN>(p, pgc, ptok0, prem);
 #pragma unroll
@@ -198,6 +202,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         bt[tid] = tid < L ? sigmoid_fast(__bfloat162float(bval)) : 0.f;
     const float eA = expf(alog);
     const float dtb[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    cp_async_wait_all();
+    __syncthreads();
+    // this thread's 4 tokens x 8 channels of q, k, g
+    uint4 qv[4], kv[4], gv[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int o = OFF_STG + stg_off(4 * run + r, 2 * warp + cgrp);
+        qv[r] = *reinterpret_cast<const uint4 *>(sm + o);
+        kv[r] = *reinterpret_cast<const uint4 *>(sm + o + CH * D * 2);
+        gv[r] = *reinterpret_cast<const uint4 *>(sm + o + 2 * CH * D * 2);
+    }
 
     // -------- phase 1: row norms of q and k
     {
