@@ -96,7 +96,34 @@ __device__ __forceinline__ uint32_t to_tf32(float x)
 // Round to tf32 (10 explicit mantissa bits), to nearest with ties away from zero, on the integer
 // pipe: adding half a tf32 ulp to the magnitude bits and truncating is that rounding for finite
 // values (a carry into the exponent is the correct round-up).
-__device__ __forceinline__ float tf32r(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
+// fp32 value prepared for a kind::tf32 tensor-core operand: the tensor cores use the top 19 bits of an
+// fp32 operand and drop the low 13, so adding half a tf32 unit to the bit pattern makes that drop a
+// round-to-nearest (ties away from zero, as cvt.rna.tf32.f32 rounds finite values)
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(__float_as_uint(x) + 0x1000u); }
+
+// ---------------------------------------------------------------- packed fp32 pairs (f32x2)
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2_pack(float lo, float hi)
+{
+    return ((f2)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(f2 a) { return __uint_as_float((uint32_t)a); }
+__device__ __forceinline__ float f2_hi(f2 a) { return __uint_as_float((uint32_t)(a >> 32)); }
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b)
+{
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// bf16x2 word (low half = the even element) -> packed fp32 pair, exactly
+__device__ __forceinline__ f2 f2_bf16x2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ f2 f2_tf32r(f2 a) { return f2_pack(tf32r(f2_lo(a)), tf32r(f2_hi(a))); }
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 {
     const __half2 h = __floats2half2_rn(lo, hi);

@@ -337,21 +337,32 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 const uint32_t qw[2] = {hc ? qv[r].z : qv[r].x, hc ? qv[r].w : qv[r].y};
                 const uint32_t kw[2] = {hc ? kv[r].z : kv[r].x, hc ? kv[r].w : kv[r].y};
                 float lq[4], lk[4], r0[4], r1[4], qt[4], kg[4], kt[4];
+                // channel pairs (2 pp, 2 pp + 1) as packed fp32: the same products, two per instruction
+                const f2 rq2 = f2_pack(rqt[r], rqt[r]), rk2 = f2_pack(rkt[r], rkt[r]);
+                const bool even = (sblk & 1) == 0;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float qh = ((i & 1) ? bf16_hi(qw[i >> 1]) : bf16_lo(qw[i >> 1])) * rqt[r];
-                    const float kh = ((i & 1) ? bf16_hi(kw[i >> 1]) : bf16_lo(kw[i >> 1])) * rkt[r];
-                    const float P = pf[r][i], rc = rcp_approx(P), E = Dv[i] * rc;   // rc = 1 / P
-                    const bool even = (sblk & 1) == 0;
-                    const float Lf = even ? P * iD[i] : P;                         // 1 / E or P
-                    lq[i] = tf32r(qh * Lf);
-                    lk[i] = tf32r(kh * Lf);
-                    r1[i] = tf32r(kh * (sblk == 3 ? rc : E * f1[i]));
-                    r0[i] = tf32r(kh * (sblk == 0 ? E : rc));
-                    const float G = pre[i] * P;
-                    qt[i] = qh * G;
-                    kg[i] = kh * G;
-                    kt[i] = kh * (E * post[i]);
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int i = 2 * pp;
+                    const f2 qh = f2_mul(f2_bf16x2(qw[pp]), rq2);
+                    const f2 kh = f2_mul(f2_bf16x2(kw[pp]), rk2);
+                    const f2 P = f2_pack(pf[r][i], pf[r][i + 1]);
+                    const f2 rc = f2_pack(rcp_approx(pf[r][i]), rcp_approx(pf[r][i + 1]));   // 1 / P
+                    const f2 E = f2_mul(f2_pack(Dv[i], Dv[i + 1]), rc);
+                    const f2 Lf = even ? f2_mul(P, f2_pack(iD[i], iD[i + 1])) : P;      // 1 / E or P
+                    const f2 l_q = f2_tf32r(f2_mul(qh, Lf)), l_k = f2_tf32r(f2_mul(kh, Lf));
+                    const f2 s1 = sblk == 3 ? rc : f2_mul(E, f2_pack(f1[i], f1[i + 1]));
+                    const f2 r_1 = f2_tf32r(f2_mul(kh, s1));
+                    const f2 r_0 = f2_tf32r(f2_mul(kh, sblk == 0 ? E : rc));
+                    const f2 G = f2_mul(f2_pack(pre[i], pre[i + 1]), P);
+                    const f2 q_t = f2_mul(qh, G), k_g = f2_mul(kh, G);
+                    const f2 k_t = f2_mul(kh, f2_mul(E, f2_pack(post[i], post[i + 1])));
+                    lq[i] = f2_lo(l_q); lq[i + 1] = f2_hi(l_q);
+                    lk[i] = f2_lo(l_k); lk[i + 1] = f2_hi(l_k);
+                    r1[i] = f2_lo(r_1); r1[i + 1] = f2_hi(r_1);
+                    r0[i] = f2_lo(r_0); r0[i + 1] = f2_hi(r_0);
+                    qt[i] = f2_lo(q_t); qt[i + 1] = f2_hi(q_t);
+                    kg[i] = f2_lo(k_g); kg[i + 1] = f2_hi(k_g);
+                    kt[i] = f2_lo(k_t); kt[i + 1] = f2_hi(k_t);
                 }
                 const int ra = (t >> 5) * 64 + (t & 31);
                 *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_A + ops_off(ra, kgrp)) =

@@ -77,28 +77,6 @@ struct RcSmem {
 static_assert(sizeof(RcRaw) % 16 == 0, "raw slots keep 16-byte alignment");
 static_assert(sizeof(RcSmem<2>) <= 113 * 1024, "two CTAs per SM");
 
-// ---------------------------------------------------------------- packed fp32 pairs
-typedef unsigned long long f2;
-__device__ __forceinline__ f2 f2_pack(float lo, float hi)
-{
-    return ((f2)__float_as_uint(hi) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ float f2_lo(f2 a) { return __uint_as_float((uint32_t)a); }
-__device__ __forceinline__ float f2_hi(f2 a) { return __uint_as_float((uint32_t)(a >> 32)); }
-__device__ __forceinline__ f2 f2_mul(f2 a, f2 b)
-{
-    f2 d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c)
-{
-    f2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-// bf16x2 word (low half = even key) -> packed fp32 pair, exactly
-__device__ __forceinline__ f2 f2_bf16x2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
 
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
