@@ -518,12 +518,16 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         bulk_commit();
     }
 
-    // -------- phase 4: Tm = (I + Akk)^-1, blocked by 16-token sub-blocks: fp32 forward
-    //          substitution on the diagonal blocks, then Tm_{bi,bj} = -Tm_{bi,bi} sum_m A_{bi,m} Tm_{m,bj}
-    //          by distance bi - bj on fp16 mma.sync (fp32 accumulation)
+    // -------- phase 4: Tm = (I + Akk)^-1 by 16-token blocks: fp32 forward substitution on the
+    //          diagonal blocks, then the two 32-token halves' off-diagonal blocks
+    //          t_{1,0} = -t_{1,1} A_{1,0} t_{0,0}, t_{3,2} = -t_{3,3} A_{3,2} t_{2,2}, then the lower-left
+    //          32 x 32 block T21 = -T2 A21 T1 of the whole chunk (T1, T2 the halves' inverses), on fp16
+    //          mma.sync with fp32 accumulation.  Every block writer also stores its part of
+    //          T' = Tm diag(b) in fp16 for the WY products (blocks above the diagonal are never read).
     {
         const float *Akk = reinterpret_cast<const float *>(sm + OFF_AKK);
         float *Tm = reinterpret_cast<float *>(sm + OFF_TM);
+        unsigned char *tp = sm + OFF_TP;
         if (warp < NSB && lane < SB) {
             const int b = warp, j = lane;
             float x[SB], acc[SB];
@@ -537,67 +541,82 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 for (int i = l + 1; i < SB; ++i)
                     acc[i] = fmaf(Akk[(b * SB + i) * PA + b * SB + l], x[l], acc[i]);
             }
+            const float bj = bt[b * SB + j];
 #pragma unroll
-            for (int i = 0; i < SB; ++i)
+            for (int i = 0; i < SB; ++i) {
                 Tm[(b * SB + i) * PA + b * SB + j] = x[i];
+                *reinterpret_cast<__half *>(tp + h64(b * SB + i, b * SB + j)) = __float2half_rn(x[i] * bj);
+            }
         }
         __syncthreads();
         const int gq = lane >> 2, t4 = lane & 3;
         float *Zw = reinterpret_cast<float *>(sm + OFF_ZW) + warp * 128;   // [16][8]
-#pragma unroll 1
-        for (int dist = 1; dist < NSB; ++dist) {
-            if (warp < 2 * (NSB - dist)) {
-                const int bj = warp >> 1, nt = warp & 1, bi = bj + dist;
-                const int ra = bi * SB + gq, cn = bj * SB + nt * 8 + gq;
-                float z[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int m = bj; m < bi; ++m) {
-                    const int ka = m * SB + 2 * t4;
-                    const float2 a0 = *reinterpret_cast<const float2 *>(Akk + ra * PA + ka);
-                    const float2 a1 = *reinterpret_cast<const float2 *>(Akk + (ra + 8) * PA + ka);
-                    const float2 a2 = *reinterpret_cast<const float2 *>(Akk + ra * PA + ka + 8);
-                    const float2 a3 = *reinterpret_cast<const float2 *>(Akk + (ra + 8) * PA + ka + 8);
-                    const uint32_t af[4] = {pack_half2(a0.x, a0.y), pack_half2(a1.x, a1.y), pack_half2(a2.x, a2.y),
-                                            pack_half2(a3.x, a3.y)};
-                    const uint32_t b0 = pack_half2(Tm[ka * PA + cn], Tm[(ka + 1) * PA + cn]);
-                    const uint32_t b1 = pack_half2(Tm[(ka + 8) * PA + cn], Tm[(ka + 9) * PA + cn]);
-                    mma_f16(z, af, b0, b1);
-                }
-                // Z (16 x 8) through this warp's scratch into the B-operand layout
-                Zw[gq * 8 + 2 * t4] = z[0];
-                Zw[gq * 8 + 2 * t4 + 1] = z[1];
-                Zw[(gq + 8) * 8 + 2 * t4] = z[2];
-                Zw[(gq + 8) * 8 + 2 * t4 + 1] = z[3];
-                __syncwarp();
-                const int kd = bi * SB + 2 * t4;
-                const float2 d0 = *reinterpret_cast<const float2 *>(Tm + ra * PA + kd);
-                const float2 d1 = *reinterpret_cast<const float2 *>(Tm + (ra + 8) * PA + kd);
-                const float2 d2 = *reinterpret_cast<const float2 *>(Tm + ra * PA + kd + 8);
-                const float2 d3 = *reinterpret_cast<const float2 *>(Tm + (ra + 8) * PA + kd + 8);
-                const uint32_t df[4] = {pack_half2(d0.x, d0.y), pack_half2(d1.x, d1.y), pack_half2(d2.x, d2.y),
-                                        pack_half2(d3.x, d3.y)};
-                const uint32_t zb0 = pack_half2(Zw[(2 * t4) * 8 + gq], Zw[(2 * t4 + 1) * 8 + gq]);
-                const uint32_t zb1 = pack_half2(Zw[(2 * t4 + 8) * 8 + gq], Zw[(2 * t4 + 9) * 8 + gq]);
-                float tt[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16(tt, df, zb0, zb1);
-                const int cc = bj * SB + nt * 8 + 2 * t4;
-                *reinterpret_cast<float2 *>(Tm + ra * PA + cc) = make_float2(-tt[0], -tt[1]);
-                *reinterpret_cast<float2 *>(Tm + (ra + 8) * PA + cc) = make_float2(-tt[2], -tt[3]);
-            }
-            __syncthreads();
+        // A operand (16 x 16 block at rows r0, columns k0) of an fp32 [64][PA] matrix, as fp16
+        auto frag_a = [&](const float *M, int r0, int k0, uint32_t (&f)[4]) {
+            const float2 a0 = *reinterpret_cast<const float2 *>(M + (r0 + gq) * PA + k0 + 2 * t4);
+            const float2 a1 = *reinterpret_cast<const float2 *>(M + (r0 + gq + 8) * PA + k0 + 2 * t4);
+            const float2 a2 = *reinterpret_cast<const float2 *>(M + (r0 + gq) * PA + k0 + 2 * t4 + 8);
+            const float2 a3 = *reinterpret_cast<const float2 *>(M + (r0 + gq + 8) * PA + k0 + 2 * t4 + 8);
+            f[0] = pack_half2(a0.x, a0.y);
+            f[1] = pack_half2(a1.x, a1.y);
+            f[2] = pack_half2(a2.x, a2.y);
+            f[3] = pack_half2(a3.x, a3.y);
+        };
+        // z += A_{m, k} Tm_{k, n-tile}: rows m0 .. + 15, Tm rows k0 .. + 15, column cn of this lane
+        auto acc_az = [&](float (&z)[4], int m0, int k0, int cn) {
+            uint32_t af[4];
+            frag_a(Akk, m0, k0, af);
+            const uint32_t b0 = pack_half2(Tm[(k0 + 2 * t4) * PA + cn], Tm[(k0 + 2 * t4 + 1) * PA + cn]);
+            const uint32_t b1 = pack_half2(Tm[(k0 + 2 * t4 + 8) * PA + cn], Tm[(k0 + 2 * t4 + 9) * PA + cn]);
+            mma_f16(z, af, b0, b1);
+        };
+        // tt += Tm_{r0.., c0..} Z, with Z (16 x 8, this warp's fragment z) through the warp's scratch
+        auto acc_tz = [&](float (&tt)[4], int r0, int c0t, const float (&z)[4]) {
+            Zw[gq * 8 + 2 * t4] = z[0];
+            Zw[gq * 8 + 2 * t4 + 1] = z[1];
+            Zw[(gq + 8) * 8 + 2 * t4] = z[2];
+            Zw[(gq + 8) * 8 + 2 * t4 + 1] = z[3];
+            __syncwarp();
+            uint32_t df[4];
+            frag_a(Tm, r0, c0t, df);
+            const uint32_t zb0 = pack_half2(Zw[(2 * t4) * 8 + gq], Zw[(2 * t4 + 1) * 8 + gq]);
+            const uint32_t zb1 = pack_half2(Zw[(2 * t4 + 8) * 8 + gq], Zw[(2 * t4 + 9) * 8 + gq]);
+            mma_f16(tt, df, zb0, zb1);
+            __syncwarp();   // the scratch is free again
+        };
+        // -tt -> Tm block (rows r0.., columns cc = n-tile column base + 2 t4) and T'
+        auto put = [&](int r0, int cc, const float (&tt)[4]) {
+            *reinterpret_cast<float2 *>(Tm + (r0 + gq) * PA + cc) = make_float2(-tt[0], -tt[1]);
+            *reinterpret_cast<float2 *>(Tm + (r0 + gq + 8) * PA + cc) = make_float2(-tt[2], -tt[3]);
+            const float b0 = bt[cc], b1 = bt[cc + 1];
+            *reinterpret_cast<uint32_t *>(tp + h64(r0 + gq, cc)) = pack_half2(-tt[0] * b0, -tt[1] * b1);
+            *reinterpret_cast<uint32_t *>(tp + h64(r0 + gq + 8, cc)) = pack_half2(-tt[2] * b0, -tt[3] * b1);
+        };
+        // level A: t_{1,0} and t_{3,2} (warps 0..3: block, n-tile)
+        if (warp < 4) {
+            const int bj = (warp >> 1) * 2, bi = bj + 1, nt = warp & 1;
+            float z[4] = {0.f, 0.f, 0.f, 0.f}, tt[4] = {0.f, 0.f, 0.f, 0.f};
+            acc_az(z, bi * SB, bj * SB, bj * SB + nt * 8 + gq);
+            acc_tz(tt, bi * SB, bi * SB, z);
+            put(bi * SB, bj * SB + nt * 8 + 2 * t4, tt);
         }
-        // T' = Tm diag(b), fp16 [t][j]; blocks above the diagonal are zero
+        __syncthreads();
+        // level B: T21 blocks (bi, bj), bi in {2, 3}, bj in {0, 1} (warps: bi, bj, n-tile):
+        //   Z_{m,bj} = sum_{k=bj..1} A_{m,k} t_{k,bj},  t_{bi,bj} = -sum_{m=2..bi} t_{bi,m} Z_{m,bj}
+        {
+            const int bi = 2 + (warp >> 2), bj = (warp >> 1) & 1, nt = warp & 1;
+            const int cn = bj * SB + nt * 8 + gq;
+            float tt[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < (CH * CH / 8) / PREP_THREADS; ++m) {
-            const int idx = tid + m * PREP_THREADS, r = idx >> 3, c = (idx & 7) * 8;
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int ca = c + 2 * e, cbb = ca + 1;
-                const float x0 = (ca >> 4) <= (r >> 4) ? Tm[r * PA + ca] * bt[ca] : 0.f;
-                const float x1 = (cbb >> 4) <= (r >> 4) ? Tm[r * PA + cbb] * bt[cbb] : 0.f;
-                w[e] = pack_half2(x0, x1);
+            for (int m = 2; m < 4; ++m) {
+                if (m > bi)
+                    break;
+                float z[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int k = bj; k < 2; ++k)
+                    acc_az(z, m * SB, k * SB, cn);
+                acc_tz(tt, bi * SB, m * SB, z);
             }
-            *reinterpret_cast<uint4 *>(sm + OFF_TP + h64(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            put(bi * SB, bj * SB + nt * 8 + 2 * t4, tt);
         }
     }
     cp_async_wait_all();
