@@ -91,9 +91,9 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary under profiles/, if it was taken
-    on the kernel's current sources."""
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` (a workload index, or "decode") from a committed
+    ncu summary under profiles/, if it was taken on that workload and on the kernel's current sources."""
     want = kernel_source_hash(kernel)
     for name in sorted(os.listdir(PROFILE_DIR)):
         if not name.endswith(".md"):
@@ -101,7 +101,8 @@ def measured_traffic(kernel):
         text = open(os.path.join(PROFILE_DIR, name)).read()
         m_src = re.search(kernel + r" source_sha256_16:\s*([0-9a-f]+)", text)
         m_tr = re.search(kernel + r" traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
-        if m_src and m_tr and m_src.group(1) == want:
+        m_wl = re.search(kernel + r" traffic_workload:\s*(\S+)", text)
+        if m_src and m_tr and m_wl and m_src.group(1) == want and m_wl.group(1) == str(workload):
             return float(m_tr.group(1))
     return None
 
@@ -308,7 +309,7 @@ def measure_decode(stream, steps=50, warmup=5):
             "ms": ms_rec, "value": th / (ms_rec * 1e-3), "unit": "tokens*heads/s",
             "bytes_per_step": state_bytes + token_bytes,
             "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel", "achieved": ach, "peak": hbm,
-                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic("kda_recurrent_kernel")},
+                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic("kda_recurrent_kernel", "decode")},
             "chunked_entry_ms": ms_chk, "steps": steps, "warmup": warmup}
 
 
@@ -413,7 +414,7 @@ def run_ours(args, p, idx, rank, world):
     for name, kms in kernel_ms.items():
         ach = kbytes[name] / (kms * 1e-3) / 1e9
         kernels[name] = {"ms": kms, "bytes_per_launch": kbytes[name], "achieved": ach, "frac": ach / hbm,
-                         "traffic": measured_traffic(name)}
+                         "traffic": measured_traffic(name, idx if args.T is None else f"{idx}@T{args.T}")}
     dom = max(kernel_ms, key=kernel_ms.get)
     achieved = kernels[dom]["achieved"]
     line = {
