@@ -316,7 +316,7 @@ def measure_decode(stream, steps=50, warmup=5):
 def run_ours(args, p, idx, rank, world):
     import torch
     import torch.distributed as dist
-    from gated_delta_rule_23_gb300 import KDAHostRunner, kda_fwd
+    from gated_delta_rule_23_gb300 import kda_fwd, kda_fwd_host
     from tests.gpu_util import to_device
 
     dev = to_device(p)
@@ -376,33 +376,33 @@ def run_ours(args, p, idx, rank, world):
                   flush=True)
         return
 
-    # end to end through the public API with host buffers (copies inside the timed region)
+    # end to end through the C-ABI host-buffer entry point (kda_fwd_host): pinned host inputs in, host
+    # results out; the call copies, computes and copies back before it returns
     has_init = p.initial_state is not None
-    runner = KDAHostRunner(p.B, p.T, p.H, N=(None if p.cu_seqlens is None else p.N), state_dtype=dev["sdt"],
-                           has_initial=has_init, want_final=p.want_final and dev["sdt"] is not None)
     pin = lambda t: t.cpu().pin_memory()
     host = dict(q=pin(dev["q"]), k=pin(dev["k"]), v=pin(dev["v"]), g=pin(dev["g"]), beta=pin(dev["beta"]),
                 A_log=pin(dev["A_log"]), dt_bias=pin(dev["dt_bias"]),
                 init=pin(dev["init"]) if has_init else None, cu=pin(dev["cu"]) if dev["cu"] is not None else None)
     out_h = torch.empty(p.q.shape, dtype=torch.bfloat16).pin_memory()
-    fin_h = torch.empty(runner.fin.shape, dtype=runner.fin.dtype).pin_memory() if runner.fin is not None else None
+    fin_h = (torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"]).pin_memory()
+             if (p.want_final and dev["sdt"] is not None) else None)
 
     def e2e_step():
-        runner.run(host["q"], host["k"], host["v"], host["g"], host["beta"], p.scale, host["A_log"],
-                   host["dt_bias"], p.lower_bound, initial_state=host["init"], cu_seqlens=host["cu"],
-                   out_host=out_h, final_host=fin_h)
+        kda_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"], p.scale, out_h, host["A_log"],
+                     host["dt_bias"], p.lower_bound, initial_state=host["init"], final_state=fin_h,
+                     cu_seqlens=host["cu"])
 
     for _ in range(2):
         e2e_step()
-    runner.stream.synchronize()
     n_e2e = max(3, min(args.steps, 10))
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(runner.stream)
+    if world > 1:
+        dist.barrier()
+    t_e0 = time.perf_counter()
     for _ in range(n_e2e):
         e2e_step()
-    f1.record(runner.stream)
-    runner.stream.synchronize()
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, "cuda")
+    e2e_ms = max_over_ranks((time.perf_counter() - t_e0) * 1e3 / n_e2e, world, "cuda")
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h_bytes = sum(t.numel() * t.element_size() for t in (out_h, fin_h) if t is not None)
 
     if rank != 0:
         return
@@ -435,8 +435,8 @@ def run_ours(args, p, idx, rank, world):
                               "roofline_ms": abytes / (hbm * 1e9) * 1e3}},
         "cpu_baseline": cpu_baseline(p, idx),
         "e2e": {"value": aggregate_throughput(p.token_heads(), world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": runner.h2d_bytes(p.cu_seqlens is not None),
-                "d2h_bytes_per_step": runner.d2h_bytes()},
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "entry": "kda_fwd_host (C ABI, pinned host buffers, host wall clock)"},
         "clocks": sampler.summary(),
         "gpu_launches": args.steps * (3 if p.cu_seqlens is not None else 2),
         "decode": measure_decode(stream) if world == 1 else None,

@@ -17,7 +17,7 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
-UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_noalloc"]
+UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_host", "kda_noalloc"]
 SOURCES = [os.path.join(CSRC, u + ".cu") for u in UNITS]
 HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh"), os.path.join(CSRC, "kda_internal.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd_noalloc.restype = I
         lib.kda_fwd_recurrent.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P]
         lib.kda_fwd_recurrent.restype = I
+        lib.kda_fwd_host.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I]
+        lib.kda_fwd_host.restype = I
         lib.kda_fwd_ws.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t, P]
         lib.kda_fwd_ws.restype = I
         lib.kda_fwd_ws_profiled.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t,

@@ -58,7 +58,7 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     B, T, H, _ = q.shape
     dev = q.device
     if dev.type != "cuda":
-        raise ValueError("kda_fwd needs CUDA tensors (use KDAHostRunner for host data)")
+        raise ValueError("kda_fwd needs CUDA tensors (kda_fwd_host takes host tensors)")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("out", out)):
         _check(t, name, torch.bfloat16, (B, T, H, D), dev)
     _check(beta, "beta", torch.bfloat16, (B, T, H), dev)
@@ -132,58 +132,47 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> None:
         raise KDAError(rc)
 
 
-class KDAHostRunner:
-    """Runs kda_fwd on host (pinned) tensors: copies inputs in, computes, copies results out.
-
-    Device buffers for one problem shape are allocated once at construction; ``run``
-    then issues, on one stream, the host-to-device copies of the step's inputs, the
-    forward kernel, and the device-to-host copies of ``out`` and ``final_state``.
-    """
-
-    def __init__(self, B: int, T: int, H: int, N: Optional[int] = None, state_dtype=None,
-                 has_initial: bool = True, want_final: bool = True, device="cuda"):
-        self.device = torch.device(device)
-        self.N = B if N is None else N
-        self.shape = (B, T, H, D)
-        z = lambda shape, dt: torch.empty(shape, dtype=dt, device=self.device)
-        self.q, self.k, self.v, self.g, self.out = (z(self.shape, torch.bfloat16) for _ in range(5))
-        self.beta = z((B, T, H), torch.bfloat16)
-        self.A_log = z((H,), torch.float32)
-        self.dt_bias = z((H, D), torch.float32)
-        self.cu = z((self.N + 1,), torch.int64) if N is not None else None
-        self.state_dtype = state_dtype
-        self.init = z((self.N, H, D, D), state_dtype) if (state_dtype is not None and has_initial) else None
-        self.fin = z((self.N, H, D, D), state_dtype) if (state_dtype is not None and want_final) else None
-        self.stream = torch.cuda.Stream(self.device)
-
-    def h2d_bytes(self, has_cu: bool) -> int:
-        ts = [self.q, self.k, self.v, self.g, self.beta, self.A_log, self.dt_bias]
-        ts += [t for t in (self.init, self.cu if has_cu else None) if t is not None]
-        return sum(t.numel() * t.element_size() for t in ts)
-
-    def d2h_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.out, self.fin) if t is not None)
-
-    def run(self, q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=None,
-            cu_seqlens=None, out_host=None, final_host=None):
-        """Host tensors in, host tensors out (written into out_host / final_host when given)."""
-        with torch.cuda.stream(self.stream):
-            for dst, src in ((self.q, q), (self.k, k), (self.v, v), (self.g, g), (self.beta, beta),
-                             (self.A_log, A_log), (self.dt_bias, dt_bias)):
-                dst.copy_(src, non_blocking=True)
-            if initial_state is not None:
-                self.init.copy_(initial_state, non_blocking=True)
-            if cu_seqlens is not None:
-                self.cu.copy_(cu_seqlens, non_blocking=True)
-            kda_fwd(self.q, self.k, self.v, self.g, self.beta, scale, self.out, self.A_log, self.dt_bias,
-                    lower_bound, initial_state=self.init if initial_state is not None else None,
-                    final_state=self.fin, cu_seqlens=self.cu if cu_seqlens is not None else None,
-                    stream=self.stream)
-            if out_host is None:
-                out_host = torch.empty(self.shape, dtype=torch.bfloat16, pin_memory=True)
-            out_host.copy_(self.out, non_blocking=True)
-            if self.fin is not None:
-                if final_host is None:
-                    final_host = torch.empty(self.fin.shape, dtype=self.fin.dtype, pin_memory=True)
-                final_host.copy_(self.fin, non_blocking=True)
-        return out_host, final_host
+def kda_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                 scale: float, out: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor, lower_bound: float,
+                 initial_state: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                 cu_seqlens: Optional[torch.Tensor] = None, device: Optional[int] = None) -> None:
+    """kda_fwd on host (CPU) tensors (the C entry point kda_fwd_host): the library copies the inputs
+    to the CUDA device, runs the forward pass and copies ``out`` and ``final_state`` back, with the
+    copies pipelined against the kernels.  Returns when the results are in host memory.  Same shapes
+    and dtypes as kda_fwd; pinned tensors let the copies overlap the kernels."""
+    lib = _native.load()
+    if q.dim() != 4 or q.shape[-1] != D:
+        raise ValueError("q must be [B, T, H, 128]")
+    B, T, H, _ = q.shape
+    cpu = torch.device("cpu")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("out", out)):
+        _check(t, name, torch.bfloat16, (B, T, H, D), cpu)
+    _check(beta, "beta", torch.bfloat16, (B, T, H), cpu)
+    _check(A_log, "A_log", torch.float32, (H,), cpu)
+    _check(dt_bias, "dt_bias", torch.float32, (H, D), cpu)
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be int64 [N + 1]")
+        N = cu_seqlens.numel() - 1
+        _check(cu_seqlens, "cu_seqlens", torch.int64, (N + 1,), cpu)
+    else:
+        N = B
+    sd = None
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is None:
+            continue
+        if sd is None:
+            sd = t.dtype
+        if t.dtype not in (torch.bfloat16, torch.float32) or t.dtype != sd:
+            raise TypeError("states must both be bf16 or both fp32")
+        _check(t, name, sd, (N, H, D, D), cpu)
+    state_dtype = KDA_DTYPE_NONE if sd is None else (KDA_DTYPE_BF16 if sd == torch.bfloat16 else KDA_DTYPE_FP32)
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    with torch.cuda.device(dev):
+        rc = lib.kda_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log),
+                              _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _ptr(final_state), state_dtype,
+                              _ptr(cu_seqlens), int(N), int(T), int(H))
+    if rc != KDA_OK:
+        raise KDAError(rc)

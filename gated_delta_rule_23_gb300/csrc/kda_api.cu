@@ -128,6 +128,21 @@ cudaError_t get_pool(int dev, cudaMemPool_t *out)
 
 }  // namespace
 
+cudaError_t pool_alloc(void **p, size_t bytes, cudaStream_t stream)
+{
+    *p = nullptr;
+    if (bytes == 0)
+        return cudaSuccess;
+    int dev = 0;
+    cudaMemPool_t pool;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess)
+        err = get_pool(dev, &pool);
+    if (err == cudaSuccess)
+        err = cudaMallocFromPoolAsync(p, bytes, pool, stream);
+    return err;
+}
+
 kda_status_t check_args(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                         const void *out, const float *A_log, const float *dt_bias, float lower_bound,
                         const void *initial_state, const void *final_state, kda_dtype_t state_dtype,
@@ -325,6 +340,21 @@ extern "C" kda_status_t kda_fwd_recurrent(const void *q, const void *k, const vo
                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KDA_OK
                : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_fwd_host(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                     float scale, void *out, const float *A_log, const float *dt_bias,
+                                     float lower_bound, const void *initial_state, void *final_state,
+                                     kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H)
+{
+    kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s != KDA_OK)
+        return s;
+    if (cu_seqlens && kda_check_cu_seqlens(cu_seqlens, N, T) != KDA_OK)
+        return KDA_ERR_INVALID_ARGUMENT;
+    return run_host(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
+                    cu_seqlens, N, T, H);
 }
 
 extern "C" kda_status_t kda_workspace_trim(void)

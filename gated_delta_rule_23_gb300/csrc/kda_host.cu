@@ -1,0 +1,269 @@
+// Host-buffer entry point (kda_fwd_host): the forward pass on host memory, with the host-to-device
+// copies, the kernels and the device-to-host copies pipelined over pieces of the sequence.
+//
+// Fixed-length problems are cut into pieces of whole 64-token chunks.  Piece p's rows of q, k, v, g,
+// beta go to a device ring slot on a copy-in stream, the forward pass for the piece runs on a
+// compute stream with the state chained between pieces in fp32, and the piece's output rows go
+// back on a copy-out stream, so the copies of neighbouring pieces overlap the kernels.  Because the
+// pieces start at chunk boundaries and the chained state is fp32 (the state the recurrence keeps
+// internally), the results are bit-identical to one kda_fwd call over the whole problem.  Varlen
+// problems (cu_seqlens) run as one piece.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int HOST_RING = 2;            // device piece buffers in flight
+constexpr int64_t HOST_MAX_PIECES = 8;
+constexpr int64_t HOST_MIN_PIECE = 512; // tokens
+
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16 *src, float *dst, size_t n)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __bfloat162float(src[i]);
+}
+__global__ void f32_to_bf16_kernel(const float *src, __nv_bfloat16 *dst, size_t n)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+// streams and events of the pipeline, one set per device, created on first use
+struct HostCtx {
+    cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+    cudaEvent_t e_in[HOST_RING] = {}, e_comp[HOST_RING] = {}, e_out[HOST_RING] = {}, e_start = nullptr;
+    bool ready = false;
+};
+std::mutex g_host_mu;
+HostCtx g_host[64];
+
+cudaError_t host_ctx(int dev, HostCtx **out)
+{
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    HostCtx &c = g_host[dev];
+    if (!c.ready) {
+        cudaError_t e = cudaSuccess;
+        for (cudaStream_t *s : {&c.s_in, &c.s_comp, &c.s_out})
+            if (e == cudaSuccess)
+                e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+        for (int i = 0; i < HOST_RING && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&c.e_in[i], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&c.e_comp[i], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&c.e_out[i], cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&c.e_start, cudaEventDisableTiming);
+        if (e != cudaSuccess)
+            return e;
+        c.ready = true;
+    }
+    *out = &c;
+    return cudaSuccess;
+}
+
+// device allocations of one call, from the library's pool on the compute stream, returned at the end
+struct DevBufs {
+    void *ptr[64] = {};
+    int n = 0;
+    cudaStream_t s = nullptr;
+    cudaError_t get(void **p, size_t bytes)
+    {
+        *p = nullptr;
+        if (bytes == 0)
+            return cudaSuccess;
+        if (n == 64)
+            return cudaErrorMemoryAllocation;
+        const cudaError_t e = pool_alloc(p, bytes, s);
+        if (e == cudaSuccess)
+            ptr[n++] = *p;
+        return e;
+    }
+    ~DevBufs()
+    {
+        for (int i = 0; i < n; ++i)
+            cudaFreeAsync(ptr[i], s);
+    }
+};
+
+cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cudaStream_t s)
+{
+    if (n == 0)
+        return cudaSuccess;
+    const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
+    if (to_f32)
+        bf16_to_f32_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), static_cast<float *>(dst), n);
+    else
+        f32_to_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(src), static_cast<__nv_bfloat16 *>(dst), n);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+kda_status_t run_host(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
+                      void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
+                      void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_host_mu);   // one pipeline per device at a time
+    HostCtx *c = nullptr;
+    if (host_ctx(dev, &c) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const bool varlen = cu_seqlens != nullptr;
+    const int B = varlen ? 1 : N;
+    const size_t row = (size_t)H * D;                  // elements of one token's q / k / v / g / out
+    const size_t state_elems = (size_t)N * H * D * D;
+    const size_t sbytes = state_dtype == KDA_DTYPE_FP32 ? 4 : 2;
+    const bool has_state = initial_state || final_state;
+
+    // pieces: whole 64-token chunks, at most HOST_MAX_PIECES, at least HOST_MIN_PIECE tokens each
+    int64_t pieces = 1, PT = T;
+    if (!varlen && T > HOST_MIN_PIECE) {
+        pieces = std::min<int64_t>(HOST_MAX_PIECES, (T + HOST_MIN_PIECE - 1) / HOST_MIN_PIECE);
+        PT = ((T + pieces - 1) / pieces + CH - 1) / CH * CH;
+        pieces = (T + PT - 1) / PT;
+    }
+    const int ring = pieces > 1 ? HOST_RING : 1;
+    const size_t tok_cap = (size_t)B * (size_t)PT;     // tokens of one piece (all batch rows)
+
+    // device buffers (stream-ordered on the compute stream; the other streams start after them)
+    cudaStream_t sc = c->s_comp;
+    DevBufs bufs;
+    bufs.s = sc;
+    void *dq[HOST_RING] = {}, *dk[HOST_RING] = {}, *dv[HOST_RING] = {}, *dg[HOST_RING] = {}, *db[HOST_RING] = {},
+         *dout[HOST_RING] = {};
+    void *dalog = nullptr, *ddt = nullptr, *dcu = nullptr, *dstate = nullptr, *dinit = nullptr, *dfin = nullptr,
+         *dws = nullptr;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < ring && e == cudaSuccess; ++i) {
+        e = bufs.get(&dq[i], tok_cap * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&dk[i], tok_cap * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&dv[i], tok_cap * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&dg[i], tok_cap * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&db[i], tok_cap * H * 2);
+        if (e == cudaSuccess) e = bufs.get(&dout[i], tok_cap * row * 2);
+    }
+    if (e == cudaSuccess) e = bufs.get(&dalog, (size_t)H * 4);
+    if (e == cudaSuccess) e = bufs.get(&ddt, (size_t)H * D * 4);
+    if (e == cudaSuccess && varlen) e = bufs.get(&dcu, (size_t)(N + 1) * 8);
+    // the chained state: fp32 whenever the problem has more than one piece
+    const bool chain = pieces > 1;
+    if (e == cudaSuccess && chain) e = bufs.get(&dstate, state_elems * 4);
+    if (e == cudaSuccess && !chain && initial_state) e = bufs.get(&dinit, state_elems * sbytes);
+    if (e == cudaSuccess && !chain && final_state) e = bufs.get(&dfin, state_elems * sbytes);
+    if (e == cudaSuccess && chain && initial_state && state_dtype == KDA_DTYPE_BF16) e = bufs.get(&dinit, state_elems * 2);
+    if (e == cudaSuccess && chain && final_state && state_dtype == KDA_DTYPE_BF16) e = bufs.get(&dfin, state_elems * 2);
+    if (e == cudaSuccess) e = bufs.get(&dws, workspace_bytes(N, PT, H, varlen));
+    if (e == cudaSuccess) e = cudaEventRecord(c->e_start, sc);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_in, c->e_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_start, 0);
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(sc);
+        return KDA_ERR_CUDA;
+    }
+
+    // parameters, cu_seqlens and the initial state (compute stream)
+    e = cudaMemcpyAsync(dalog, A_log, (size_t)H * 4, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ddt, dt_bias, (size_t)H * D * 4, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess && varlen) e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(N + 1) * 8, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess && initial_state) {
+        if (!chain) {
+            e = cudaMemcpyAsync(dinit, initial_state, state_elems * sbytes, cudaMemcpyHostToDevice, sc);
+        } else if (state_dtype == KDA_DTYPE_FP32) {
+            e = cudaMemcpyAsync(dstate, initial_state, state_elems * 4, cudaMemcpyHostToDevice, sc);
+        } else {
+            e = cudaMemcpyAsync(dinit, initial_state, state_elems * 2, cudaMemcpyHostToDevice, sc);
+            if (e == cudaSuccess) e = launch_convert(dinit, dstate, state_elems, true, sc);
+        }
+    }
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(sc);
+        return KDA_ERR_CUDA;
+    }
+
+    const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k);
+    const char *hv = static_cast<const char *>(v), *hg = static_cast<const char *>(g);
+    const char *hb = static_cast<const char *>(beta);
+    char *ho = static_cast<char *>(out);
+    kda_status_t st = KDA_OK;
+    for (int64_t p = 0; p < pieces && st == KDA_OK; ++p) {
+        const int slot = (int)(p % ring);
+        const int64_t t0 = p * PT, pt = std::min<int64_t>(PT, T - t0);
+        const size_t w = (size_t)pt * row * 2, wb = (size_t)pt * H * 2;                 // bytes per batch row
+        const size_t sp = (size_t)T * row * 2, spb = (size_t)T * H * 2;                 // host pitches
+        const size_t o = (size_t)t0 * row * 2, ob = (size_t)t0 * H * 2;                 // host offsets
+        // copy in (after the slot's previous piece has been computed)
+        if (p >= ring) e = cudaStreamWaitEvent(c->s_in, c->e_comp[slot], 0);
+        if (pt > 0) {
+            if (e == cudaSuccess) e = cudaMemcpy2DAsync(dq[slot], w, hq + o, sp, w, B, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpy2DAsync(dk[slot], w, hk + o, sp, w, B, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpy2DAsync(dv[slot], w, hv + o, sp, w, B, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpy2DAsync(dg[slot], w, hg + o, sp, w, B, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpy2DAsync(db[slot], wb, hb + ob, spb, wb, B, cudaMemcpyHostToDevice, c->s_in);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(c->e_in[slot], c->s_in);
+        // compute (after the copy in, and after the slot's previous output has been copied out)
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, c->e_in[slot], 0);
+        if (e == cudaSuccess && p >= ring) e = cudaStreamWaitEvent(sc, c->e_out[slot], 0);
+        if (e != cudaSuccess) {
+            st = KDA_ERR_CUDA;
+            break;
+        }
+        const void *init_p;
+        void *fin_p;
+        kda_dtype_t sdt;
+        if (chain) {
+            init_p = (p == 0 && !initial_state) ? nullptr : dstate;
+            fin_p = has_state || p + 1 < pieces ? dstate : nullptr;
+            sdt = KDA_DTYPE_FP32;
+        } else {
+            init_p = initial_state ? dinit : nullptr;
+            fin_p = final_state ? dfin : nullptr;
+            sdt = state_dtype;
+        }
+        st = run(dq[slot], dk[slot], dv[slot], dg[slot], db[slot], scale, dout[slot],
+                 static_cast<const float *>(dalog), static_cast<const float *>(ddt), lower_bound, init_p, fin_p,
+                 (init_p || fin_p) ? sdt : KDA_DTYPE_NONE, varlen ? static_cast<const int64_t *>(dcu) : nullptr, N,
+                 varlen ? T : pt, H, static_cast<unsigned char *>(dws), sc);
+        if (st != KDA_OK)
+            break;
+        e = cudaEventRecord(c->e_comp[slot], sc);
+        // copy out
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_comp[slot], 0);
+        if (e == cudaSuccess && pt > 0)
+            e = cudaMemcpy2DAsync(ho + o, sp, dout[slot], w, w, B, cudaMemcpyDeviceToHost, c->s_out);
+        if (e == cudaSuccess) e = cudaEventRecord(c->e_out[slot], c->s_out);
+        if (e != cudaSuccess)
+            st = KDA_ERR_CUDA;
+    }
+    // final state
+    if (st == KDA_OK && final_state) {
+        e = cudaSuccess;
+        if (chain && state_dtype == KDA_DTYPE_BF16)
+            e = launch_convert(dstate, dfin, state_elems, false, sc);
+        const void *src = chain ? (state_dtype == KDA_DTYPE_BF16 ? dfin : dstate) : dfin;
+        if (e == cudaSuccess) e = cudaMemcpyAsync(final_state, src, state_elems * sbytes, cudaMemcpyDeviceToHost, sc);
+        if (e != cudaSuccess)
+            st = KDA_ERR_CUDA;
+    }
+    // wait for everything (the buffers go back to the pool, in stream order, on return)
+    const cudaError_t e1 = cudaStreamSynchronize(sc), e2 = cudaStreamSynchronize(c->s_out),
+                      e3 = cudaStreamSynchronize(c->s_in);
+    if (st == KDA_OK && (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess))
+        st = KDA_ERR_CUDA;
+    return st;
+}
+
+}  // namespace kda

@@ -182,6 +182,25 @@ kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, cons
                                kda_stream_t stream);
 
 /*
+ * kda_fwd_host -- kda_fwd on HOST buffers: q, k, v, g, beta, out, A_log, dt_bias,
+ * initial_state, final_state and cu_seqlens are host pointers with kda_fwd's layouts and
+ * alignments.  The library copies the inputs to the current device, runs the forward pass there
+ * and copies out (and final_state) back, and returns when the results are in host memory.  The
+ * FlashKDA pages have no counterpart: it is this library's end-to-end entry point.  Fixed-length
+ * problems are cut into pieces of whole 64-token chunks and the copies of neighbouring pieces
+ * overlap the kernels on three streams of the library's own; the state passes between pieces in
+ * fp32, so the results are bit-identical to kda_fwd on the same data.  Page-locked (pinned) host
+ * memory lets the copies run asynchronously; pageable memory works but the copies do not overlap.
+ * Device memory comes from the library's pool (see kda_workspace_trim).  Calls are serialised per
+ * device.  Errors: those of kda_fwd (cu_seqlens is also checked, on the host, as
+ * kda_check_cu_seqlens does), KDA_ERR_CUDA for a failed copy, allocation or launch.
+ */
+kda_status_t kda_fwd_host(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                          float scale, void *out, const float *A_log, const float *dt_bias,
+                          float lower_bound, const void *initial_state, void *final_state,
+                          kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H);
+
+/*
  * Returns the workspace memory kda_fwd's pools hold but no call is using to the driver.
  * KDA_ERR_CUDA if a pool could not be trimmed.
  */

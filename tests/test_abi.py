@@ -18,7 +18,8 @@ def lib():
 def test_exports_every_declared_function(lib):
     names = _native.declared_functions()
     assert {"kda_fwd", "kda_fwd_ws", "kda_fwd_workspace_size", "kda_workspace_trim", "kda_check_cu_seqlens",
-            "kda_status_string", "kda_fwd_smem_bytes", "kda_device_status", "kda_fwd_recurrent"} <= set(names)
+            "kda_status_string", "kda_fwd_smem_bytes", "kda_device_status", "kda_fwd_recurrent",
+            "kda_fwd_host"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -116,3 +117,19 @@ def test_ws_entry_rejects_missing_workspace(lib):
     assert lib.kda_fwd_ws(*args, None, need, None) == KDA_ERR_INVALID_ARGUMENT
     assert lib.kda_fwd_ws(*args, A + 0x100000, need - 16, None) == KDA_ERR_INVALID_ARGUMENT
     assert lib.kda_fwd_ws(*args, A + 0x100010, need, None) == KDA_ERR_INVALID_ARGUMENT   # not 256-byte aligned
+
+
+def test_host_entry_rejects_bad_arguments_before_any_cuda_call(lib):
+    """kda_fwd_host checks its (host) arguments like kda_fwd, and cu_seqlens on the host."""
+    args = [A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 0.1, A + 0x5000, A + 0x6000, A + 0x7000, -5.0,
+            None, None, KDA_DTYPE_NONE, None, 1, 64, 2]
+    bad = list(args)
+    bad[0] = None
+    assert lib.kda_fwd_host(*bad) == KDA_ERR_INVALID_ARGUMENT
+    bad = list(args)
+    bad[9] = 1.0
+    assert lib.kda_fwd_host(*bad) == KDA_ERR_UNSUPPORTED
+    cu = (ctypes.c_int64 * 3)(0, 40, 70)          # ends at 70, not T = 64
+    bad = list(args)
+    bad[13], bad[14] = ctypes.cast(cu, ctypes.c_void_p).value, 2
+    assert lib.kda_fwd_host(*bad) == KDA_ERR_INVALID_ARGUMENT

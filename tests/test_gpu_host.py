@@ -1,0 +1,80 @@
+"""The host-buffer entry point kda_fwd_host against kda_fwd on the device: the pipelined pieces
+(whole 64-token chunks, state chained in fp32) give the same bits as one device call, for every state
+dtype and presence, ragged last pieces, batches, varlen problems, pageable memory and T = 0."""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_23_gb300 import kda_fwd_host
+from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, STATE_NONE, make_problem
+from tests.gpu_util import bf16_tensor, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def host_tensors(p, pinned=True):
+    fix = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    h = dict(q=fix(bf16_tensor(p.q, "cpu")), k=fix(bf16_tensor(p.k, "cpu")), v=fix(bf16_tensor(p.v, "cpu")),
+             g=fix(bf16_tensor(p.g, "cpu")), beta=fix(bf16_tensor(p.beta, "cpu")),
+             A_log=fix(torch.from_numpy(p.A_log)), dt_bias=fix(torch.from_numpy(p.dt_bias)))
+    h["cu"] = None if p.cu_seqlens is None else fix(torch.from_numpy(p.cu_seqlens))
+    sdt = {STATE_BF16: torch.bfloat16, STATE_FP32: torch.float32}.get(p.state_dtype)
+    h["init"] = None
+    if p.initial_state is not None:
+        h["init"] = fix(bf16_tensor(p.initial_state, "cpu") if p.state_dtype == STATE_BF16
+                        else torch.from_numpy(p.initial_state))
+    h["out"] = fix(torch.empty(p.q.shape, dtype=torch.bfloat16))
+    h["fin"] = fix(torch.empty((p.N, p.H, 128, 128), dtype=sdt)) if (sdt is not None and p.want_final) else None
+    return h
+
+
+def run_host(p, pinned=True):
+    h = host_tensors(p, pinned)
+    kda_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], p.scale, h["out"], h["A_log"], h["dt_bias"],
+                 p.lower_bound, initial_state=h["init"], final_state=h["fin"], cu_seqlens=h["cu"])
+    return h["out"].float().numpy(), (None if h["fin"] is None else h["fin"].float().numpy())
+
+
+def assert_same(p, pinned=True):
+    out_h, fin_h = run_host(p, pinned)
+    out_d, fin_d = run_gpu(p)
+    assert np.array_equal(out_h, out_d)
+    if fin_d is None:
+        assert fin_h is None
+    else:
+        assert np.array_equal(fin_h, fin_d)
+
+
+@pytest.mark.parametrize("T", [1, 64, 512, 513, 2500, 4096])
+def test_pieces_equal_one_device_call(T):
+    assert_same(make_problem(B=1, T=T, H=3, seed=400 + T))
+
+
+@pytest.mark.parametrize("state", [STATE_NONE, STATE_BF16, STATE_FP32])
+@pytest.mark.parametrize("with_initial", [False, True])
+def test_state_dtypes_and_presence(state, with_initial):
+    assert_same(make_problem(B=2, T=1300, H=2, seed=410, state_dtype=state, with_initial=with_initial))
+
+
+def test_initial_state_without_final_state():
+    assert_same(make_problem(B=1, T=1500, H=2, seed=411, state_dtype=STATE_FP32, want_final=False))
+
+
+def test_batch_rows_are_strided_copies():
+    assert_same(make_problem(B=3, T=1100, H=4, seed=412))
+
+
+def test_varlen_runs_as_one_piece():
+    cu = np.array([0, 5, 5, 700, 1800, 1801], dtype=np.int64)
+    assert_same(make_problem(B=1, T=1801, H=3, seed=413, cu_seqlens=cu))
+
+
+def test_pageable_memory():
+    assert_same(make_problem(B=1, T=1200, H=2, seed=414), pinned=False)
+
+
+def test_no_tokens():
+    p = make_problem(B=1, T=0, H=2, seed=415, cu_seqlens=np.zeros(3, dtype=np.int64))
+    out, fin = run_host(p)
+    assert out.size == 0
+    assert np.array_equal(fin, p.initial_state)
