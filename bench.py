@@ -41,7 +41,8 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 # device sources each kernel is compiled from (a profile summary is valid only for these)
 KERNEL_SOURCES = {"kda_prep_kernel": ["kda_device.cuh", "kda_prep.cu"],
                   "kda_recur_kernel": ["kda_device.cuh", "kda_recur.cu"],
-                  "kda_recurrent_kernel": ["kda_device.cuh", "kda_recurrent.cu"]}
+                  "kda_recurrent_kernel": ["kda_device.cuh", "kda_recurrent.cu"],
+                  "kda_decode_kernel": ["kda_device.cuh", "kda_decode.cu"]}
 SLOT_BYTES_PER_CHUNK_HEAD = 74240   # fp16 operands the prep kernel hands to the recurrence kernel per (64-token chunk, head)
 # FlashKDA on GB200, H=96 fixed length, T=8192: 1.01 ms (guancyxx.cn FlashKDA article, section 三,
 # GB200 table) -> tokens*heads per second.  Another machine: context, not the target.
@@ -308,8 +309,8 @@ def measure_decode(stream, steps=50, warmup=5):
                                                       "fp32 state in place",
             "ms": ms_rec, "value": th / (ms_rec * 1e-3), "unit": "tokens*heads/s",
             "bytes_per_step": state_bytes + token_bytes,
-            "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel", "achieved": ach, "peak": hbm,
-                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic("kda_recurrent_kernel", "decode")},
+            "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": ach, "peak": hbm,
+                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic("kda_decode_kernel", "decode")},
             "chunked_entry_ms": ms_chk, "steps": steps, "warmup": warmup}
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
-UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_host", "kda_noalloc"]
+UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_decode", "kda_host", "kda_noalloc"]
 SOURCES = [os.path.join(CSRC, u + ".cu") for u in UNITS]
 HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh"), os.path.join(CSRC, "kda_internal.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -336,10 +336,10 @@ extern "C" kda_status_t kda_fwd_recurrent(const void *q, const void *k, const vo
         return KDA_ERR_UNSUPPORTED;
     const Problem p = make_problem(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                                    final_state, cu_seqlens, N, T, H);
-    return launch_recurrent(p, state_kind(initial_state, final_state, state_dtype),
-                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? KDA_OK
-               : KDA_ERR_CUDA;
+    const int sk = state_kind(initial_state, final_state, state_dtype);
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t err = decode_applies(p) ? launch_decode(p, sk, st) : launch_recurrent(p, sk, st);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 extern "C" kda_status_t kda_fwd_host(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -398,9 +398,9 @@ extern "C" kda_status_t kda_device_status(kda_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KDA_ERR_CUDA;
-    unsigned int flag = 0, flag2 = 0, flag3 = 0;
+    unsigned int flag = 0, flag2 = 0, flag3 = 0, flag4 = 0;
     if (read_and_clear_device_error(&flag) != cudaSuccess || prep_read_and_clear_error(&flag2) != cudaSuccess ||
-        recurrent_read_and_clear_error(&flag3) != cudaSuccess)
+        recurrent_read_and_clear_error(&flag3) != cudaSuccess || decode_read_and_clear_error(&flag4) != cudaSuccess)
         return KDA_ERR_CUDA;
-    return (flag | flag2 | flag3) ? KDA_ERR_TIMEOUT : KDA_OK;
+    return (flag | flag2 | flag3 | flag4) ? KDA_ERR_TIMEOUT : KDA_OK;
 }

@@ -39,6 +39,11 @@ cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream);
 // Token-recurrent kernel, persistent over the N x H x 2 (sequence, head, value half) items; no workspace.
 cudaError_t launch_recurrent(const Problem &p, int state_kind, cudaStream_t stream);
 size_t recurrent_smem_bytes();
+// Decode kernel (fixed-length problems of 1 to 4 tokens per sequence), persistent over the same items.
+bool decode_applies(const Problem &p);
+cudaError_t launch_decode(const Problem &p, int state_kind, cudaStream_t stream);
+size_t decode_smem_bytes();
+cudaError_t decode_read_and_clear_error(unsigned int *flag);
 size_t prep_smem_bytes();
 size_t recur_smem_bytes();
 // Read the device-side "bounded wait expired" words of the recurrence / prep kernels and clear them.

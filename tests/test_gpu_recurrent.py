@@ -169,3 +169,19 @@ def test_repeat_calls_are_deterministic():
     a = run_rec(p, dev)
     b = run_rec(p, dev)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+@pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
+def test_decode_kernel_matches_staged_kernel(T, state):
+    """Fixed-length problems of 1-4 tokens take the barrier-free decode kernel; the same tokens as varlen
+    sequences take the staged kernel.  Both evaluate the tokens as one stage with the same rounding: the
+    bits agree."""
+    p = make_problem(B=5, T=T, H=3, seed=320 + T, state_dtype=state)
+    o_dec, f_dec = run_rec(p)
+    cu = np.arange(0, 5 * T + 1, T, dtype=np.int64)
+    flat = lambda a: a.reshape((1, 5 * T) + a.shape[2:]).copy()
+    pv = dataclasses.replace(p, q=flat(p.q), k=flat(p.k), v=flat(p.v), g=flat(p.g), beta=flat(p.beta), cu_seqlens=cu)
+    o_stg, f_stg = run_rec(pv)
+    assert np.array_equal(o_dec.reshape(o_stg.shape), o_stg)
+    assert np.array_equal(f_dec, f_stg)
