@@ -270,16 +270,17 @@ def aggregate_throughput(units_per_rank, world, ms):
 DECODE_N, DECODE_H = 256, 96
 
 
-def measure_decode(stream, steps=50, warmup=5):
+def measure_decode(stream, steps=50, warmup=5, n_seq=DECODE_N, T=1):
     """One decode step (T = 1) for 256 sequences at 96 heads with an fp32 state updated in place,
-    through the token-recurrent entry point and, for comparison, through the chunked one.  The
-    state (1.6 GB) is larger than L2, so no flush is needed between steps."""
+    through the token-recurrent entry point (its decode kernel) and, for comparison, through the
+    chunked one; then the same step with a bf16 state.  The states (1.6 / 0.8 GB) are larger than
+    L2, so no flush is needed between steps."""
     import torch
     from gated_delta_rule_23_gb300 import kda_fwd, kda_fwd_recurrent
     from gated_delta_rule_23_gb300.inputs import make_problem
     from tests.gpu_util import to_device
 
-    p = make_problem(B=DECODE_N, T=1, H=DECODE_H, seed=77)
+    p = make_problem(B=n_seq, T=T, H=DECODE_H, seed=77)
     dev = to_device(p)
     out = torch.empty_like(dev["q"])
     st = dev["init"]
@@ -300,18 +301,28 @@ def measure_decode(stream, steps=50, warmup=5):
 
     ms_rec = timed(lambda: kda_fwd_recurrent(*args, initial_state=st, final_state=st, stream=stream))
     ms_chk = timed(lambda: kda_fwd(*args, initial_state=st, final_state=st, stream=stream))
-    th = DECODE_N * DECODE_H
-    state_bytes = 2 * th * 128 * 128 * 4
+    st16 = st.to(torch.bfloat16)
+    ms_rec16 = timed(lambda: kda_fwd_recurrent(*args, initial_state=st16, final_state=st16, stream=stream))
+    th = n_seq * T * DECODE_H
+    state_bytes = 2 * n_seq * DECODE_H * 128 * 128 * 4
     token_bytes = th * (4 * 128 * 2 + 2 + 128 * 2)
     hbm = peaks()[0]
     ach = (state_bytes + token_bytes) / (ms_rec * 1e-3) / 1e9
-    return {"entry": "kda_fwd_recurrent", "workload": f"decode step: N={DECODE_N} sequences x T=1, H={DECODE_H}, "
+    kern = "kda_decode_kernel" if 2 <= T <= 4 else "kda_recurrent_kernel"   # fp32 state: T = 1 runs staged
+    wkey = "decode" if (n_seq, T) == (DECODE_N, 1) else f"decode_N{n_seq}_T{T}"
+    return {"entry": "kda_fwd_recurrent", "workload": f"decode step: N={n_seq} sequences x T={T}, H={DECODE_H}, "
                                                       "fp32 state in place",
             "ms": ms_rec, "value": th / (ms_rec * 1e-3), "unit": "tokens*heads/s",
             "bytes_per_step": state_bytes + token_bytes,
-            "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": ach, "peak": hbm,
-                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic("kda_decode_kernel", "decode")},
-            "chunked_entry_ms": ms_chk, "steps": steps, "warmup": warmup}
+            "roofline": {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": hbm,
+                         "unit": "GB/s", "frac": ach / hbm, "traffic": measured_traffic(kern, wkey)},
+            "chunked_entry_ms": ms_chk, "steps": steps, "warmup": warmup,
+            "bf16_state": {"ms": ms_rec16, "kernel": "kda_decode_kernel" if T <= 4 else "kda_recurrent_kernel",
+                       "bytes_per_step": state_bytes // 2 + token_bytes,
+                           "achieved": (state_bytes // 2 + token_bytes) / (ms_rec16 * 1e-3) / 1e9,
+                           "frac": (state_bytes // 2 + token_bytes) / (ms_rec16 * 1e-3) / 1e9 / hbm,
+                           "traffic": measured_traffic("kda_decode_kernel" if T <= 4 else "kda_recurrent_kernel",
+                                                       wkey + "_bf16")}}
 
 
 def run_ours(args, p, idx, rank, world):
@@ -459,6 +470,8 @@ def main():
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode step (token-recurrent entry point, N=256 x T=1, H=96) and print "
                          "its measurement")
+    ap.add_argument("--decode-N", type=int, default=DECODE_N, help="sequences of the --decode-only step")
+    ap.add_argument("--decode-T", type=int, default=1, help="tokens per sequence of the --decode-only step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
@@ -478,8 +491,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     if args.decode_only:
         if rank == 0:
-            print(json.dumps(measure_decode(torch.cuda.current_stream(), steps=args.steps, warmup=args.warmup)),
-                  flush=True)
+            print(json.dumps(measure_decode(torch.cuda.current_stream(), steps=args.steps, warmup=args.warmup,
+                                            n_seq=args.decode_N, T=args.decode_T)), flush=True)
         return
     p = make_workload(args.workload)
     if args.T is not None:

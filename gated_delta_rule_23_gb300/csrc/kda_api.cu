@@ -338,7 +338,7 @@ extern "C" kda_status_t kda_fwd_recurrent(const void *q, const void *k, const vo
                                    final_state, cu_seqlens, N, T, H);
     const int sk = state_kind(initial_state, final_state, state_dtype);
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t err = decode_applies(p) ? launch_decode(p, sk, st) : launch_recurrent(p, sk, st);
+    const cudaError_t err = decode_applies(p, sk) ? launch_decode(p, sk, st) : launch_recurrent(p, sk, st);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

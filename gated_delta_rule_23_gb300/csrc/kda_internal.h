@@ -40,7 +40,7 @@ cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream);
 cudaError_t launch_recurrent(const Problem &p, int state_kind, cudaStream_t stream);
 size_t recurrent_smem_bytes();
 // Decode kernel (fixed-length problems of 1 to 4 tokens per sequence), persistent over the same items.
-bool decode_applies(const Problem &p);
+bool decode_applies(const Problem &p, int state_kind);
 cudaError_t launch_decode(const Problem &p, int state_kind, cudaStream_t stream);
 size_t decode_smem_bytes();
 cudaError_t decode_read_and_clear_error(unsigned int *flag);

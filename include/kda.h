@@ -167,8 +167,9 @@ kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v, const 
  * that the chunked form of section 2.2 reorganises).  A persistent grid walks the
  * (sequence, head, half of the values) items; each CTA holds an item's 64 state columns
  * in fp32 registers while the next items' states and tokens stream in (fixed-length
- * problems of 1 to 4 tokens per sequence take a decode kernel whose warps work without
- * CTA barriers; longer or varlen problems take 8-token stages).  Meant for decode
+ * problems of 1 to 4 tokens per sequence mostly take a decode kernel whose warps work
+ * without CTA barriers, longer or varlen problems 8-token stages; both give the same
+ * bits).  Meant for decode
  * steps (one or a few tokens per sequence) and short prefills, where it moves only the
  * state and the tokens (no per-chunk operands, no workspace, no allocation); its cost
  * grows linearly with the longest sequence, so long sequences belong to kda_fwd.  Same
