@@ -87,12 +87,6 @@ __device__ __forceinline__ float rcp_approx(float x)
 __device__ __forceinline__ float sigmoid_fast(float z) { return rcp_approx(1.0f + ex2_approx(-z * LOG2E)); }
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-__device__ __forceinline__ uint32_t to_tf32(float x)
-{
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return y;
-}
 // Round to tf32 (10 explicit mantissa bits), to nearest with ties away from zero, on the integer
 // pipe: adding half a tf32 ulp to the magnitude bits and truncating is that rounding for finite
 // values (a carry into the exponent is the correct round-up).
@@ -132,22 +126,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 // bf16x2 word -> fp16x2 word (both halves through fp32)
 __device__ __forceinline__ uint32_t bf16x2_to_half2(uint32_t u) { return pack_half2(bf16_lo(u), bf16_hi(u)); }
 
-__device__ __forceinline__ uint4 ldg_nc16(const void *p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
 
-// D += A * B, m16n8k8, tf32 operands, fp32 accumulators
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                 "{%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulators
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
@@ -220,23 +199,8 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // waits until every bulk copy this thread committed has finished reading its shared-memory source
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// waits until every bulk copy this thread committed has completed (writes performed)
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// named barrier over `nthreads` threads (a multiple of 32) of the CTA
-__device__ __forceinline__ void named_bar(int id, int nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-// named barrier that also returns whether any participating thread passed pred = true
-__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred)
-{
-    uint32_t r;
-    asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
-                 : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
-    return r != 0;
-}
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor: start address, leading (K-direction) and stride
