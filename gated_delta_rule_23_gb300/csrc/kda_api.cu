@@ -14,11 +14,13 @@ namespace {
 constexpr int PLAN_THREADS = 1024;
 constexpr int LPT_MAX_SEQS = 2048;   // longest-first ordering of varlen sequences up to this count
 
-// Varlen plan, one CTA: chunk_off[n] = sum_{m < n} ceil(len_m / 64) (exclusive scan, [N + 1]),
-// and, when order != nullptr, order[rank] = sequence with that rank by length (longest first,
-// ties by index), so that the recurrence CTAs that start first take the longest sequences.
+// Varlen plan, one CTA: chunk_off[n] = sum_{m < n} ceil(len_m / 64) (exclusive scan, [N + 1]);
+// chunk_info[c] = (first token, tokens left in the sequence) of every chunk c < chunk_off[N], so
+// that a prep CTA finds its chunk with one load; and, when order != nullptr, order[rank] =
+// sequence with that rank by length (longest first, ties by index), so that the recurrence CTAs
+// that start first take the longest sequences.
 __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *cu, int N, int64_t *chunk_off,
-                                                              int *order)
+                                                              longlong2 *chunk_info, int *order)
 {
     __shared__ int64_t wsum[PLAN_THREADS / 32];
     __shared__ int64_t carry;
@@ -60,6 +62,19 @@ __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *c
     }
     if (tid == 0)
         chunk_off[N] = carry;
+    __syncthreads();   // chunk_off is complete (global writes of this CTA, ordered by the barrier)
+    for (int64_t c = tid; c < carry; c += PLAN_THREADS) {
+        int lo = 0, hi = N - 1;   // the last sequence whose first chunk is <= c
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (chunk_off[mid] <= c)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int64_t tok0 = cu[lo] + (c - chunk_off[lo]) * CH;
+        chunk_info[c] = make_longlong2(tok0, cu[lo + 1] - tok0);
+    }
     if (order) {
         for (int s = tid; s < N; s += PLAN_THREADS) {
             const int64_t ls = cu[s + 1] - cu[s];
@@ -77,20 +92,25 @@ bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// workspace: [chunk_off: (N + 1) int64][order: N int32] (varlen only), then the operand slots
-size_t header_bytes(int N, bool varlen) { return varlen ? round_up((size_t)(N + 1) * 8 + (size_t)N * 4, 256) : 0; }
-
 int64_t max_chunks(int N, int64_t T, bool varlen)
 {
     // varlen: sum_n ceil(len_n / 64) <= (T + 63 N) / 64
     return varlen ? (T + (int64_t)(CH - 1) * N) / CH : (int64_t)N * ((T + CH - 1) / CH);
 }
 
+// workspace (varlen only: the plan): [chunk_off: (N + 1) int64][order: N int32][chunk_info: max_chunks
+// x (int64, int64), 16-byte aligned], then the operand slots (256-byte aligned)
+size_t info_offset(int N) { return round_up((size_t)(N + 1) * 8 + (size_t)N * 4, 16); }
+size_t header_bytes(int N, int64_t T, bool varlen)
+{
+    return varlen ? round_up(info_offset(N) + (size_t)max_chunks(N, T, true) * 16, 256) : 0;
+}
+
 }  // namespace
 
 size_t workspace_bytes(int N, int64_t T, int H, bool varlen)
 {
-    return header_bytes(N, varlen) + (size_t)max_chunks(N, T, varlen) * (size_t)H * SLOT_BYTES;
+    return header_bytes(N, T, varlen) + (size_t)max_chunks(N, T, varlen) * (size_t)H * SLOT_BYTES;
 }
 
 namespace {
@@ -199,6 +219,7 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.T = T;
     p.nch_fixed = (T + CH - 1) / CH;
     p.chunk_off = nullptr;
+    p.chunk_info = nullptr;
     p.order = nullptr;
     p.slots = nullptr;
     p.prep_pf = 0;
@@ -224,14 +245,16 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
     };
     Problem p = make_problem(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
                              cu_seqlens, N, T, H);
-    p.slots = ws + header_bytes(N, varlen);
+    p.slots = ws + header_bytes(N, T, varlen);
     cudaError_t err = cudaSuccess;
     if (varlen) {
         int64_t *chunk_off = reinterpret_cast<int64_t *>(ws);
         int *order = N > 1 && N <= LPT_MAX_SEQS ? reinterpret_cast<int *>(ws + (size_t)(N + 1) * 8) : nullptr;
-        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, chunk_off, order);
+        longlong2 *chunk_info = reinterpret_cast<longlong2 *>(ws + info_offset(N));
+        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, chunk_off, chunk_info, order);
         err = cudaGetLastError();
         p.chunk_off = chunk_off;
+        p.chunk_info = chunk_info;
         p.order = order;
     }
     if (err == cudaSuccess)

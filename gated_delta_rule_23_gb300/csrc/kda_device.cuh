@@ -58,6 +58,7 @@ struct Problem {
     void *fin;
     const int64_t *cu;        // cu_seqlens (device) or nullptr
     const int64_t *chunk_off; // varlen: first chunk of each sequence, [N + 1] (workspace)
+    const longlong2 *chunk_info; // varlen: (first token, tokens left in its sequence) per chunk (workspace)
     const int *order;         // varlen: sequences longest first, [N] (workspace), or nullptr
     unsigned char *slots;     // operand slots (workspace)
     float scale, lb_log2e;    // lb_log2e = lower_bound * log2(e)

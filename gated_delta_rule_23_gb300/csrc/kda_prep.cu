@@ -93,23 +93,17 @@ __device__ __forceinline__ int stg_off(int t, int c16) { return t * 256 + ((c16 
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 
-// first token and valid length of chunk gc (a global chunk index over all sequences; the launch
-// keeps every item index, and so gc, below 2^31, so the divisions are 32-bit)
+// first token and tokens left of chunk gc (a global chunk index over all sequences; the launch keeps
+// every item index, and so gc, below 2^31, so the divisions are 32-bit); varlen chunks come from the
+// plan's per-chunk table, which has an entry for every launched chunk index (only those below
+// chunk_off[N] are filled: callers check that)
 template <bool VARLEN>
 __device__ __forceinline__ void chunk_tokens(const Problem &p, uint32_t gc, int64_t &tok0, int64_t &rem)
 {
     if (VARLEN) {
-        int lo = 0, hi = p.N - 1;   // the last sequence whose first chunk is <= gc
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.chunk_off[mid] <= gc)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const int64_t c = (int64_t)gc - p.chunk_off[lo];
-        tok0 = p.cu[lo] + c * CH;
-        rem = p.cu[lo + 1] - tok0;
+        const longlong2 ci = p.chunk_info[gc];
+        tok0 = ci.x;
+        rem = ci.y;
     } else {
         const uint32_t nch = (uint32_t)p.nch_fixed, n = gc / nch, c = gc - n * nch;
         tok0 = (int64_t)n * p.T + (int64_t)c * CH;
@@ -128,10 +122,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     const int h = (int)(item - gc * (uint32_t)H);
 
     // -------- this CTA's chunk: first token tok0 and L valid tokens
+    int64_t tok0, rem;
+    chunk_tokens<VARLEN>(p, gc, tok0, rem);   // the table has an entry for every launched CTA
     if (VARLEN && (int64_t)gc >= p.chunk_off[p.N])
         return;
-    int64_t tok0, rem;
-    chunk_tokens<VARLEN>(p, gc, tok0, rem);
     const int L = (int)(rem < CH ? rem : CH);
     unsigned char *slot = p.slots + (size_t)item * SLOT_BYTES;
 
@@ -177,9 +171,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     if (p.prep_pf > 0 && item + (uint32_t)p.prep_pf < gridDim.x) {
         const uint32_t pit = item + (uint32_t)p.prep_pf, pgc = pit / (uint32_t)H;
         const int ph = (int)(pit - pgc * (uint32_t)H);
+        int64_t ptok0, prem;
+        chunk_tokens<VARLEN>(p, pgc, ptok0, prem);
         if (!VARLEN || (int64_t)pgc < p.chunk_off[p.N]) {
-            int64_t ptok0, prem;
-            chunk_tokens<VARLEN>(p, pgc, ptok0, prem);
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const int li = tid + m * PREP_THREADS, which = li >> 7, t = (li >> 1) & (CH - 1);

@@ -104,9 +104,11 @@ def test_workspace_size(lib):
     assert lib.kda_fwd_workspace_size(1, 8192, 96, 0) == 128 * 96 * slot
     assert lib.kda_fwd_workspace_size(2, 65, 3, 0) == 2 * 2 * 3 * slot
     assert lib.kda_fwd_workspace_size(1, 0, 4, 0) == 0
-    # varlen: a header (chunk offsets, order), then at most (T + 63 N) / 64 chunks
-    hdr = -(-(9 * 8 + 8 * 4) // 256) * 256
-    assert lib.kda_fwd_workspace_size(8, 8192, 96, 1) == hdr + (8192 + 63 * 8) // 64 * 96 * slot
+    # varlen: a header (chunk offsets, order, 16 bytes per chunk of chunk info), then at most
+    # (T + 63 N) / 64 chunks
+    mc = (8192 + 63 * 8) // 64
+    hdr = -(-(-(-(9 * 8 + 8 * 4) // 16) * 16 + mc * 16) // 256) * 256
+    assert lib.kda_fwd_workspace_size(8, 8192, 96, 1) == hdr + mc * 96 * slot
     assert lib.kda_fwd_workspace_size(0, 10, 1, 0) == 0
 
 
