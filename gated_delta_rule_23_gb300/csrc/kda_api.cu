@@ -108,8 +108,17 @@ size_t header_bytes(int N, int64_t T, bool varlen)
 
 }  // namespace
 
+// Fixed-length problems of at most 4 tokens per sequence (decode steps) are evaluated token by token by
+// the kernels of kda_fwd_recurrent: they stream the state once and need no workspace.
+bool short_problem(int N, int64_t T, int H, bool varlen)
+{
+    return !varlen && T >= 1 && T <= 4 && 2 * (int64_t)N * H <= INT32_MAX;
+}
+
 size_t workspace_bytes(int N, int64_t T, int H, bool varlen)
 {
+    if (short_problem(N, T, H, varlen))
+        return 0;
     return header_bytes(N, T, varlen) + (size_t)max_chunks(N, T, varlen) * (size_t)H * SLOT_BYTES;
 }
 
@@ -245,6 +254,17 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
     };
     Problem p = make_problem(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
                              cu_seqlens, N, T, H);
+    if (short_problem(N, T, H, varlen)) {
+        const int sk = state_kind(initial_state, final_state, state_dtype);
+        cudaError_t e = mark(0);
+        if (e == cudaSuccess)
+            e = decode_applies(p, sk) ? launch_decode(p, sk, stream) : launch_recurrent(p, sk, stream);
+        if (e == cudaSuccess)
+            e = mark(1);
+        if (e == cudaSuccess)
+            e = mark(2);
+        return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     p.slots = ws + header_bytes(N, T, varlen);
     cudaError_t err = cudaSuccess;
     if (varlen) {

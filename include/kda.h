@@ -99,6 +99,10 @@ typedef enum {
  *
  * When T == 0 (no tokens at all) q, k, v, g, beta and out may be NULL.
  *
+ * Fixed-length problems of 1 to 4 tokens per sequence (decode steps) are evaluated token by
+ * token, as kda_fwd_recurrent does (same kernels, same bits, no workspace); everything else
+ * takes the chunked form.
+ *
  * Returns KDA_OK once the work is enqueued.  Argument errors are reported
  * synchronously before anything is launched; the kernel itself never traps.
  */
@@ -110,7 +114,8 @@ kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g,
 
 /*
  * Bytes of workspace kda_fwd_ws needs for this problem size (an upper bound that depends
- * only on N, T, H and whether cu_seqlens is given: varlen != 0).  0 for invalid sizes.
+ * only on N, T, H and whether cu_seqlens is given: varlen != 0).  0 for invalid sizes and for
+ * the fixed-length problems of 1 to 4 tokens per sequence, which need none.
  */
 size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen);
 

@@ -110,6 +110,10 @@ def test_workspace_size(lib):
     hdr = -(-(-(-(9 * 8 + 8 * 4) // 16) * 16 + mc * 16) // 256) * 256
     assert lib.kda_fwd_workspace_size(8, 8192, 96, 1) == hdr + mc * 96 * slot
     assert lib.kda_fwd_workspace_size(0, 10, 1, 0) == 0
+    # fixed-length problems of 1-4 tokens per sequence take the token-recurrent kernels: no workspace
+    assert lib.kda_fwd_workspace_size(256, 1, 96, 0) == 0
+    assert lib.kda_fwd_workspace_size(256, 4, 96, 0) == 0
+    assert lib.kda_fwd_workspace_size(256, 5, 96, 0) == 256 * 96 * slot
 
 
 def test_ws_entry_rejects_missing_workspace(lib):

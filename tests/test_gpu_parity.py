@@ -65,7 +65,9 @@ def test_fixed_length_batch():
 
 
 def test_varlen_bitexact_against_separate_calls():
-    """One varlen call equals separate per-sequence calls bit for bit (cu_seqlens indexing)."""
+    """One varlen call equals separate per-sequence calls bit for bit (cu_seqlens indexing).  The separate
+    calls are one-sequence varlen calls, so that every call takes the chunked form (fixed-length calls of
+    1-4 tokens take the token-recurrent kernels)."""
     lens = [5, 0, 64, 131, 1, 17]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     p = make_problem(B=1, T=int(cu[-1]), H=3, seed=10, cu_seqlens=cu)
@@ -75,7 +77,7 @@ def test_varlen_bitexact_against_separate_calls():
         s = slice(int(cu[n]), int(cu[n + 1]))
         pn = dataclasses.replace(p, q=p.q[:, s].copy(), k=p.k[:, s].copy(), v=p.v[:, s].copy(), g=p.g[:, s].copy(),
                                  beta=p.beta[:, s].copy(), initial_state=p.initial_state[n:n + 1].copy(),
-                                 cu_seqlens=None)
+                                 cu_seqlens=np.array([0, lens[n]], dtype=np.int64))
         o_n, f_n = run_gpu(pn)
         assert np.array_equal(o_n, out[:, s]), n
         assert np.array_equal(f_n[0], fin[n]), n
@@ -222,3 +224,16 @@ def test_workspace_too_small_rejected():
     out = torch.empty_like(dev["q"])
     with pytest.raises(KDAError):
         _call(p, dev, out, None, workspace=ws)
+
+
+@pytest.mark.parametrize("T", [1, 3, 4])
+@pytest.mark.parametrize("state", [STATE_NONE, STATE_BF16, STATE_FP32])
+def test_short_fixed_length_takes_the_token_recurrent_kernels(T, state):
+    """kda_fwd on fixed-length problems of 1-4 tokens gives the bits of kda_fwd_recurrent (the same
+    kernels) and meets the oracle."""
+    p = make_problem(B=6, T=T, H=3, seed=60 + T, state_dtype=state)
+    a = run_gpu(p)
+    b = run_gpu(p, recurrent=True)
+    assert np.array_equal(a[0], b[0])
+    assert (a[1] is None and b[1] is None) or np.array_equal(a[1], b[1])
+    assert_parity(*a, *oracle_run(p))
