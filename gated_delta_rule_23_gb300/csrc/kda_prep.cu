@@ -72,7 +72,7 @@ static_assert(OFF_AQS + 64 * CH * 2 <= OPS_BYTES, "post-product overlay");
 // after T' is formed, the W and U0^T parts of the slot are staged over Akk / Tm for bulk copies
 constexpr int OFF_WS = OFF_AKK, OFF_US = OFF_AKK + 64 * D * 2;
 static_assert(OFF_US + D * CH * 2 <= OFF_TP, "W / U0 staging overlaps T'");
-constexpr int OFF_KG = 72192;                       // fp16 [64 j][128 c] K^ . Gamma (swizzled)
+constexpr int OFF_KG = 72192;                       // fp16 [64 j][128 c] K^ . Gamma (kg_off swizzle)
 constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizzled)
 constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 [64] 1 / |q|
 constexpr int OFF_RK = OFF_RQ + 256;                // fp32 [64] 1 / |k|
@@ -90,6 +90,18 @@ __device__ __forceinline__ int h64(int r, int c) { return r * 128 + ((((c >> 3) 
 // byte offset of 16-byte chunk c16 of token row t in the q / k / g staging tiles: swizzled by t / 4, so
 // that the 8 runs a quarter-warp reads (rows 4 run + r) fall on 8 different bank groups
 __device__ __forceinline__ int stg_off(int t, int c16) { return t * 256 + ((c16 ^ ((t >> 2) & 7)) << 4); }
+// byte offset of element (token t, channel c) in the K^.Gamma tile: 16-byte chunks XOR-swizzled by t % 8 and
+// (t / 8) % 4, so that both the gate pass's stores (tokens 4 m + r of one channel group: two wavefronts per
+// half-warp) and ldmatrix (8 consecutive tokens) spread over the banks
+__device__ __forceinline__ int kg_off(int t, int c) { return t * 256 + ((((c >> 3) ^ (t & 7) ^ ((t >> 3) & 3))) << 4) + ((c & 7) << 1); }
+
+__device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
 
@@ -325,6 +337,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
             if (hc == 1 && !mbar_wait(mbarA, 0))
                 hung = true;
             uint32_t ktw[4][2];   // K~ for (channel i, tokens r = 0,1 / 2,3) as fp16 pairs
+            uint32_t qodd[2];     // Q~ of the pass's even token, second half of the channels
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * run + r;
@@ -368,15 +381,19 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 if (t < 32)
                     *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_B + ops_off(t, kgrp)) =
                         make_float4(r0[0], r0[1], r0[2], r0[3]);
-                *reinterpret_cast<uint2 *>(sm + OFF_KG + h128(t, cb)) =
+                *reinterpret_cast<uint2 *>(sm + OFF_KG + kg_off(t, cb)) =
                     make_uint2(pack_half2(kg[0], kg[1]), pack_half2(kg[2], kg[3]));
-                // Q~: the first pass keeps its 4 channels, the second stores all 8 as one 16-byte row piece
+                // Q~: the first pass keeps its 4 channels; the second stores all 8 of two consecutive tokens (two
+                // 16-byte rows of one core matrix, contiguous) with one 32-byte store
                 if (hc == 0) {
                     qkeep[r][0] = pack_half2(qt[0], qt[1]);
                     qkeep[r][1] = pack_half2(qt[2], qt[3]);
+                } else if ((r & 1) == 0) {
+                    qodd[0] = pack_half2(qt[0], qt[1]);
+                    qodd[1] = pack_half2(qt[2], qt[3]);
                 } else {
-                    *reinterpret_cast<uint4 *>(slot + qw_off(CH + t, c0)) =
-                        make_uint4(qkeep[r][0], qkeep[r][1], pack_half2(qt[0], qt[1]), pack_half2(qt[2], qt[3]));
+                    st_global_v8(slot + qw_off(CH + t - 1, c0), qkeep[r - 1][0], qkeep[r - 1][1], qodd[0], qodd[1],
+                                 qkeep[r][0], qkeep[r][1], pack_half2(qt[0], qt[1]), pack_half2(qt[2], qt[3]));
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -389,26 +406,23 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 }
             }
             // K~ (slot rows = key channel, 8 tokens per 16-byte core row): the lanes of runs 2m and 2m + 1
-            // swap halves so that each stores two full rows (even run: channels 0, 2; odd run: 1, 3)
+            // swap halves so that each holds two full, adjacent rows (even run: channels 0, 1; odd run: 2, 3),
+            // 32 contiguous bytes of one core matrix, stored at once
             {
                 const bool ev = (run & 1) == 0;
-                uint32_t ra_[2], rb_[2];
+                uint32_t ra_[2], rb_[2];   // the partner's rows of channel 0 / 1 (even lane) or 2 / 3 (odd lane)
 #pragma unroll
                 for (int w = 0; w < 2; ++w) {
-                    ra_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[1][w] : ktw[0][w], 1);
-                    rb_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[3][w] : ktw[2][w], 1);
+                    ra_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[2][w] : ktw[0][w], 1);
+                    rb_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[3][w] : ktw[1][w], 1);
                 }
                 const int j8 = 8 * (run >> 1);
-                if (ev) {
-                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb, j8)) = make_uint4(ktw[0][0], ktw[0][1], ra_[0], ra_[1]);
-                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb + 2, j8)) =
-                        make_uint4(ktw[2][0], ktw[2][1], rb_[0], rb_[1]);
-                } else {
-                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb + 1, j8)) =
-                        make_uint4(ra_[0], ra_[1], ktw[1][0], ktw[1][1]);
-                    *reinterpret_cast<uint4 *>(slot + ka_off(CH + cb + 3, j8)) =
-                        make_uint4(rb_[0], rb_[1], ktw[3][0], ktw[3][1]);
-                }
+                if (ev)
+                    st_global_v8(slot + ka_off(CH + cb, j8), ktw[0][0], ktw[0][1], ra_[0], ra_[1], ktw[1][0], ktw[1][1],
+                                 rb_[0], rb_[1]);
+                else
+                    st_global_v8(slot + ka_off(CH + cb + 2, j8), ra_[0], ra_[1], ktw[2][0], ktw[2][1], rb_[0], rb_[1],
+                                 ktw[3][0], ktw[3][1]);
             }
             // this half of the channels: [Akk | Aqk] (+)= A B^T on the tensor cores
             fence_async_smem();
@@ -633,7 +647,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
 #pragma unroll
             for (int ks = 0; ks < CH / 16; ++ks) {
                 uint32_t bf[4];   // K^.Gamma rows j of k-step ks, the warp's two n-tiles
-                ldsm_x4_t(s_kg + h128(ks * 16 + (lsel & 1) * 8 + lr, (2 * warp + (lsel >> 1)) * 8), bf);
+                ldsm_x4_t(s_kg + kg_off(ks * 16 + (lsel & 1) * 8 + lr, (2 * warp + (lsel >> 1)) * 8), bf);
 #pragma unroll
                 for (int mt = ks; mt < 4; ++mt) {
                     uint32_t af[4];
