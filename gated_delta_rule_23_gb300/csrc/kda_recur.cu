@@ -35,6 +35,57 @@ constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load0, load1, product 
 static_assert(RECUR_SMEM <= 232448, "shared memory budget");
 static_assert(OFF_BUF1 % 128 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
+// S^T (64 columns) and O^T (32 columns) of this thread's lane in one round trip
+__device__ __forceinline__ void tmem_ld64_ld32(uint32_t taddr_s, uint32_t (&u)[64], uint32_t taddr_o, uint32_t (&o)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+                 "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+                 "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%96];\n"
+                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+                 "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%97];\n"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+                   "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
+                   "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]),
+                   "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31]),
+                   "=r"(u[32]), "=r"(u[33]), "=r"(u[34]), "=r"(u[35]), "=r"(u[36]), "=r"(u[37]), "=r"(u[38]), "=r"(u[39]),
+                   "=r"(u[40]), "=r"(u[41]), "=r"(u[42]), "=r"(u[43]), "=r"(u[44]), "=r"(u[45]), "=r"(u[46]), "=r"(u[47]),
+                   "=r"(u[48]), "=r"(u[49]), "=r"(u[50]), "=r"(u[51]), "=r"(u[52]), "=r"(u[53]), "=r"(u[54]), "=r"(u[55]),
+                   "=r"(u[56]), "=r"(u[57]), "=r"(u[58]), "=r"(u[59]), "=r"(u[60]), "=r"(u[61]), "=r"(u[62]), "=r"(u[63]),
+                   "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]), "=r"(o[4]), "=r"(o[5]), "=r"(o[6]), "=r"(o[7]),
+                   "=r"(o[8]), "=r"(o[9]), "=r"(o[10]), "=r"(o[11]), "=r"(o[12]), "=r"(o[13]), "=r"(o[14]), "=r"(o[15]),
+                   "=r"(o[16]), "=r"(o[17]), "=r"(o[18]), "=r"(o[19]), "=r"(o[20]), "=r"(o[21]), "=r"(o[22]), "=r"(o[23]),
+                   "=r"(o[24]), "=r"(o[25]), "=r"(o[26]), "=r"(o[27]), "=r"(o[28]), "=r"(o[29]), "=r"(o[30]), "=r"(o[31])
+                 : "r"(taddr_s), "r"(taddr_o));
+}
+// tcgen05.st without the completion wait (tmem_wait_st() before the tensor core or another thread reads the data)
+__device__ __forceinline__ void tmem_st64_nw(uint32_t taddr, const uint32_t (&u)[64])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+                 "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+                 "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
+                 ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+                    "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]),
+                    "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]),
+                    "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31]),
+                    "r"(u[32]), "r"(u[33]), "r"(u[34]), "r"(u[35]), "r"(u[36]), "r"(u[37]), "r"(u[38]), "r"(u[39]),
+                    "r"(u[40]), "r"(u[41]), "r"(u[42]), "r"(u[43]), "r"(u[44]), "r"(u[45]), "r"(u[46]), "r"(u[47]),
+                    "r"(u[48]), "r"(u[49]), "r"(u[50]), "r"(u[51]), "r"(u[52]), "r"(u[53]), "r"(u[54]), "r"(u[55]),
+                    "r"(u[56]), "r"(u[57]), "r"(u[58]), "r"(u[59]), "r"(u[60]), "r"(u[61]), "r"(u[62]), "r"(u[63]));
+}
+__device__ __forceinline__ void tmem_st32_nw(uint32_t taddr, const uint32_t (&u)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+                    "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]),
+                    "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]),
+                    "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31]));
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <int STATE, bool VARLEN>  // STATE: 0 none, 1 bf16, 2 fp32
 __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 {
@@ -137,12 +188,15 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 
     __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST);
     // O^T of the chunk just updated -> bf16 staging tile [t][v] (this thread: tokens 32 half .. + 31)
-    auto read_out = [&]() {
-        uint32_t o[32];
-        tmem_ld32(trow + TM_O + half * 32, o);
+    auto write_out = [&](const uint32_t (&o)[32]) {
 #pragma unroll
         for (int m = 0; m < 32; ++m)
             Ost[(half * 32 + m) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[m]) * p.scale);
+    };
+    auto read_out = [&]() {
+        uint32_t o[32];
+        tmem_ld32(trow + TM_O + half * 32, o);
+        write_out(o);
     };
     auto store_out = [&](int64_t ptok0, int pL) {
 #pragma unroll
@@ -184,24 +238,26 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         if (c >= 1 && c + 1 < nch)
             ++loads_issued;
 
-        // ---- P1: fp16 copy of S^T (A operand), S^T <- S^T Diag(Gamma_C), previous output read-out
+        // ---- P1: fp16 copy of S^T (A operand), S^T <- S^T Diag(Gamma_C), previous output read-out (one
+        //      tensor-memory load of S^T and O^T; the stores complete together before the barrier)
         {
             const float *gam = reinterpret_cast<const float *>(sb + SLOT_GC) + half * 64;
+            uint32_t u[64], o[32];
+            tmem_ld64_ld32(trow + TM_S + half * 64, u, trow + TM_O + half * 32, o);   // O^T unused at c = 0
+            {
+                uint32_t hv[32];
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                uint32_t u[32], hv[16];
-                tmem_ld32(trow + TM_S + half * 64 + 32 * part, u);
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
+                for (int m = 0; m < 32; ++m)
                     hv[m] = pack_half2(__uint_as_float(u[2 * m]), __uint_as_float(u[2 * m + 1]));
-                tmem_st16(trow + TM_S16 + half * 32 + 16 * part, hv);
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[32 * part + e]);
-                tmem_st32(trow + TM_S + half * 64 + 32 * part, u);
+                tmem_st32_nw(trow + TM_S16 + half * 32, hv);
             }
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[e]);
+            tmem_st64_nw(trow + TM_S + half * 64, u);
             if (c > 0)
-                read_out();
+                write_out(o);
+            tmem_wait_st();
         }
         tc_fence_before();
         __syncthreads();
