@@ -35,15 +35,17 @@ constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load0, load1, product 
 static_assert(RECUR_SMEM <= 232448, "shared memory budget");
 static_assert(OFF_BUF1 % 128 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 
-// S^T (64 columns) and O^T (32 columns) of this thread's lane in one round trip
-__device__ __forceinline__ void tmem_ld64_ld32(uint32_t taddr_s, uint32_t (&u)[64], uint32_t taddr_o, uint32_t (&o)[32])
+// S^T (64 columns, one lane per thread) and O^T (32 columns of the warp's 32 lanes in the mma accumulator
+// fragment layout: registers 16 h + 4 k + {0, 1} hold lane 16 h + i / 4 and 16 h + 8 + i / 4 for + {2, 3},
+// columns 8 k + 2 (i % 4) + {0, 1}) in one round trip
+__device__ __forceinline__ void tmem_ld_s_ofrag(uint32_t taddr_s, uint32_t (&u)[64], uint32_t taddr_o, uint32_t (&o)[32])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
                  "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
                  "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
                  "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%96];\n"
-                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
-                 "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%97];\n"
+                 "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79}, [%97];\n"
+                 "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%98];\n"
                  "tcgen05.wait::ld.sync.aligned;"
                  : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
                    "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
@@ -57,7 +59,7 @@ __device__ __forceinline__ void tmem_ld64_ld32(uint32_t taddr_s, uint32_t (&u)[6
                    "=r"(o[8]), "=r"(o[9]), "=r"(o[10]), "=r"(o[11]), "=r"(o[12]), "=r"(o[13]), "=r"(o[14]), "=r"(o[15]),
                    "=r"(o[16]), "=r"(o[17]), "=r"(o[18]), "=r"(o[19]), "=r"(o[20]), "=r"(o[21]), "=r"(o[22]), "=r"(o[23]),
                    "=r"(o[24]), "=r"(o[25]), "=r"(o[26]), "=r"(o[27]), "=r"(o[28]), "=r"(o[29]), "=r"(o[30]), "=r"(o[31])
-                 : "r"(taddr_s), "r"(taddr_o));
+                 : "r"(taddr_s), "r"(taddr_o), "r"(taddr_o + (16u << 16)));
 }
 // tcgen05.st without the completion wait (tmem_wait_st() before the tensor core or another thread reads the data)
 __device__ __forceinline__ void tmem_st64_nw(uint32_t taddr, const uint32_t (&u)[64])
@@ -188,14 +190,29 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 
     __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST);
     // O^T of the chunk just updated -> bf16 staging tile [t][v] (this thread: tokens 32 half .. + 31)
+    // o: O^T of this warp's 32 value lanes x tokens 32 half .. + 31 in fragment form (tmem_ld_s_ofrag); each 8 x 8
+    // (value, token) block goes to the staging tile transposed by stmatrix
+    const int lr = lane & 7, mi = lane >> 3;
     auto write_out = [&](const uint32_t (&o)[32]) {
 #pragma unroll
-        for (int m = 0; m < 32; ++m)
-            Ost[(half * 32 + m) * PH + vrow] = __float2bfloat16_rn(__uint_as_float(o[m]) * p.scale);
+        for (int sh = 0; sh < 2; ++sh)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t f[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[16 * sh + 8 * kk + 2 * m]) * p.scale,
+                                                                    __uint_as_float(o[16 * sh + 8 * kk + 2 * m + 1]) * p.scale);
+                    f[m] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                // matrix m: values q4 32 + 16 sh + 8 (m & 1) .., tokens of column group 2 kk + (m >> 1)
+                const int t = half * 32 + 8 * (2 * kk + (mi >> 1)) + lr, v = q4 * 32 + 16 * sh + 8 * (mi & 1);
+                stsm_x4_t(smem_u32(Ost + t * PH + v), f);
+            }
     };
     auto read_out = [&]() {
-        uint32_t o[32];
-        tmem_ld32(trow + TM_O + half * 32, o);
+        uint32_t u[64], o[32];
+        tmem_ld_s_ofrag(trow + TM_S, u, trow + TM_O + half * 32, o);
         write_out(o);
     };
     auto store_out = [&](int64_t ptok0, int pL) {
@@ -243,7 +260,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         {
             const float *gam = reinterpret_cast<const float *>(sb + SLOT_GC) + half * 64;
             uint32_t u[64], o[32];
-            tmem_ld64_ld32(trow + TM_S + half * 64, u, trow + TM_O + half * 32, o);   // O^T unused at c = 0
+            tmem_ld_s_ofrag(trow + TM_S + half * 64, u, trow + TM_O + half * 32, o);   // O^T unused at c = 0
             {
                 uint32_t hv[32];
 #pragma unroll
