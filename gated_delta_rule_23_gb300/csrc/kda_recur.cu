@@ -26,14 +26,18 @@ namespace {
 constexpr int RT = 256;                     // threads: warp w reads lanes 32 (w % 4) .. + 31
 constexpr int TMEM_COLS = 512;
 constexpr int TM_X = 0, TM_O = 64, TM_S = 128, TM_S16 = 256, TM_U16 = 320;
-constexpr int PH = 136;                     // bf16 pitch of the output staging tile
-constexpr int OFF_BUF0 = 0;
-constexpr int OFF_BUF1 = SLOT_BYTES;
-constexpr int OFF_OST = 2 * SLOT_BYTES;     // bf16 [64 t][136] output staging
-constexpr int OFF_BAR = OFF_OST + CH * PH * 2;
-constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load0, load1, product X|O, update; tmem slot; flag
+// Three slot buffers: chunk c lives in buffer c % 3.  The slot of chunk c + 2 is requested while chunk c runs, in
+// two bulk copies: QW and KA when chunk c starts (chunk c - 1's products, their only readers, are complete), U0^T
+// and Gamma_C once chunk c's last product is issued, because the output of chunk c - 1 is staged in that part of
+// chunk c - 1's buffer (bf16 [64 t][128 v], 16-byte pieces XOR-swizzled by t % 8) until it is stored.
+constexpr int NBUF = 3;
+constexpr int SLOT_HEAD = SLOT_U0;          // bytes of the first copy
+constexpr int OFF_BAR = NBUF * SLOT_BYTES;
+constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load 0..2, product X|O, update; tmem slot; flag
 static_assert(RECUR_SMEM <= 232448, "shared memory budget");
-static_assert(OFF_BUF1 % 128 == 0 && OFF_OST % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+static_assert(SLOT_BYTES % 128 == 0 && SLOT_HEAD % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+static_assert(SLOT_BYTES - SLOT_HEAD >= CH * D * 2, "output staging fits in U0^T and Gamma_C");
+__device__ __forceinline__ int ost_off(int t, int v) { return t * (D * 2) + ((((v >> 3) ^ (t & 7))) << 4) + ((v & 7) << 1); }
 
 // S^T (64 columns, one lane per thread) and O^T (32 columns of the warp's 32 lanes in the mma accumulator
 // fragment layout: registers 16 h + 4 k + {0, 1} hold lane 16 h + i / 4 and 16 h + 8 + i / 4 for + {2, 3},
@@ -110,17 +114,25 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     }
     const int nch = (int)((len + CH - 1) / CH);
 
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 32);
-    volatile uint32_t *hang_flag = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 36);
-    const uint32_t mbarL0 = smem_u32(sm + OFF_BAR), mbarL1 = smem_u32(sm + OFF_BAR + 8);
-    const uint32_t mbarQ = smem_u32(sm + OFF_BAR + 16), mbarB = smem_u32(sm + OFF_BAR + 24);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 40);
+    volatile uint32_t *hang_flag = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 44);
+    const uint32_t mbarL = smem_u32(sm + OFF_BAR);   // + 8 b: slot of buffer b landed
+    const uint32_t mbarQ = smem_u32(sm + OFF_BAR + 24), mbarB = smem_u32(sm + OFF_BAR + 32);
     auto slot_ptr = [&](int c) -> const unsigned char * {
         return p.slots + (size_t)((slot0 + c) * H + h) * SLOT_BYTES;
     };
-    auto issue_load = [&](int c) {   // one thread: the whole slot of chunk c into buffer c % 2
-        const uint32_t mb = (c & 1) ? mbarL1 : mbarL0;
+    auto buf_of = [&](int c) -> unsigned char * { return sm + (c % NBUF) * SLOT_BYTES; };
+    // one thread: the first / second part of the slot of chunk c into buffer c % 3 (both complete one phase
+    // of that buffer's mbarrier)
+    auto issue_head = [&](int c) {
+        const uint32_t mb = mbarL + 8 * (c % NBUF);
         mbar_expect_tx(mb, SLOT_BYTES);
-        bulk_g2s(smem_u32(sm + ((c & 1) ? OFF_BUF1 : OFF_BUF0)), slot_ptr(c), SLOT_BYTES, mb);
+        bulk_g2s(smem_u32(buf_of(c)), slot_ptr(c), SLOT_HEAD, mb);
+    };
+    auto issue_tail = [&](int c) {
+        fence_async_smem();   // the buffer's generic-proxy readers and writers finished before a barrier
+        bulk_g2s(smem_u32(buf_of(c) + SLOT_HEAD), slot_ptr(c) + SLOT_HEAD, SLOT_BYTES - SLOT_HEAD,
+                 mbarL + 8 * (c % NBUF));
     };
 
     if (warp == 0) {
@@ -130,8 +142,8 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         tc_fence_before();
     }
     if (tid == 0) {
-        mbar_init(mbarL0, 1);
-        mbar_init(mbarL1, 1);
+        for (int b = 0; b < NBUF; ++b)
+            mbar_init(mbarL + 8 * b, 1);
         mbar_init(mbarQ, 1);
         mbar_init(mbarB, 1);
         *hang_flag = 0u;
@@ -140,12 +152,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    int loads_issued = 0;
-    if (tid == 0) {
-        if (nch > 0) issue_load(0);
-        if (nch > 1) issue_load(1);
-    }
-    loads_issued = nch < 2 ? nch : 2;
+    // copies requested so far (the same count in every thread): heads and tails of chunks 0 .. heads - 1 / tails - 1
+    int heads = nch < 2 ? nch : 2, tails = heads;
+    if (tid == 0)
+        for (int k = 0; k < heads; ++k) {
+            issue_head(k);
+            issue_tail(k);
+        }
 
     const int q4 = warp & 3, half = warp >> 2;
     const int vrow = q4 * 32 + lane;
@@ -188,12 +201,11 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     }
     tc_fence_before();
 
-    __nv_bfloat16 *Ost = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OST);
     // O^T of the chunk just updated -> bf16 staging tile [t][v] (this thread: tokens 32 half .. + 31)
     // o: O^T of this warp's 32 value lanes x tokens 32 half .. + 31 in fragment form (tmem_ld_s_ofrag); each 8 x 8
     // (value, token) block goes to the staging tile transposed by stmatrix
     const int lr = lane & 7, mi = lane >> 3;
-    auto write_out = [&](const uint32_t (&o)[32]) {
+    auto write_out = [&](unsigned char *ost, const uint32_t (&o)[32]) {
 #pragma unroll
         for (int sh = 0; sh < 2; ++sh)
 #pragma unroll
@@ -207,21 +219,21 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                 }
                 // matrix m: values q4 32 + 16 sh + 8 (m & 1) .., tokens of column group 2 kk + (m >> 1)
                 const int t = half * 32 + 8 * (2 * kk + (mi >> 1)) + lr, v = q4 * 32 + 16 * sh + 8 * (mi & 1);
-                stsm_x4_t(smem_u32(Ost + t * PH + v), f);
+                stsm_x4_t(smem_u32(ost + ost_off(t, v)), f);
             }
     };
-    auto read_out = [&]() {
+    auto read_out = [&](unsigned char *ost) {
         uint32_t u[64], o[32];
         tmem_ld_s_ofrag(trow + TM_S, u, trow + TM_O + half * 32, o);
-        write_out(o);
+        write_out(ost, o);
     };
-    auto store_out = [&](int64_t ptok0, int pL) {
+    auto store_out = [&](const unsigned char *ost, int64_t ptok0, int pL) {
 #pragma unroll
         for (int m = 0; m < (CH * 16) / RT; ++m) {
             const int idx = tid + m * RT, r = idx >> 4, c16 = idx & 15;
             if (r < pL)
                 *reinterpret_cast<uint4 *>(p.out + ((ptok0 + r) * H + h) * D + c16 * 8) =
-                    *reinterpret_cast<const uint4 *>(sm + OFF_OST + r * PH * 2 + c16 * 16);
+                    *reinterpret_cast<const uint4 *>(ost + r * (D * 2) + ((c16 ^ (r & 7)) << 4));
         }
     };
 
@@ -231,9 +243,9 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     int prev_L = 0;
     int c = 0;
     for (; c < nch; ++c) {
-        const int buf = c & 1;
-        const unsigned char *sb = sm + (buf ? OFF_BUF1 : OFF_BUF0);
+        const unsigned char *sb = buf_of(c);
         const uint32_t s_buf = smem_u32(sb);
+        unsigned char *ost = buf_of(c + NBUF - 1) + SLOT_HEAD;   // staging of chunk c - 1's output
         const int64_t tok0 = bos + (int64_t)c * CH;
         const int64_t rem = len - (int64_t)c * CH;
         const int L = (int)(rem < CH ? rem : CH);
@@ -242,18 +254,18 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         bool ok = true;
         if (c > 0)
             ok = mbar_wait(mbarB, (c - 1) & 1);
-        ok = ok && mbar_wait(buf ? mbarL1 : mbarL0, (c >> 1) & 1);
+        ok = ok && mbar_wait(mbarL + 8 * (c % NBUF), (c / NBUF) & 1);
         if (__syncthreads_or(!ok)) {
             hung = true;
             break;
         }
         tc_fence_after();
-        if (tid == 0 && c >= 1 && c + 1 < nch) {
-            fence_async_smem();   // the other buffer's last readers finished before the barrier above
-            issue_load(c + 1);
+        // QW and KA of chunk c + 2 into chunk c - 1's buffer: only chunk c - 1's products (complete) read them
+        if (c + 2 < nch) {
+            if (tid == 0)
+                issue_head(c + 2);
+            ++heads;
         }
-        if (c >= 1 && c + 1 < nch)
-            ++loads_issued;
 
         // ---- P1: fp16 copy of S^T (A operand), S^T <- S^T Diag(Gamma_C), previous output read-out (one
         //      tensor-memory load of S^T and O^T; the stores complete together before the barrier)
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                 u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[e]);
             tmem_st64_nw(trow + TM_S + half * 64, u);
             if (c > 0)
-                write_out(o);
+                write_out(ost, o);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         }
         ++nq;
         if (c > 0)
-            store_out(prev_tok0, prev_L);
+            store_out(ost, prev_tok0, prev_L);
 
         // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
         ok = mbar_wait(mbarQ, c & 1);
@@ -325,6 +337,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             umma_commit(mbarB);
         }
         ++nb;
+        // U0^T and Gamma_C of chunk c + 2: chunk c - 1's staged output was stored before the barrier after the
+        // first product, and chunk c - 1 read its U0^T and Gamma_C before the barriers of its own chunk
+        if (c + 2 < nch) {
+            if (tid == 32)
+                issue_tail(c + 2);
+            ++tails;
+        }
         prev_tok0 = tok0;
         prev_L = L;
     }
@@ -335,9 +354,9 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             hung = true;
         } else {
             tc_fence_after();
-            read_out();
+            read_out(buf_of(nch - 1) + SLOT_HEAD);
             __syncthreads();
-            store_out(prev_tok0, prev_L);
+            store_out(buf_of(nch - 1) + SLOT_HEAD, prev_tok0, prev_L);
         }
     }
 
@@ -349,8 +368,11 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                 mbar_wait(mbarQ, (nq - 1) & 1);
             if (nb > 0)
                 mbar_wait(mbarB, (nb - 1) & 1);
-            for (int k = c; k < loads_issued; ++k)
-                mbar_wait((k & 1) ? mbarL1 : mbarL0, (k >> 1) & 1);
+            for (int k = c; k < heads; ++k) {
+                if (k >= tails)
+                    issue_tail(k);   // completes the phase the head's expect_tx opened
+                mbar_wait(mbarL + 8 * (k % NBUF), (k / NBUF) & 1);
+            }
             atomicOr(&g_kda_device_error, 1u);
         }
     } else if (STATE != 0 && p.fin) {
