@@ -9,8 +9,9 @@
 //   U^T = U0^T - X^T                            (threads; fp16 into tensor memory)
 //   [O^T | S^T] += U^T [Aqk ; K~^T]^T           (A = U^T, K = 64; S^T decayed beforehand)
 // The fp32 master state S^T never leaves tensor memory; an fp16 copy of it is the A operand of
-// the first product.  The slot of chunk c + 1 is bulk-copied into shared memory while chunk c
-// runs.
+// the first product.  The slots stream through three shared-memory buffers, each requested two
+// chunks ahead; the output of a chunk is transposed (stmatrix) into its consumed slot and stored
+// during the next chunk.
 //
 // Tensor-memory columns: X^T 0..63 | O^T 64..127 | S^T 128..255 | fp16 S^T 256..319 |
 // fp16 U^T 320..351 (512 allocated).
