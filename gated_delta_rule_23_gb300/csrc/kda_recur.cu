@@ -304,11 +304,10 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             store_out(ost, prev_tok0, prev_L);
 
         // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
-        ok = mbar_wait(mbarQ, c & 1);
-        if (__syncthreads_or(!ok)) {
-            hung = true;
-            break;
-        }
+        // (no barrier: each thread waits for the product itself; a wait that gave up is reported through the
+        // flag, which every thread reads after the next barrier)
+        if (!mbar_wait(mbarQ, c & 1))
+            *hang_flag = 1u;
         tc_fence_after();
         {
             uint32_t x[32], hv[16];
@@ -329,6 +328,10 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         }
         tc_fence_before();
         __syncthreads();
+        if (*hang_flag) {
+            hung = true;
+            break;
+        }
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
