@@ -147,15 +147,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 
-// stmatrix.trans: four 8x8 16-bit matrices from mma-fragment registers, each stored transposed (matrix m:
-// rows at the addresses of lanes 8m .. 8m + 7)
-__device__ __forceinline__ void stsm_x4_t(uint32_t addr, const uint32_t (&r)[4])
-{
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid)
 {
     const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled

@@ -66,6 +66,15 @@ __device__ __forceinline__ void tmem_ld_s_ofrag(uint32_t taddr_s, uint32_t (&u)[
                    "=r"(o[24]), "=r"(o[25]), "=r"(o[26]), "=r"(o[27]), "=r"(o[28]), "=r"(o[29]), "=r"(o[30]), "=r"(o[31])
                  : "r"(taddr_s), "r"(taddr_o), "r"(taddr_o + (16u << 16)));
 }
+// stmatrix.trans: four 8x8 16-bit matrices from mma-fragment registers, each stored transposed (matrix m:
+// rows at the addresses of lanes 8m .. 8m + 7)
+__device__ __forceinline__ void stsm_x4_t(uint32_t addr, const uint32_t (&r)[4])
+{
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // tcgen05.st without the completion wait (tmem_wait_st() before the tensor core or another thread reads the data)
 __device__ __forceinline__ void tmem_st64_nw(uint32_t taddr, const uint32_t (&u)[64])
 {
