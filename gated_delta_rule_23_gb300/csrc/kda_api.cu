@@ -15,12 +15,13 @@ constexpr int PLAN_THREADS = 1024;
 constexpr int LPT_MAX_SEQS = 2048;   // longest-first ordering of varlen sequences up to this count
 
 // Varlen plan, one CTA: chunk_off[n] = sum_{m < n} ceil(len_m / 64) (exclusive scan, [N + 1]);
-// chunk_info[c] = (first token, tokens left in the sequence) of every chunk c < chunk_off[N], so
-// that a prep CTA finds its chunk with one load; and, when order != nullptr, order[rank] =
+// chunk_info[c] = (first token, tokens left in the sequence) of every chunk c < chunk_off[N] and (0, 0)
+// for the launched chunk indices past it (c < n_info), so that a prep CTA finds its chunk, or that it
+// has none, with one load; and, when order != nullptr, order[rank] =
 // sequence with that rank by length (longest first, ties by index), so that the recurrence CTAs
 // that start first take the longest sequences.
 __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *cu, int N, int64_t *chunk_off,
-                                                              longlong2 *chunk_info, int *order)
+                                                              longlong2 *chunk_info, int64_t n_info, int *order)
 {
     __shared__ int64_t wsum[PLAN_THREADS / 32];
     __shared__ int64_t carry;
@@ -75,6 +76,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *c
         const int64_t tok0 = cu[lo] + (c - chunk_off[lo]) * CH;
         chunk_info[c] = make_longlong2(tok0, cu[lo + 1] - tok0);
     }
+    for (int64_t c = carry + tid; c < n_info; c += PLAN_THREADS)
+        chunk_info[c] = make_longlong2(0, 0);
     if (order) {
         for (int s = tid; s < N; s += PLAN_THREADS) {
             const int64_t ls = cu[s + 1] - cu[s];
@@ -271,7 +274,8 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
         int64_t *chunk_off = reinterpret_cast<int64_t *>(ws);
         int *order = N > 1 && N <= LPT_MAX_SEQS ? reinterpret_cast<int *>(ws + (size_t)(N + 1) * 8) : nullptr;
         longlong2 *chunk_info = reinterpret_cast<longlong2 *>(ws + info_offset(N));
-        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, chunk_off, chunk_info, order);
+        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, chunk_off, chunk_info, max_chunks(N, T, true),
+                                                        order);
         err = cudaGetLastError();
         p.chunk_off = chunk_off;
         p.chunk_info = chunk_info;

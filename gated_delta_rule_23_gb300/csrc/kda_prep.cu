@@ -107,8 +107,8 @@ __device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("pre
 
 // first token and tokens left of chunk gc (a global chunk index over all sequences; the launch keeps
 // every item index, and so gc, below 2^31, so the divisions are 32-bit); varlen chunks come from the
-// plan's per-chunk table, which has an entry for every launched chunk index (only those below
-// chunk_off[N] are filled: callers check that)
+// plan's per-chunk table, which has an entry for every launched chunk index (0 tokens left past the
+// last chunk)
 template <bool VARLEN>
 __device__ __forceinline__ void chunk_tokens(const Problem &p, uint32_t gc, int64_t &tok0, int64_t &rem)
 {
@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     // -------- this CTA's chunk: first token tok0 and L valid tokens
     int64_t tok0, rem;
     chunk_tokens<VARLEN>(p, gc, tok0, rem);   // the table has an entry for every launched CTA
-    if (VARLEN && (int64_t)gc >= p.chunk_off[p.N])
-        return;
+    if (VARLEN && rem <= 0)
+        return;   // past the last chunk
     const int L = (int)(rem < CH ? rem : CH);
     unsigned char *slot = p.slots + (size_t)item * SLOT_BYTES;
 
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         const int ph = (int)(pit - pgc * (uint32_t)H);
         int64_t ptok0, prem;
         chunk_tokens<VARLEN>(p, pgc, ptok0, prem);
-        if (!VARLEN || (int64_t)pgc < p.chunk_off[p.N]) {
+        {   // (varlen: 0 tokens left past the last chunk)
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const int li = tid + m * PREP_THREADS, which = li >> 7, t = (li >> 1) & (CH - 1);
