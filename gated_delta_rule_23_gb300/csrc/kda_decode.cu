@@ -188,11 +188,10 @@ __global__ void __launch_bounds__(DC_THREADS, 2) kda_decode_kernel(const Problem
             const int hn = hdp->n, hh = hdp->h, hvh = hdp->vhalf;
             const float halog = hdp->alog;
             const float gz = -expf(halog) * LOG2E;
-            float gd[8];
-#pragma unroll
-            for (int f = 0; f < 2; ++f) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(s + lay.dtb + (64 * f + 4 * kg) * 4);
-                gd[4 * f] = gz * d4.x; gd[4 * f + 1] = gz * d4.y; gd[4 * f + 2] = gz * d4.z; gd[4 * f + 3] = gz * d4.w;
+            float gd[4];   // this lane's key group (see below)
+            {
+                const float4 d4 = *reinterpret_cast<const float4 *>(s + lay.dtb + (64 * (lane >> 4) + 4 * kg) * 4);
+                gd[0] = gz * d4.x; gd[1] = gz * d4.y; gd[2] = gz * d4.z; gd[3] = gz * d4.w;
             }
             // the state columns of this thread
             f2 S2[4][4];
@@ -219,53 +218,55 @@ __global__ void __launch_bounds__(DC_THREADS, 2) kda_decode_kernel(const Problem
             // kernel's stages (same rounding, so both kernels give the same bits): per key, A_t = 2^(sum of
             // log2 alpha through token t); S holds S / A_t; p = (S/A)^T (A k^), S/A += (k^ / A) u^T,
             // o = (S/A)^T (scale A q^); at the end S = A_T (S / A)
-            float Lk[8];
+            // The two half-warps hold the same keys (they differ in values), so each computes the per-key
+            // quantities of one key group, fo = lane / 16 (keys 64 fo + 4 kg + j), with the expressions and
+            // summation orders of the staged kernel, and takes the other group's from its partner lane.
+            const int fo = lane >> 4;
+            float Lk[4];   // log2 of A for this lane's 4 keys
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 4; ++j)
                 Lk[j] = 0.f;
             for (int t = 0; t < T; ++t) {
-                uint2 qw[2], kw[2];
-                float s4q[2], s4k[2];
+                const int key = 64 * fo + 4 * kg;
+                const uint2 qw = *reinterpret_cast<const uint2 *>(s + lay.q + (t * D + key) * 2);
+                const uint2 kw = *reinterpret_cast<const uint2 *>(s + lay.k + (t * D + key) * 2);
+                const uint2 gw = *reinterpret_cast<const uint2 *>(s + lay.g + (t * D + key) * 2);
+                const float q4[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
+                const float k4[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+                const float g4[4] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y)};
+                float sq = 0.f, sk = 0.f;
 #pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    const int key = 64 * f + 4 * kg;
-                    qw[f] = *reinterpret_cast<const uint2 *>(s + lay.q + (t * D + key) * 2);
-                    kw[f] = *reinterpret_cast<const uint2 *>(s + lay.k + (t * D + key) * 2);
-                    const uint2 gw = *reinterpret_cast<const uint2 *>(s + lay.g + (t * D + key) * 2);
-                    const float q4[4] = {bf16_lo(qw[f].x), bf16_hi(qw[f].x), bf16_lo(qw[f].y), bf16_hi(qw[f].y)};
-                    const float k4[4] = {bf16_lo(kw[f].x), bf16_hi(kw[f].x), bf16_lo(kw[f].y), bf16_hi(kw[f].y)};
-                    const float g4[4] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y)};
-                    float sq = 0.f, sk = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        sq = fmaf(q4[j], q4[j], sq);
-                        sk = fmaf(k4[j], k4[j], sk);
-                        // the product is rounded before the sum (no contraction), as in the staged kernel
-                        Lk[4 * f + j] += __fmul_rn(p.lb_log2e, rcp_approx(1.f + ex2_approx(fmaf(g4[j], gz, gd[4 * f + j]))));
-                    }
-                    s4q[f] = sq;
-                    s4k[f] = sk;
+                for (int j = 0; j < 4; ++j) {
+                    sq = fmaf(q4[j], q4[j], sq);
+                    sk = fmaf(k4[j], k4[j], sk);
+                    // the product is rounded before the sum (no contraction), as in the staged kernel
+                    Lk[j] += __fmul_rn(p.lb_log2e, rcp_approx(1.f + ex2_approx(fmaf(g4[j], gz, gd[j]))));
                 }
                 // the norms: the same summation tree as a warp over 4-channel groups (groups f = 0, 1 first)
-                const float rq = rsqrtf(allsum16(s4q[0] + s4q[1]) + 1e-6f) * p.scale;
-                const float rk = rsqrtf(allsum16(s4k[0] + s4k[1]) + 1e-6f);
+                const float sqp = __shfl_xor_sync(0xffffffffu, sq, 16), skp = __shfl_xor_sync(0xffffffffu, sk, 16);
+                const float rq = rsqrtf(allsum16(fo ? sqp + sq : sq + sqp) + 1e-6f) * p.scale;
+                const float rk = rsqrtf(allsum16(fo ? skp + sk : sk + skp) + 1e-6f);
                 const float b = sigmoid_fast(__uint_as_float((uint32_t)hdp->beta[t] << 16));
+                float a4[4], d4[4], e4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float A = ex2_approx(Lk[j]), kh = k4[j] * rk;
+                    a4[j] = kh * A;
+                    d4[j] = kh * ex2_approx(-Lk[j]);
+                    e4[j] = q4[j] * rq * A;
+                }
+                // key group f's pairs in slots 2 f, 2 f + 1: this lane's group from itself, the other from lane ^ 16
                 f2 ka[4], kd[4], qa[4];
+                {
+                    const f2 o[6] = {f2_pack(a4[0], a4[1]), f2_pack(a4[2], a4[3]), f2_pack(d4[0], d4[1]),
+                                     f2_pack(d4[2], d4[3]), f2_pack(e4[0], e4[1]), f2_pack(e4[2], e4[3])};
+                    f2 x[6];
 #pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    const float q4[4] = {bf16_lo(qw[f].x), bf16_hi(qw[f].x), bf16_lo(qw[f].y), bf16_hi(qw[f].y)};
-                    const float k4[4] = {bf16_lo(kw[f].x), bf16_hi(kw[f].x), bf16_lo(kw[f].y), bf16_hi(kw[f].y)};
-                    float a4[4], d4[4], e4[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float A = ex2_approx(Lk[4 * f + j]), kh = k4[j] * rk;
-                        a4[j] = kh * A;
-                        d4[j] = kh * ex2_approx(-Lk[4 * f + j]);
-                        e4[j] = q4[j] * rq * A;
-                    }
-                    ka[2 * f] = f2_pack(a4[0], a4[1]); ka[2 * f + 1] = f2_pack(a4[2], a4[3]);
-                    kd[2 * f] = f2_pack(d4[0], d4[1]); kd[2 * f + 1] = f2_pack(d4[2], d4[3]);
-                    qa[2 * f] = f2_pack(e4[0], e4[1]); qa[2 * f + 1] = f2_pack(e4[2], e4[3]);
+                    for (int m = 0; m < 6; ++m)
+                        x[m] = __shfl_xor_sync(0xffffffffu, o[m], 16);
+                    ka[0] = fo ? x[0] : o[0]; ka[1] = fo ? x[1] : o[1]; ka[2] = fo ? o[0] : x[0]; ka[3] = fo ? o[1] : x[1];
+                    kd[0] = fo ? x[2] : o[2]; kd[1] = fo ? x[3] : o[3]; kd[2] = fo ? o[2] : x[2]; kd[3] = fo ? o[3] : x[3];
+                    qa[0] = fo ? x[4] : o[4]; qa[1] = fo ? x[5] : o[5]; qa[2] = fo ? o[4] : x[4]; qa[3] = fo ? o[5] : x[5];
                 }
                 float pk[4];
 #pragma unroll
@@ -299,16 +300,17 @@ __global__ void __launch_bounds__(DC_THREADS, 2) kda_decode_kernel(const Problem
                     *outp = __float2bfloat16_rn(om);
                 outp += (size_t)H * D;
             }
-            // back from S / A to S
+            // back from S / A to S (this lane's key group's A from itself, the other group's from lane ^ 16)
+            {
+                const f2 o01 = f2_pack(ex2_approx(Lk[0]), ex2_approx(Lk[1]));
+                const f2 o23 = f2_pack(ex2_approx(Lk[2]), ex2_approx(Lk[3]));
+                const f2 x01 = __shfl_xor_sync(0xffffffffu, o01, 16), x23 = __shfl_xor_sync(0xffffffffu, o23, 16);
+                const f2 a[4] = {fo ? x01 : o01, fo ? x23 : o23, fo ? o01 : x01, fo ? o23 : x23};
 #pragma unroll
-            for (int f = 0; f < 2; ++f) {
-                const f2 a01 = f2_pack(ex2_approx(Lk[4 * f]), ex2_approx(Lk[4 * f + 1]));
-                const f2 a23 = f2_pack(ex2_approx(Lk[4 * f + 2]), ex2_approx(Lk[4 * f + 3]));
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    S2[c][2 * f] = f2_mul(S2[c][2 * f], a01);
-                    S2[c][2 * f + 1] = f2_mul(S2[c][2 * f + 1], a23);
-                }
+                    for (int i2 = 0; i2 < 4; ++i2)
+                        S2[c][i2] = f2_mul(S2[c][i2], a[i2]);
             }
             // the slot is read: release it to the producer
             __syncwarp();

@@ -270,12 +270,6 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             break;
         }
         tc_fence_after();
-        // QW and KA of chunk c + 2 into chunk c - 1's buffer: only chunk c - 1's products (complete) read them
-        if (c + 2 < nch) {
-            if (tid == 0)
-                issue_head(c + 2);
-            ++heads;
-        }
 
         // ---- P1: fp16 copy of S^T (A operand), S^T <- S^T Diag(Gamma_C), previous output read-out (one
         //      tensor-memory load of S^T and O^T; the stores complete together before the barrier)
@@ -300,6 +294,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         }
         tc_fence_before();
         __syncthreads();
+        // QW and KA of chunk c + 2 into chunk c - 1's buffer (only chunk c - 1's products, complete, read them), by
+        // another warp while the first product is issued
+        if (c + 2 < nch) {
+            if (tid == 32)
+                issue_head(c + 2);
+            ++heads;
+        }
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
