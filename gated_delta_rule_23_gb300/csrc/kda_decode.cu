@@ -382,8 +382,9 @@ cudaError_t launch_decode_t(const Problem &p, cudaStream_t stream)
 
 // Fixed-length problems of 1-4 tokens.  Both kernels give the same bits; the choice is by measurement on
 // GB300: for one token with an fp32 state (64 KB of state traffic per item) the staged kernel streams the
-// state slightly faster (0.494 against 0.525 ms at 256 sequences x 96 heads); for bf16 states (0.267 against
-// 0.395 ms) and for 2-4 tokens the decode kernel is faster.
+// state slightly faster (0.493 against 0.519 ms at 256 sequences x 96 heads); for bf16 states (0.252 against
+// 0.394 ms) and for 2-4 tokens (64 sequences x 4 tokens: 0.180 / 0.164 against 0.211 / 0.187 ms for fp32 /
+// bf16 states) the decode kernel is faster.
 bool decode_applies(const Problem &p, int state_kind)
 {
     return p.cu == nullptr && p.T >= 1 && p.T <= DC_MAX_T && !(state_kind == 2 && p.T == 1);
