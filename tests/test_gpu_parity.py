@@ -84,6 +84,20 @@ def test_varlen_bitexact_against_separate_calls():
     assert np.array_equal(fin[1], p.initial_state[1])    # zero-length: final = initial exactly
 
 
+def test_more_sequences_than_the_plan_orders():
+    """2100 varlen sequences of 0-3 tokens: the plan kernel scans more sequences than its block has threads and
+    leaves the longest-first order off (beyond 2048 sequences); every output and final state (empty sequences:
+    final = initial exactly) against the oracle."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(0, 4, size=2100)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    p = make_problem(B=1, T=int(cu[-1]), H=1, seed=78, cu_seqlens=cu)
+    out, fin = run_gpu(p)
+    assert_parity(out, fin, *oracle_run(p))
+    empty = np.flatnonzero(lens == 0)
+    assert np.array_equal(fin[empty], p.initial_state[empty])
+
+
 def test_all_sequences_empty():
     cu = np.zeros(4, dtype=np.int64)
     p = make_problem(B=1, T=0, H=2, seed=11, cu_seqlens=cu)
