@@ -635,70 +635,55 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         const uint32_t s_tp = smem_u32(sm + OFF_TP), s_kg = smem_u32(sm + OFF_KG), s_v = smem_u32(sm + OFF_V);
         const int gq = lane >> 2, t4 = lane & 3;
         const int lr = lane & 7, lsel = lane >> 3;   // ldmatrix: row within a matrix, matrix index
-        // W: channels of n-tiles 2 warp, 2 warp + 1, all rows t.  T' is block lower triangular, so
-        // m-tile mt needs k-steps 0..mt only.
-        {
-            float acc[4][2][4];
+        // W (channels of n-tiles 2 warp, 2 warp + 1, all rows t) and U0^T (value rows 16 warp .. + 15, all tokens)
+        // together: T' is block lower triangular, so k-step ks needs its blocks (mt, ks), mt >= ks, only, and each
+        // block's A fragment of W's product is also the B fragment of U0^T's (T'^T) for the tokens of m-tile mt
+        float accw[4][2][4], accu[8][4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    acc[m][a][0] = acc[m][a][1] = acc[m][a][2] = acc[m][a][3] = 0.f;
+            for (int a = 0; a < 2; ++a)
+                accw[m][a][0] = accw[m][a][1] = accw[m][a][2] = accw[m][a][3] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < CH / 16; ++ks) {
-                uint32_t bf[4];   // K^.Gamma rows j of k-step ks, the warp's two n-tiles
-                ldsm_x4_t(s_kg + kg_off(ks * 16 + (lsel & 1) * 8 + lr, (2 * warp + (lsel >> 1)) * 8), bf);
+        for (int a = 0; a < 8; ++a)
+            accu[a][0] = accu[a][1] = accu[a][2] = accu[a][3] = 0.f;
 #pragma unroll
-                for (int mt = ks; mt < 4; ++mt) {
-                    uint32_t af[4];
-                    ldsm_x4(s_tp + h64(mt * 16 + (lsel & 1) * 8 + lr, ks * 16 + (lsel >> 1) * 8), af);
-                    mma_f16(acc[mt][0], af, bf[0], bf[1]);
-                    mma_f16(acc[mt][1], af, bf[2], bf[3]);
-                }
+        for (int ks = 0; ks < CH / 16; ++ks) {
+            uint32_t bf[4];   // K^.Gamma rows j of k-step ks, the warp's two n-tiles
+            ldsm_x4_t(s_kg + kg_off(ks * 16 + (lsel & 1) * 8 + lr, (2 * warp + (lsel >> 1)) * 8), bf);
+            uint32_t vf[4];   // A = V^T: matrices (v 0-7, j 0-7), (v 8-15, j 0-7), (v 0-7, j 8-15), (v 8-15, j 8-15)
+            ldsm_x4_t(s_v + h128(ks * 16 + (lsel >> 1) * 8 + lr, warp * 16 + (lsel & 1) * 8), vf);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                vf[e] = bf16x2_to_half2(vf[e]);
+#pragma unroll
+            for (int mt = ks; mt < 4; ++mt) {
+                uint32_t af[4];   // T' block (mt, ks): (t 0-7, j 0-7), (t 8-15, j 0-7), (t 0-7, j 8-15), (t 8-15, j 8-15)
+                ldsm_x4(s_tp + h64(mt * 16 + (lsel & 1) * 8 + lr, ks * 16 + (lsel >> 1) * 8), af);
+                mma_f16(accw[mt][0], af, bf[0], bf[1]);
+                mma_f16(accw[mt][1], af, bf[2], bf[3]);
+                mma_f16(accu[2 * mt], vf, af[0], af[2]);       // tokens 16 mt .. + 7
+                mma_f16(accu[2 * mt + 1], vf, af[1], af[3]);   // tokens 16 mt + 8 .. + 15
             }
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int t = mt * 16 + gq + 8 * hh, c = (2 * warp + a) * 8 + 2 * t4;
-                        *reinterpret_cast<uint32_t *>(sm + OFF_WS + qw_off(t, c)) =
-                            pack_half2(acc[mt][a][2 * hh], acc[mt][a][2 * hh + 1]);
-                    }
         }
-        // U0^T: value rows 16 warp .. + 15, all 64 tokens
-        {
-            float acc[8][4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
-                acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int ks = 0; ks < CH / 16; ++ks) {
-                uint32_t af[4];
-                // A = V^T: matrices (v 0-7, j 0-7), (v 8-15, j 0-7), (v 0-7, j 8-15), (v 8-15, j 8-15)
-                ldsm_x4_t(s_v + h128(ks * 16 + (lsel >> 1) * 8 + lr, warp * 16 + (lsel & 1) * 8), af);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    af[e] = bf16x2_to_half2(af[e]);
-#pragma unroll
-                for (int np = ks; np < 4; ++np) {   // T'^T rows j of k-step ks are zero for tokens t < 16 ks
-                    uint32_t bf[4];
-                    // B = T'^T: matrices (t-tile 2np, j 0-7), (2np, j 8-15), (2np+1, j 0-7), (2np+1, j 8-15)
-                    ldsm_x4(s_tp + h64((2 * np + (lsel >> 1)) * 8 + lr, ks * 16 + (lsel & 1) * 8), bf);
-                    mma_f16(acc[2 * np], af, bf[0], bf[1]);
-                    mma_f16(acc[2 * np + 1], af, bf[2], bf[3]);
-                }
-            }
-#pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < 2; ++a)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int vr = warp * 16 + gq + 8 * hh, t = a * 8 + 2 * t4;
-                    *reinterpret_cast<uint32_t *>(sm + OFF_US + u0_off(vr, t) - SLOT_U0) =
-                        pack_half2(acc[a][2 * hh], acc[a][2 * hh + 1]);
+                    const int t = mt * 16 + gq + 8 * hh, c = (2 * warp + a) * 8 + 2 * t4;
+                    *reinterpret_cast<uint32_t *>(sm + OFF_WS + qw_off(t, c)) =
+                        pack_half2(accw[mt][a][2 * hh], accw[mt][a][2 * hh + 1]);
                 }
-        }
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int vr = warp * 16 + gq + 8 * hh, t = a * 8 + 2 * t4;
+                *reinterpret_cast<uint32_t *>(sm + OFF_US + u0_off(vr, t) - SLOT_U0) =
+                    pack_half2(accu[a][2 * hh], accu[a][2 * hh + 1]);
+            }
     }
     fence_async_smem();
     __syncthreads();
