@@ -83,6 +83,24 @@ def kernel_bytes(p):
     return {"kda_prep_kernel": prep, "kda_recur_kernel": recur}
 
 
+def algorithmic_flops(p, chunk=64):
+    """Dense FLOPs of the chunked method per token*head: 6 K V for the three state products
+    (W S, Q~ S, K~^T U) plus 10 C 128 for the intra-chunk products (Akk, Aqk, W, U0, Aqk U)."""
+    return p.token_heads() * (6 * 128 * 128 + 10 * chunk * 128)
+
+
+def kernel_algorithmic_bytes(p):
+    """The share of the call's algorithmic bytes each kernel moves: the prep kernel reads the token
+    tensors and parameters, the recurrence kernel writes out and reads / writes the states."""
+    th = p.token_heads()
+    es = {STATE_BF16: 2, STATE_FP32: 4}.get(p.state_dtype, 0)
+    per_state = p.N * p.H * 128 * 128 * es
+    states = per_state * ((p.initial_state is not None) + bool(p.want_final and es))
+    cu = 0 if p.cu_seqlens is None else 8 * (p.N + 1)
+    return {"kda_prep_kernel": th * (4 * 128 * 2 + 2) + p.H * (4 + 128 * 4),
+            "kda_recur_kernel": th * 128 * 2 + states + cu}
+
+
 def kernel_source_hash(kernel):
     """Hash of the device sources `kernel` is built from."""
     h = hashlib.sha256()
@@ -278,7 +296,7 @@ def measure_decode(stream, steps=50, warmup=5, n_seq=DECODE_N, T=1):
     import torch
     from gated_delta_rule_23_gb300 import kda_fwd, kda_fwd_recurrent
     from gated_delta_rule_23_gb300.inputs import make_problem
-    from tests.gpu_util import to_device
+    from gated_delta_rule_23_gb300.device import to_device
 
     p = make_problem(B=n_seq, T=T, H=DECODE_H, seed=77)
     dev = to_device(p)
@@ -329,7 +347,7 @@ def run_ours(args, p, idx, rank, world):
     import torch
     import torch.distributed as dist
     from gated_delta_rule_23_gb300 import kda_fwd, kda_fwd_host
-    from tests.gpu_util import to_device
+    from gated_delta_rule_23_gb300.device import to_device
 
     dev = to_device(p)
     out = torch.empty_like(dev["q"])
@@ -421,14 +439,22 @@ def run_ours(args, p, idx, rank, world):
     th = p.token_heads() * world   # replicas: every rank processes the whole workload
     hbm, tc, peak_src = peaks()
     abytes = algorithmic_bytes(p)
+    aflops = algorithmic_flops(p)
     kbytes = kernel_bytes(p)
+    kalg = kernel_algorithmic_bytes(p)
     kernels = {}
     for name, kms in kernel_ms.items():
         ach = kbytes[name] / (kms * 1e-3) / 1e9
-        kernels[name] = {"ms": kms, "bytes_per_launch": kbytes[name], "achieved": ach, "frac": ach / hbm,
+        ach_alg = kalg[name] / (kms * 1e-3) / 1e9
+        kernels[name] = {"ms": kms, "design_bytes_per_launch": kbytes[name], "design_achieved": ach,
+                         "design_frac": ach / hbm, "algorithmic_bytes_per_launch": kalg[name],
+                         "achieved": ach_alg, "frac": ach_alg / hbm,
                          "traffic": measured_traffic(name, idx if args.T is None else f"{idx}@T{args.T}")}
     dom = max(kernel_ms, key=kernel_ms.get)
-    achieved = kernels[dom]["achieved"]
+    t_hbm = abytes / (hbm * 1e9)
+    t_tc = aflops / (tc * 1e12)
+    path_ach = abytes / (ms_step * 1e-3) / 1e9
+    traffic = [kernels[k]["traffic"] for k in kernels]
     line = {
         "metric": METRIC, "value": aggregate_throughput(p.token_heads(), world, ms_step), "unit": UNIT,
         "n_gpus": world, "steps": args.steps,
@@ -437,14 +463,22 @@ def run_ours(args, p, idx, rank, world):
         "dtype": "bf16", "precision": "bf16 inputs/outputs; tf32 and fp16 tensor-core operands; fp32 accumulation "
                                       "and fp32 state master",
         "data": "synthetic", "config": workload_config(p, idx),
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": kernels[dom]["traffic"],
+        # the whole call against its roofline: algorithmic bytes (q, k, v, g, beta in, out, states,
+        # parameters) over the measured time, against the measured HBM copy bandwidth; the FLOP bound is
+        # the algorithmic FLOPs over the measured bf16 dense peak, and the slower of the two is the bound
+        "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "achieved": path_ach, "peak": hbm,
+                     "unit": "GB/s", "frac": path_ach / hbm,
+                     "traffic": None if any(t is None for t in traffic) else float(sum(traffic)),
+                     "traffic_note": "sum over the step's kernels of ncu dram__bytes_read.sum + "
+                                     "dram__bytes_write.sum per launch (profiles/)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
-                     "kernel_bytes_per_launch": kbytes[dom], "kernels": kernels,
-                     "path": {"algorithmic_bytes_per_launch": abytes, "ms": ms_step,
-                              "achieved": abytes / (ms_step * 1e-3) / 1e9,
-                              "frac": abytes / (ms_step * 1e-3) / 1e9 / hbm,
-                              "roofline_ms": abytes / (hbm * 1e9) * 1e3}},
+                     "algorithmic_bytes_per_step": abytes, "algorithmic_flops_per_step": aflops,
+                     "tensor_peak_tflops": tc, "t_hbm_ms": t_hbm * 1e3, "t_tensor_ms": t_tc * 1e3,
+                     "roofline_ms": max(t_hbm, t_tc) * 1e3,
+                     "dominant_kernel": {"name": dom, "ms": kernel_ms[dom],
+                                         "algorithmic_bytes_per_launch": kalg[dom],
+                                         "achieved": kernels[dom]["achieved"], "frac": kernels[dom]["frac"]},
+                     "kernels": kernels},
         "cpu_baseline": cpu_baseline(p, idx),
         "e2e": {"value": aggregate_throughput(p.token_heads(), world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,

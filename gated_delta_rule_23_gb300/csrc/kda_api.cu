@@ -122,7 +122,29 @@ size_t workspace_bytes(int N, int64_t T, int H, bool varlen)
 {
     if (short_problem(N, T, H, varlen))
         return 0;
-    return header_bytes(N, T, varlen) + (size_t)max_chunks(N, T, varlen) * (size_t)H * SLOT_BYTES;
+    // checked arguments: N >= 1, H >= 1, 0 <= T <= 2^40, so the varlen chunk bound fits; the fixed-length
+    // count and the slot bytes may not fit in 64 bits
+    uint64_t chunks = 0;
+    if (varlen)
+        chunks = (uint64_t)max_chunks(N, T, true);
+    else if (__builtin_mul_overflow((uint64_t)N, ((uint64_t)T + CH - 1) / CH, &chunks))
+        return SIZE_MAX;
+    uint64_t slots = 0, bytes = 0, total = 0;
+    if (__builtin_mul_overflow(chunks, (uint64_t)H, &slots) || __builtin_mul_overflow(slots, (uint64_t)SLOT_BYTES, &bytes) ||
+        __builtin_add_overflow(bytes, (uint64_t)header_bytes(N, T, varlen), &total) || total > (uint64_t)SIZE_MAX)
+        return SIZE_MAX;
+    return (size_t)total;
+}
+
+kda_status_t check_size(int N, int64_t T, int H, bool varlen)
+{
+    if (short_problem(N, T, H, varlen))
+        return KDA_OK;
+    if (workspace_bytes(N, T, H, varlen) == SIZE_MAX)
+        return KDA_ERR_UNSUPPORTED;
+    // one prep CTA per (chunk, head): the grid and the kernels' item arithmetic are 32-bit
+    const uint64_t items = (uint64_t)(varlen ? max_chunks(N, T, true) : (int64_t)N * ((T + CH - 1) / CH)) * (uint64_t)H;
+    return items > (uint64_t)INT32_MAX ? KDA_ERR_UNSUPPORTED : KDA_OK;
 }
 
 namespace {
@@ -301,7 +323,8 @@ using namespace kda;
 
 extern "C" size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen)
 {
-    if (N < 1 || H < 1 || T < 0)
+    if (N < 1 || H < 1 || T < 0 || T > ((int64_t)1 << 40) || (int64_t)N * H > INT32_MAX ||
+        check_size(N, T, H, varlen != 0) != KDA_OK)
         return 0;
     return workspace_bytes(N, T, H, varlen != 0);
 }
@@ -314,6 +337,8 @@ extern "C" kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, 
 {
     kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                                 final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s == KDA_OK)
+        s = check_size(N, T, H, cu_seqlens != nullptr);
     if (s != KDA_OK)
         return s;
     const size_t need = workspace_bytes(N, T, H, cu_seqlens != nullptr);
@@ -332,6 +357,8 @@ extern "C" kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const 
 {
     kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                                 final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s == KDA_OK)
+        s = check_size(N, T, H, cu_seqlens != nullptr);
     if (s != KDA_OK)
         return s;
     const size_t need = workspace_bytes(N, T, H, cu_seqlens != nullptr);
@@ -350,6 +377,8 @@ extern "C" kda_status_t kda_fwd(const void *q, const void *k, const void *v, con
 {
     kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                                 final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s == KDA_OK)
+        s = check_size(N, T, H, cu_seqlens != nullptr);
     if (s != KDA_OK)
         return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -396,6 +425,8 @@ extern "C" kda_status_t kda_fwd_host(const void *q, const void *k, const void *v
 {
     kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                                 final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s == KDA_OK)
+        s = check_size(N, T, H, cu_seqlens != nullptr);
     if (s != KDA_OK)
         return s;
     if (cu_seqlens && kda_check_cu_seqlens(cu_seqlens, N, T) != KDA_OK)

@@ -15,8 +15,11 @@ kda_status_t check_args(const void *q, const void *k, const void *v, const void 
                         const void *out, const float *A_log, const float *dt_bias, float lower_bound,
                         const void *initial_state, const void *final_state, kda_dtype_t state_dtype,
                         const int64_t *cu_seqlens, int N, int64_t T, int H);
-// Workspace bytes of one call (kda_fwd_workspace_size).
+// Workspace bytes of one call (kda_fwd_workspace_size); SIZE_MAX when the count does not fit in 64 bits.
 size_t workspace_bytes(int N, int64_t T, int H, bool varlen);
+// KDA_ERR_UNSUPPORTED when the chunked path cannot take the problem size (workspace size not
+// representable, or more than 2^31 - 1 (chunk, head) items); KDA_OK otherwise.  No CUDA calls.
+kda_status_t check_size(int N, int64_t T, int H, bool varlen);
 // The launch sequence on `stream` with workspace `ws` (checked arguments).
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,

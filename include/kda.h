@@ -150,15 +150,28 @@ kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, co
 #define KDA_NOALLOC_SCRATCH_BYTES 268435456
 
 /*
- * kda_fwd_noalloc -- kda_fwd whose workspace is a fixed device array of
- * KDA_NOALLOC_SCRATCH_BYTES inside the library (one per device, created with the library's
- * module on that device): the call allocates no memory at all.  The FlashKDA pages have no
- * counterpart of this entry point; it exists for callers that must not allocate inside the
- * call (for instance while capturing a CUDA graph without allocation nodes).  Because the
- * array is shared, calls on one device must be ordered (the same stream, or serialised by the
- * caller).  Same arguments, results and errors as kda_fwd, plus KDA_ERR_UNSUPPORTED when
- * kda_fwd_workspace_size(N, T, H, cu_seqlens != NULL) exceeds KDA_NOALLOC_SCRATCH_BYTES
- * (reported before any CUDA call).
+ * kda_fwd_noalloc -- kda_fwd that allocates no memory: its workspace is a fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES in the library's device code (a file-scope __device__ array).  The
+ * FlashKDA pages have no counterpart of this entry point.  It is meant for callers that cannot
+ * allocate device memory while they run the forward pass: a runtime that reserves its whole
+ * memory budget up front and forbids allocator calls afterwards, or code whose latency-critical
+ * path must not enter the CUDA allocator (cudaMalloc, stream-ordered pools) at all.
+ *
+ *   - Every device that loads the library holds its own copy of the array from then until the
+ *     process exits (256 MiB of device memory each, whether or not this entry point is called).
+ *   - The first call on a device that needs a workspace looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; later calls reuse it.  Make
+ *     that first call on each device before capturing any stream.
+ *   - All calls on one device share the array and it keeps the contents of the last call: calls
+ *     whose kernels may overlap on the GPU (different streams without an ordering between them)
+ *     race and give undefined results.  The forward pass writes every part of the array it reads
+ *     before reading it, so nothing has to be cleared between calls.
+ *   - Problems whose workspace (kda_fwd_workspace_size(N, T, H, cu_seqlens != NULL)) exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES (a single 8192-token sequence with 96 heads does) are rejected
+ *     with KDA_ERR_UNSUPPORTED before any CUDA call.  Fixed-length problems of 1 to 4 tokens per
+ *     sequence need no workspace and make no lookup.
+ *
+ * Same arguments, results and other errors as kda_fwd; KDA_ERR_CUDA if the address lookup fails.
  */
 kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, const void *beta,
                              float scale, void *out, const float *A_log, const float *dt_bias,

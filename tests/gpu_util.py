@@ -4,31 +4,13 @@ import numpy as np
 import torch
 
 from gated_delta_rule_23_gb300 import device_status, kda_fwd
-from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, bf16_to_f32
+from gated_delta_rule_23_gb300.device import bf16_tensor, to_device  # noqa: F401
+from gated_delta_rule_23_gb300.inputs import bf16_to_f32
 
 # Parity bar: outputs rel-L2 <= 5e-3 and max-abs <= 3e-2; final states rel-L2 <= 5e-3.
 OUT_REL_L2 = 5e-3
 OUT_MAX_ABS = 3e-2
 STATE_REL_L2 = 5e-3
-
-
-def bf16_tensor(bits, device="cuda"):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
-
-
-def to_device(p, device="cuda"):
-    d = dict(q=bf16_tensor(p.q, device), k=bf16_tensor(p.k, device), v=bf16_tensor(p.v, device),
-             g=bf16_tensor(p.g, device), beta=bf16_tensor(p.beta, device),
-             A_log=torch.from_numpy(p.A_log).to(device), dt_bias=torch.from_numpy(p.dt_bias).to(device))
-    d["cu"] = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(device)
-    sdt = {STATE_BF16: torch.bfloat16, STATE_FP32: torch.float32}.get(p.state_dtype)
-    d["sdt"] = sdt
-    if p.initial_state is not None:
-        d["init"] = (bf16_tensor(p.initial_state, device) if p.state_dtype == STATE_BF16
-                     else torch.from_numpy(p.initial_state).to(device))
-    else:
-        d["init"] = None
-    return d
 
 
 def run_gpu(p, dev=None, inplace=False, recurrent=False):

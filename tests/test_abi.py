@@ -139,3 +139,17 @@ def test_host_entry_rejects_bad_arguments_before_any_cuda_call(lib):
     bad = list(args)
     bad[13], bad[14] = ctypes.cast(cu, ctypes.c_void_p).value, 2
     assert lib.kda_fwd_host(*bad) == KDA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("N,T,H", [(1 << 20, 1 << 40, 1 << 10),   # workspace bytes do not fit in 64 bits
+                                   (1, 1 << 40, 1)])              # more than 2^31 - 1 (chunk, head) items
+def test_oversize_problems_unsupported_before_any_cuda_call(lib, N, T, H):
+    """Sizes that pass the argument checks but whose workspace size or item count the chunked path cannot
+    represent are refused with KDA_ERR_UNSUPPORTED on the host (the pointers are fake)."""
+    assert lib.kda_fwd_workspace_size(N, T, H, 0) == 0
+    assert call(lib, "kda_fwd", N=N, T=T, H=H) == KDA_ERR_UNSUPPORTED
+    assert call(lib, "kda_fwd_noalloc", N=N, T=T, H=H) == KDA_ERR_UNSUPPORTED
+    args = [A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 0.1, A + 0x5000, A + 0x6000, A + 0x7000, -5.0,
+            None, None, KDA_DTYPE_NONE, None, N, T, H]
+    assert lib.kda_fwd_ws(*args, A + 0x100000, 1 << 30, None) == KDA_ERR_UNSUPPORTED
+    assert lib.kda_fwd_host(*args) == KDA_ERR_UNSUPPORTED
