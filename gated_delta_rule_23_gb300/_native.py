@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
 UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_decode", "kda_host", "kda_noalloc"]
 SOURCES = [os.path.join(CSRC, u + ".cu") for u in UNITS]
-HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh"), os.path.join(CSRC, "kda_internal.h")]
+HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh"), os.path.join(CSRC, "kda_internal.h"),
+           os.path.join(CSRC, "kda_plan.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -112,7 +113,7 @@ def declared_functions() -> List[str]:
 
 
 # status codes, as in include/kda.h
-KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(5)
+KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_NONFINITE = range(6)
 KDA_DTYPE_NONE, KDA_DTYPE_BF16, KDA_DTYPE_FP32 = range(3)
 
 

@@ -125,7 +125,8 @@ def workspace_size(N: int, T: int, H: int, varlen: bool) -> int:
 
 
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Synchronise `stream` and raise KDAError if a kernel gave up a bounded device wait."""
+    """Synchronise `stream` and raise KDAError with what the kernels reported since the last call
+    (kda_device_status: a bounded wait that gave up, a malformed device cu_seqlens, a non-finite state)."""
     s = stream if stream is not None else torch.cuda.current_stream()
     rc = _native.load().kda_device_status(s.cuda_stream)
     if rc != KDA_OK:

@@ -7,6 +7,10 @@
 #include "kda.h"
 #include "kda_device.cuh"
 #include "kda_internal.h"
+#include "kda_plan.h"
+
+// Set by the varlen plan kernel when cu_seqlens breaks its contract (read by kda_device_status).
+__device__ unsigned int g_kda_plan_error;
 
 namespace kda {
 namespace {
@@ -19,19 +23,28 @@ constexpr int LPT_MAX_SEQS = 2048;   // longest-first ordering of varlen sequenc
 // for the launched chunk indices past it (c < n_info), so that a prep CTA finds its chunk, or that it
 // has none, with one load; and, when order != nullptr, order[rank] =
 // sequence with that rank by length (longest first, ties by index), so that the recurrence CTAs
-// that start first take the longest sequences.
-__global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *cu, int N, int64_t *chunk_off,
-                                                              longlong2 *chunk_info, int64_t n_info, int *order)
+// that start first take the longest sequences.  Sequences are the clamped ranges of seq_range and
+// the table writes stop at n_info, so a malformed cu_seqlens cannot move an access out of its buffer;
+// it sets DEVERR_CU_SEQLENS instead.
+__global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *cu, int N, int64_t T,
+                                                              int64_t *chunk_off, longlong2 *chunk_info,
+                                                              int64_t n_info, int *order)
 {
     __shared__ int64_t wsum[PLAN_THREADS / 32];
     __shared__ int64_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    bool bad = false;
     if (tid == 0)
         carry = 0;
     __syncthreads();
     for (int base = 0; base < N; base += PLAN_THREADS) {
         const int n = base + tid;
-        const int64_t cnt = n < N ? (cu[n + 1] - cu[n] + CH - 1) / CH : 0;
+        int64_t cnt = 0;
+        if (n < N) {
+            int64_t bos, len;
+            bad |= seq_range(cu, n, N, T, bos, len);
+            cnt = seq_chunks(len);
+        }
         int64_t x = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -64,31 +77,32 @@ __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *c
     if (tid == 0)
         chunk_off[N] = carry;
     __syncthreads();   // chunk_off is complete (global writes of this CTA, ordered by the barrier)
-    for (int64_t c = tid; c < carry; c += PLAN_THREADS) {
-        int lo = 0, hi = N - 1;   // the last sequence whose first chunk is <= c
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (chunk_off[mid] <= c)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const int64_t tok0 = cu[lo] + (c - chunk_off[lo]) * CH;
-        chunk_info[c] = make_longlong2(tok0, cu[lo + 1] - tok0);
+    const int64_t used = carry < n_info ? carry : n_info;   // carry > n_info only for a malformed cu_seqlens
+    bad |= tid == 0 && carry > n_info;
+    for (int64_t c = tid; c < used; c += PLAN_THREADS) {
+        const int s = owner_of_chunk(chunk_off, N, c);
+        int64_t bos, len;
+        seq_range(cu, s, N, T, bos, len);
+        const int64_t tok0 = bos + (c - chunk_off[s]) * CH;
+        chunk_info[c] = make_longlong2(tok0, bos + len - tok0);
     }
-    for (int64_t c = carry + tid; c < n_info; c += PLAN_THREADS)
+    for (int64_t c = used + tid; c < n_info; c += PLAN_THREADS)
         chunk_info[c] = make_longlong2(0, 0);
     if (order) {
         for (int s = tid; s < N; s += PLAN_THREADS) {
-            const int64_t ls = cu[s + 1] - cu[s];
+            int64_t bs, ls;
+            seq_range(cu, s, N, T, bs, ls);
             int rank = 0;
             for (int m = 0; m < N; ++m) {
-                const int64_t lm = cu[m + 1] - cu[m];
+                int64_t bm, lm;
+                seq_range(cu, m, N, T, bm, lm);
                 rank += (lm > ls) || (lm == ls && m < s);
             }
             order[rank] = s;
         }
     }
+    if (__syncthreads_or(bad) && tid == 0)
+        atomicOr(&g_kda_plan_error, DEVERR_CU_SEQLENS);
 }
 
 bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
@@ -98,7 +112,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t max_chunks(int N, int64_t T, bool varlen)
 {
     // varlen: sum_n ceil(len_n / 64) <= (T + 63 N) / 64
-    return varlen ? (T + (int64_t)(CH - 1) * N) / CH : (int64_t)N * ((T + CH - 1) / CH);
+    return varlen ? varlen_chunk_capacity(N, T) : (int64_t)N * ((T + CH - 1) / CH);
 }
 
 // workspace (varlen only: the plan): [chunk_off: (N + 1) int64][order: N int32][chunk_info: max_chunks
@@ -257,6 +271,7 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.order = nullptr;
     p.slots = nullptr;
     p.prep_pf = 0;
+    p.chunk_cap = cu_seqlens ? varlen_chunk_capacity(N, T) : 0;
     return p;
 }
 
@@ -296,8 +311,8 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
         int64_t *chunk_off = reinterpret_cast<int64_t *>(ws);
         int *order = N > 1 && N <= LPT_MAX_SEQS ? reinterpret_cast<int *>(ws + (size_t)(N + 1) * 8) : nullptr;
         longlong2 *chunk_info = reinterpret_cast<longlong2 *>(ws + info_offset(N));
-        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, chunk_off, chunk_info, max_chunks(N, T, true),
-                                                        order);
+        kda_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu_seqlens, N, T, chunk_off, chunk_info,
+                                                        max_chunks(N, T, true), order);
         err = cudaGetLastError();
         p.chunk_off = chunk_off;
         p.chunk_info = chunk_info;
@@ -462,6 +477,7 @@ extern "C" const char *kda_status_string(kda_status_t s)
     case KDA_ERR_UNSUPPORTED: return "unsupported argument value";
     case KDA_ERR_CUDA: return "CUDA error";
     case KDA_ERR_TIMEOUT: return "device wait timed out";
+    case KDA_ERR_NONFINITE: return "non-finite state (fp16 operand range exceeded or inf/NaN input)";
     }
     return "unknown status";
 }
@@ -476,9 +492,23 @@ extern "C" kda_status_t kda_device_status(kda_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return KDA_ERR_CUDA;
-    unsigned int flag = 0, flag2 = 0, flag3 = 0, flag4 = 0;
+    unsigned int flag = 0, flag2 = 0, flag3 = 0, flag4 = 0, flag5 = 0;
     if (read_and_clear_device_error(&flag) != cudaSuccess || prep_read_and_clear_error(&flag2) != cudaSuccess ||
         recurrent_read_and_clear_error(&flag3) != cudaSuccess || decode_read_and_clear_error(&flag4) != cudaSuccess)
         return KDA_ERR_CUDA;
-    return (flag | flag2 | flag3 | flag4) ? KDA_ERR_TIMEOUT : KDA_OK;
+    if (cudaMemcpyFromSymbol(&flag5, g_kda_plan_error, sizeof flag5) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (flag5) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_kda_plan_error, &zero, sizeof zero) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    const unsigned int bits = flag | flag2 | flag3 | flag4 | flag5;
+    if (bits & DEVERR_TIMEOUT)
+        return KDA_ERR_TIMEOUT;
+    if (bits & DEVERR_CU_SEQLENS)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (bits & DEVERR_NONFINITE)
+        return KDA_ERR_NONFINITE;
+    return KDA_OK;
 }

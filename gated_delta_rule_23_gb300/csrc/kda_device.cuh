@@ -9,6 +9,8 @@
 
 #include <cstdint>
 
+#include "kda_plan.h"
+
 namespace kda {
 
 constexpr int D = 128;                     // K = V = 128
@@ -17,6 +19,10 @@ constexpr int SB = 16;                     // tokens per decay sub-block
 constexpr int NSB = CH / SB;               // sub-blocks per chunk
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t WAIT_LIMIT = 1u << 24;  // mbarrier polls before a wait is declared hung
+// Bits of the kernels' device-side error words (read and cleared by kda_device_status).
+constexpr unsigned int DEVERR_TIMEOUT = 1u;     // a bounded wait gave up; the call's results are not valid
+constexpr unsigned int DEVERR_NONFINITE = 2u;   // a state ended non-finite (fp16 operand overflow or inf/NaN inputs)
+constexpr unsigned int DEVERR_CU_SEQLENS = 4u;  // cu_seqlens broke its contract; it was clamped into range
 
 // ---------------------------------------------------------------- per-chunk operand slot
 // The prep kernel writes, for every (chunk, head), one slot of fp16 operands in exactly the
@@ -66,6 +72,7 @@ struct Problem {
     int64_t T;
     int64_t nch_fixed;        // chunks per sequence without cu_seqlens
     int prep_pf;              // prep: a CTA prefetches into L2 the rows of item blockIdx.x + prep_pf (0: off)
+    int64_t chunk_cap;        // varlen: entries of the per-chunk table (every sequence's chunks are clamped to it)
 };
 
 // ---------------------------------------------------------------- small helpers

@@ -18,7 +18,8 @@
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
-// Set when a bounded wait on the tensor cores or a bulk copy expires (read by kda_device_status).
+// Error bits of the recurrence kernel (DEVERR_*: a bounded wait expired, a non-finite final state),
+// read and cleared by kda_device_status.
 __device__ unsigned int g_kda_device_error;
 
 namespace kda {
@@ -114,9 +115,11 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         n = p.order[n];   // longest sequences first
     int64_t bos, len, slot0;
     if (VARLEN) {
-        bos = p.cu[n];
-        len = p.cu[n + 1] - bos;
+        seq_range(p.cu, n, p.N, p.T, bos, len);   // clamped into [0, T]; the plan flags a malformed cu_seqlens
         slot0 = p.chunk_off[n];
+        const int64_t usable = usable_chunks(slot0, seq_chunks(len), p.chunk_cap);
+        if (usable * CH < len)
+            len = usable * CH;   // only a malformed cu_seqlens gets here: chunks past the table are skipped
     } else {
         bos = (int64_t)n * p.T;
         len = p.T;
@@ -387,21 +390,27 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                     issue_tail(k);   // completes the phase the head's expect_tx opened
                 mbar_wait(mbarL + 8 * (k % NBUF), (k / NBUF) & 1);
             }
-            atomicOr(&g_kda_device_error, 1u);
+            atomicOr(&g_kda_device_error, DEVERR_TIMEOUT);
         }
-    } else if (STATE != 0 && p.fin) {
+    } else {
+        // the final state (stored if requested) and a finiteness check of it: an fp16 tensor-core operand
+        // that overflowed (or an inf / NaN input) leaves the fp32 state non-finite from that chunk on
         tc_fence_after();
+        bool bad = false;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             uint32_t u[32];
             tmem_ld32(trow + TM_S + half * 64 + 32 * part, u);
-            if (STATE == 2) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                bad |= !(fabsf(__uint_as_float(u[e])) <= 3.402823466e38f);
+            if (STATE == 2 && p.fin) {
                 float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.fin) + srow + 32 * part);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
                                          __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
-            } else {
+            } else if (STATE == 1 && p.fin) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.fin) + srow + 32 * part);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -416,6 +425,8 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                 }
             }
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0)
+            atomicOr(&g_kda_device_error, DEVERR_NONFINITE);
     }
     tc_fence_before();
     __syncthreads();

@@ -137,9 +137,12 @@ __global__ void __launch_bounds__(RC_THREADS, 2) kda_recurrent_kernel(const Prob
 
     auto seq_of = [&](int k, long long &bos, int &len) {
         const ItemId id = item_id(k, H);
-        if (VARLEN) {
-            bos = p.cu[id.n];
-            len = (int)(p.cu[id.n + 1] - bos);
+        if (VARLEN) {   // clamped into [0, T] (the entry point keeps T below 2^31)
+            int64_t b, l;
+            if (seq_range(p.cu, id.n, p.N, p.T, b, l) && tid == 0)
+                atomicOr(&g_kda_rc_error, DEVERR_CU_SEQLENS);
+            bos = b;
+            len = (int)l;
         } else {
             bos = (long long)id.n * p.T;
             len = (int)p.T;

@@ -45,7 +45,10 @@
  * magnitude except T' V and T' (K^ . Gamma), which are delta-rule residuals of the
  * inputs).  A recurrence kernel then runs the chunk-to-chunk state update on the tensor
  * cores with fp16 operands and fp32 accumulation; the state itself stays fp32 for the
- * whole call.  States and outputs therefore need |values| well below 6.5e4.
+ * whole call.  The fp16 operands (the state's copy, T' V and the corrected values U) bound
+ * the magnitudes: states and values must stay well below the fp16 limit of 6.5e4.  Tested
+ * with v scaled by 256 (|v| up to ~1.3e3) and fp32 initial states ~N(0, 300); past the limit
+ * the state turns inf / NaN and kda_device_status reports KDA_ERR_NONFINITE.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -70,7 +73,8 @@ typedef enum {
     KDA_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, bad size, misaligned pointer, bad dtype/state combination */
     KDA_ERR_UNSUPPORTED = 2,      /* lower_bound outside [-5, 0], scale not finite, or a size limit of the entry point */
     KDA_ERR_CUDA = 3,             /* a CUDA runtime call or the kernel launch failed */
-    KDA_ERR_TIMEOUT = 4           /* a bounded device wait expired (reported by kda_device_status) */
+    KDA_ERR_TIMEOUT = 4,          /* a bounded device wait expired (reported by kda_device_status) */
+    KDA_ERR_NONFINITE = 5         /* a final state came out inf / NaN (reported by kda_device_status) */
 } kda_status_t;
 
 /*
@@ -237,10 +241,18 @@ kda_status_t kda_check_cu_seqlens(const int64_t *host_cu_seqlens, int N, int64_t
 const char *kda_status_string(kda_status_t status);
 
 /*
- * Waits for `stream`, then reports whether any kernel of this library on this device
- * (kda_fwd and its variants, kda_fwd_recurrent) gave up a bounded wait on the tensor
- * cores or on a bulk copy since the last call (KDA_ERR_TIMEOUT; the outputs of that call
- * are not valid), and clears the report.  KDA_ERR_CUDA if the stream or the query failed.
+ * Waits for `stream`, then reports what the kernels of this library on this device (kda_fwd and
+ * its variants, kda_fwd_recurrent) recorded since the last call, and clears it:
+ *   KDA_ERR_TIMEOUT           a kernel gave up a bounded wait on the tensor cores or a bulk copy;
+ *                             the outputs of that call are not valid;
+ *   KDA_ERR_INVALID_ARGUMENT  a device-resident cu_seqlens broke its contract (cu[0] != 0,
+ *                             cu[N] != T or a decreasing entry); the kernels clamped every
+ *                             sequence into [0, T] and the chunk table into the workspace, so no
+ *                             access left the buffers, but the outputs are not valid;
+ *   KDA_ERR_NONFINITE         the chunked path ended a (sequence, head) with a non-finite state:
+ *                             an inf / NaN input, or a value beyond the fp16 range of its
+ *                             tensor-core operands (see Numerics above);
+ * in that order of precedence, else KDA_OK.  KDA_ERR_CUDA if the stream or the query failed.
  * The kernels never spin without a limit and never trap.
  */
 kda_status_t kda_device_status(kda_stream_t stream);

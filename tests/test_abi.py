@@ -29,8 +29,8 @@ def test_smem_fits_one_cta_per_sm(lib):
 
 
 def test_status_strings(lib):
-    for s in range(5):
-        assert lib.kda_status_string(s)
+    for s in range(6):
+        assert lib.kda_status_string(s) and lib.kda_status_string(s) != b"unknown status"
     assert lib.kda_status_string(99) == b"unknown status"
 
 

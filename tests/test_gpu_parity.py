@@ -251,3 +251,43 @@ def test_short_fixed_length_takes_the_token_recurrent_kernels(T, state):
     assert np.array_equal(a[0], b[0])
     assert (a[1] is None and b[1] is None) or np.array_equal(a[1], b[1])
     assert_parity(*a, *oracle_run(p))
+
+
+def _scaled(p, v_scale, state_std, seed):
+    """Problem p with v multiplied by a power of two (exact in bf16) and fp32 initial states ~N(0, state_std)."""
+    from gated_delta_rule_23_gb300.inputs import bf16_to_f32
+    rng = np.random.default_rng(seed)
+    v = bf16_bits(bf16_to_f32(p.v) * np.float32(v_scale))
+    init = (rng.standard_normal(size=(p.N, p.H, 128, 128), dtype=np.float32) * np.float32(state_std))
+    return dataclasses.replace(p, v=v, initial_state=init.astype(np.float32), state_dtype=STATE_FP32,
+                               want_final=True)
+
+
+@pytest.mark.parametrize("lb", [-5.0, -0.05])
+def test_large_values_within_fp16_operand_range(lb):
+    """Magnitudes that bf16 inputs allow and that approach the fp16 range of the tensor-core operands:
+    v scaled by 256 (|v| up to ~1.3e3) and fp32 initial states ~N(0, 300), at strong and at slow decay."""
+    from tests.gpu_util import OUT_REL_L2, STATE_REL_L2, parity_report
+    p = _scaled(make_problem(B=1, T=333, H=4, seed=61, lower_bound=lb), 256.0, 300.0, 62)
+    out, fin = run_gpu(p)   # raises if kda_device_status reports anything
+    o_ref, f_ref = oracle_run(p)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(fin))
+    # the relative bars (the absolute max-abs bar is for unit-scale inputs; these outputs are ~1e3 larger)
+    r = parity_report(out, fin, o_ref, f_ref)
+    assert r["out_rel_l2"] <= OUT_REL_L2 and r["state_rel_l2"] <= STATE_REL_L2, r
+
+
+def test_values_beyond_fp16_operand_range_are_reported():
+    """v scaled by 2^17 (|v| up to ~6e5) overflows the fp16 operands: the state turns non-finite and
+    kda_device_status reports KDA_ERR_NONFINITE once (the report is cleared by reading it)."""
+    from gated_delta_rule_23_gb300 import KDAError, device_status
+    from gated_delta_rule_23_gb300._native import KDA_ERR_NONFINITE
+    p = _scaled(make_problem(B=1, T=200, H=2, seed=63), 2.0 ** 17, 0.1, 64)
+    dev = to_device(p)
+    out = torch.empty_like(dev["q"])
+    kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+            p.lower_bound, initial_state=dev["init"], final_state=None)
+    with pytest.raises(KDAError) as e:
+        device_status()
+    assert e.value.status == KDA_ERR_NONFINITE
+    device_status()   # cleared
