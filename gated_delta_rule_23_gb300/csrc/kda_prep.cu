@@ -46,18 +46,19 @@ constexpr int PREP_PF_QUARTER_WAVES = KDA_PREP_PF_QUARTER_WAVES;
 constexpr int TMEM_COLS = 128;          // Akk / Aqk accumulators: 128 lanes x 96 columns
 // tf32 operand tiles of the Akk / Aqk product for one half of the channels (the gate pass runs in
 // two passes of 64 channels; the tensor cores accumulate both).  No-swizzle K-major core-matrix
-// layout, element (row r, compact channel kk) at (r / 8) * OPS_SBO + (kk / 4) * OPS_LBO
-// + (r % 8) * 16 + (kk % 4) * 4; the padded strides make the gate pass's 16-byte stores
-// conflict-light.  Rows of A: [k^ L_0 (tokens 0..31) ; q^ L_0 ; k^ L_1 (tokens 32..63) ; q^ L_1];
-// rows of B: [k^ R_0 (tokens 0..31) ; k^ R_1 (tokens 0..63)].
-constexpr int OPS_LBO = 160, OPS_SBO = 2576;
+// layout, element (row r, pass channel kk) at (r / 8) * OPS_SBO + (kk / 4) * OPS_LBO
+// + (r % 8) * 16 + (kk % 4) * 4.  The strides (LBO = 16 mod 128, SBO = 32 mod 128) make the gate
+// pass's 8-byte stores (8 row groups x 4 channel pairs per warp) conflict-free.  Rows of A:
+// [k^ L_0 (tokens 0..31) ; q^ L_0 ; k^ L_1 (tokens 32..63) ; q^ L_1]; rows of B: [k^ R_0 (tokens 0..31) ;
+// k^ R_1 (tokens 0..63)].
+constexpr int OPS_LBO = 144, OPS_SBO = 2336;
 constexpr int OPS_A = 0;
-constexpr int OPS_B = 16 * OPS_SBO;                 // 41216
-constexpr int OPS_BYTES = OPS_B + 12 * OPS_SBO;     // 72128
+constexpr int OPS_B = 16 * OPS_SBO;                 // 37376
+constexpr int OPS_BYTES = OPS_B + 12 * OPS_SBO;     // 65408
 // shared memory map (bytes)
 constexpr int OFF_OPS = 0;
 constexpr int OFF_PART = OFF_OPS;                   // fp32 [8 warps][2][64] sums of squares (before the gate pass)
-// q, k, g of the chunk as loaded (bf16 [64 t][128 c] each, 16-byte chunks XOR-swizzled by t / 4), read into
+// q, k, g of the chunk as loaded (bf16 [64 t][128 c] each, 16-byte chunks XOR-swizzled by t / 8), read into
 // registers before the gate pass overwrites the region
 constexpr int OFF_STG = OFF_PART + 8 * 2 * CH * 4;   // 4096
 static_assert(OFF_STG + 3 * CH * D * 2 <= OPS_BYTES, "staging inside the operand tiles");
@@ -72,28 +73,27 @@ static_assert(OFF_AQS + 64 * CH * 2 <= OPS_BYTES, "post-product overlay");
 // after T' is formed, the W and U0^T parts of the slot are staged over Akk / Tm for bulk copies
 constexpr int OFF_WS = OFF_AKK, OFF_US = OFF_AKK + 64 * D * 2;
 static_assert(OFF_US + D * CH * 2 <= OFF_TP, "W / U0 staging overlaps T'");
-constexpr int OFF_KG = 72192;                       // fp16 [64 j][128 c] K^ . Gamma (kg_off swizzle)
+constexpr int OFF_KG = 65536;                       // fp16 [64 j][128 c] K^ . Gamma (kg_off swizzle)
 constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizzled)
-constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 [64] 1 / |q|
-constexpr int OFF_RK = OFF_RQ + 256;                // fp32 [64] 1 / |k|
-constexpr int OFF_BT = OFF_RK + 256;                // fp32 [64] b = sigmoid(beta), 0 past the end
+constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 pairs [64][2] 1 / |q| (both halves)
+constexpr int OFF_RK = OFF_RQ + 512;                // fp32 pairs [64][2] 1 / |k|
+constexpr int OFF_BT = OFF_RK + 512;                // fp32 [64] b = sigmoid(beta), 0 past the end
 constexpr int OFF_MISC = OFF_BT + 256;              // mbarrier, tensor-memory base
 constexpr int PREP_SMEM = OFF_MISC + 16;
 static_assert(OFF_KG >= OPS_BYTES && OFF_KG % 128 == 0, "shared memory map");
 static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two CTAs per SM");
 
-__host__ __device__ constexpr int ops_off(int r, int kgrp) { return (r >> 3) * OPS_SBO + kgrp * OPS_LBO + ((r & 7) << 4); }
 // byte offset of a 16-bit element in a [64][128] / [64][64] tile; 16-byte chunks XOR-swizzled
 // by row (conflict-free ldmatrix)
 __device__ __forceinline__ int h128(int r, int c) { return r * 256 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
 __device__ __forceinline__ int h64(int r, int c) { return r * 128 + ((((c >> 3) ^ (r & 7))) << 4) + ((c & 7) << 1); }
-// byte offset of 16-byte chunk c16 of token row t in the q / k / g staging tiles: swizzled by t / 4, so
-// that the 8 runs a quarter-warp reads (rows 4 run + r) fall on 8 different bank groups
-__device__ __forceinline__ int stg_off(int t, int c16) { return t * 256 + ((c16 ^ ((t >> 2) & 7)) << 4); }
+// byte offset of 16-byte chunk c16 of token row t in the q / k / g staging tiles: swizzled by t / 8, so
+// that the 8 token runs a warp reads at once (rows 8 m + j) fall on 8 different bank groups
+__device__ __forceinline__ int stg_off(int t, int c16) { return t * 256 + ((c16 ^ ((t >> 3) & 7)) << 4); }
 // byte offset of element (token t, channel c) in the K^.Gamma tile: 16-byte chunks XOR-swizzled by t % 8 and
-// (t / 8) % 4, so that both the gate pass's stores (tokens 4 m + r of one channel group: two wavefronts per
-// half-warp) and ldmatrix (8 consecutive tokens) spread over the banks
-__device__ __forceinline__ int kg_off(int t, int c) { return t * 256 + ((((c >> 3) ^ (t & 7) ^ ((t >> 3) & 3))) << 4) + ((c & 7) << 1); }
+// t / 8, so that both the gate pass's stores (tokens 8 m + j of one channel group) and ldmatrix (8
+// consecutive tokens) spread over the banks
+__device__ __forceinline__ int kg_off(int t, int c) { return t * 256 + ((((c >> 3) ^ (t & 7) ^ ((t >> 3) & 7))) << 4) + ((c & 7) << 1); }
 
 __device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
                                              uint32_t a5, uint32_t a6, uint32_t a7)
@@ -104,6 +104,22 @@ __device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a0, uint32_t a1
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b)
+{
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b)
+{
+    f2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 f2_ex2(f2 a) { return f2_pack(ex2_approx(f2_lo(a)), ex2_approx(f2_hi(a))); }
+__device__ __forceinline__ uint2 u2_tf32r(f2 a) { return make_uint2(__float_as_uint(tf32r(f2_lo(a))), __float_as_uint(tf32r(f2_hi(a)))); }
+__device__ __forceinline__ uint32_t half2_of(f2 a) { return pack_half2(f2_lo(a), f2_hi(a)); }
 
 // first token and tokens left of chunk gc (a global chunk index over all sequences; the launch keeps
 // every item index, and so gc, below 2^31, so the divisions are 32-bit); varlen chunks come from the
@@ -159,14 +175,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                    base + ((size_t)(tok0 + (valid ? t : 0)) * H + h) * D + c16 * 8, valid);
     }
     cp_async_commit();
-    // lane roles: channel group cgrp (8 channels), run (4 consecutive tokens); sub-block = run / 4
-    const int cgrp = lane >> 4, run = lane & 15, sblk = run >> 2, s4 = run & 3;
-    const int c0 = warp * 16 + cgrp * 8;
-    const int kgrp = warp * 2 + cgrp;   // this thread's 4-channel group in each pass's compact K
+    // lane roles in the gate pass: sub-block sb (16 tokens), run half hh (8 tokens of it), channel pair cpl of
+    // the warp's 8 channels in each pass; the thread's tokens are t0 .. t0 + 7
+    const int sb = lane >> 3, hh = (lane >> 2) & 1, cpl = lane & 3;
+    const int t0 = 16 * sb + 8 * hh;
     const __nv_bfloat16 bval = tid < L ? p.beta[(tok0 + (tid < L ? tid : 0)) * H + h] : __float2bfloat16(0.f);
     const float alog = p.A_log[h];
-    const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0);
-    const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + (size_t)h * D + c0 + 4);
+    const float2 dtb0 = *reinterpret_cast<const float2 *>(p.dt_bias + (size_t)h * D + 8 * warp + 2 * cpl);
+    const float2 dtb1 = *reinterpret_cast<const float2 *>(p.dt_bias + (size_t)h * D + 64 + 8 * warp + 2 * cpl);
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
@@ -207,38 +223,41 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     if (tid < CH)
         bt[tid] = tid < L ? sigmoid_fast(__bfloat162float(bval)) : 0.f;
     const float eA = expf(alog);
-    const float dtb[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
     cp_async_wait_all();
     __syncthreads();
-    // this thread's 4 tokens x 8 channels of q, k, g
-    uint4 qv[4], kv[4], gv[4];
+    // this thread's q, k, g words: tokens t0 + j, channels 64 ps + 8 warp + 2 cpl + {0, 1} (bf16 pairs)
+    uint32_t qw[2][8], kw[2][8], gw[2][8];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int o = OFF_STG + stg_off(4 * run + r, 2 * warp + cgrp);
-        qv[r] = *reinterpret_cast<const uint4 *>(sm + o);
-        kv[r] = *reinterpret_cast<const uint4 *>(sm + o + CH * D * 2);
-        gv[r] = *reinterpret_cast<const uint4 *>(sm + o + 2 * CH * D * 2);
-    }
+    for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int o = OFF_STG + stg_off(t0 + j, 8 * ps + warp) + 4 * cpl;
+            qw[ps][j] = *reinterpret_cast<const uint32_t *>(sm + o);
+            kw[ps][j] = *reinterpret_cast<const uint32_t *>(sm + o + CH * D * 2);
+            gw[ps][j] = *reinterpret_cast<const uint32_t *>(sm + o + 2 * CH * D * 2);
+        }
 
-    // -------- phase 1: row norms of q and k
+    // -------- phase 1: row norms of q and k (partial sums over the thread's 4 channels, then over the
+    //          warp's 4 channel pairs by shuffles, then over the 8 warps in shared memory)
     {
-        float *part = reinterpret_cast<float *>(sm + OFF_PART);
+        float *part = reinterpret_cast<float *>(sm + OFF_PART);   // below the staging tiles
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const uint32_t qw[4] = {qv[r].x, qv[r].y, qv[r].z, qv[r].w};
-            const uint32_t kw[4] = {kv[r].x, kv[r].y, kv[r].z, kv[r].w};
+        for (int j = 0; j < 8; ++j) {
             float sq = 0.f, sk = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float q0 = bf16_lo(qw[e]), q1 = bf16_hi(qw[e]), k0 = bf16_lo(kw[e]), k1 = bf16_hi(kw[e]);
+            for (int ps = 0; ps < 2; ++ps) {
+                const float q0 = bf16_lo(qw[ps][j]), q1 = bf16_hi(qw[ps][j]);
+                const float k0 = bf16_lo(kw[ps][j]), k1 = bf16_hi(kw[ps][j]);
                 sq = fmaf(q0, q0, fmaf(q1, q1, sq));
                 sk = fmaf(k0, k0, fmaf(k1, k1, sk));
             }
-            sq += __shfl_xor_sync(0xffffffffu, sq, 16);
-            sk += __shfl_xor_sync(0xffffffffu, sk, 16);
-            if (cgrp == 0) {
-                part[(warp * 2) * CH + 4 * run + r] = sq;
-                part[(warp * 2 + 1) * CH + 4 * run + r] = sk;
+            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+            if (cpl == 0) {
+                part[(warp * 2) * CH + t0 + j] = sq;
+                part[(warp * 2 + 1) * CH + t0 + j] = sk;
             }
         }
         __syncthreads();
@@ -248,7 +267,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
 #pragma unroll
             for (int w = 0; w < 8; ++w)
                 s += part[(w * 2 + which) * CH + t];
-            (which ? rk : rq)[t] = rsqrtf(s + 1e-6f);
+            const float r = rsqrtf(s + 1e-6f);
+            reinterpret_cast<float2 *>(which ? rk : rq)[t] = make_float2(r, r);
         }
         __syncthreads();
     }
@@ -256,173 +276,144 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     const uint32_t tbase = *tslot;
     const uint32_t s_ops = smem_u32(sm + OFF_OPS);
 
-    // -------- phase 2: gate, decay factors and every per-token operand (two passes of 4 channels;
-    //          each pass fills one half of the channels of the Akk / Aqk operands, then the tensor
-    //          cores accumulate that half)
+    // -------- phase 2: gate, decay factors and every per-token operand, in two passes of 64 channels; each
+    //          pass fills the Akk / Aqk operand tiles for its channels, then the tensor cores accumulate them.
+    //          Per channel the thread walks its 8 tokens in order: the log2-decay a = lb log2(e) sigmoid(.)
+    //          is summed serially (G, inclusive, from the start of the run), then shuffles give the run and
+    //          sub-block offsets.  Every factor below is an exponential of a difference of these sums.
     {
-        float rqt[4], rkt[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            rqt[r] = rq[4 * run + r];
-            rkt[r] = rk[4 * run + r];
-        }
-        // gate constants: sigmoid(eA (g + dt)) = 1 / (1 + 2^(g gz + gd))
+        // sigmoid(eA (g + dt)) = 1 / (1 + 2^(g gz + gz dt))
         const float gz = -eA * LOG2E;
-        float gd[8];
+        const f2 gz2 = f2_pack(gz, gz), lb2 = f2_pack(p.lb_log2e, p.lb_log2e);
+        // 1 / |q_t|, 1 / |k_t| of the thread's tokens, stored twice over (as the pair multiplier)
+        const f2 *rq2 = reinterpret_cast<const f2 *>(rq) + t0, *rk2 = reinterpret_cast<const f2 *>(rk) + t0;
+        const bool first_half = sb < 2, anchor_sb = (sb & 1) == 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            gd[i] = gz * dtb[i];
-        uint32_t qkeep[4][2];   // Q~ of the first pass (4 tokens x 4 channels, fp16 pairs)
+        for (int ps = 0; ps < 2; ++ps) {
+            const int c0 = 64 * ps + 8 * warp + 2 * cpl;     // this thread's channels c0, c0 + 1
+            const int kk = 8 * warp + 2 * cpl;               // their index in the pass's operand tiles
+            const float2 dtb = ps ? dtb1 : dtb0;
+            const f2 gd2 = f2_pack(gz * dtb.x, gz * dtb.y);
+            // log2-decay per token, summed along the run (past the end of a partial chunk: no decay)
+            f2 G[8];
+            f2 acc = f2_pack(0.f, 0.f);
+            if (L == CH) {
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-            // alpha and its inclusive prefix pf inside the 4-token run
-            float pf[4][4];
+                for (int j = 0; j < 8; ++j) {
+                    const f2 e = f2_add(f2_ex2(f2_fma(f2_bf16x2(gw[ps][j]), gz2, gd2)), f2_pack(1.f, 1.f));
+                    acc = f2_add(acc, f2_mul(f2_pack(rcp_approx(f2_lo(e)), rcp_approx(f2_hi(e))), lb2));
+                    G[j] = acc;
+                }
+            } else {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t gw[2] = {hc ? gv[r].z : gv[r].x, hc ? gv[r].w : gv[r].y};
-                const bool valid = 4 * run + r < L;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float gval = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-                    // sigmoid(eA (g + dt)) = 1 / (1 + 2^(g gz + gd))
-                    const float sig = rcp_approx(1.f + ex2_approx(fmaf(gval, gz, gd[4 * hc + i])));
-                    const float a = valid ? ex2_approx(p.lb_log2e * sig) : 1.f;   // alpha (no decay past the end)
-                    pf[r][i] = r == 0 ? a : pf[r - 1][i] * a;
+                for (int j = 0; j < 8; ++j) {
+                    const f2 e = f2_add(f2_ex2(f2_fma(f2_bf16x2(gw[ps][j]), gz2, gd2)), f2_pack(1.f, 1.f));
+                    const f2 a = f2_mul(f2_pack(rcp_approx(f2_lo(e)), rcp_approx(f2_hi(e))), lb2);
+                    if (t0 + j < L)
+                        acc = f2_add(acc, a);
+                    G[j] = acc;
                 }
             }
-            // per channel: pf *= X (the earlier runs of the sub-block) so that pf = P; Dv = D_b, the
-            // sub-block product; pre / post over the earlier / later sub-blocks; f1, the extra right
-            // factor of the second anchor.  The exclusive suffix is E = D_b / P.
-            float Dv[4], iD[4], pre[4], post[4], gcv[4], f1[4];
+            // the second run of each sub-block adds the first run's total; Tot = the sub-block's total
+            const f2 prev = f2_pack(__shfl_xor_sync(0xffffffffu, f2_lo(acc), 4), __shfl_xor_sync(0xffffffffu, f2_hi(acc), 4));
+            const f2 tot = hh ? f2_add(prev, acc) : f2_add(acc, prev);   // the same sum, in the same order, in both lanes
+            if (hh) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float Rt = pf[3][i];   // product over the run
-                // runs of one sub-block: lanes differing in bits 0..1
-                float inc = Rt, t1;
-                t1 = __shfl_up_sync(0xffffffffu, inc, 1, 4);
-                if (s4 >= 1) inc *= t1;
-                t1 = __shfl_up_sync(0xffffffffu, inc, 2, 4);
-                if (s4 >= 2) inc *= t1;
-                float X = __shfl_up_sync(0xffffffffu, inc, 1, 4);
-                if (s4 == 0) X = 1.f;
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    pf[r][i] *= X;
-                const float Db = __shfl_sync(0xffffffffu, inc, (lane & ~3) | 3);
-                Dv[i] = Db;
-                iD[i] = rcp_approx(Db);
-                // sub-blocks: lanes differing in bits 2..3
-                float inc2 = Db, sinc2 = Db;
-                t1 = __shfl_up_sync(0xffffffffu, inc2, 4, 16);
-                if (sblk >= 1) inc2 *= t1;
-                t1 = __shfl_up_sync(0xffffffffu, inc2, 8, 16);
-                if (sblk >= 2) inc2 *= t1;
-                t1 = __shfl_down_sync(0xffffffffu, sinc2, 4, 16);
-                if (sblk <= 2) sinc2 *= t1;
-                t1 = __shfl_down_sync(0xffffffffu, sinc2, 8, 16);
-                if (sblk <= 1) sinc2 *= t1;
-                pre[i] = __shfl_up_sync(0xffffffffu, inc2, 4, 16);
-                if (sblk == 0) pre[i] = 1.f;
-                post[i] = __shfl_down_sync(0xffffffffu, sinc2, 4, 16);
-                if (sblk == 3) post[i] = 1.f;
-                gcv[i] = inc2;   // on the last sub-block: the whole chunk's decay
-                const float D1 = __shfl_sync(0xffffffffu, Db, (lane & ~12) | 4);
-                const float D2 = __shfl_sync(0xffffffffu, Db, (lane & ~12) | 8);
-                f1[i] = sblk == 0 ? D1 * D2 : (sblk == 1 ? D2 : 1.f);
+                for (int j = 0; j < 8; ++j)
+                    G[j] = f2_add(prev, G[j]);
             }
-            const int cb = c0 + 4 * hc;
-            if (run == 15)
-                *reinterpret_cast<float4 *>(slot + SLOT_GC + cb * 4) = make_float4(gcv[0], gcv[1], gcv[2], gcv[3]);
+            // the four sub-block totals of these channels
+            f2 T[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                T[b] = f2_pack(__shfl_sync(0xffffffffu, f2_lo(tot), 8 * b + (lane & 7)),
+                               __shfl_sync(0xffffffffu, f2_hi(tot), 8 * b + (lane & 7)));
+            // Anchors: the end of sub-block 0 (token 15) for the first half, of sub-block 2 (token 47) for the
+            // second.  Every factor formed below is either at most 1 (and may underflow only where its true value
+            // is below fp32 range) or lies within 16 tokens of an anchor (within 2^+-115.5 for lower_bound >= -5).
+            const f2 e2 = f2_add(f2_add(T[0], T[1]), T[2]);
+            const f2 e3 = f2_add(e2, T[3]);
+            const f2 zero2 = f2_pack(0.f, 0.f), one2 = f2_pack(1.f, 1.f);
+            const f2 cq = f2_ex2(first_half ? T[0] : e2);  // Gamma_anchor: Q~ = q^ L cq, K^.Gamma = k^ L cq
+            // per-lane constants of the sub-block's role (one per pass, so the token loop has no selects):
+            //   gr = G - toff = log2 (Gamma_t / Gamma_anchor);  Rs = 2^(rbase - gr) = Gamma_end(sb) / Gamma_t <= 1;
+            //   R = Gamma_anchor / Gamma_t = Rs rmul;  K~ = k^ Rs ks;  the B rows of the second anchor: k^ Rs r1m
+            const f2 toff = anchor_sb ? tot : zero2, rbase = anchor_sb ? zero2 : tot;
+            const f2 rmul = anchor_sb ? one2 : f2_ex2(f2_sub(zero2, tot));
+            const f2 ks = f2_ex2(sb == 0 ? f2_add(f2_add(T[1], T[2]), T[3]) : sb == 1 ? f2_add(T[2], T[3])
+                                 : sb == 2 ? T[3] : zero2);
+            const f2 r1m = first_half ? f2_ex2(sb == 0 ? f2_add(T[1], T[2]) : T[2]) : rmul;
+            if (sb == 3 && hh == 1)
+                *reinterpret_cast<float2 *>(slot + SLOT_GC + c0 * 4) = make_float2(ex2_approx(f2_lo(e3)), ex2_approx(f2_hi(e3)));
             // the previous pass's tensor-core product has read the operand tiles
-            if (hc == 1 && !mbar_wait(mbarA, 0))
+            if (ps == 1 && !mbar_wait(mbarA, 0))
                 hung = true;
-            uint32_t ktw[4][2];   // K~ for (channel i, tokens r = 0,1 / 2,3) as fp16 pairs
-            uint32_t qodd[2];     // Q~ of the pass's even token, second half of the channels
+            const int co = (kk >> 2) * OPS_LBO + (kk & 3) * 4;
+            unsigned char *const opsA = sm + OFF_OPS + OPS_A + co, *const opsB = sm + OFF_OPS + OPS_B + co;
+            uint32_t qt[8], ktp[8];   // Q~ and K~ of tokens t0 + j (fp16 pairs of the two channels)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int t = 4 * run + r;
-                const uint32_t qw[2] = {hc ? qv[r].z : qv[r].x, hc ? qv[r].w : qv[r].y};
-                const uint32_t kw[2] = {hc ? kv[r].z : kv[r].x, hc ? kv[r].w : kv[r].y};
-                float lq[4], lk[4], r0[4], r1[4], qt[4], kg[4], kt[4];
-                // channel pairs (2 pp, 2 pp + 1) as packed fp32: the same products, two per instruction
-                const f2 rq2 = f2_pack(rqt[r], rqt[r]), rk2 = f2_pack(rkt[r], rkt[r]);
-                const bool even = (sblk & 1) == 0;
-#pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    const int i = 2 * pp;
-                    const f2 qh = f2_mul(f2_bf16x2(qw[pp]), rq2);
-                    const f2 kh = f2_mul(f2_bf16x2(kw[pp]), rk2);
-                    const f2 P = f2_pack(pf[r][i], pf[r][i + 1]);
-                    const f2 rc = f2_pack(rcp_approx(pf[r][i]), rcp_approx(pf[r][i + 1]));   // 1 / P
-                    const f2 E = f2_mul(f2_pack(Dv[i], Dv[i + 1]), rc);
-                    const f2 Lf = even ? f2_mul(P, f2_pack(iD[i], iD[i + 1])) : P;      // 1 / E or P
-                    const f2 l_q = f2_tf32r(f2_mul(qh, Lf)), l_k = f2_tf32r(f2_mul(kh, Lf));
-                    const f2 s1 = sblk == 3 ? rc : f2_mul(E, f2_pack(f1[i], f1[i + 1]));
-                    const f2 r_1 = f2_tf32r(f2_mul(kh, s1));
-                    const f2 r_0 = f2_tf32r(f2_mul(kh, sblk == 0 ? E : rc));
-                    const f2 G = f2_mul(f2_pack(pre[i], pre[i + 1]), P);
-                    const f2 q_t = f2_mul(qh, G), k_g = f2_mul(kh, G);
-                    const f2 k_t = f2_mul(kh, f2_mul(E, f2_pack(post[i], post[i + 1])));
-                    lq[i] = f2_lo(l_q); lq[i + 1] = f2_hi(l_q);
-                    lk[i] = f2_lo(l_k); lk[i + 1] = f2_hi(l_k);
-                    r1[i] = f2_lo(r_1); r1[i + 1] = f2_hi(r_1);
-                    r0[i] = f2_lo(r_0); r0[i + 1] = f2_hi(r_0);
-                    qt[i] = f2_lo(q_t); qt[i + 1] = f2_hi(q_t);
-                    kg[i] = f2_lo(k_g); kg[i + 1] = f2_hi(k_g);
-                    kt[i] = f2_lo(k_t); kt[i + 1] = f2_hi(k_t);
-                }
+            for (int j = 0; j < 8; ++j) {
+                const int t = t0 + j;
+                const f2 gr = f2_sub(G[j], toff);
+                const f2 Lf = f2_ex2(gr), Rs = f2_ex2(f2_sub(rbase, gr));
+                const f2 qh = f2_mul(f2_bf16x2(qw[ps][j]), rq2[j]);
+                const f2 kh = f2_mul(f2_bf16x2(kw[ps][j]), rk2[j]);
+                const f2 kL = f2_mul(kh, Lf), qL = f2_mul(qh, Lf), kS = f2_mul(kh, Rs);
+                const f2 kR = f2_mul(kS, rmul);
                 const int ra = (t >> 5) * 64 + (t & 31);
-                *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_A + ops_off(ra, kgrp)) =
-                    make_float4(lk[0], lk[1], lk[2], lk[3]);
-                *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_A + ops_off(ra + 32, kgrp)) =
-                    make_float4(lq[0], lq[1], lq[2], lq[3]);
-                *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_B + ops_off(32 + t, kgrp)) =
-                    make_float4(r1[0], r1[1], r1[2], r1[3]);
-                if (t < 32)
-                    *reinterpret_cast<float4 *>(sm + OFF_OPS + OPS_B + ops_off(t, kgrp)) =
-                        make_float4(r0[0], r0[1], r0[2], r0[3]);
-                *reinterpret_cast<uint2 *>(sm + OFF_KG + kg_off(t, cb)) =
-                    make_uint2(pack_half2(kg[0], kg[1]), pack_half2(kg[2], kg[3]));
-                // Q~: the first pass keeps its 4 channels; the second stores all 8 of two consecutive tokens (two
-                // 16-byte rows of one core matrix, contiguous) with one 32-byte store
-                if (hc == 0) {
-                    qkeep[r][0] = pack_half2(qt[0], qt[1]);
-                    qkeep[r][1] = pack_half2(qt[2], qt[3]);
-                } else if ((r & 1) == 0) {
-                    qodd[0] = pack_half2(qt[0], qt[1]);
-                    qodd[1] = pack_half2(qt[2], qt[3]);
-                } else {
-                    st_global_v8(slot + qw_off(CH + t - 1, c0), qkeep[r - 1][0], qkeep[r - 1][1], qodd[0], qodd[1],
-                                 qkeep[r][0], qkeep[r][1], pack_half2(qt[0], qt[1]), pack_half2(qt[2], qt[3]));
+                *reinterpret_cast<uint2 *>(opsA + ((ra >> 3) * OPS_SBO) + ((ra & 7) << 4)) = u2_tf32r(kL);
+                *reinterpret_cast<uint2 *>(opsA + (((ra + 32) >> 3) * OPS_SBO) + ((ra & 7) << 4)) = u2_tf32r(qL);
+                *reinterpret_cast<uint2 *>(opsB + (((32 + t) >> 3) * OPS_SBO) + ((t & 7) << 4)) = u2_tf32r(f2_mul(kS, r1m));
+                if (first_half)
+                    *reinterpret_cast<uint2 *>(opsB + ((t >> 3) * OPS_SBO) + ((t & 7) << 4)) = u2_tf32r(kR);
+                *reinterpret_cast<uint32_t *>(sm + OFF_KG + kg_off(t, c0)) = half2_of(f2_mul(kL, cq));
+                qt[j] = half2_of(f2_mul(qL, cq));
+                ktp[j] = half2_of(f2_mul(kS, ks));
+            }
+            // K~ (slot rows = key channels c0, c0 + 1; 8 tokens per 16-byte core row): rows c0 and c0 + 1 of
+            // tokens t0 .. t0 + 7 are 32 contiguous bytes
+            {
+                uint32_t r0[4], r1[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    r0[m] = __byte_perm(ktp[2 * m], ktp[2 * m + 1], 0x5410);
+                    r1[m] = __byte_perm(ktp[2 * m], ktp[2 * m + 1], 0x7632);
                 }
+                st_global_v8(slot + ka_off(CH + c0, t0), r0[0], r0[1], r0[2], r0[3], r1[0], r1[1], r1[2], r1[3]);
+            }
+            // Q~ (slot rows = tokens, 8 channels per 16-byte core row): the four lanes of a run hold the four
+            // channel pairs of rows t0 .. t0 + 7; a two-step butterfly over lanes ^2 and ^1 leaves rows
+            // t0 + 2 cpl and t0 + 2 cpl + 1 (all four pairs, 32 contiguous bytes) in lane cpl
+            {
+                const bool b = (cpl >> 1) & 1, a = cpl & 1;
+                uint32_t kp[4], rv[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const __half hv = __float2half_rn(kt[i]);
-                    const uint32_t bits = *reinterpret_cast<const uint16_t *>(&hv);
-                    if (r & 1)
-                        ktw[i][r >> 1] |= bits << 16;
-                    else
-                        ktw[i][r >> 1] = bits;
+                    const uint32_t snd = b ? qt[i] : qt[4 + i];
+                    kp[i] = b ? qt[4 + i] : qt[i];
+                    rv[i] = __shfl_xor_sync(0xffffffffu, snd, 2);
                 }
-            }
-            // K~ (slot rows = key channel, 8 tokens per 16-byte core row): the lanes of runs 2m and 2m + 1
-            // swap halves so that each holds two full, adjacent rows (even run: channels 0, 1; odd run: 2, 3),
-            // 32 contiguous bytes of one core matrix, stored at once
-            {
-                const bool ev = (run & 1) == 0;
-                uint32_t ra_[2], rb_[2];   // the partner's rows of channel 0 / 1 (even lane) or 2 / 3 (odd lane)
+                // rows 4 b + i now: own pair (kp[i]) and pair cpl ^ 2 (rv[i])
+                uint32_t own[2][2], got[2][2];
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    ra_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[2][w] : ktw[0][w], 1);
-                    rb_[w] = __shfl_xor_sync(0xffffffffu, ev ? ktw[3][w] : ktw[1][w], 1);
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t s0 = a ? kp[e] : kp[2 + e], s1 = a ? rv[e] : rv[2 + e];
+                    own[e][0] = a ? kp[2 + e] : kp[e];
+                    own[e][1] = a ? rv[2 + e] : rv[e];
+                    got[e][0] = __shfl_xor_sync(0xffffffffu, s0, 1);
+                    got[e][1] = __shfl_xor_sync(0xffffffffu, s1, 1);
                 }
-                const int j8 = 8 * (run >> 1);
-                if (ev)
-                    st_global_v8(slot + ka_off(CH + cb, j8), ktw[0][0], ktw[0][1], ra_[0], ra_[1], ktw[1][0], ktw[1][1],
-                                 rb_[0], rb_[1]);
-                else
-                    st_global_v8(slot + ka_off(CH + cb + 2, j8), ra_[0], ra_[1], ktw[2][0], ktw[2][1], rb_[0], rb_[1],
-                                 ktw[3][0], ktw[3][1]);
+                // row t0 + 2 cpl + e, pair p: p ^ cpl = 0 own, 1 partner's own, 2 own's ^2, 3 partner's ^2
+                uint32_t y[2][4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const int d = pp ^ cpl;
+                        y[e][pp] = (d & 2) ? ((d & 1) ? got[e][1] : own[e][1]) : ((d & 1) ? got[e][0] : own[e][0]);
+                    }
+                st_global_v8(slot + qw_off(CH + t0 + 2 * cpl, 64 * ps + 8 * warp), y[0][0], y[0][1], y[0][2], y[0][3],
+                             y[1][0], y[1][1], y[1][2], y[1][3]);
             }
             // this half of the channels: [Akk | Aqk] (+)= A B^T on the tensor cores
             fence_async_smem();
@@ -433,7 +424,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 for (int s = 0; s < 8; ++s)
                     mma_tf32_ss(tbase, umma_desc(s_ops + OPS_A + s * 2 * OPS_LBO, OPS_LBO, OPS_SBO),
                                 umma_desc(s_ops + OPS_B + s * 2 * OPS_LBO, OPS_LBO, OPS_SBO), idesc_tf32(128, 96),
-                                hc > 0 || s > 0);
+                                ps > 0 || s > 0);
                 umma_commit(mbarA);
             }
         }
