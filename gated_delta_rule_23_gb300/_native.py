@@ -99,6 +99,8 @@ def load() -> ctypes.CDLL:
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_device_status.argtypes = [P]
         lib.kda_device_status.restype = I
+        lib.kda_set_wait_limit.argtypes = [ctypes.c_uint32]
+        lib.kda_set_wait_limit.restype = None
         lib.kda_fwd_smem_bytes.argtypes = []
         lib.kda_fwd_smem_bytes.restype = ctypes.c_size_t
         _lib = lib
@@ -112,6 +114,7 @@ def declared_functions() -> List[str]:
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(kda_[a-z_0-9]+)\s*\(", text, re.M)))
 
 
+KDA_DEFAULT_WAIT_POLLS = 16777216
 # status codes, as in include/kda.h
 KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_NONFINITE = range(6)
 KDA_DTYPE_NONE, KDA_DTYPE_BF16, KDA_DTYPE_FP32 = range(3)

@@ -1,5 +1,6 @@
 // C ABI of the KDA forward library (include/kda.h): argument checks, workspace layout and the
 // launch sequence  [plan (varlen only)] -> prep -> recurrence  on the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -16,6 +17,7 @@ namespace kda {
 namespace {
 
 constexpr int PLAN_THREADS = 1024;
+std::atomic<uint32_t> g_wait_polls{KDA_DEFAULT_WAIT_POLLS};   // kda_set_wait_limit
 constexpr int LPT_MAX_SEQS = 2048;   // longest-first ordering of varlen sequences up to this count
 
 // Varlen plan, one CTA: chunk_off[n] = sum_{m < n} ceil(len_m / 64) (exclusive scan, [N + 1]);
@@ -272,6 +274,7 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.slots = nullptr;
     p.prep_pf = 0;
     p.chunk_cap = cu_seqlens ? varlen_chunk_capacity(N, T) : 0;
+    p.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
     return p;
 }
 
@@ -481,6 +484,8 @@ extern "C" const char *kda_status_string(kda_status_t s)
     }
     return "unknown status";
 }
+
+extern "C" void kda_set_wait_limit(uint32_t polls) { g_wait_polls.store(polls, std::memory_order_relaxed); }
 
 extern "C" size_t kda_fwd_smem_bytes(void)
 {

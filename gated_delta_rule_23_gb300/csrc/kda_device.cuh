@@ -73,6 +73,7 @@ struct Problem {
     int64_t nch_fixed;        // chunks per sequence without cu_seqlens
     int prep_pf;              // prep: a CTA prefetches into L2 the rows of item blockIdx.x + prep_pf (0: off)
     int64_t chunk_cap;        // varlen: entries of the per-chunk table (every sequence's chunks are clamped to it)
+    uint32_t wait_polls;      // chunked kernels: polls of a wait before it gives up (kda_set_wait_limit)
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -180,11 +181,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
-// Bounded wait for an mbarrier phase; returns false if the wait gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
+// Bounded wait for an mbarrier phase: at most `polls` try_wait polls (0: give up at once); returns false if
+// the wait gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t polls = WAIT_LIMIT)
 {
     uint32_t done = 0;
-    for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+    for (uint32_t it = 0; it < polls; ++it) {
         asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
                      : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
         if (done)

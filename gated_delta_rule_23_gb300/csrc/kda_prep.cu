@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
             if (sb == 3 && hh == 1)
                 *reinterpret_cast<float2 *>(slot + SLOT_GC + c0 * 4) = make_float2(ex2_approx(f2_lo(e3)), ex2_approx(f2_hi(e3)));
             // the previous pass's tensor-core product has read the operand tiles
-            if (ps == 1 && !mbar_wait(mbarA, 0))
+            if (ps == 1 && !mbar_wait(mbarA, 0, p.wait_polls))
                 hung = true;
             const int co = (kk >> 2) * OPS_LBO + (kk & 3) * 4;
             unsigned char *const opsA = sm + OFF_OPS + OPS_A + co, *const opsB = sm + OFF_OPS + OPS_B + co;
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     // -------- phase 3: Akk / Aqk out of tensor memory.  Lanes 0..31 / 32..63: Akk / Aqk rows 0..31
     //          (columns 0..31 = tokens 0..31); lanes 64..95 / 96..127: rows 32..63 (columns 32..95 =
     //          tokens 0..63).  Aqk (causal) goes to the slot, b_i Akk (strictly lower) to shared memory.
-    if (!mbar_wait(mbarA, 1))
+    if (!mbar_wait(mbarA, 1, p.wait_polls))
         hung = true;
     tc_fence_after();
     {
@@ -687,9 +687,16 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         bulk_wait_read_all();
     }
 
-    // -------- release tensor memory; report a bounded wait that gave up
-    if (hung && lane == 0)
-        atomicOr(&g_kda_prep_error, 1u);
+    // -------- release tensor memory; report a bounded wait that gave up.  A wait that gave up left the
+    //          CTA's tensor-core work possibly in flight: both commit phases are awaited, in order and with
+    //          the long limit, before the columns are freed.
+    if (__syncthreads_or(hung)) {
+        if (tid == 0) {
+            mbar_wait(mbarA, 0);
+            mbar_wait(mbarA, 1);
+            atomicOr(&g_kda_prep_error, DEVERR_TIMEOUT);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {

@@ -266,8 +266,8 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         // the previous update is complete and this chunk's slot has landed
         bool ok = true;
         if (c > 0)
-            ok = mbar_wait(mbarB, (c - 1) & 1);
-        ok = ok && mbar_wait(mbarL + 8 * (c % NBUF), (c / NBUF) & 1);
+            ok = mbar_wait(mbarB, (c - 1) & 1, p.wait_polls);
+        ok = ok && mbar_wait(mbarL + 8 * (c % NBUF), (c / NBUF) & 1, p.wait_polls);
         if (__syncthreads_or(!ok)) {
             hung = true;
             break;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
         // (no barrier: each thread waits for the product itself; a wait that gave up is reported through the
         // flag, which every thread reads after the next barrier)
-        if (!mbar_wait(mbarQ, c & 1))
+        if (!mbar_wait(mbarQ, c & 1, p.wait_polls))
             *hang_flag = 1u;
         tc_fence_after();
         {
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     }
 
     if (!hung && nch > 0) {
-        const bool ok = mbar_wait(mbarB, (nch - 1) & 1);
+        const bool ok = mbar_wait(mbarB, (nch - 1) & 1, p.wait_polls);
         if (__syncthreads_or(!ok)) {
             hung = true;
         } else {

@@ -257,6 +257,21 @@ const char *kda_status_string(kda_status_t status);
  */
 kda_status_t kda_device_status(kda_stream_t stream);
 
+/* Default of kda_set_wait_limit: mbarrier polls before a wait of the chunked kernels gives up. */
+#define KDA_DEFAULT_WAIT_POLLS 16777216u
+
+/*
+ * Sets how many times a wait of the chunked kernels (kda_fwd and its variants, on the tensor cores
+ * and on bulk copies) polls before it gives up, for the kernels launched after the call, process-wide
+ * (default KDA_DEFAULT_WAIT_POLLS, which is far beyond any wait of a working kernel).  A wait that
+ * gives up makes its CTA wait for its own work in flight (with the default limit), free its tensor
+ * memory and leave; kda_device_status then reports KDA_ERR_TIMEOUT and the call's outputs are not
+ * valid.  polls = 0 makes every such wait give up at once: a way to exercise that error path without
+ * a hang.  The token-recurrent kernels (kda_fwd_recurrent, decode-sized kda_fwd calls) always use
+ * the default.  Thread-safe; not a diagnostic of anything on its own.
+ */
+void kda_set_wait_limit(uint32_t polls);
+
 /* Largest dynamic shared memory one CTA of the forward kernels uses (for diagnostics). */
 size_t kda_fwd_smem_bytes(void);
 
