@@ -343,6 +343,39 @@ def measure_decode(stream, steps=50, warmup=5, n_seq=DECODE_N, T=1):
                                                        wkey + "_bf16")}}
 
 
+def measure_link(h2d_bytes, d2h_bytes, reps=3):
+    """Host-link bandwidth of plain pinned copies of the e2e step's byte counts: H2D alone, D2H alone, and both
+    at once on two streams (best of `reps`, CUDA events on the copy streams)."""
+    import torch
+    hin = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    din = torch.empty(h2d_bytes, dtype=torch.uint8, device="cuda")
+    dout = torch.empty(d2h_bytes, dtype=torch.uint8, device="cuda")
+    hout = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(pairs):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            evs = []
+            for dst, src, st in pairs:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(st):
+                    e0.record(st)
+                    dst.copy_(src, non_blocking=True)
+                    e1.record(st)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            ms = max(e0.elapsed_time(e1) for e0, e1 in evs)
+            best = ms if best is None else min(best, ms)
+        return best
+    h2d_ms = timed([(din, hin, s1)])
+    d2h_ms = timed([(hout, dout, s2)])
+    both_ms = timed([(din, hin, s1), (hout, dout, s2)])
+    return {"h2d_ms": h2d_ms, "h2d_gbs": h2d_bytes / (h2d_ms * 1e-3) / 1e9, "d2h_ms": d2h_ms,
+            "d2h_gbs": d2h_bytes / (d2h_ms * 1e-3) / 1e9, "both_ms": both_ms, "floor_ms": both_ms}
+
+
 def run_ours(args, p, idx, rank, world):
     import torch
     import torch.distributed as dist
@@ -398,11 +431,28 @@ def run_ours(args, p, idx, rank, world):
     torch.cuda.synchronize()
     kernel_ms = {"kda_prep_kernel": statistics.mean(t[0].elapsed_time(t[1]) for t in evs),
                  "kda_recur_kernel": statistics.mean(t[1].elapsed_time(t[2]) for t in evs)}
+    # the pages' own precision choices as measurement variants of the same call (kda_fwd_ws_variant)
+    variant_ms = {}
+    for name, bits in (("bf16_state", 1), ("neumann_inverse", 2), ("both", 3)):
+        def vstep():
+            kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+                    p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], stream=stream,
+                    workspace=ws, variant=bits)
+        for _ in range(3):
+            vstep()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record(stream)
+        for _ in range(n_prof):
+            vstep()
+        v1.record(stream)
+        torch.cuda.synchronize()
+        variant_ms[name] = v0.elapsed_time(v1) / n_prof
     del ws
     if args.kernel_only:
         if rank == 0:
             print(json.dumps({"kernel_only": True, "ms_per_step": ms_step, "T": p.T, "H": p.H,
-                              "algorithmic_bytes_per_launch": algorithmic_bytes(p), "kernel_ms": kernel_ms}),
+                              "algorithmic_bytes_per_launch": algorithmic_bytes(p), "kernel_ms": kernel_ms,
+                              "variant_ms": variant_ms}),
                   flush=True)
         return
 
@@ -433,6 +483,7 @@ def run_ours(args, p, idx, rank, world):
     e2e_ms = max_over_ranks((time.perf_counter() - t_e0) * 1e3 / n_e2e, world, "cuda")
     h2d_bytes = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h_bytes = sum(t.numel() * t.element_size() for t in (out_h, fin_h) if t is not None)
+    link = measure_link(h2d_bytes, d2h_bytes) if rank == 0 else None
 
     if rank != 0:
         return
@@ -482,8 +533,13 @@ def run_ours(args, p, idx, rank, world):
         "cpu_baseline": cpu_baseline(p, idx),
         "e2e": {"value": aggregate_throughput(p.token_heads(), world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-                "entry": "kda_fwd_host (C ABI, pinned host buffers, host wall clock)"},
+                "entry": "kda_fwd_host (C ABI, pinned host buffers, host wall clock)",
+                # the host link as the bound of the end-to-end call: one plain copy of the step's input bytes
+                # and one of its output bytes (pinned memory, CUDA events), alone and both directions at once;
+                # the floor is the slower of the concurrent pair, frac = floor / e2e time
+                "link": link, "link_frac": None if link is None else link["floor_ms"] / e2e_ms},
         "clocks": sampler.summary(),
+        "variants_ms_per_step": variant_ms,
         "gpu_launches": args.steps * (3 if p.cu_seqlens is not None else 2),
         "decode": measure_decode(stream) if world == 1 else None,
     }

@@ -89,6 +89,9 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd_ws_profiled.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t,
                                              P, P]
         lib.kda_fwd_ws_profiled.restype = I
+        lib.kda_fwd_ws_variant.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t,
+                                           ctypes.c_uint, P]
+        lib.kda_fwd_ws_variant.restype = I
         lib.kda_fwd_workspace_size.argtypes = [I, I64, I, I]
         lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_workspace_trim.argtypes = []
@@ -115,6 +118,7 @@ def declared_functions() -> List[str]:
 
 
 KDA_DEFAULT_WAIT_POLLS = 16777216
+KDA_VARIANT_BF16_STATE, KDA_VARIANT_NEUMANN_INVERSE = 1, 2
 # status codes, as in include/kda.h
 KDA_OK, KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_NONFINITE = range(6)
 KDA_DTYPE_NONE, KDA_DTYPE_BF16, KDA_DTYPE_FP32 = range(3)

@@ -38,7 +38,7 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             initial_state: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
             cu_seqlens: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
             workspace: Optional[torch.Tensor] = None, stage_events=None, noalloc: bool = False,
-            recurrent: bool = False) -> None:
+            recurrent: bool = False, variant: int = 0) -> None:
     """KDA chunked forward on CUDA tensors; writes ``out`` and ``final_state`` in place.
 
     q, k, v, g: bf16 [B, T, H, 128]; beta: bf16 [B, T, H]; out: bf16 [B, T, H, 128];
@@ -50,7 +50,8 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     the prep kernel, the prep/recurrence boundary and the end (kda_fwd_ws_profiled; needs
     ``workspace``).  ``noalloc``: use the library's static workspace (kda_fwd_noalloc).
     ``recurrent``: evaluate token by token (kda_fwd_recurrent; decode and short sequences, no
-    workspace).
+    workspace).  ``variant``: KDA_VARIANT_* bits of the measurement variants (kda_fwd_ws_variant; needs
+    ``workspace``).
     """
     lib = _native.load()
     if q.dim() != 4 or q.shape[-1] != D:
@@ -97,6 +98,8 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         raise ValueError("noalloc and recurrent take no workspace or stage events")
     if noalloc and recurrent:
         raise ValueError("noalloc and recurrent are exclusive")
+    if variant and (workspace is None or stage_events is not None or noalloc or recurrent):
+        raise ValueError("variant needs a workspace and excludes stage_events, noalloc and recurrent")
     with torch.cuda.device(dev):
         if recurrent:
             rc = lib.kda_fwd_recurrent(*args, s.cuda_stream)
@@ -104,6 +107,8 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             rc = lib.kda_fwd_noalloc(*args, s.cuda_stream)
         elif workspace is None:
             rc = lib.kda_fwd(*args, s.cuda_stream)
+        elif variant:
+            rc = lib.kda_fwd_ws_variant(*args, _ptr(workspace), wsz, int(variant), s.cuda_stream)
         elif stage_events is None:
             rc = lib.kda_fwd_ws(*args, _ptr(workspace), wsz, s.cuda_stream)
         else:

@@ -275,6 +275,7 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.prep_pf = 0;
     p.chunk_cap = cu_seqlens ? varlen_chunk_capacity(N, T) : 0;
     p.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
+    p.variant = 0;
     return p;
 }
 
@@ -288,7 +289,7 @@ int state_kind(const void *initial_state, const void *final_state, kda_dtype_t s
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                  void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream, void *const *stage_events)
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events, uint32_t variant)
 {
     const bool varlen = cu_seqlens != nullptr;
     auto mark = [&](int i) -> cudaError_t {
@@ -308,6 +309,7 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
             e = mark(2);
         return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
+    p.variant = variant;
     p.slots = ws + header_bytes(N, T, varlen);
     cudaError_t err = cudaSuccess;
     if (varlen) {
@@ -385,6 +387,29 @@ extern "C" kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const 
     return run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
                cu_seqlens, N, T, H, static_cast<unsigned char *>(workspace), reinterpret_cast<cudaStream_t>(stream),
                stage_events);
+}
+
+extern "C" kda_status_t kda_fwd_ws_variant(const void *q, const void *k, const void *v, const void *g,
+                                           const void *beta, float scale, void *out, const float *A_log,
+                                           const float *dt_bias, float lower_bound, const void *initial_state,
+                                           void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens,
+                                           int N, int64_t T, int H, void *workspace, size_t workspace_bytes_,
+                                           unsigned variant, kda_stream_t stream)
+{
+    kda_status_t s = check_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                                final_state, state_dtype, cu_seqlens, N, T, H);
+    if (s == KDA_OK)
+        s = check_size(N, T, H, cu_seqlens != nullptr);
+    if (s != KDA_OK)
+        return s;
+    if (variant & ~(unsigned)(KDA_VARIANT_BF16_STATE | KDA_VARIANT_NEUMANN_INVERSE))
+        return KDA_ERR_INVALID_ARGUMENT;
+    const size_t need = workspace_bytes(N, T, H, cu_seqlens != nullptr);
+    if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes_ < need))
+        return KDA_ERR_INVALID_ARGUMENT;
+    return run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
+               cu_seqlens, N, T, H, static_cast<unsigned char *>(workspace), reinterpret_cast<cudaStream_t>(stream),
+               nullptr, variant);
 }
 
 extern "C" kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,

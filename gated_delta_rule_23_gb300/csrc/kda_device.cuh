@@ -74,7 +74,11 @@ struct Problem {
     int prep_pf;              // prep: a CTA prefetches into L2 the rows of item blockIdx.x + prep_pf (0: off)
     int64_t chunk_cap;        // varlen: entries of the per-chunk table (every sequence's chunks are clamped to it)
     uint32_t wait_polls;      // chunked kernels: polls of a wait before it gives up (kda_set_wait_limit)
+    uint32_t variant;         // VARIANT_* bits (kda_fwd_ws_variant); 0 for the library's own design
 };
+// Measurement variants of the chunked path after the FlashKDA pages' own choices (kda_fwd_ws_variant).
+constexpr uint32_t VARIANT_BF16_STATE = 1u;        // the state rounded to bf16 between chunks
+constexpr uint32_t VARIANT_NEUMANN_INVERSE = 2u;   // (I + A)^-1 by the fp16 Neumann-series product
 
 // ---------------------------------------------------------------- small helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)

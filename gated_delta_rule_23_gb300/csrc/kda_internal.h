@@ -24,7 +24,7 @@ kda_status_t check_size(int N, int64_t T, int H, bool varlen);
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                  void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr);
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr, uint32_t variant = 0);
 
 // Stream-ordered allocation from the library's memory pool of the current device (kept between calls).
 cudaError_t pool_alloc(void **p, size_t bytes, cudaStream_t stream);

@@ -121,6 +121,42 @@ __device__ __forceinline__ f2 f2_ex2(f2 a) { return f2_pack(ex2_approx(f2_lo(a))
 __device__ __forceinline__ uint2 u2_tf32r(f2 a) { return make_uint2(__float_as_uint(tf32r(f2_lo(a))), __float_as_uint(tf32r(f2_hi(a)))); }
 __device__ __forceinline__ uint32_t half2_of(f2 a) { return pack_half2(f2_lo(a), f2_hi(a)); }
 
+// C = X Y (+ Z) for fp16 [64][64] matrices in the h64 layout (row-major, 16-byte chunks XOR-swizzled by row), fp32
+// accumulation on mma.sync, result rounded to fp16; warp w computes rows 16 (w / 2) .. + 15, columns 32 (w % 2) .. + 31.
+__device__ __forceinline__ void mm64_f16(uint32_t sx, uint32_t sy, const unsigned char *z, unsigned char *c, int warp, int lane)
+{
+    const int mt = warp >> 1, nh = warp & 1, gq = lane >> 2, t4 = lane & 3, lr = lane & 7, lsel = lane >> 3;
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float2 v = make_float2(0.f, 0.f);
+            if (z)
+                v = __half22float2(*reinterpret_cast<const __half2 *>(z + h64(16 * mt + gq + 8 * hh, 32 * nh + 8 * nt + 2 * t4)));
+            acc[nt][2 * hh] = v.x;
+            acc[nt][2 * hh + 1] = v.y;
+        }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t af[4];
+        ldsm_x4(sx + h64(16 * mt + (lsel & 1) * 8 + lr, 16 * ks + (lsel >> 1) * 8), af);
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            uint32_t bf[4];
+            ldsm_x4_t(sy + h64(16 * ks + (lsel & 1) * 8 + lr, 32 * nh + 16 * pr + (lsel >> 1) * 8), bf);
+            mma_f16(acc[2 * pr], af, bf[0], bf[1]);
+            mma_f16(acc[2 * pr + 1], af, bf[2], bf[3]);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+            *reinterpret_cast<uint32_t *>(c + h64(16 * mt + gq + 8 * hh, 32 * nh + 8 * nt + 2 * t4)) =
+                pack_half2(acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+}
+
 // first token and tokens left of chunk gc (a global chunk index over all sequences; the launch keeps
 // every item index, and so gc, below 2^31, so the divisions are 32-bit); varlen chunks come from the
 // plan's per-chunk table, which has an entry for every launched chunk index (0 tokens left past the
@@ -139,7 +175,9 @@ __device__ __forceinline__ void chunk_tokens(const Problem &p, uint32_t gc, int6
     }
 }
 
-template <bool VARLEN>
+// NEUMANN: the measurement variant that forms (I + A)^-1 as the fp16 Neumann-series product (the guancyxx.cn
+// FlashKDA article, section 2.3) instead of the blocked fp32 substitution.
+template <bool VARLEN, bool NEUMANN>
 __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem p)
 {
     extern __shared__ __align__(128) unsigned char sm[];
@@ -517,6 +555,61 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         bulk_commit();
     }
 
+    if (NEUMANN) {
+        // -------- phase 4 (variant): T = (I + A)^-1 = (I + B)(I + B^2)(I + B^4)(I + B^8)(I + B^16)(I + B^32) with
+        //          B = -A (strictly lower, so B^64 = 0): five squarings and five products P += P B^(2^k), fp16
+        //          operands and fp32 accumulation, then T' = T diag(b) in fp16
+        const float *Akk = reinterpret_cast<const float *>(sm + OFF_AKK);
+        unsigned char *bufs[4] = {sm + OFF_TM, sm + OFF_TM + CH * CH * 2, sm, sm + CH * CH * 2};
+        {
+            const int i = tid >> 2, j0 = (tid & 3) * 16;
+            uint32_t bw[8], pw[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                // the strictly lower part only: the readout leaves the block above rows 0..31 unwritten
+                const int j = j0 + 2 * e;
+                const float a0 = j < i ? -Akk[i * PA + j] : 0.f, a1 = j + 1 < i ? -Akk[i * PA + j + 1] : 0.f;
+                bw[e] = pack_half2(a0, a1);
+                pw[e] = pack_half2(a0 + (i == j0 + 2 * e ? 1.f : 0.f), a1 + (i == j0 + 2 * e + 1 ? 1.f : 0.f));
+            }
+            __syncthreads();   // every thread has read its part of Akk: buffers 2 and 3 may overwrite it
+#pragma unroll
+            for (int e = 0; e < 8; e += 4) {
+                *reinterpret_cast<uint4 *>(bufs[0] + h64(i, j0 + 2 * e)) = make_uint4(bw[e], bw[e + 1], bw[e + 2], bw[e + 3]);
+                *reinterpret_cast<uint4 *>(bufs[1] + h64(i, j0 + 2 * e)) = make_uint4(pw[e], pw[e + 1], pw[e + 2], pw[e + 3]);
+            }
+        }
+        __syncthreads();
+        int ib = 0, ip = 1, in_ = 2, ip2 = 3;   // B^(2^(k-1)), P, B^(2^k), next P
+#pragma unroll 1
+        for (int k = 0; k < 5; ++k) {
+            mm64_f16(smem_u32(bufs[ib]), smem_u32(bufs[ib]), nullptr, bufs[in_], warp, lane);
+            __syncthreads();
+            mm64_f16(smem_u32(bufs[ip]), smem_u32(bufs[in_]), bufs[ip], bufs[ip2], warp, lane);
+            __syncthreads();
+            const int ob = ib, op = ip;
+            ib = in_;
+            ip = ip2;
+            in_ = ob;
+            ip2 = op;
+        }
+        {
+            const int i = tid >> 2, j0 = (tid & 3) * 16;
+            unsigned char *tp = sm + OFF_TP;
+#pragma unroll
+            for (int e = 0; e < 16; e += 8) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(bufs[ip] + h64(i, j0 + e));
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&ww[f]));
+                    o[f] = pack_half2(v.x * bt[j0 + e + 2 * f], v.y * bt[j0 + e + 2 * f + 1]);
+                }
+                *reinterpret_cast<uint4 *>(tp + h64(i, j0 + e)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    } else
     // -------- phase 4: Tm = (I + Akk)^-1 by 16-token blocks: fp32 forward substitution on the
     //          diagonal blocks, then the two 32-token halves' off-diagonal blocks
     //          t_{1,0} = -t_{1,1} A_{1,0} t_{0,0}, t_{3,2} = -t_{3,3} A_{3,2} t_{2,2}, then the lower-left
@@ -705,7 +798,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     }
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool NEUMANN>
 cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
 {
     static bool configured[64] = {};
@@ -714,7 +807,8 @@ cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
     if (err != cudaSuccess)
         return err;
     if (dev >= 64 || !configured[dev]) {
-        err = cudaFuncSetAttribute(kda_prep_kernel<VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+        err = cudaFuncSetAttribute(kda_prep_kernel<VARLEN, NEUMANN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   PREP_SMEM);
         if (err != cudaSuccess)
             return err;
         if (dev < 64)
@@ -731,7 +825,7 @@ cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
     }
     Problem q = p;
     q.prep_pf = PREP_PF_QUARTER_WAVES * 2 * nsm / 4;   // two resident CTAs per SM
-    kda_prep_kernel<VARLEN><<<(unsigned)items, PREP_THREADS, PREP_SMEM, stream>>>(q);
+    kda_prep_kernel<VARLEN, NEUMANN><<<(unsigned)items, PREP_THREADS, PREP_SMEM, stream>>>(q);
     return cudaGetLastError();
 }
 
@@ -744,7 +838,9 @@ cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t strea
         return cudaSuccess;
     if (items > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    return p.cu ? launch_prep_t<true>(p, items, stream) : launch_prep_t<false>(p, items, stream);
+    if (p.variant & VARIANT_NEUMANN_INVERSE)
+        return p.cu ? launch_prep_t<true, true>(p, items, stream) : launch_prep_t<false, true>(p, items, stream);
+    return p.cu ? launch_prep_t<true, false>(p, items, stream) : launch_prep_t<false, false>(p, items, stream);
 }
 
 size_t prep_smem_bytes() { return PREP_SMEM; }

@@ -103,7 +103,10 @@ __device__ __forceinline__ void tmem_st32_nw(uint32_t taddr, const uint32_t (&u)
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int STATE, bool VARLEN>  // STATE: 0 none, 1 bf16, 2 fp32
+// STATE: 0 none, 1 bf16, 2 fp32.  BSTATE: the measurement variant that keeps the state in bf16 between chunks
+// (rounded to nearest at each chunk boundary, as the guancyxx.cn FlashKDA article's design does, section 2.3);
+// the default keeps the fp32 accumulator as the state.
+template <int STATE, bool VARLEN, bool BSTATE>
 __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 {
     extern __shared__ __align__(128) unsigned char sm[];
@@ -280,6 +283,11 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             const float *gam = reinterpret_cast<const float *>(sb + SLOT_GC) + half * 64;
             uint32_t u[64], o[32];
             tmem_ld_s_ofrag(trow + TM_S + half * 64, u, trow + TM_O + half * 32, o);   // O^T unused at c = 0
+            if (BSTATE) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    u[e] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(u[e]))));
+            }
             {
                 uint32_t hv[32];
 #pragma unroll
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     }
 }
 
-template <int STATE, bool VARLEN>
+template <int STATE, bool VARLEN, bool BSTATE>
 cudaError_t launch_recur_t(const Problem &p, int grid, cudaStream_t stream)
 {
     static bool configured[64] = {};
@@ -445,29 +453,36 @@ cudaError_t launch_recur_t(const Problem &p, int grid, cudaStream_t stream)
     if (err != cudaSuccess)
         return err;
     if (dev >= 64 || !configured[dev]) {
-        err = cudaFuncSetAttribute(kda_recur_kernel<STATE, VARLEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(kda_recur_kernel<STATE, VARLEN, BSTATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    RECUR_SMEM);
         if (err != cudaSuccess)
             return err;
         if (dev < 64)
             configured[dev] = true;
     }
-    kda_recur_kernel<STATE, VARLEN><<<grid, RT, RECUR_SMEM, stream>>>(p);
+    kda_recur_kernel<STATE, VARLEN, BSTATE><<<grid, RT, RECUR_SMEM, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <bool BSTATE>
+cudaError_t launch_recur_b(const Problem &p, int state_kind, cudaStream_t stream)
+{
+    const int grid = p.N * p.H;
+    if (p.cu)
+        return state_kind == 2 ? launch_recur_t<2, true, BSTATE>(p, grid, stream)
+             : state_kind == 1 ? launch_recur_t<1, true, BSTATE>(p, grid, stream)
+                               : launch_recur_t<0, true, BSTATE>(p, grid, stream);
+    return state_kind == 2 ? launch_recur_t<2, false, BSTATE>(p, grid, stream)
+         : state_kind == 1 ? launch_recur_t<1, false, BSTATE>(p, grid, stream)
+                           : launch_recur_t<0, false, BSTATE>(p, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream)
 {
-    const int grid = p.N * p.H;
-    if (p.cu)
-        return state_kind == 2 ? launch_recur_t<2, true>(p, grid, stream)
-             : state_kind == 1 ? launch_recur_t<1, true>(p, grid, stream)
-                               : launch_recur_t<0, true>(p, grid, stream);
-    return state_kind == 2 ? launch_recur_t<2, false>(p, grid, stream)
-         : state_kind == 1 ? launch_recur_t<1, false>(p, grid, stream)
-                           : launch_recur_t<0, false>(p, grid, stream);
+    return (p.variant & VARIANT_BF16_STATE) ? launch_recur_b<true>(p, state_kind, stream)
+                                            : launch_recur_b<false>(p, state_kind, stream);
 }
 
 size_t recur_smem_bytes() { return RECUR_SMEM; }

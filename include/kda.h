@@ -150,6 +150,27 @@ kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, co
                                  void *workspace, size_t workspace_bytes, void *const *stage_events,
                                  kda_stream_t stream);
 
+/* Bits of kda_fwd_ws_variant: the FlashKDA pages' own precision choices for the chunked path. */
+#define KDA_VARIANT_BF16_STATE 1u       /* the state kept in bf16 between 64-token chunks (rounded to nearest) */
+#define KDA_VARIANT_NEUMANN_INVERSE 2u  /* (I + A)^-1 as the fp16 Neumann-series product */
+
+/*
+ * kda_fwd_ws_variant -- kda_fwd_ws with measurement variants that follow the guancyxx.cn FlashKDA
+ * article, section 2.3 ("bf16 循环状态 + fp16 矩阵求逆"): a state stored in bf16 between chunks instead
+ * of the library's fp32 state, and an fp16 Neumann-series product (I - A)(I + A^2)(I + A^4) ...
+ * (I + A^32) for the chunk inverse instead of the library's blocked fp32 substitution.  variant is
+ * an OR of KDA_VARIANT_* bits (0 gives exactly kda_fwd_ws).  They exist to measure those choices on
+ * this hardware: the bf16 state is less precise (its rounding accumulates over the chunks) and the
+ * Neumann product costs more tensor-core steps; neither is faster here.  Same arguments, layouts and
+ * errors as kda_fwd_ws, plus KDA_ERR_INVALID_ARGUMENT for unknown variant bits.  Fixed-length
+ * problems of 1 to 4 tokens per sequence take the token-recurrent kernels whatever the variant.
+ */
+kda_status_t kda_fwd_ws_variant(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                float scale, void *out, const float *A_log, const float *dt_bias,
+                                float lower_bound, const void *initial_state, void *final_state,
+                                kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
+                                void *workspace, size_t workspace_bytes, unsigned variant, kda_stream_t stream);
+
 /* Capacity of the static workspace of kda_fwd_noalloc (256 MiB per device). */
 #define KDA_NOALLOC_SCRATCH_BYTES 268435456
 

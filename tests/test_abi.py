@@ -153,3 +153,11 @@ def test_oversize_problems_unsupported_before_any_cuda_call(lib, N, T, H):
             None, None, KDA_DTYPE_NONE, None, N, T, H]
     assert lib.kda_fwd_ws(*args, A + 0x100000, 1 << 30, None) == KDA_ERR_UNSUPPORTED
     assert lib.kda_fwd_host(*args) == KDA_ERR_UNSUPPORTED
+
+
+def test_variant_entry_rejects_unknown_bits(lib):
+    args = [A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 0.1, A + 0x5000, A + 0x6000, A + 0x7000, -5.0,
+            None, None, KDA_DTYPE_NONE, None, 1, 64, 2]
+    need = lib.kda_fwd_workspace_size(1, 64, 2, 0)
+    assert lib.kda_fwd_ws_variant(*args, A + 0x100000, need, 4, None) == KDA_ERR_INVALID_ARGUMENT
+    assert lib.kda_fwd_ws_variant(*args, None, need, 1, None) == KDA_ERR_INVALID_ARGUMENT

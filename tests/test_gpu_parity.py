@@ -319,3 +319,27 @@ def test_wait_that_gives_up_is_reported_and_the_next_call_is_correct():
         device_status()   # the report was cleared
         out, fin = run_gpu(p, dev)
         assert_parity(out, fin, *oracle_run(p))
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("lb", [-5.0, -0.05])
+def test_measurement_variants_within_parity(variant, lb):
+    """The pages' own precision choices, as measurement variants of the chunked path (kda_fwd_ws_variant): the
+    state rounded to bf16 between chunks (1), the fp16 Neumann-series inverse (2), both (3).  They stay within
+    the parity bar against the oracle at strong and at slow decay, fixed length and varlen."""
+    from gated_delta_rule_23_gb300 import device_status, workspace_size
+    from tests.gpu_util import parity_report
+    for cu in (None, np.array([0, 90, 333])):
+        p = make_problem(B=1, T=333, H=3, seed=81, lower_bound=lb, cu_seqlens=cu)
+        dev = to_device(p)
+        out = torch.empty_like(dev["q"])
+        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda")
+        ws = torch.empty(workspace_size(p.N, p.T, p.H, cu is not None), dtype=torch.uint8, device="cuda")
+        kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"], dev["dt_bias"],
+                p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], workspace=ws,
+                variant=variant)
+        device_status()
+        o, f = out.float().cpu().numpy(), fin.float().cpu().numpy()
+        o_ref, f_ref = oracle_run(p)
+        r = assert_parity(o, f, o_ref, f_ref)
+        print(f"variant {variant} lb {lb} varlen {cu is not None}: {parity_report(o, f, o_ref, f_ref)}")
