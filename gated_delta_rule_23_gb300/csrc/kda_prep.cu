@@ -75,9 +75,9 @@ constexpr int OFF_WS = OFF_AKK, OFF_US = OFF_AKK + 64 * D * 2;
 static_assert(OFF_US + D * CH * 2 <= OFF_TP, "W / U0 staging overlaps T'");
 constexpr int OFF_KG = 65536;                       // fp16 [64 j][128 c] K^ . Gamma (kg_off swizzle)
 constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizzled)
-constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 pairs [64][2] 1 / |q| (both halves)
-constexpr int OFF_RK = OFF_RQ + 512;                // fp32 pairs [64][2] 1 / |k|
-constexpr int OFF_BT = OFF_RK + 512;                // fp32 [64] b = sigmoid(beta), 0 past the end
+constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 pairs [68][2] 1 / |q| (both halves; norm_slot order)
+constexpr int OFF_RK = OFF_RQ + 544;                // fp32 pairs [68][2] 1 / |k|
+constexpr int OFF_BT = OFF_RK + 544;                // fp32 [64] b = sigmoid(beta), 0 past the end
 constexpr int OFF_MISC = OFF_BT + 256;              // mbarrier, tensor-memory base
 constexpr int PREP_SMEM = OFF_MISC + 16;
 static_assert(OFF_KG >= OPS_BYTES && OFF_KG % 128 == 0, "shared memory map");
@@ -94,6 +94,10 @@ __device__ __forceinline__ int stg_off(int t, int c16) { return t * 256 + ((c16 
 // t / 8, so that both the gate pass's stores (tokens 8 m + j of one channel group) and ldmatrix (8
 // consecutive tokens) spread over the banks
 __device__ __forceinline__ int kg_off(int t, int c) { return t * 256 + ((((c >> 3) ^ (t & 7) ^ ((t >> 3) & 7))) << 4) + ((c & 7) << 1); }
+
+// slot of token t in the pair tables of the norms: one 8-byte pad every 16 tokens, so that the eight token runs a
+// warp reads at once (tokens 16 sb + 8 hh + j) fall on eight different bank pairs
+__host__ __device__ constexpr int norm_slot(int t) { return t + (t >> 4); }
 
 __device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
                                              uint32_t a5, uint32_t a6, uint32_t a7)
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
             for (int w = 0; w < 8; ++w)
                 s += part[(w * 2 + which) * CH + t];
             const float r = rsqrtf(s + 1e-6f);
-            reinterpret_cast<float2 *>(which ? rk : rq)[t] = make_float2(r, r);
+            reinterpret_cast<float2 *>(which ? rk : rq)[norm_slot(t)] = make_float2(r, r);
         }
         __syncthreads();
     }
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         const float gz = -eA * LOG2E;
         const f2 gz2 = f2_pack(gz, gz), lb2 = f2_pack(p.lb_log2e, p.lb_log2e);
         // 1 / |q_t|, 1 / |k_t| of the thread's tokens, stored twice over (as the pair multiplier)
-        const f2 *rq2 = reinterpret_cast<const f2 *>(rq) + t0, *rk2 = reinterpret_cast<const f2 *>(rk) + t0;
+        const f2 *rq2 = reinterpret_cast<const f2 *>(rq) + norm_slot(t0), *rk2 = reinterpret_cast<const f2 *>(rk) + norm_slot(t0);
         const bool first_half = sb < 2, anchor_sb = (sb & 1) == 0;
 #pragma unroll
         for (int ps = 0; ps < 2; ++ps) {
