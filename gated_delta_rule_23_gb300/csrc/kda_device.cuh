@@ -71,7 +71,7 @@ struct Problem {
     int N, H;
     int64_t T;
     int64_t nch_fixed;        // chunks per sequence without cu_seqlens
-    int prep_pf;              // prep: a CTA prefetches into L2 the rows of item blockIdx.x + prep_pf (0: off)
+    int prep_pf;              // prep: each CTA prefetches its next item's rows into L2 (0: off)
     int64_t chunk_cap;        // varlen: entries of the per-chunk table (every sequence's chunks are clamped to it)
     uint32_t wait_polls;      // chunked kernels: polls of a wait before it gives up (kda_set_wait_limit)
     uint32_t variant;         // VARIANT_* bits (kda_fwd_ws_variant); 0 for the library's own design

@@ -38,11 +38,9 @@ constexpr int PREP_THREADS = 256;
 #ifndef KDA_PREP_PF_BETA
 #define KDA_PREP_PF_BETA 1
 #endif
-#ifndef KDA_PREP_PF_QUARTER_WAVES
-#define KDA_PREP_PF_QUARTER_WAVES 3
+#ifndef KDA_PREP_PREFETCH
+#define KDA_PREP_PREFETCH 1
 #endif
-// L2 prefetch distance in quarters of a wave of resident CTAs (0: off)
-constexpr int PREP_PF_QUARTER_WAVES = KDA_PREP_PF_QUARTER_WAVES;
 constexpr int TMEM_COLS = 128;          // Akk / Aqk accumulators: 128 lanes x 96 columns
 // tf32 operand tiles of the Akk / Aqk product for one half of the channels (the gate pass runs in
 // two passes of 64 channels; the tensor cores accumulate both).  No-swizzle K-major core-matrix
@@ -78,8 +76,8 @@ constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizz
 constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 pairs [68][2] 1 / |q| (both halves; norm_slot order)
 constexpr int OFF_RK = OFF_RQ + 544;                // fp32 pairs [68][2] 1 / |k|
 constexpr int OFF_BT = OFF_RK + 544;                // fp32 [64] b = sigmoid(beta), 0 past the end
-constexpr int OFF_MISC = OFF_BT + 256;              // mbarrier, tensor-memory base
-constexpr int PREP_SMEM = OFF_MISC + 16;
+constexpr int OFF_MISC = OFF_BT + 256;              // mbarriers (+0 products, +16 drain), tensor-memory base (+8)
+constexpr int PREP_SMEM = OFF_MISC + 24;
 static_assert(OFF_KG >= OPS_BYTES && OFF_KG % 128 == 0, "shared memory map");
 static_assert(2 * (PREP_SMEM + 1024) <= 233472, "two CTAs per SM");
 
@@ -182,29 +180,48 @@ __device__ __forceinline__ void chunk_tokens(const Problem &p, uint32_t gc, int6
 // NEUMANN: the measurement variant that forms (I + A)^-1 as the fp16 Neumann-series product (the guancyxx.cn
 // FlashKDA article, section 2.3) instead of the blocked fp32 substitution.
 template <bool VARLEN, bool NEUMANN>
-__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem p)
+__global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem p, uint32_t n_items)
 {
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
-    const uint32_t item = blockIdx.x;
-    const uint32_t gc = item / (uint32_t)H;
-    const int h = (int)(item - gc * (uint32_t)H);
-
-    // -------- this CTA's chunk: first token tok0 and L valid tokens
-    int64_t tok0, rem;
-    chunk_tokens<VARLEN>(p, gc, tok0, rem);   // the table has an entry for every launched CTA
-    if (VARLEN && rem <= 0)
-        return;   // past the last chunk
-    const int L = (int)(rem < CH ? rem : CH);
-    unsigned char *slot = p.slots + (size_t)item * SLOT_BYTES;
-
     float *rq = reinterpret_cast<float *>(sm + OFF_RQ);
     float *rk = reinterpret_cast<float *>(sm + OFF_RK);
     float *bt = reinterpret_cast<float *>(sm + OFF_BT);
-    const uint32_t mbarA = smem_u32(sm + OFF_MISC);
+    const uint32_t mbarA = smem_u32(sm + OFF_MISC), mbarD = smem_u32(sm + OFF_MISC + 16);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 8);
     bool hung = false;
+
+    // -------- once per CTA: the Akk / Aqk accumulator columns and the tensor-core mbarrier (two phases per item)
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    if (tid == 32) {
+        mbar_init(mbarA, 1);
+        mbar_init(mbarD, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t s_ops = smem_u32(sm + OFF_OPS);
+
+    // -------- the items of this CTA: blockIdx.x, + gridDim.x, ... (every item's work is the same)
+#pragma unroll 1
+    for (uint32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const uint32_t gc = item / (uint32_t)H;
+    const int h = (int)(item - gc * (uint32_t)H);
+
+    // -------- this item's chunk: first token tok0 and L valid tokens
+    int64_t tok0, rem;
+    chunk_tokens<VARLEN>(p, gc, tok0, rem);   // the table has an entry for every launched item
+    if (VARLEN && rem <= 0)
+        continue;   // past the last chunk (the same for every thread)
+    const int L = (int)(rem < CH ? rem : CH);
+    unsigned char *slot = p.slots + (size_t)item * SLOT_BYTES;
 
     // -------- phase 0: the chunk's q, k, g rows into the staging tiles (cp.async, 512 contiguous bytes per
     // warp instruction; rows past the end zero-filled), the beta and gate parameters into registers
@@ -226,20 +243,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     const float2 dtb0 = *reinterpret_cast<const float2 *>(p.dt_bias + (size_t)h * D + 8 * warp + 2 * cpl);
     const float2 dtb1 = *reinterpret_cast<const float2 *>(p.dt_bias + (size_t)h * D + 64 + 8 * warp + 2 * cpl);
 
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
-                     "r"(TMEM_COLS));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-        tc_fence_before();
-    }
-    if (tid == 32) {
-        mbar_init(mbarA, 1);
-        mbar_fence_init();
-    }
-    // rows of the item that starts about prep_pf / resident CTAs waves later: q, k, g and v
-    // into L2 (two 128-byte lines per token and tensor), so that its first loads hit L2
-    if (p.prep_pf > 0 && item + (uint32_t)p.prep_pf < gridDim.x) {
-        const uint32_t pit = item + (uint32_t)p.prep_pf, pgc = pit / (uint32_t)H;
+    // rows of this CTA's next item: q, k, g and v into L2 (two 128-byte lines per token and tensor), so that its
+    // first loads hit L2
+    if (p.prep_pf > 0 && item + gridDim.x < n_items) {
+        const uint32_t pit = item + gridDim.x, pgc = pit / (uint32_t)H;
         const int ph = (int)(pit - pgc * (uint32_t)H);
         int64_t ptok0, prem;
         chunk_tokens<VARLEN>(p, pgc, ptok0, prem);
@@ -315,8 +322,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         __syncthreads();
     }
     tc_fence_after();
-    const uint32_t tbase = *tslot;
-    const uint32_t s_ops = smem_u32(sm + OFF_OPS);
 
     // -------- phase 2: gate, decay factors and every per-token operand, in two passes of 64 channels; each
     //          pass fills the Akk / Aqk operand tiles for its channels, then the tensor cores accumulate them.
@@ -776,23 +781,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
-        // W rows (QW rows 0..63) and U0^T of the slot: bulk copies.  The CTA may leave once every copy
-        // has read its shared-memory source; the writes complete before the kernel does.
+        // W rows (QW rows 0..63) and U0^T of the slot: bulk copies.  The next item may overwrite the shared
+        // memory once every copy has read it; the writes complete before the kernel does.
         bulk_s2g(slot + SLOT_QW, smem_u32(sm + OFF_WS), 64 * D * 2);
         bulk_s2g(slot + SLOT_U0, smem_u32(sm + OFF_US), D * CH * 2);
         bulk_commit();
         bulk_wait_read_all();
     }
+    // the next item's tensor-core product reuses the accumulator columns this item read out
+    tc_fence_before();
+    if (__syncthreads_or(hung))
+        break;   // a wait gave up: stop, and drain below
+    tc_fence_after();
+    }
 
-    // -------- release tensor memory; report a bounded wait that gave up.  A wait that gave up left the
-    //          CTA's tensor-core work possibly in flight: both commit phases are awaited, in order and with
-    //          the long limit, before the columns are freed.
-    if (__syncthreads_or(hung)) {
-        if (tid == 0) {
-            mbar_wait(mbarA, 0);
-            mbar_wait(mbarA, 1);
-            atomicOr(&g_kda_prep_error, DEVERR_TIMEOUT);
-        }
+    // -------- release tensor memory; report a bounded wait that gave up.  A wait that gave up may have left
+    //          tensor-core work in flight, and the product mbarrier's phase is then no longer known: the thread
+    //          that issued every product commits once more to a fresh mbarrier, whose single phase completes
+    //          after all of them (awaited with the long limit), before the columns are freed.
+    if (hung && tid == 0) {
+        umma_commit(mbarD);
+        mbar_wait(mbarD, 0);
+        atomicOr(&g_kda_prep_error, DEVERR_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
@@ -828,8 +838,10 @@ cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
             sms[dev] = nsm;
     }
     Problem q = p;
-    q.prep_pf = PREP_PF_QUARTER_WAVES * 2 * nsm / 4;   // two resident CTAs per SM
-    kda_prep_kernel<VARLEN, NEUMANN><<<(unsigned)items, PREP_THREADS, PREP_SMEM, stream>>>(q);
+    q.prep_pf = KDA_PREP_PREFETCH;   // each CTA prefetches its next item's rows into L2
+    // persistent: two CTAs per SM (their shared memory), each walking the items blockIdx.x + k gridDim.x
+    const int64_t grid = items < 2 * (int64_t)nsm ? items : 2 * (int64_t)nsm;
+    kda_prep_kernel<VARLEN, NEUMANN><<<(unsigned)grid, PREP_THREADS, PREP_SMEM, stream>>>(q, (uint32_t)items);
     return cudaGetLastError();
 }
 
