@@ -91,17 +91,30 @@ __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *c
     for (int64_t c = used + tid; c < n_info; c += PLAN_THREADS)
         chunk_info[c] = make_longlong2(0, 0);
     if (order) {
-        for (int s = tid; s < N; s += PLAN_THREADS) {
-            int64_t bs, ls;
-            seq_range(cu, s, N, T, bs, ls);
-            int rank = 0;
-            for (int m = 0; m < N; ++m) {
-                int64_t bm, lm;
-                seq_range(cu, m, N, T, bm, lm);
-                rank += (lm > ls) || (lm == ls && m < s);
-            }
-            order[rank] = s;
+        // longest-first order: a bitonic sort (descending) of the keys length * 4096 + (4095 - index) in shared
+        // memory, padded with -1 to LPT_MAX_SEQS entries; ties keep the lower index first.  Each of the 66 stages
+        // is one compare-exchange per thread (LPT_MAX_SEQS / 2 = PLAN_THREADS pairs).
+        static_assert(LPT_MAX_SEQS == 2 * PLAN_THREADS && LPT_MAX_SEQS <= 4096, "bitonic sort layout");
+        __shared__ int64_t keys[LPT_MAX_SEQS];
+        for (int s = tid; s < LPT_MAX_SEQS; s += PLAN_THREADS) {
+            int64_t bs, ls = -1;
+            if (s < N)
+                seq_range(cu, s, N, T, bs, ls);
+            keys[s] = s < N ? ls * 4096 + (4095 - s) : -1;
         }
+        __syncthreads();
+        for (int k = 2; k <= LPT_MAX_SEQS; k <<= 1)
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const int i = 2 * j * (tid / j) + (tid % j), ixj = i + j;
+                const int64_t x = keys[i], y = keys[ixj];
+                if ((i & k) == 0 ? x < y : x > y) {
+                    keys[i] = y;
+                    keys[ixj] = x;
+                }
+                __syncthreads();
+            }
+        for (int r = tid; r < N; r += PLAN_THREADS)
+            order[r] = 4095 - (int)(keys[r] & 4095);
     }
     if (__syncthreads_or(bad) && tid == 0)
         atomicOr(&g_kda_plan_error, DEVERR_CU_SEQLENS);
