@@ -415,7 +415,8 @@ def run_ours(args, p, idx, rank, world):
     ms_step = ms_total / args.steps
 
     # per-kernel breakdown: the same calls through kda_fwd_ws_profiled, which records events at the
-    # kernel boundaries on the launching stream
+    # kernel boundaries on the launching stream (always the single-launch schedule: one prep launch over
+    # every chunk, then the recurrence, also where the timed step runs in pieces)
     from gated_delta_rule_23_gb300 import workspace_size
     ws = torch.empty(workspace_size(p.N, p.T, p.H, p.cu_seqlens is not None), dtype=torch.uint8, device="cuda")
     n_prof = max(3, min(args.steps, 100))
@@ -540,10 +541,32 @@ def run_ours(args, p, idx, rank, world):
                 "link": link, "link_frac": None if link is None else link["floor_ms"] / e2e_ms},
         "clocks": sampler.summary(),
         "variants_ms_per_step": variant_ms,
-        "gpu_launches": args.steps * (3 if p.cu_seqlens is not None else 2),
+        "pieces_per_step": pieces_per_step(p),
+        "gpu_launches": args.steps * launches_per_step(p),
         "decode": measure_decode(stream) if world == 1 else None,
     }
     print(json.dumps(line), flush=True)
+
+
+def pieces_per_step(p):
+    """Pieces along T in which one call runs this workload on the current device (kda_fwd_pieces)."""
+    from gated_delta_rule_23_gb300 import _native
+    return int(_native.load().kda_fwd_pieces(p.N, p.T, p.H, int(p.cu_seqlens is not None)))
+
+
+def launches_per_step(p):
+    """Kernels one call launches: the varlen plan, prep and recurrence; a decode step's single kernel; or,
+    in pieces, a prep and a recurrence launch per piece plus the bf16 state conversions into and out of the
+    fp32 state that passes between pieces."""
+    if p.cu_seqlens is not None:
+        return 3
+    if 1 <= p.T <= 4:
+        return 1
+    pieces = pieces_per_step(p)
+    if pieces > 1:
+        conv = int(p.state_dtype == STATE_BF16) * (int(p.initial_state is not None) + int(p.want_final))
+        return 2 * pieces + conv
+    return 2
 
 
 def main():

@@ -94,6 +94,8 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd_ws_variant.restype = I
         lib.kda_fwd_workspace_size.argtypes = [I, I64, I, I]
         lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.kda_fwd_pieces.argtypes = [I, I64, I, I]
+        lib.kda_fwd_pieces.restype = I
         lib.kda_workspace_trim.argtypes = []
         lib.kda_workspace_trim.restype = I
         lib.kda_check_cu_seqlens.argtypes = [P, I, I64]

@@ -46,9 +46,9 @@ def kda_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     when both are given); cu_seqlens: int64 [N + 1] with B = 1.  Runs asynchronously on
     ``stream`` (default: the current stream).  ``workspace``: optional uint8 CUDA tensor of at
     least ``workspace_size(...)`` bytes (kda_fwd_ws); without it the library's pool provides one.
-    ``stage_events``: optional three recorded-once torch.cuda.Event objects marking the start of
-    the prep kernel, the prep/recurrence boundary and the end (kda_fwd_ws_profiled; needs
-    ``workspace``).  ``noalloc``: use the library's static workspace (kda_fwd_noalloc).
+    ``stage_events``: optional three recorded-once torch.cuda.Event objects (or None) marking the
+    start of the prep kernel, the prep/recurrence boundary and the end (kda_fwd_ws_profiled, which
+    always runs the single-launch schedule, never pieces; needs ``workspace``).  ``noalloc``: use the library's static workspace (kda_fwd_noalloc).
     ``recurrent``: evaluate token by token (kda_fwd_recurrent; decode and short sequences, no
     workspace).  ``variant``: KDA_VARIANT_* bits of the measurement variants (kda_fwd_ws_variant; needs
     ``workspace``).

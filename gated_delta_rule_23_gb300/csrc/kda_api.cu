@@ -1,5 +1,6 @@
 // C ABI of the KDA forward library (include/kda.h): argument checks, workspace layout and the
 // launch sequence  [plan (varlen only)] -> prep -> recurrence  on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -130,12 +131,51 @@ int64_t max_chunks(int N, int64_t T, bool varlen)
     return varlen ? varlen_chunk_capacity(N, T) : (int64_t)N * ((T + CH - 1) / CH);
 }
 
-// workspace (varlen only: the plan): [chunk_off: (N + 1) int64][order: N int32][chunk_info: max_chunks
-// x (int64, int64), 16-byte aligned], then the operand slots (256-byte aligned)
-size_t info_offset(int N) { return round_up((size_t)(N + 1) * 8 + (size_t)N * 4, 16); }
-size_t header_bytes(int N, int64_t T, bool varlen)
+// Long fixed-length problems on few (sequence, head) pairs run in pieces of whole chunks along T: the
+// recurrence over piece i (one CTA per pair, on a part of the SMs) runs beside the prep kernel of piece
+// i + 1 on the SMs it leaves free, and the state passes from piece to piece in fp32, exactly as the
+// recurrence keeps it between chunks, so the results are the same bits as one launch over all chunks.
+// With P pieces the overlap hides about (1 - 1/P) of the shorter of two times: the recurrence's (≈1.52 us
+// per chunk step on GB300) scaled by the fraction of SMs it leaves free, and the prep kernel's (≈5.9 us
+// per (chunk, head) item per SM); each piece costs about 12 us (the prep kernel's last wave and the
+// recurrence's start), so the best P is near sqrt(hidden time / 12 us), rounded down.  With more than 64
+// pairs the recurrence already draws most of the HBM bandwidth and the pieces measured no gain.
+#ifndef KDA_PIECE_MAX_PAIRS
+#define KDA_PIECE_MAX_PAIRS 64
+#endif
+#ifndef KDA_PIECES_FORCE
+#define KDA_PIECES_FORCE 0   // > 0: this many pieces wherever piece_mode holds (measurement builds)
+#endif
+constexpr int MAX_PIECES = 8;
+constexpr int64_t PIECE_MIN_CHUNKS = 16;   // chunks per piece at least
+
+bool piece_mode(int N, int64_t T, int H, bool varlen)
 {
-    return varlen ? round_up(info_offset(N) + (size_t)max_chunks(N, T, true) * 16, 256) : 0;
+    return !varlen && (int64_t)N * H <= KDA_PIECE_MAX_PAIRS && (T + CH - 1) / CH >= 2 * PIECE_MIN_CHUNKS;
+}
+
+// pieces for a problem of nch chunks per sequence and `pairs` (sequence, head) pairs on nsm SMs
+int piece_count(int64_t nch, int64_t pairs, int nsm)
+{
+    const int64_t most = std::min<int64_t>(MAX_PIECES, nch / PIECE_MIN_CHUNKS);
+    int64_t n = KDA_PIECES_FORCE;
+    if (n <= 0 && nsm > 0) {
+        const double recur_us = 1.52 * (double)nch * (double)std::max<int64_t>(nsm - pairs, 0) / nsm;
+        const double prep_us = 5.9 * (double)nch * (double)pairs / nsm;
+        n = (int64_t)std::sqrt(std::min(recur_us, prep_us) / 12.0);
+    }
+    return (int)std::max<int64_t>(1, std::min<int64_t>(n, most));
+}
+
+// workspace: a header, then the operand slots (256-byte aligned).  varlen: the plan, [chunk_off: (N + 1)
+// int64][order: N int32][chunk_info: max_chunks x (int64, int64), 16-byte aligned]; fixed length in
+// pieces: the fp32 state passed between pieces, [N][H][128][128]; otherwise nothing.
+size_t info_offset(int N) { return round_up((size_t)(N + 1) * 8 + (size_t)N * 4, 16); }
+size_t header_bytes(int N, int64_t T, int H, bool varlen)
+{
+    if (varlen)
+        return round_up(info_offset(N) + (size_t)max_chunks(N, T, true) * 16, 256);
+    return piece_mode(N, T, H, false) ? (size_t)N * H * D * D * sizeof(float) : 0;
 }
 
 }  // namespace
@@ -160,7 +200,7 @@ size_t workspace_bytes(int N, int64_t T, int H, bool varlen)
         return SIZE_MAX;
     uint64_t slots = 0, bytes = 0, total = 0;
     if (__builtin_mul_overflow(chunks, (uint64_t)H, &slots) || __builtin_mul_overflow(slots, (uint64_t)SLOT_BYTES, &bytes) ||
-        __builtin_add_overflow(bytes, (uint64_t)header_bytes(N, T, varlen), &total) || total > (uint64_t)SIZE_MAX)
+        __builtin_add_overflow(bytes, (uint64_t)header_bytes(N, T, H, varlen), &total) || total > (uint64_t)SIZE_MAX)
         return SIZE_MAX;
     return (size_t)total;
 }
@@ -281,6 +321,7 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.H = H;
     p.T = T;
     p.nch_fixed = (T + CH - 1) / CH;
+    p.ch_base = 0;
     p.chunk_off = nullptr;
     p.chunk_info = nullptr;
     p.order = nullptr;
@@ -297,12 +338,84 @@ int state_kind(const void *initial_state, const void *final_state, kda_dtype_t s
     return (initial_state || final_state) ? (state_dtype == KDA_DTYPE_FP32 ? 2 : 1) : 0;
 }
 
+// SMs of the current device (looked up once per device)
+cudaError_t sm_count(int *nsm)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    int n = dev >= 0 && dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            cache[dev].store(n, std::memory_order_relaxed);
+    }
+    *nsm = n;
+    return cudaSuccess;
+}
+
+// pieces of a (checked) problem on the current device; 1 without pieces
+cudaError_t pieces_on_device(int N, int64_t T, int H, bool varlen, int *pieces)
+{
+    *pieces = 1;
+    if (!piece_mode(N, T, H, varlen))
+        return cudaSuccess;
+    int nsm = 0;
+    const cudaError_t e = sm_count(&nsm);
+    if (e == cudaSuccess)
+        *pieces = piece_count((T + CH - 1) / CH, (int64_t)N * H, nsm);
+    return e;
+}
+
+// Piece i covers chunks [nch i / P, nch (i + 1) / P) of every sequence; everything runs on the caller's
+// stream.  The prep kernel of piece i + 1 (one CTA per item, so that it takes SMs as they come free) is launched as a programmatic dependent of the
+// recurrence over piece i: it starts once every recurrence CTA runs (one per pair, on a part of the SMs),
+// fills the SMs they leave free, and its last CTA waits for that recurrence to complete before it exits.
+// The recurrence over piece i + 1 is a normal launch after that prep kernel, so it starts after both.  The
+// state between pieces is the workspace header (fp32); a bf16 initial or final state is converted into or
+// out of it.
+cudaError_t run_pieces(const Problem &p, int pieces, int state_kind, kda_dtype_t state_dtype, unsigned char *ws,
+                       cudaStream_t stream)
+{
+    float *st = reinterpret_cast<float *>(ws);
+    const size_t st_elems = (size_t)p.N * p.H * D * D;
+    const bool bf16 = state_kind != 0 && state_dtype == KDA_DTYPE_BF16;
+    const void *init0 = p.init;
+    cudaError_t e = cudaSuccess;
+    if (bf16 && p.init) {
+        e = launch_convert(p.init, st, st_elems, true, stream);
+        init0 = st;
+    }
+    const int64_t nch = p.nch_fixed;
+    for (int i = 0; i < pieces && e == cudaSuccess; ++i) {
+        const int64_t c0 = nch * i / pieces, c1 = nch * (i + 1) / pieces;
+        Problem q = p;
+        q.ch_base = c0;
+        q.nch_fixed = c1 - c0;
+        q.slots = p.slots + (size_t)p.N * c0 * p.H * SLOT_BYTES;
+        q.init = i == 0 ? init0 : st;
+        q.fin = i < pieces - 1 ? st : (bf16 ? (p.fin ? st : nullptr) : p.fin);
+        // piece 0 has the GPU to itself (persistent grid); later pieces run beside a recurrence
+        e = launch_prep(q, (int64_t)p.N * (c1 - c0), stream, i == 0, i > 0);
+        if (e == cudaSuccess)
+            e = launch_recur(q, 2, stream);
+    }
+    if (e == cudaSuccess && bf16 && p.fin)
+        e = launch_convert(st, p.fin, st_elems, false, stream);
+    return e;
+}
+
 }  // namespace
 
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                  void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream, void *const *stage_events, uint32_t variant)
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events, uint32_t variant,
+                 bool single_launch)
 {
     const bool varlen = cu_seqlens != nullptr;
     auto mark = [&](int i) -> cudaError_t {
@@ -323,7 +436,16 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
         return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     p.variant = variant;
-    p.slots = ws + header_bytes(N, T, varlen);
+    p.slots = ws + header_bytes(N, T, H, varlen);
+    // the measurement variants keep the single-launch schedule
+    if (piece_mode(N, T, H, varlen) && variant == 0 && !single_launch) {
+        int pieces = 0;
+        if (pieces_on_device(N, T, H, false, &pieces) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (pieces > 1)
+            return run_pieces(p, pieces, state_kind(initial_state, final_state, state_dtype), state_dtype, ws,
+                              stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     cudaError_t err = cudaSuccess;
     if (varlen) {
         int64_t *chunk_off = reinterpret_cast<int64_t *>(ws);
@@ -360,6 +482,15 @@ extern "C" size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen)
         check_size(N, T, H, varlen != 0) != KDA_OK)
         return 0;
     return workspace_bytes(N, T, H, varlen != 0);
+}
+
+extern "C" int kda_fwd_pieces(int N, int64_t T, int H, int varlen)
+{
+    if (N < 1 || H < 1 || T < 0 || T > ((int64_t)1 << 40) || (int64_t)N * H > INT32_MAX ||
+        check_size(N, T, H, varlen != 0) != KDA_OK)
+        return 0;
+    int pieces = 0;
+    return pieces_on_device(N, T, H, varlen != 0, &pieces) == cudaSuccess ? pieces : 0;
 }
 
 extern "C" kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -399,7 +530,7 @@ extern "C" kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const 
         return KDA_ERR_INVALID_ARGUMENT;
     return run(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, state_dtype,
                cu_seqlens, N, T, H, static_cast<unsigned char *>(workspace), reinterpret_cast<cudaStream_t>(stream),
-               stage_events);
+               stage_events, 0, true);
 }
 
 extern "C" kda_status_t kda_fwd_ws_variant(const void *q, const void *k, const void *v, const void *g,

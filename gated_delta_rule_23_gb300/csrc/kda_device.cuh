@@ -70,7 +70,8 @@ struct Problem {
     float scale, lb_log2e;    // lb_log2e = lower_bound * log2(e)
     int N, H;
     int64_t T;
-    int64_t nch_fixed;        // chunks per sequence without cu_seqlens
+    int64_t nch_fixed;        // without cu_seqlens: chunks of each sequence in this launch
+    int64_t ch_base;          // without cu_seqlens: first chunk of this launch within each sequence
     int prep_pf;              // prep: each CTA prefetches its next item's rows into L2 (0: off)
     int64_t chunk_cap;        // varlen: entries of the per-chunk table (every sequence's chunks are clamped to it)
     uint32_t wait_polls;      // chunked kernels: polls of a wait before it gives up (kda_set_wait_limit)

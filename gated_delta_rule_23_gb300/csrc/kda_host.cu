@@ -96,6 +96,8 @@ struct DevBufs {
     }
 };
 
+}  // namespace
+
 cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cudaStream_t s)
 {
     if (n == 0)
@@ -107,8 +109,6 @@ cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cu
         f32_to_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const float *>(src), static_cast<__nv_bfloat16 *>(dst), n);
     return cudaGetLastError();
 }
-
-}  // namespace
 
 kda_status_t run_host(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                       void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,

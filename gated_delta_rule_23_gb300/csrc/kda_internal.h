@@ -20,11 +20,13 @@ size_t workspace_bytes(int N, int64_t T, int H, bool varlen);
 // KDA_ERR_UNSUPPORTED when the chunked path cannot take the problem size (workspace size not
 // representable, or more than 2^31 - 1 (chunk, head) items); KDA_OK otherwise.  No CUDA calls.
 kda_status_t check_size(int N, int64_t T, int H, bool varlen);
-// The launch sequence on `stream` with workspace `ws` (checked arguments).
+// The launch sequence on `stream` with workspace `ws` (checked arguments).  single_launch: one prep launch
+// over every chunk, then one recurrence launch, also where the problem would run in pieces.
 kda_status_t run(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                  void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                  void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H,
-                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr, uint32_t variant = 0);
+                 unsigned char *ws, cudaStream_t stream, void *const *stage_events = nullptr, uint32_t variant = 0,
+                 bool single_launch = false);
 
 // Stream-ordered allocation from the library's memory pool of the current device (kept between calls).
 cudaError_t pool_alloc(void **p, size_t bytes, cudaStream_t stream);
@@ -35,8 +37,14 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
 
 struct Problem;
 
-// Prep kernel over max_chunks x H (chunk, head) items; CTAs past the real chunk count exit.
-cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t stream);
+// Prep kernel over max_chunks x H (chunk, head) items; CTAs past the real chunk count exit.  persistent:
+// at most two CTAs per SM walking the items; otherwise one CTA per item.  early: launched as a programmatic
+// dependent of the recurrence kernel before it on `stream` (it reads nothing that recurrence writes), so it
+// starts once every recurrence CTA runs, on the SMs they leave free, and completes after that recurrence.
+cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t stream, bool persistent = true,
+                        bool early = false);
+// Elementwise bf16 <-> fp32 conversion of n values on `stream` (to_f32: bf16 src to fp32 dst).
+cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cudaStream_t stream);
 // Recurrence kernel over N x H (sequence, head) pairs; state_kind 0 none, 1 bf16, 2 fp32.
 cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream);
 // Token-recurrent kernel, persistent over the N x H x 2 (sequence, head, value half) items; no workspace.

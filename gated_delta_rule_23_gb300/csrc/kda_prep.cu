@@ -159,8 +159,9 @@ __device__ __forceinline__ void mm64_f16(uint32_t sx, uint32_t sy, const unsigne
                 pack_half2(acc[nt][2 * hh], acc[nt][2 * hh + 1]);
 }
 
-// first token and tokens left of chunk gc (a global chunk index over all sequences; the launch keeps
-// every item index, and so gc, below 2^31, so the divisions are 32-bit); varlen chunks come from the
+// first token and tokens left of chunk gc (a chunk index over all sequences of the launch; the launch keeps
+// every item index, and so gc, below 2^31, so the divisions are 32-bit); fixed-length launches cover
+// chunks ch_base .. ch_base + nch_fixed - 1 of every sequence; varlen chunks come from the
 // plan's per-chunk table, which has an entry for every launched chunk index (0 tokens left past the
 // last chunk)
 template <bool VARLEN>
@@ -171,9 +172,10 @@ __device__ __forceinline__ void chunk_tokens(const Problem &p, uint32_t gc, int6
         tok0 = ci.x;
         rem = ci.y;
     } else {
-        const uint32_t nch = (uint32_t)p.nch_fixed, n = gc / nch, c = gc - n * nch;
-        tok0 = (int64_t)n * p.T + (int64_t)c * CH;
-        rem = p.T - (int64_t)c * CH;
+        const uint32_t nch = (uint32_t)p.nch_fixed, n = gc / nch;
+        const int64_t c = p.ch_base + (int64_t)(gc - n * nch);   // chunk index within sequence n
+        tok0 = (int64_t)n * p.T + c * CH;
+        rem = p.T - c * CH;
     }
 }
 
@@ -810,10 +812,15 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TMEM_COLS));
     }
+    // launched early beside a recurrence (a programmatic dependent of it): the grid's last CTA exits only
+    // after that recurrence has completed, so work ordered after this kernel is ordered after both (a
+    // no-op for a normal launch)
+    if (blockIdx.x == gridDim.x - 1)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <bool VARLEN, bool NEUMANN>
-cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
+cudaError_t launch_prep_t(const Problem &p, int64_t items, bool persistent, bool early, cudaStream_t stream)
 {
     static bool configured[64] = {};
     int dev = 0;
@@ -839,15 +846,26 @@ cudaError_t launch_prep_t(const Problem &p, int64_t items, cudaStream_t stream)
     }
     Problem q = p;
     q.prep_pf = KDA_PREP_PREFETCH;   // each CTA prefetches its next item's rows into L2
-    // persistent: two CTAs per SM (their shared memory), each walking the items blockIdx.x + k gridDim.x
-    const int64_t grid = items < 2 * (int64_t)nsm ? items : 2 * (int64_t)nsm;
-    kda_prep_kernel<VARLEN, NEUMANN><<<(unsigned)grid, PREP_THREADS, PREP_SMEM, stream>>>(q, (uint32_t)items);
-    return cudaGetLastError();
+    // persistent: two CTAs per SM (their shared memory), each walking the items blockIdx.x + k gridDim.x;
+    // otherwise one CTA per item, so that the SMs come free item by item for a kernel running beside it
+    const int64_t cap = persistent ? 2 * (int64_t)nsm : items;
+    const int64_t grid = items < cap ? items : cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(PREP_THREADS);
+    cfg.dynamicSmemBytes = PREP_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kda_prep_kernel<VARLEN, NEUMANN>, q, (uint32_t)items);
 }
 
 }  // namespace
 
-cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t stream)
+cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t stream, bool persistent, bool early)
 {
     const int64_t items = max_chunks * p.H;
     if (items <= 0)
@@ -855,8 +873,10 @@ cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t strea
     if (items > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     if (p.variant & VARIANT_NEUMANN_INVERSE)
-        return p.cu ? launch_prep_t<true, true>(p, items, stream) : launch_prep_t<false, true>(p, items, stream);
-    return p.cu ? launch_prep_t<true, false>(p, items, stream) : launch_prep_t<false, false>(p, items, stream);
+        return p.cu ? launch_prep_t<true, true>(p, items, persistent, early, stream)
+                    : launch_prep_t<false, true>(p, items, persistent, early, stream);
+    return p.cu ? launch_prep_t<true, false>(p, items, persistent, early, stream)
+                : launch_prep_t<false, false>(p, items, persistent, early, stream);
 }
 
 size_t prep_smem_bytes() { return PREP_SMEM; }

@@ -110,6 +110,9 @@ template <int STATE, bool VARLEN, bool BSTATE>
 __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 {
     extern __shared__ __align__(128) unsigned char sm[];
+    // a kernel launched after this one as its programmatic dependent (the next piece's prep kernel, which
+    // reads nothing this kernel writes) may start once every CTA of this grid runs
+    asm volatile("griddepcontrol.launch_dependents;");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
     const int h = blockIdx.x % H;
@@ -124,8 +127,9 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         if (usable * CH < len)
             len = usable * CH;   // only a malformed cu_seqlens gets here: chunks past the table are skipped
     } else {
-        bos = (int64_t)n * p.T;
-        len = p.T;
+        // chunks ch_base .. ch_base + nch_fixed - 1 of the sequence (all of them unless the call runs in pieces)
+        bos = (int64_t)n * p.T + p.ch_base * CH;
+        len = p.T - p.ch_base * CH < p.nch_fixed * CH ? p.T - p.ch_base * CH : p.nch_fixed * CH;
         slot0 = (int64_t)n * p.nch_fixed;
     }
     const int nch = (int)((len + CH - 1) / CH);

@@ -107,6 +107,15 @@ typedef enum {
  * token, as kda_fwd_recurrent does (same kernels, same bits, no workspace); everything else
  * takes the chunked form.
  *
+ * Fixed-length problems with N x H <= 64 (sequence, head) pairs and at least 32 chunks of 64
+ * tokens per sequence run in up to 8 pieces of whole chunks along T (more for longer sequences
+ * and fewer pairs; at least 16 chunks each), all on `stream`: the prep kernel
+ * of the next piece is launched as a programmatic dependent of the recurrence over the current
+ * one (it reads nothing that recurrence writes), so the two run side by side on different SMs;
+ * the prep kernel completes only after that recurrence has.  The state passes between pieces in
+ * fp32 (through the workspace), as it does between chunks, so the results are the same bits as
+ * without pieces.
+ *
  * Returns KDA_OK once the work is enqueued.  Argument errors are reported
  * synchronously before anything is launched; the kernel itself never traps.
  */
@@ -122,6 +131,14 @@ kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g,
  * the fixed-length problems of 1 to 4 tokens per sequence, which need none.
  */
 size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen);
+
+/*
+ * Number of pieces along T in which kda_fwd, kda_fwd_ws and kda_fwd_noalloc run a problem of this
+ * size on the current device (see kda_fwd): 1 when the call runs without pieces (every varlen
+ * problem, and the fixed-length problems outside the piece rule), 2 to 8 otherwise.  0 for invalid
+ * sizes, or when the device's SM count cannot be read.  Launches nothing.
+ */
+int kda_fwd_pieces(int N, int64_t T, int H, int varlen);
 
 /*
  * kda_fwd_ws -- kda_fwd with a caller-owned device workspace of at least
@@ -141,7 +158,8 @@ kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void 
  * boundaries, for timing the two kernels separately: stage_events[0] right before the prep
  * kernel (after the varlen plan), [1] between the prep and recurrence kernels, [2] after the
  * recurrence kernel.  stage_events points to 3 cudaEvent_t handles (any may be NULL).  The
- * computation and its results are exactly those of kda_fwd_ws.
+ * prep kernel always runs over every chunk before the recurrence starts, all on `stream`, also
+ * for the problems that kda_fwd_ws runs in pieces; the results are exactly those of kda_fwd_ws.
  */
 kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, const void *g, const void *beta,
                                  float scale, void *out, const float *A_log, const float *dt_bias,

@@ -101,7 +101,16 @@ def test_binding_rejects_cpu_tensors():
 
 def test_workspace_size(lib):
     slot = 74240   # fp16 operands of one (64-token chunk, head)
+    state = 128 * 128 * 4   # fp32 state of one (sequence, head)
+    # fixed length with N x H <= 64 and at least 32 chunks: may run in pieces, the fp32 state between
+    # pieces ahead of the slots
     assert lib.kda_fwd_workspace_size(1, 8192, 96, 0) == 128 * 96 * slot
+    assert lib.kda_fwd_workspace_size(1, 8192, 64, 0) == 64 * state + 128 * 64 * slot
+    assert lib.kda_fwd_workspace_size(2, 4096, 32, 0) == 64 * state + 2 * 64 * 32 * slot
+    assert lib.kda_fwd_workspace_size(1, 2049, 3, 0) == 3 * state + 33 * 3 * slot
+    assert lib.kda_fwd_workspace_size(1, 1985, 3, 0) == 3 * state + 32 * 3 * slot
+    assert lib.kda_fwd_workspace_size(1, 1984, 3, 0) == 31 * 3 * slot
+    assert lib.kda_fwd_workspace_size(1, 8192, 65, 0) == 128 * 65 * slot
     assert lib.kda_fwd_workspace_size(2, 65, 3, 0) == 2 * 2 * 3 * slot
     assert lib.kda_fwd_workspace_size(1, 0, 4, 0) == 0
     # varlen: a header (chunk offsets, order, 16 bytes per chunk of chunk info), then at most
@@ -114,6 +123,17 @@ def test_workspace_size(lib):
     assert lib.kda_fwd_workspace_size(256, 1, 96, 0) == 0
     assert lib.kda_fwd_workspace_size(256, 4, 96, 0) == 0
     assert lib.kda_fwd_workspace_size(256, 5, 96, 0) == 256 * 96 * slot
+
+
+def test_pieces_query_without_pieces(lib):
+    # problems outside the piece rule report 1 without touching the device; invalid sizes 0
+    assert lib.kda_fwd_pieces(1, 8192, 96, 0) == 1      # more than 64 (sequence, head) pairs
+    assert lib.kda_fwd_pieces(1, 1984, 8, 0) == 1       # fewer than 32 chunks
+    assert lib.kda_fwd_pieces(8, 8192, 8, 1) == 1       # varlen
+    assert lib.kda_fwd_pieces(256, 1, 96, 0) == 1       # decode step
+    assert lib.kda_fwd_pieces(0, 100, 8, 0) == 0
+    assert lib.kda_fwd_pieces(1, -1, 8, 0) == 0
+    assert lib.kda_fwd_pieces(1, 100, 0, 0) == 0
 
 
 def test_ws_entry_rejects_missing_workspace(lib):

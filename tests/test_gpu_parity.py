@@ -230,6 +230,59 @@ def test_caller_workspace_matches_pool_workspace(varlen):
     assert_parity(results[0][0], results[0][1], *oracle_run(p))
 
 
+# (B, T, H) -> pieces on a 152-SM GB300
+PIECE_SHAPES = {(2, 8200, 8): 2, (1, 4097, 40): 2, (1, 32768, 24): 6}
+
+
+@pytest.mark.parametrize("B,T,H,state,with_initial", [
+    (2, 8200, 8, STATE_NONE, False), (2, 8200, 8, STATE_BF16, True), (2, 8200, 8, STATE_BF16, False),
+    (2, 8200, 8, STATE_FP32, True), (2, 8200, 8, STATE_FP32, False), (1, 4097, 40, STATE_BF16, True),
+    (1, 32768, 24, STATE_FP32, True)])
+def test_pieces_match_single_launch(B, T, H, state, with_initial):
+    """Long fixed-length problems on few (sequence, head) pairs run in pieces along T (the next piece's prep
+    kernel launched beside the recurrence over the current one): the same bits as the single-launch schedule
+    of kda_fwd_ws_profiled, for every state kind, with 2 to 6 pieces and ragged last chunks; and work that
+    the caller enqueues on the same stream after the call sees the finished results."""
+    from gated_delta_rule_23_gb300 import _native, workspace_size
+    pieces = _native.load().kda_fwd_pieces(B, T, H, 0)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert pieces == PIECE_SHAPES[(B, T, H)]
+    assert pieces >= 2
+    p = make_problem(B=B, T=T, H=H, seed=23, state_dtype=state, with_initial=with_initial)
+    dev = to_device(p)
+    ws = torch.empty(workspace_size(p.N, p.T, p.H, False), dtype=torch.uint8, device="cuda")
+    nch = -(-T // 64)
+    assert ws.numel() == p.N * p.H * 128 * 128 * 4 + p.N * nch * p.H * 74240   # the piece-state header is there
+    s = torch.cuda.Stream()
+    results = []
+    for kw in ({"workspace": ws, "stage_events": [None, None, None]}, {"workspace": ws}, {}):
+        out = torch.empty_like(dev["q"])
+        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda") if dev["sdt"] is not None else None
+        torch.cuda.synchronize()
+        _call(p, dev, out, fin, stream=s, **kw)
+        with torch.cuda.stream(s):   # ordered after the call on s only
+            out_c = out.clone()
+            fin_c = fin.clone() if fin is not None else None
+        s.synchronize()
+        assert torch.equal(out_c, out) and (fin is None or torch.equal(fin_c, fin))
+        results.append((out.float().cpu().numpy(), None if fin is None else fin.float().cpu().numpy()))
+    for o, f in results[1:]:
+        assert np.array_equal(o, results[0][0])
+        assert (f is None and results[0][1] is None) or np.array_equal(f, results[0][1])
+    o_ref, f_ref = oracle_run(p)
+    assert_parity(results[1][0], results[1][1], o_ref, f_ref)
+
+
+@pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
+def test_pieces_in_place_state(state):
+    """In pieces, an initial state updated in place (final_state = initial_state) gives the oracle's result."""
+    from gated_delta_rule_23_gb300 import _native
+    assert _native.load().kda_fwd_pieces(2, 8200, 8, 0) >= 2
+    p = make_problem(B=2, T=8200, H=8, seed=24, state_dtype=state)
+    out, fin = run_gpu(p, inplace=True)
+    assert_parity(out, fin, *oracle_run(p))
+
+
 def test_workspace_too_small_rejected():
     from gated_delta_rule_23_gb300 import KDAError, workspace_size
     p = make_problem(B=1, T=130, H=2, seed=22)
