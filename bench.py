@@ -542,6 +542,7 @@ def run_ours(args, p, idx, rank, world):
         "clocks": sampler.summary(),
         "variants_ms_per_step": variant_ms,
         "pieces_per_step": pieces_per_step(p),
+        "scan_groups_per_step": scan_groups_per_step(p),
         "gpu_launches": args.steps * launches_per_step(p),
         "decode": measure_decode(stream) if world == 1 else None,
     }
@@ -554,17 +555,26 @@ def pieces_per_step(p):
     return int(_native.load().kda_fwd_pieces(p.N, p.T, p.H, int(p.cu_seqlens is not None)))
 
 
+def scan_groups_per_step(p):
+    """Groups of the chunk-transition scan along T for this workload (kda_fwd_scan_groups; 1: no scan)."""
+    from gated_delta_rule_23_gb300 import _native
+    return int(_native.load().kda_fwd_scan_groups(p.N, p.T, p.H, int(p.cu_seqlens is not None)))
+
+
 def launches_per_step(p):
-    """Kernels one call launches: the varlen plan, prep and recurrence; a decode step's single kernel; or,
-    in pieces, a prep and a recurrence launch per piece plus the bf16 state conversions into and out of the
-    fp32 state that passes between pieces."""
+    """Kernels one call launches: the varlen plan, prep and recurrence; a decode step's single kernel; with
+    the scan along T, prep, the groups' transitions, their start states and the grouped recurrence; or, in
+    pieces, a prep and a recurrence launch per piece; plus, for the scan and the pieces, the bf16 state
+    conversions into and out of the fp32 states they pass on."""
     if p.cu_seqlens is not None:
         return 3
     if 1 <= p.T <= 4:
         return 1
+    conv = int(p.state_dtype == STATE_BF16) * (int(p.initial_state is not None) + int(p.want_final))
+    if scan_groups_per_step(p) > 1:
+        return 4 + conv
     pieces = pieces_per_step(p)
     if pieces > 1:
-        conv = int(p.state_dtype == STATE_BF16) * (int(p.initial_state is not None) + int(p.want_final))
         return 2 * pieces + conv
     return 2
 

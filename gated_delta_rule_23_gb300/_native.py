@@ -17,7 +17,7 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
-UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_decode", "kda_host", "kda_noalloc"]
+UNITS = ["kda_api", "kda_prep", "kda_recur", "kda_recurrent", "kda_decode", "kda_host", "kda_noalloc", "kda_scan"]
 SOURCES = [os.path.join(CSRC, u + ".cu") for u in UNITS]
 HEADERS = [os.path.join(INCLUDE, "kda.h"), os.path.join(CSRC, "kda_device.cuh"), os.path.join(CSRC, "kda_internal.h"),
            os.path.join(CSRC, "kda_plan.h")]
@@ -96,6 +96,8 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_fwd_pieces.argtypes = [I, I64, I, I]
         lib.kda_fwd_pieces.restype = I
+        lib.kda_fwd_scan_groups.argtypes = [I, I64, I, I]
+        lib.kda_fwd_scan_groups.restype = I
         lib.kda_workspace_trim.argtypes = []
         lib.kda_workspace_trim.restype = I
         lib.kda_check_cu_seqlens.argtypes = [P, I, I64]

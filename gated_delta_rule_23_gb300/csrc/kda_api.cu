@@ -167,15 +167,68 @@ int piece_count(int64_t nch, int64_t pairs, int nsm)
     return (int)std::max<int64_t>(1, std::min<int64_t>(n, most));
 }
 
+// Fixed-length problems on at most 16 (sequence, head) pairs with long sequences replace the serial chain of the
+// recurrence by the chunk-transition scan along T (kda_scan.cu): G groups of L chunks per pair, composed in
+// parallel (2 (G - 1) CTAs per pair), chained serially (G - 1 fp32 steps of ≈2 us), then run in parallel
+// (G CTAs per pair).  G comes from a cost model of those three launches against the serial chain (≈1.52 us
+// per chunk, less what the pieces hide) on the 152 SMs of a GB300; it depends only on N, T and H, like the
+// workspace that holds the scan's matrices.
+#ifndef KDA_SCAN_GROUPS_FORCE
+#define KDA_SCAN_GROUPS_FORCE 0   // > 0: this many groups wherever the scan may run (measurement builds)
+#endif
+constexpr int SCAN_MAX_PAIRS = 16;
+constexpr int SCAN_MAX_GROUPS = 16;
+constexpr int MODEL_SMS = 152;
+constexpr double CHUNK_STEP_US = 1.52, COMPOSE_STEP_US = 1.3, SCAN_STEP_US = 2.0, SCAN_FIXED_US = 10.0;
+
+// (groups, chunks per group) for a scan over nch chunks with about g groups: every group but the last full
+int64_t scan_len(int64_t nch, int g) { return (nch + g - 1) / g; }
+int scan_groups_of(int64_t nch, int g) { return (int)((nch + scan_len(nch, g) - 1) / scan_len(nch, g)); }
+
+// groups of the scan for this problem; 1 when the recurrence runs as one chain per pair
+int scan_groups(int N, int64_t T, int H, bool varlen)
+{
+    const int64_t pairs = (int64_t)N * H, nch = (T + CH - 1) / CH;
+    if (varlen || pairs > SCAN_MAX_PAIRS || nch < 2 * PIECE_MIN_CHUNKS)
+        return 1;
+    if (KDA_SCAN_GROUPS_FORCE > 1)
+        return scan_groups_of(nch, (int)std::min<int64_t>(KDA_SCAN_GROUPS_FORCE, nch));
+    auto waves = [](int64_t ctas) { return (double)((ctas + MODEL_SMS - 1) / MODEL_SMS); };
+    // the serial chain, with what the pieces hide behind it
+    const double recur_us = CHUNK_STEP_US * (double)nch;
+    const double prep_us = 5.9 * (double)nch * (double)pairs / MODEL_SMS;
+    const int pc = piece_count(nch, pairs, MODEL_SMS);
+    const double hidden = pc > 1 ? std::min(recur_us * (MODEL_SMS - pairs) / MODEL_SMS, prep_us) * (1.0 - 1.0 / pc) -
+                                       12.0 * pc : 0.0;
+    double best = recur_us - std::max(hidden, 0.0);
+    int best_g = 1;
+    for (int g = 2; g <= SCAN_MAX_GROUPS && g <= nch; ++g) {
+        const int G = scan_groups_of(nch, g);
+        const double L = (double)scan_len(nch, g);
+        const double t = waves(2 * (G - 1) * pairs) * L * COMPOSE_STEP_US + (G - 1) * SCAN_STEP_US +
+                         waves(G * pairs) * L * CHUNK_STEP_US + SCAN_FIXED_US;
+        if (t < best) {
+            best = t;
+            best_g = G;
+        }
+    }
+    return best_g;
+}
+
 // workspace: a header, then the operand slots (256-byte aligned).  varlen: the plan, [chunk_off: (N + 1)
-// int64][order: N int32][chunk_info: max_chunks x (int64, int64), 16-byte aligned]; fixed length in
-// pieces: the fp32 state passed between pieces, [N][H][128][128]; otherwise nothing.
+// int64][order: N int32][chunk_info: max_chunks x (int64, int64), 16-byte aligned]; fixed length with the
+// scan: [initial state][M_g][B_g][start states], fp32 [N][H][128][128] each, the last three for G - 1 groups;
+// fixed length in pieces: the fp32 state passed between pieces, [N][H][128][128]; otherwise nothing.
 size_t info_offset(int N) { return round_up((size_t)(N + 1) * 8 + (size_t)N * 4, 16); }
 size_t header_bytes(int N, int64_t T, int H, bool varlen)
 {
     if (varlen)
         return round_up(info_offset(N) + (size_t)max_chunks(N, T, true) * 16, 256);
-    return piece_mode(N, T, H, false) ? (size_t)N * H * D * D * sizeof(float) : 0;
+    const size_t state = (size_t)N * H * D * D * sizeof(float);
+    const int G = scan_groups(N, T, H, false);
+    if (G > 1)
+        return (1 + 3 * (size_t)(G - 1)) * state;
+    return piece_mode(N, T, H, false) ? state : 0;
 }
 
 }  // namespace
@@ -322,6 +375,10 @@ Problem make_problem(const void *q, const void *k, const void *v, const void *g,
     p.T = T;
     p.nch_fixed = (T + CH - 1) / CH;
     p.ch_base = 0;
+    p.groups = 1;
+    p.group_len = p.nch_fixed;
+    p.sc_a = p.sc_b = nullptr;
+    p.sc_s = nullptr;
     p.chunk_off = nullptr;
     p.chunk_info = nullptr;
     p.order = nullptr;
@@ -362,12 +419,53 @@ cudaError_t sm_count(int *nsm)
 cudaError_t pieces_on_device(int N, int64_t T, int H, bool varlen, int *pieces)
 {
     *pieces = 1;
-    if (!piece_mode(N, T, H, varlen))
+    if (!piece_mode(N, T, H, varlen) || scan_groups(N, T, H, varlen) > 1)
         return cudaSuccess;
     int nsm = 0;
     const cudaError_t e = sm_count(&nsm);
     if (e == cudaSuccess)
         *pieces = piece_count((T + CH - 1) / CH, (int64_t)N * H, nsm);
+    return e;
+}
+
+// The chunk-transition scan (see scan_groups): prep over every chunk, the groups' transitions, their start
+// states, then the grouped recurrence.  The initial state is first copied (fp32) or converted (bf16) into
+// the header, so that the last group's final state may overwrite the caller's initial state (in place)
+// while other groups start; a bf16 final state goes through the last start-state buffer, which only the
+// last group's CTAs read (each its own rows, before writing them).
+cudaError_t run_scan(const Problem &p, int groups, int state_kind, kda_dtype_t state_dtype, unsigned char *ws,
+                     cudaStream_t stream)
+{
+    const size_t mat = (size_t)D * D, pairs = (size_t)p.N * p.H;
+    float *st0 = reinterpret_cast<float *>(ws);
+    float *ma = st0 + pairs * mat, *mb = ma + (groups - 1) * pairs * mat, *ss = mb + (groups - 1) * pairs * mat;
+    const bool bf16 = state_kind != 0 && state_dtype == KDA_DTYPE_BF16;
+    const float *init0 = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (p.init) {
+        e = bf16 ? launch_convert(p.init, st0, pairs * mat, true, stream)
+                 : cudaMemcpyAsync(st0, p.init, pairs * mat * sizeof(float), cudaMemcpyDeviceToDevice, stream);
+        init0 = st0;
+    }
+    if (e == cudaSuccess)
+        e = launch_prep(p, (int64_t)p.N * p.nch_fixed, stream);
+    Problem q = p;
+    q.groups = groups;
+    q.group_len = scan_len(p.nch_fixed, groups);
+    q.sc_a = ma;
+    q.sc_b = mb;
+    q.sc_s = ss;
+    q.init = init0;
+    float *last = ss + (size_t)(groups - 2) * pairs * mat;
+    q.fin = bf16 ? (p.fin ? last : nullptr) : p.fin;
+    if (e == cudaSuccess)
+        e = launch_compose(q, stream);
+    if (e == cudaSuccess)
+        e = launch_scan_states(init0, ma, mb, ss, (int)pairs, groups, stream);
+    if (e == cudaSuccess)
+        e = launch_recur(q, 2, stream);
+    if (e == cudaSuccess && bf16 && p.fin)
+        e = launch_convert(last, p.fin, pairs * mat, false, stream);
     return e;
 }
 
@@ -396,6 +494,7 @@ cudaError_t run_pieces(const Problem &p, int pieces, int state_kind, kda_dtype_t
         Problem q = p;
         q.ch_base = c0;
         q.nch_fixed = c1 - c0;
+        q.group_len = c1 - c0;
         q.slots = p.slots + (size_t)p.N * c0 * p.H * SLOT_BYTES;
         q.init = i == 0 ? init0 : st;
         q.fin = i < pieces - 1 ? st : (bf16 ? (p.fin ? st : nullptr) : p.fin);
@@ -438,6 +537,12 @@ kda_status_t run(const void *q, const void *k, const void *v, const void *g, con
     p.variant = variant;
     p.slots = ws + header_bytes(N, T, H, varlen);
     // the measurement variants keep the single-launch schedule
+    if (!varlen && variant == 0 && !single_launch) {
+        const int groups = scan_groups(N, T, H, false);
+        if (groups > 1)
+            return run_scan(p, groups, state_kind(initial_state, final_state, state_dtype), state_dtype, ws, stream) ==
+                           cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     if (piece_mode(N, T, H, varlen) && variant == 0 && !single_launch) {
         int pieces = 0;
         if (pieces_on_device(N, T, H, false, &pieces) != cudaSuccess)
@@ -491,6 +596,14 @@ extern "C" int kda_fwd_pieces(int N, int64_t T, int H, int varlen)
         return 0;
     int pieces = 0;
     return pieces_on_device(N, T, H, varlen != 0, &pieces) == cudaSuccess ? pieces : 0;
+}
+
+extern "C" int kda_fwd_scan_groups(int N, int64_t T, int H, int varlen)
+{
+    if (N < 1 || H < 1 || T < 0 || T > ((int64_t)1 << 40) || (int64_t)N * H > INT32_MAX ||
+        check_size(N, T, H, varlen != 0) != KDA_OK)
+        return 0;
+    return scan_groups(N, T, H, varlen != 0);
 }
 
 extern "C" kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,

@@ -72,6 +72,12 @@ struct Problem {
     int64_t T;
     int64_t nch_fixed;        // without cu_seqlens: chunks of each sequence in this launch
     int64_t ch_base;          // without cu_seqlens: first chunk of this launch within each sequence
+    // chunk-transition scan (fixed length): the recurrence kernel runs `groups` groups of group_len chunks
+    // of every sequence side by side (group_len = nch_fixed and groups = 1 otherwise)
+    int groups;
+    int64_t group_len;
+    float *sc_a, *sc_b;       // compose launches: each group's transition, [groups - 1][N][H][128][128] fp32
+    const float *sc_s;        // grouped launches: start states of groups 1 .. groups - 1, same layout
     int prep_pf;              // prep: each CTA prefetches its next item's rows into L2 (0: off)
     int64_t chunk_cap;        // varlen: entries of the per-chunk table (every sequence's chunks are clamped to it)
     uint32_t wait_polls;      // chunked kernels: polls of a wait before it gives up (kda_set_wait_limit)

@@ -45,8 +45,15 @@ cudaError_t launch_prep(const Problem &p, int64_t max_chunks, cudaStream_t strea
                         bool early = false);
 // Elementwise bf16 <-> fp32 conversion of n values on `stream` (to_f32: bf16 src to fp32 dst).
 cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cudaStream_t stream);
-// Recurrence kernel over N x H (sequence, head) pairs; state_kind 0 none, 1 bf16, 2 fp32.
+// Recurrence kernel over N x H (sequence, head) pairs (x p.groups without cu_seqlens); state_kind 0 none,
+// 1 bf16, 2 fp32.
 cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream);
+// The chunk-transition scan: each group's transition (recurrence kernel, compose form; groups 0 .. p.groups - 2
+// into p.sc_a / p.sc_b), then the group start states, serially over the groups (p.sc_s, from the fp32 initial
+// state init0 or zeros).
+cudaError_t launch_compose(const Problem &p, cudaStream_t stream);
+cudaError_t launch_scan_states(const float *init0, const float *a, const float *b, float *s, int pairs, int groups,
+                               cudaStream_t stream);
 // Token-recurrent kernel, persistent over the N x H x 2 (sequence, head, value half) items; no workspace.
 cudaError_t launch_recurrent(const Problem &p, int state_kind, cudaStream_t stream);
 size_t recurrent_smem_bytes();

@@ -106,7 +106,14 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // STATE: 0 none, 1 bf16, 2 fp32.  BSTATE: the measurement variant that keeps the state in bf16 between chunks
 // (rounded to nearest at each chunk boundary, as the guancyxx.cn FlashKDA article's design does, section 2.3);
 // the default keeps the fp32 accumulator as the state.
-template <int STATE, bool VARLEN, bool BSTATE>
+//
+// Fixed length, p.groups > 1 (the chunk-transition scan): CTA (group g, sequence n, head h) runs chunks
+// g group_len .. of sequence n from the start state of group g (the initial state for g = 0, else sc_s) and
+// stores a final state for the last group only.  COMPOSE: the scan's first level, two CTAs per (group, n, h)
+// and no outputs: the group's chunks map a start state S to M S + B (M = the product of the chunks'
+// Diag(Gamma_C) - K~^T W, B = the state reached from S = 0); tile 0 runs from S = I with U0 taken as 0 and
+// leaves M, tile 1 runs from S = 0 and leaves B, both stored transposed like a state (sc_a / sc_b).
+template <int STATE, bool VARLEN, bool BSTATE, bool COMPOSE>
 __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 {
     extern __shared__ __align__(128) unsigned char sm[];
@@ -115,10 +122,26 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     asm volatile("griddepcontrol.launch_dependents;");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
-    const int h = blockIdx.x % H;
-    int n = blockIdx.x / H;
+    const int tile = COMPOSE ? (int)(blockIdx.x & 1u) : 0;
+    const int cta = COMPOSE ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int NH = p.N * H;
+    const int grp = VARLEN ? 0 : cta / NH;   // group of the scan (0 without one)
+    const int pr = cta - grp * NH;
+    const int h = pr % H;
+    int n = pr / H;
     if (VARLEN && p.order)
         n = p.order[n];   // longest sequences first
+    // the state this CTA starts from and the one it leaves (fp32 in the scan's launches)
+    const void *init = p.init;
+    void *fin = p.fin;
+    if (!VARLEN && grp > 0)
+        init = p.sc_s + (size_t)(grp - 1) * NH * D * D;
+    if (!VARLEN && grp < p.groups - 1)
+        fin = nullptr;
+    if (COMPOSE) {
+        init = nullptr;
+        fin = (tile ? p.sc_b : p.sc_a) + (size_t)grp * NH * D * D;
+    }
     int64_t bos, len, slot0;
     if (VARLEN) {
         seq_range(p.cu, n, p.N, p.T, bos, len);   // clamped into [0, T]; the plan flags a malformed cu_seqlens
@@ -127,10 +150,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         if (usable * CH < len)
             len = usable * CH;   // only a malformed cu_seqlens gets here: chunks past the table are skipped
     } else {
-        // chunks ch_base .. ch_base + nch_fixed - 1 of the sequence (all of them unless the call runs in pieces)
-        bos = (int64_t)n * p.T + p.ch_base * CH;
-        len = p.T - p.ch_base * CH < p.nch_fixed * CH ? p.T - p.ch_base * CH : p.nch_fixed * CH;
-        slot0 = (int64_t)n * p.nch_fixed;
+        // chunks cb .. cb + group_len - 1 of the sequence (all of them unless the call runs in pieces or groups)
+        const int64_t cb = p.ch_base + (int64_t)grp * p.group_len;
+        bos = (int64_t)n * p.T + cb * CH;
+        len = p.T - cb * CH < p.group_len * CH ? p.T - cb * CH : p.group_len * CH;
+        if (len < 0)
+            len = 0;
+        slot0 = (int64_t)n * p.nch_fixed + (int64_t)grp * p.group_len;
     }
     const int nch = (int)((len + CH - 1) / CH);
 
@@ -189,8 +215,12 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
         uint32_t u[32];
-        if (STATE == 2 && p.init) {
-            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(p.init) + srow + 32 * part);
+        if (COMPOSE && tile == 0) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                u[e] = half * 64 + 32 * part + e == vrow ? 0x3f800000u : 0u;   // S = I
+        } else if (STATE == 2 && init) {
+            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(init) + srow + 32 * part);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float4 x = src[e];
@@ -199,9 +229,9 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                 u[4 * e + 2] = __float_as_uint(x.z);
                 u[4 * e + 3] = __float_as_uint(x.w);
             }
-        } else if (STATE == 1 && p.init) {
+        } else if (STATE == 1 && init) {
             const uint4 *src =
-                reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.init) + srow + 32 * part);
+                reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(init) + srow + 32 * part);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const uint4 x = src[e];
@@ -303,7 +333,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             for (int e = 0; e < 64; ++e)
                 u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[e]);
             tmem_st64_nw(trow + TM_S + half * 64, u);
-            if (c > 0)
+            if (!COMPOSE && c > 0)
                 write_out(ost, o);
             tmem_wait_st();
         }
@@ -321,11 +351,12 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 #pragma unroll
             for (int s = 0; s < D / 16; ++s)
                 mma_f16_ts(tbase + TM_X, tbase + TM_S16 + 8 * s,
-                           umma_desc(s_buf + SLOT_QW + s * 2 * CORE_LBO, CORE_LBO, QW_SBO), idesc_f16(128, 128), s > 0);
+                           umma_desc(s_buf + SLOT_QW + s * 2 * CORE_LBO, CORE_LBO, QW_SBO),
+                           idesc_f16(128, COMPOSE ? CH : 128), s > 0);   // [W ; Q~] rows (W only: no outputs)
             umma_commit(mbarQ);
         }
         ++nq;
-        if (c > 0)
+        if (!COMPOSE && c > 0)
             store_out(ost, prev_tok0, prev_L);
 
         // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
@@ -344,7 +375,9 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
+                    float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
+                if (COMPOSE && tile == 0)
+                    f = make_float2(0.f, 0.f);   // the linear part: U = -X
                     hv[4 * m + e] = pack_half2(f.x - __uint_as_float(x[8 * m + 2 * e]),
                                                f.y - __uint_as_float(x[8 * m + 2 * e + 1]));
                 }
@@ -361,8 +394,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                mma_f16_ts(tbase + TM_O, tbase + TM_U16 + 8 * s,
-                           umma_desc(s_buf + SLOT_KA + s * 2 * CORE_LBO, CORE_LBO, KA_SBO), idesc_f16(128, 64 + D), 1);
+                if (COMPOSE)   // the state update alone: B = the K~^T rows of KA (rows 64 ..)
+                    mma_f16_ts(tbase + TM_S, tbase + TM_U16 + 8 * s,
+                               umma_desc(s_buf + SLOT_KA + (CH / 8) * KA_SBO + s * 2 * CORE_LBO, CORE_LBO, KA_SBO),
+                               idesc_f16(128, D), 1);
+                else
+                    mma_f16_ts(tbase + TM_O, tbase + TM_U16 + 8 * s,
+                               umma_desc(s_buf + SLOT_KA + s * 2 * CORE_LBO, CORE_LBO, KA_SBO), idesc_f16(128, 64 + D), 1);
             umma_commit(mbarB);
         }
         ++nb;
@@ -381,7 +419,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         const bool ok = mbar_wait(mbarB, (nch - 1) & 1, p.wait_polls);
         if (__syncthreads_or(!ok)) {
             hung = true;
-        } else {
+        } else if (!COMPOSE) {
             tc_fence_after();
             read_out(buf_of(nch - 1) + SLOT_HEAD);
             __syncthreads();
@@ -416,14 +454,14 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 bad |= !(fabsf(__uint_as_float(u[e])) <= 3.402823466e38f);
-            if (STATE == 2 && p.fin) {
-                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.fin) + srow + 32 * part);
+            if (STATE == 2 && fin) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(fin) + srow + 32 * part);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
                                          __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
-            } else if (STATE == 1 && p.fin) {
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.fin) + srow + 32 * part);
+            } else if (STATE == 1 && fin) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(fin) + srow + 32 * part);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     uint32_t w4[4];
@@ -448,7 +486,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     }
 }
 
-template <int STATE, bool VARLEN, bool BSTATE>
+template <int STATE, bool VARLEN, bool BSTATE, bool COMPOSE>
 cudaError_t launch_recur_t(const Problem &p, int grid, cudaStream_t stream)
 {
     static bool configured[64] = {};
@@ -457,14 +495,16 @@ cudaError_t launch_recur_t(const Problem &p, int grid, cudaStream_t stream)
     if (err != cudaSuccess)
         return err;
     if (dev >= 64 || !configured[dev]) {
-        err = cudaFuncSetAttribute(kda_recur_kernel<STATE, VARLEN, BSTATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   RECUR_SMEM);
+        err = cudaFuncSetAttribute(kda_recur_kernel<STATE, VARLEN, BSTATE, COMPOSE>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, RECUR_SMEM);
         if (err != cudaSuccess)
             return err;
         if (dev < 64)
             configured[dev] = true;
     }
-    kda_recur_kernel<STATE, VARLEN, BSTATE><<<grid, RT, RECUR_SMEM, stream>>>(p);
+    if (grid <= 0)
+        return cudaSuccess;
+    kda_recur_kernel<STATE, VARLEN, BSTATE, COMPOSE><<<grid, RT, RECUR_SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -473,12 +513,13 @@ cudaError_t launch_recur_b(const Problem &p, int state_kind, cudaStream_t stream
 {
     const int grid = p.N * p.H;
     if (p.cu)
-        return state_kind == 2 ? launch_recur_t<2, true, BSTATE>(p, grid, stream)
-             : state_kind == 1 ? launch_recur_t<1, true, BSTATE>(p, grid, stream)
-                               : launch_recur_t<0, true, BSTATE>(p, grid, stream);
-    return state_kind == 2 ? launch_recur_t<2, false, BSTATE>(p, grid, stream)
-         : state_kind == 1 ? launch_recur_t<1, false, BSTATE>(p, grid, stream)
-                           : launch_recur_t<0, false, BSTATE>(p, grid, stream);
+        return state_kind == 2 ? launch_recur_t<2, true, BSTATE, false>(p, grid, stream)
+             : state_kind == 1 ? launch_recur_t<1, true, BSTATE, false>(p, grid, stream)
+                               : launch_recur_t<0, true, BSTATE, false>(p, grid, stream);
+    const int fgrid = grid * p.groups;
+    return state_kind == 2 ? launch_recur_t<2, false, BSTATE, false>(p, fgrid, stream)
+         : state_kind == 1 ? launch_recur_t<1, false, BSTATE, false>(p, fgrid, stream)
+                           : launch_recur_t<0, false, BSTATE, false>(p, fgrid, stream);
 }
 
 }  // namespace
@@ -487,6 +528,11 @@ cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream)
 {
     return (p.variant & VARIANT_BF16_STATE) ? launch_recur_b<true>(p, state_kind, stream)
                                             : launch_recur_b<false>(p, state_kind, stream);
+}
+
+cudaError_t launch_compose(const Problem &p, cudaStream_t stream)
+{
+    return launch_recur_t<2, false, false, true>(p, 2 * (p.groups - 1) * p.N * p.H, stream);
 }
 
 size_t recur_smem_bytes() { return RECUR_SMEM; }

@@ -107,7 +107,15 @@ typedef enum {
  * token, as kda_fwd_recurrent does (same kernels, same bits, no workspace); everything else
  * takes the chunked form.
  *
- * Fixed-length problems with N x H <= 64 (sequence, head) pairs and at least 32 chunks of 64
+ * Fixed-length problems with N x H <= 16 pairs and at least 32 chunks per sequence replace the
+ * serial chain of the recurrence by a scan along T when its cost model says it is faster
+ * (kda_fwd_scan_groups): the chunks of each pair are cut into G groups; the transition of every
+ * group (the affine map S -> M S + B its chunks apply to the state) is formed in parallel, the
+ * groups' start states follow serially in fp32 (G - 1 steps of S <- M S + B), and the groups then
+ * run in parallel from them.  The results are not the same bits as the serial chain (a different
+ * order of operations) but within the same tolerances.
+ *
+ * Otherwise, fixed-length problems with N x H <= 64 (sequence, head) pairs and at least 32 chunks of 64
  * tokens per sequence run in up to 8 pieces of whole chunks along T (more for longer sequences
  * and fewer pairs; at least 16 chunks each), all on `stream`: the prep kernel
  * of the next piece is launched as a programmatic dependent of the recurrence over the current
@@ -141,6 +149,15 @@ size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen);
 int kda_fwd_pieces(int N, int64_t T, int H, int varlen);
 
 /*
+ * Number of groups G of the chunk-transition scan along T in which kda_fwd, kda_fwd_ws and
+ * kda_fwd_noalloc run a problem of this size (see kda_fwd): 1 when the recurrence runs as one serial
+ * chain per (sequence, head) pair, 2 to 16 otherwise.  Depends on N, T, H and varlen only (the
+ * workspace holds the scan's matrices: (1 + 3 (G - 1)) x N x H x 64 KiB ahead of the operand slots).
+ * 0 for invalid sizes.  Launches nothing.
+ */
+int kda_fwd_scan_groups(int N, int64_t T, int H, int varlen);
+
+/*
  * kda_fwd_ws -- kda_fwd with a caller-owned device workspace of at least
  * kda_fwd_workspace_size(N, T, H, cu_seqlens != NULL) bytes, 256-byte aligned (it may be
  * NULL when that size is 0).  The workspace must not be used by anything else until the
@@ -158,8 +175,9 @@ kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void 
  * boundaries, for timing the two kernels separately: stage_events[0] right before the prep
  * kernel (after the varlen plan), [1] between the prep and recurrence kernels, [2] after the
  * recurrence kernel.  stage_events points to 3 cudaEvent_t handles (any may be NULL).  The
- * prep kernel always runs over every chunk before the recurrence starts, all on `stream`, also
- * for the problems that kda_fwd_ws runs in pieces; the results are exactly those of kda_fwd_ws.
+ * prep kernel always runs over every chunk before the recurrence starts, all on `stream`, and the
+ * recurrence runs as one serial chain per pair, also for the problems that kda_fwd_ws runs in pieces
+ * (same results, bit for bit) or with the scan along T (results within the same tolerances).
  */
 kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, const void *g, const void *beta,
                                  float scale, void *out, const float *A_log, const float *dt_bias,

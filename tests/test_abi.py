@@ -107,9 +107,9 @@ def test_workspace_size(lib):
     assert lib.kda_fwd_workspace_size(1, 8192, 96, 0) == 128 * 96 * slot
     assert lib.kda_fwd_workspace_size(1, 8192, 64, 0) == 64 * state + 128 * 64 * slot
     assert lib.kda_fwd_workspace_size(2, 4096, 32, 0) == 64 * state + 2 * 64 * 32 * slot
-    assert lib.kda_fwd_workspace_size(1, 2049, 3, 0) == 3 * state + 33 * 3 * slot
-    assert lib.kda_fwd_workspace_size(1, 1985, 3, 0) == 3 * state + 32 * 3 * slot
-    assert lib.kda_fwd_workspace_size(1, 1984, 3, 0) == 31 * 3 * slot
+    assert lib.kda_fwd_workspace_size(1, 2049, 40, 0) == 40 * state + 33 * 40 * slot
+    assert lib.kda_fwd_workspace_size(1, 1985, 40, 0) == 40 * state + 32 * 40 * slot
+    assert lib.kda_fwd_workspace_size(1, 1984, 40, 0) == 31 * 40 * slot
     assert lib.kda_fwd_workspace_size(1, 8192, 65, 0) == 128 * 65 * slot
     assert lib.kda_fwd_workspace_size(2, 65, 3, 0) == 2 * 2 * 3 * slot
     assert lib.kda_fwd_workspace_size(1, 0, 4, 0) == 0
@@ -123,6 +123,23 @@ def test_workspace_size(lib):
     assert lib.kda_fwd_workspace_size(256, 1, 96, 0) == 0
     assert lib.kda_fwd_workspace_size(256, 4, 96, 0) == 0
     assert lib.kda_fwd_workspace_size(256, 5, 96, 0) == 256 * 96 * slot
+
+
+def test_scan_groups_and_workspace(lib):
+    slot, state = 74240, 128 * 128 * 4
+    # the scan along T: at most 16 (sequence, head) pairs, at least 32 chunks, when the cost model prefers it;
+    # the count depends on N, T, H only
+    assert lib.kda_fwd_scan_groups(2, 8200, 8, 0) == 9      # 129 chunks: 9 groups of 15 (the last 9)
+    assert lib.kda_fwd_scan_groups(1, 2049, 3, 0) == 7      # 33 chunks: 7 groups of 5 (the last 3)
+    assert lib.kda_fwd_scan_groups(1, 32768, 8, 0) == 16
+    assert lib.kda_fwd_scan_groups(1, 8192, 17, 0) == 1     # more than 16 pairs
+    assert lib.kda_fwd_scan_groups(1, 1984, 1, 0) == 1      # fewer than 32 chunks
+    assert lib.kda_fwd_scan_groups(8, 8192, 1, 1) == 1      # varlen
+    assert lib.kda_fwd_scan_groups(0, 100, 1, 0) == 0
+    # scan problems run without pieces; their header: initial state, then M, B and start states of G - 1 groups
+    assert lib.kda_fwd_pieces(2, 8200, 8, 0) == 1
+    assert lib.kda_fwd_workspace_size(2, 8200, 8, 0) == (1 + 3 * 8) * 16 * state + 2 * 129 * 8 * slot
+    assert lib.kda_fwd_workspace_size(1, 2049, 3, 0) == (1 + 3 * 6) * 3 * state + 33 * 3 * slot
 
 
 def test_pieces_query_without_pieces(lib):

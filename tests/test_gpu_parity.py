@@ -231,12 +231,12 @@ def test_caller_workspace_matches_pool_workspace(varlen):
 
 
 # (B, T, H) -> pieces on a 152-SM GB300
-PIECE_SHAPES = {(2, 8200, 8): 2, (1, 4097, 40): 2, (1, 32768, 24): 6}
+PIECE_SHAPES = {(1, 8200, 24): 3, (1, 4097, 40): 2, (1, 32768, 24): 6}
 
 
 @pytest.mark.parametrize("B,T,H,state,with_initial", [
-    (2, 8200, 8, STATE_NONE, False), (2, 8200, 8, STATE_BF16, True), (2, 8200, 8, STATE_BF16, False),
-    (2, 8200, 8, STATE_FP32, True), (2, 8200, 8, STATE_FP32, False), (1, 4097, 40, STATE_BF16, True),
+    (1, 8200, 24, STATE_NONE, False), (1, 8200, 24, STATE_BF16, True), (1, 8200, 24, STATE_BF16, False),
+    (1, 8200, 24, STATE_FP32, True), (1, 8200, 24, STATE_FP32, False), (1, 4097, 40, STATE_BF16, True),
     (1, 32768, 24, STATE_FP32, True)])
 def test_pieces_match_single_launch(B, T, H, state, with_initial):
     """Long fixed-length problems on few (sequence, head) pairs run in pieces along T (the next piece's prep
@@ -277,8 +277,60 @@ def test_pieces_match_single_launch(B, T, H, state, with_initial):
 def test_pieces_in_place_state(state):
     """In pieces, an initial state updated in place (final_state = initial_state) gives the oracle's result."""
     from gated_delta_rule_23_gb300 import _native
-    assert _native.load().kda_fwd_pieces(2, 8200, 8, 0) >= 2
-    p = make_problem(B=2, T=8200, H=8, seed=24, state_dtype=state)
+    assert _native.load().kda_fwd_pieces(1, 8200, 24, 0) >= 2
+    p = make_problem(B=1, T=8200, H=24, seed=24, state_dtype=state)
+    out, fin = run_gpu(p, inplace=True)
+    assert_parity(out, fin, *oracle_run(p))
+
+
+@pytest.mark.parametrize("B,T,H,state,with_initial", [
+    (2, 8200, 8, STATE_NONE, False), (2, 8200, 8, STATE_BF16, True), (2, 8200, 8, STATE_BF16, False),
+    (2, 8200, 8, STATE_FP32, True), (2, 8200, 8, STATE_FP32, False), (1, 2049, 3, STATE_FP32, True),
+    (1, 32768, 8, STATE_BF16, True), (2, 30000, 1, STATE_FP32, True)])
+def test_scan_along_t_matches_oracle(B, T, H, state, with_initial):
+    """Few (sequence, head) pairs and long sequences take the chunk-transition scan along T (groups composed in
+    parallel, their start states chained in fp32, the groups run in parallel): within the parity tolerances
+    of the oracle, close to the serial chain of kda_fwd_ws_profiled, for every state kind and 7 to 16
+    groups with ragged last groups and chunks; and work that the caller enqueues on the same stream after
+    the call sees the finished results."""
+    from gated_delta_rule_23_gb300 import _native, workspace_size
+    lib = _native.load()
+    groups = lib.kda_fwd_scan_groups(B, T, H, 0)
+    assert groups >= 7 and lib.kda_fwd_pieces(B, T, H, 0) == 1
+    p = make_problem(B=B, T=T, H=H, seed=25, state_dtype=state, with_initial=with_initial)
+    dev = to_device(p)
+    ws = torch.empty(workspace_size(p.N, p.T, p.H, False), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    results = []
+    for kw in ({"workspace": ws}, {}, {"workspace": ws, "stage_events": [None, None, None]}):
+        out = torch.empty_like(dev["q"])
+        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda") if dev["sdt"] is not None else None
+        torch.cuda.synchronize()
+        _call(p, dev, out, fin, stream=s, **kw)
+        with torch.cuda.stream(s):
+            out_c = out.clone()
+            fin_c = fin.clone() if fin is not None else None
+        s.synchronize()
+        assert torch.equal(out_c, out) and (fin is None or torch.equal(fin_c, fin))
+        results.append((out.float().cpu().numpy(), None if fin is None else fin.float().cpu().numpy()))
+    # the caller's and the pool's workspace: the same schedule, the same bits
+    assert np.array_equal(results[0][0], results[1][0])
+    assert results[0][1] is None or np.array_equal(results[0][1], results[1][1])
+    o_ref, f_ref = oracle_run(p)
+    r_scan = assert_parity(results[0][0], results[0][1], o_ref, f_ref)
+    r_serial = assert_parity(results[2][0], results[2][1], o_ref, f_ref)
+    # the scan's extra rounding stays small against the tolerance
+    assert r_scan["out_rel_l2"] <= 1.5 * r_serial["out_rel_l2"] + 5e-4, (r_scan, r_serial)
+    print(f"groups {groups}: scan {r_scan} serial {r_serial}")
+
+
+@pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
+def test_scan_in_place_state(state):
+    """With the scan, an initial state updated in place (final_state = initial_state) gives the oracle's result:
+    the last group's final state may not overwrite the initial state before the other groups have read it."""
+    from gated_delta_rule_23_gb300 import _native
+    assert _native.load().kda_fwd_scan_groups(2, 8200, 8, 0) >= 2
+    p = make_problem(B=2, T=8200, H=8, seed=26, state_dtype=state)
     out, fin = run_gpu(p, inplace=True)
     assert_parity(out, fin, *oracle_run(p))
 
