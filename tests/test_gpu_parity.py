@@ -202,6 +202,11 @@ def _call(p, dev, out, fin, **kw):
             p.lower_bound, initial_state=dev["init"], final_state=fin, cu_seqlens=dev["cu"], **kw)
 
 
+def _fresh(shape, dtype):
+    """An output buffer filled with NaN, so that a call that writes nothing cannot pass on stale memory."""
+    return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
+
+
 @pytest.mark.parametrize("varlen", [False, True])
 def test_caller_workspace_matches_pool_workspace(varlen):
     """kda_fwd_ws (caller-owned workspace, reused twice) and kda_fwd_ws_profiled give the same bits as kda_fwd."""
@@ -238,7 +243,8 @@ PIECE_SHAPES = {(1, 8200, 24): 3, (1, 4097, 40): 2, (1, 32768, 24): 6}
     (1, 8200, 24, STATE_NONE, False), (1, 8200, 24, STATE_BF16, True), (1, 8200, 24, STATE_BF16, False),
     (1, 8200, 24, STATE_FP32, True), (1, 8200, 24, STATE_FP32, False), (1, 4097, 40, STATE_BF16, True),
     (1, 32768, 24, STATE_FP32, True)])
-def test_pieces_match_single_launch(B, T, H, state, with_initial):
+@pytest.mark.parametrize("lb", [-5.0, -0.05])
+def test_pieces_match_single_launch(B, T, H, state, with_initial, lb):
     """Long fixed-length problems on few (sequence, head) pairs run in pieces along T (the next piece's prep
     kernel launched beside the recurrence over the current one): the same bits as the single-launch schedule
     of kda_fwd_ws_profiled, for every state kind, with 2 to 6 pieces and ragged last chunks; and work that
@@ -248,7 +254,7 @@ def test_pieces_match_single_launch(B, T, H, state, with_initial):
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
         assert pieces == PIECE_SHAPES[(B, T, H)]
     assert pieces >= 2
-    p = make_problem(B=B, T=T, H=H, seed=23, state_dtype=state, with_initial=with_initial)
+    p = make_problem(B=B, T=T, H=H, seed=23, state_dtype=state, with_initial=with_initial, lower_bound=lb)
     dev = to_device(p)
     ws = torch.empty(workspace_size(p.N, p.T, p.H, False), dtype=torch.uint8, device="cuda")
     nch = -(-T // 64)
@@ -256,8 +262,8 @@ def test_pieces_match_single_launch(B, T, H, state, with_initial):
     s = torch.cuda.Stream()
     results = []
     for kw in ({"workspace": ws, "stage_events": [None, None, None]}, {"workspace": ws}, {}):
-        out = torch.empty_like(dev["q"])
-        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda") if dev["sdt"] is not None else None
+        out = _fresh(dev["q"].shape, torch.bfloat16)
+        fin = _fresh((p.N, p.H, 128, 128), dev["sdt"]) if dev["sdt"] is not None else None
         torch.cuda.synchronize()
         _call(p, dev, out, fin, stream=s, **kw)
         with torch.cuda.stream(s):   # ordered after the call on s only
@@ -278,33 +284,36 @@ def test_pieces_in_place_state(state):
     """In pieces, an initial state updated in place (final_state = initial_state) gives the oracle's result."""
     from gated_delta_rule_23_gb300 import _native
     assert _native.load().kda_fwd_pieces(1, 8200, 24, 0) >= 2
-    p = make_problem(B=1, T=8200, H=24, seed=24, state_dtype=state)
+    p = make_problem(B=1, T=8200, H=24, seed=24, state_dtype=state, lower_bound=-0.05)
     out, fin = run_gpu(p, inplace=True)
     assert_parity(out, fin, *oracle_run(p))
 
 
-@pytest.mark.parametrize("B,T,H,state,with_initial", [
-    (2, 8200, 8, STATE_NONE, False), (2, 8200, 8, STATE_BF16, True), (2, 8200, 8, STATE_BF16, False),
-    (2, 8200, 8, STATE_FP32, True), (2, 8200, 8, STATE_FP32, False), (1, 2049, 3, STATE_FP32, True),
-    (1, 32768, 8, STATE_BF16, True), (2, 30000, 1, STATE_FP32, True)])
-def test_scan_along_t_matches_oracle(B, T, H, state, with_initial):
+@pytest.mark.parametrize("B,T,H,state,with_initial,lb", [
+    (2, 8200, 8, STATE_NONE, False, -5.0), (2, 8200, 8, STATE_BF16, True, -5.0), (2, 8200, 8, STATE_FP32, True, -5.0),
+    (2, 8200, 8, STATE_NONE, False, -0.05), (2, 8200, 8, STATE_BF16, True, -0.05), (2, 8200, 8, STATE_BF16, False, -0.05),
+    (2, 8200, 8, STATE_FP32, True, -0.05), (2, 8200, 8, STATE_FP32, False, 0.0), (1, 2049, 3, STATE_FP32, True, -0.05),
+    (1, 32768, 8, STATE_BF16, True, -0.05), (2, 30000, 1, STATE_FP32, True, 0.0)])
+def test_scan_along_t_matches_oracle(B, T, H, state, with_initial, lb):
     """Few (sequence, head) pairs and long sequences take the chunk-transition scan along T (groups composed in
     parallel, their start states chained in fp32, the groups run in parallel): within the parity tolerances
-    of the oracle, close to the serial chain of kda_fwd_ws_profiled, for every state kind and 7 to 16
+    of the oracle and close to the serial chain of kda_fwd_ws_profiled, for every state kind and 7 to 16
     groups with ragged last groups and chunks; and work that the caller enqueues on the same stream after
-    the call sees the finished results."""
+    the call sees the finished results.  With lower_bound = -5 the state forgets a chunk's start within the
+    chunk (its decay underflows), so each group's transition is exactly zero and the scan gives the serial
+    chain's bits; with -0.05 and 0 (no decay) the state carries across many chunks and groups."""
     from gated_delta_rule_23_gb300 import _native, workspace_size
     lib = _native.load()
     groups = lib.kda_fwd_scan_groups(B, T, H, 0)
     assert groups >= 7 and lib.kda_fwd_pieces(B, T, H, 0) == 1
-    p = make_problem(B=B, T=T, H=H, seed=25, state_dtype=state, with_initial=with_initial)
+    p = make_problem(B=B, T=T, H=H, seed=25, state_dtype=state, with_initial=with_initial, lower_bound=lb)
     dev = to_device(p)
     ws = torch.empty(workspace_size(p.N, p.T, p.H, False), dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
     results = []
     for kw in ({"workspace": ws}, {}, {"workspace": ws, "stage_events": [None, None, None]}):
-        out = torch.empty_like(dev["q"])
-        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda") if dev["sdt"] is not None else None
+        out = _fresh(dev["q"].shape, torch.bfloat16)
+        fin = _fresh((p.N, p.H, 128, 128), dev["sdt"]) if dev["sdt"] is not None else None
         torch.cuda.synchronize()
         _call(p, dev, out, fin, stream=s, **kw)
         with torch.cuda.stream(s):
@@ -319,9 +328,12 @@ def test_scan_along_t_matches_oracle(B, T, H, state, with_initial):
     o_ref, f_ref = oracle_run(p)
     r_scan = assert_parity(results[0][0], results[0][1], o_ref, f_ref)
     r_serial = assert_parity(results[2][0], results[2][1], o_ref, f_ref)
-    # the scan's extra rounding stays small against the tolerance
+    # the scan's own rounding stays small against the tolerance
     assert r_scan["out_rel_l2"] <= 1.5 * r_serial["out_rel_l2"] + 5e-4, (r_scan, r_serial)
-    print(f"groups {groups}: scan {r_scan} serial {r_serial}")
+    if lb == -5.0:
+        assert np.array_equal(results[0][0], results[2][0])
+    print(f"groups {groups} lb {lb}: scan {r_scan} serial {r_serial} "
+          f"scan-serial out rel-L2 {rel_l2(results[0][0], results[2][0]):.3e}")
 
 
 @pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
@@ -330,7 +342,7 @@ def test_scan_in_place_state(state):
     the last group's final state may not overwrite the initial state before the other groups have read it."""
     from gated_delta_rule_23_gb300 import _native
     assert _native.load().kda_fwd_scan_groups(2, 8200, 8, 0) >= 2
-    p = make_problem(B=2, T=8200, H=8, seed=26, state_dtype=state)
+    p = make_problem(B=2, T=8200, H=8, seed=26, state_dtype=state, lower_bound=-0.05)
     out, fin = run_gpu(p, inplace=True)
     assert_parity(out, fin, *oracle_run(p))
 
