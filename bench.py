@@ -452,6 +452,8 @@ def run_ours(args, p, idx, rank, world):
     if args.kernel_only:
         if rank == 0:
             print(json.dumps({"kernel_only": True, "ms_per_step": ms_step, "T": p.T, "H": p.H,
+                              "pieces_per_step": pieces_per_step(p), "scan_groups_per_step": scan_groups_per_step(p),
+                              "launches_per_step": launches_per_step(p),
                               "algorithmic_bytes_per_launch": algorithmic_bytes(p), "kernel_ms": kernel_ms,
                               "variant_ms": variant_ms}),
                   flush=True)
@@ -588,6 +590,9 @@ def main():
     ap.add_argument("--workload", type=int, default=2, help="0-4; 2 = T=8192 H=96 fixed length")
     ap.add_argument("--T", type=int, default=None,
                     help="profiling aid: shorten a fixed-length workload to T tokens (not a bench line)")
+    ap.add_argument("--shape", default=None,
+                    help="profiling aid: T:H, a fixed-length problem of T tokens and H heads (B = 1) with workload 1's "
+                         "value distributions, no initial state and an fp32 final state (not a bench line)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="profiling aid: time only the device launches (no e2e, CPU baseline or clock sampling)")
     ap.add_argument("--decode-only", action="store_true",
@@ -618,6 +623,13 @@ def main():
                                             n_seq=args.decode_N, T=args.decode_T)), flush=True)
         return
     p = make_workload(args.workload)
+    if args.shape is not None:
+        if not args.kernel_only:
+            raise SystemExit("--shape is a profiling aid: use it with --kernel-only")
+        from gated_delta_rule_23_gb300.inputs import make_problem
+        T_, H_ = (int(x) for x in args.shape.split(":"))
+        p = make_problem(B=1, T=T_, H=H_, seed=1, state_dtype=STATE_FP32, with_initial=False,
+                         name=f"fixed-length T={T_} H={H_}")
     if args.T is not None:
         if p.cu_seqlens is not None:
             raise SystemExit("--T applies to fixed-length workloads only")
