@@ -93,24 +93,30 @@ __global__ void __launch_bounds__(PLAN_THREADS) kda_plan_kernel(const int64_t *c
         chunk_info[c] = make_longlong2(0, 0);
     if (order) {
         // longest-first order: a bitonic sort (descending) of the keys length * 4096 + (4095 - index) in shared
-        // memory, padded with -1 to LPT_MAX_SEQS entries; ties keep the lower index first.  Each of the 66 stages
-        // is one compare-exchange per thread (LPT_MAX_SEQS / 2 = PLAN_THREADS pairs).
+        // memory, padded with -1 to m entries (the power of two from N up, at most LPT_MAX_SEQS); ties keep the
+        // lower index first.  Each of the log2(m) (log2(m) + 1) / 2 stages is one compare-exchange in each of the
+        // first m / 2 threads.
         static_assert(LPT_MAX_SEQS == 2 * PLAN_THREADS && LPT_MAX_SEQS <= 4096, "bitonic sort layout");
         __shared__ int64_t keys[LPT_MAX_SEQS];
-        for (int s = tid; s < LPT_MAX_SEQS; s += PLAN_THREADS) {
+        int m = 2;
+        while (m < N)
+            m <<= 1;
+        for (int s = tid; s < m; s += PLAN_THREADS) {
             int64_t bs, ls = -1;
             if (s < N)
                 seq_range(cu, s, N, T, bs, ls);
             keys[s] = s < N ? ls * 4096 + (4095 - s) : -1;
         }
         __syncthreads();
-        for (int k = 2; k <= LPT_MAX_SEQS; k <<= 1)
+        for (int k = 2; k <= m; k <<= 1)
             for (int j = k >> 1; j > 0; j >>= 1) {
-                const int i = 2 * j * (tid / j) + (tid % j), ixj = i + j;
-                const int64_t x = keys[i], y = keys[ixj];
-                if ((i & k) == 0 ? x < y : x > y) {
-                    keys[i] = y;
-                    keys[ixj] = x;
+                if (tid < (m >> 1)) {
+                    const int i = 2 * j * (tid / j) + (tid % j), ixj = i + j;
+                    const int64_t x = keys[i], y = keys[ixj];
+                    if ((i & k) == 0 ? x < y : x > y) {
+                        keys[i] = y;
+                        keys[ixj] = x;
+                    }
                 }
                 __syncthreads();
             }
@@ -169,17 +175,17 @@ int piece_count(int64_t nch, int64_t pairs, int nsm)
 
 // Fixed-length problems on at most 16 (sequence, head) pairs with long sequences replace the serial chain of the
 // recurrence by the chunk-transition scan along T (kda_scan.cu): G groups of L chunks per pair, composed in
-// parallel (2 (G - 1) CTAs per pair), chained serially (G - 1 fp32 steps of ≈2 us), then run in parallel
-// (G CTAs per pair).  G comes from a cost model of those three launches against the serial chain (≈1.52 us
-// per chunk, less what the pieces hide) on the 152 SMs of a GB300; it depends only on N, T and H, like the
-// workspace that holds the scan's matrices.
+// parallel (2 (G - 1) CTAs per pair, ≈1.38 us per chunk step), chained serially (G - 1 fp32 steps of ≈1.7 us),
+// then run in parallel (G CTAs per pair).  G comes from a cost model of those three launches against the
+// serial chain (≈1.52 us per chunk, less what the pieces hide) on the 152 SMs of a GB300, with the step
+// costs measured there; it depends only on N, T and H, like the workspace that holds the scan's matrices.
 #ifndef KDA_SCAN_GROUPS_FORCE
 #define KDA_SCAN_GROUPS_FORCE 0   // > 0: this many groups wherever the scan may run (measurement builds)
 #endif
 constexpr int SCAN_MAX_PAIRS = 16;
 constexpr int SCAN_MAX_GROUPS = 16;
 constexpr int MODEL_SMS = 152;
-constexpr double CHUNK_STEP_US = 1.52, COMPOSE_STEP_US = 1.3, SCAN_STEP_US = 2.0, SCAN_FIXED_US = 10.0;
+constexpr double CHUNK_STEP_US = 1.52, COMPOSE_STEP_US = 1.38, SCAN_STEP_US = 1.7, SCAN_FIXED_US = 10.0;
 
 // (groups, chunks per group) for a scan over nch chunks with about g groups: every group but the last full
 int64_t scan_len(int64_t nch, int g) { return (nch + g - 1) / g; }

@@ -170,15 +170,25 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     auto buf_of = [&](int c) -> unsigned char * { return sm + (c % NBUF) * SLOT_BYTES; };
     // one thread: the first / second part of the slot of chunk c into buffer c % 3 (both complete one phase
     // of that buffer's mbarrier)
+    // COMPOSE reads only what the state update needs: W (QW rows 0 .. 63), K~^T (KA rows 64 .. 191) and Gamma_C,
+    // and U0^T in tile 1 (tile 0 takes U0 as 0)
+    constexpr int CMP_W = CH * D * 2, CMP_K = D * CH * 2, CMP_KOFF = SLOT_KA + (CH / 8) * KA_SBO;
+    const uint32_t tx_bytes = !COMPOSE ? (uint32_t)SLOT_BYTES
+                                       : (uint32_t)(CMP_W + CMP_K + (tile ? SLOT_BYTES - SLOT_U0 : D * 4));
     auto issue_head = [&](int c) {
         const uint32_t mb = mbarL + 8 * (c % NBUF);
-        mbar_expect_tx(mb, SLOT_BYTES);
-        bulk_g2s(smem_u32(buf_of(c)), slot_ptr(c), SLOT_HEAD, mb);
+        mbar_expect_tx(mb, tx_bytes);
+        if (COMPOSE) {
+            bulk_g2s(smem_u32(buf_of(c) + SLOT_QW), slot_ptr(c) + SLOT_QW, CMP_W, mb);
+            bulk_g2s(smem_u32(buf_of(c) + CMP_KOFF), slot_ptr(c) + CMP_KOFF, CMP_K, mb);
+        } else {
+            bulk_g2s(smem_u32(buf_of(c)), slot_ptr(c), SLOT_HEAD, mb);
+        }
     };
     auto issue_tail = [&](int c) {
         fence_async_smem();   // the buffer's generic-proxy readers and writers finished before a barrier
-        bulk_g2s(smem_u32(buf_of(c) + SLOT_HEAD), slot_ptr(c) + SLOT_HEAD, SLOT_BYTES - SLOT_HEAD,
-                 mbarL + 8 * (c % NBUF));
+        const int off = COMPOSE && tile == 0 ? SLOT_GC : SLOT_HEAD;
+        bulk_g2s(smem_u32(buf_of(c) + off), slot_ptr(c) + off, SLOT_BYTES - off, mbarL + 8 * (c % NBUF));
     };
 
     if (warp == 0) {

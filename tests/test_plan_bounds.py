@@ -125,3 +125,35 @@ def test_valid_cu_seqlens_give_the_plain_table(driver):
     (bad, used, max_w, min_tok, max_end, rec_end), = run(driver, [(cu, 1000)])
     chunks = sum(-(-(b - a) // 64) for a, b in zip(cu[:-1], cu[1:]))
     assert bad == 0 and used == chunks == rec_end and min_tok == 0 and max_end == 1000
+
+
+def _bitonic_order(lengths):
+    """The plan kernel's longest-first order restated: keys length * 4096 + (4095 - index), padded with -1 to
+    m = the power of two from N up (at least 2), sorted descending by the same compare-exchange network
+    (stage (k, j): thread t < m / 2 pairs i = 2 j (t / j) + t % j with i + j, descending where i & k == 0)."""
+    N = len(lengths)
+    m = 2
+    while m < N:
+        m <<= 1
+    keys = [int(lengths[s]) * 4096 + (4095 - s) if s < N else -1 for s in range(m)]
+    k = 2
+    while k <= m:
+        j = k >> 1
+        while j > 0:
+            for t in range(m >> 1):
+                i = 2 * j * (t // j) + t % j
+                x, y = keys[i], keys[i + j]
+                if (x < y) if (i & k) == 0 else (x > y):
+                    keys[i], keys[i + j] = y, x
+            j >>= 1
+        k <<= 1
+    return [4095 - (key & 4095) for key in keys[:N]]
+
+
+@pytest.mark.parametrize("N", [2, 3, 5, 12, 16, 17, 100, 257])
+def test_longest_first_order_network(N):
+    """The sort network sized to the sequence count orders the sequences longest first, ties by index."""
+    rng = np.random.default_rng(N)
+    lengths = rng.integers(0, 50, size=N)   # many ties
+    want = sorted(range(N), key=lambda s: (-int(lengths[s]), s))
+    assert _bitonic_order(lengths) == want
