@@ -175,17 +175,27 @@ int piece_count(int64_t nch, int64_t pairs, int nsm)
 
 // Fixed-length problems on at most 16 (sequence, head) pairs with long sequences replace the serial chain of the
 // recurrence by the chunk-transition scan along T (kda_scan.cu): G groups of L chunks per pair, composed in
-// parallel (2 (G - 1) CTAs per pair, ≈1.38 us per chunk step), chained serially (G - 1 fp32 steps of ≈1.7 us),
-// then run in parallel (G CTAs per pair).  G comes from a cost model of those three launches against the
+// parallel (2 (G - 1) CTAs per pair at ≈1.38 us per chunk step, or G - 1 CTAs that carry both states at ≈2.32 us,
+// whichever finishes first in waves of 152 CTAs), chained serially (G - 1 fp32 steps of ≈1.7 us), then run in
+// parallel (G CTAs per pair).  G comes from a cost model of those three launches against the
 // serial chain (≈1.52 us per chunk, less what the pieces hide) on the 152 SMs of a GB300, with the step
 // costs measured there; it depends only on N, T and H, like the workspace that holds the scan's matrices.
 #ifndef KDA_SCAN_GROUPS_FORCE
 #define KDA_SCAN_GROUPS_FORCE 0   // > 0: this many groups wherever the scan may run (measurement builds)
 #endif
 constexpr int SCAN_MAX_PAIRS = 16;
-constexpr int SCAN_MAX_GROUPS = 16;
+constexpr int SCAN_MAX_GROUPS = 32;
 constexpr int MODEL_SMS = 152;
-constexpr double CHUNK_STEP_US = 1.52, COMPOSE_STEP_US = 1.38, SCAN_STEP_US = 1.7, SCAN_FIXED_US = 10.0;
+constexpr double CHUNK_STEP_US = 1.52, COMPOSE_STEP_US = 1.38, COMPOSE2_STEP_US = 2.32, SCAN_STEP_US = 1.7,
+                 SCAN_FIXED_US = 10.0;
+
+int64_t model_waves(int64_t ctas) { return (ctas + MODEL_SMS - 1) / MODEL_SMS; }
+// the compose form for G groups: true = one CTA per (group, pair) carrying both states
+bool compose_two_tiles(int64_t pairs, int G)
+{
+    return (double)model_waves((G - 1) * pairs) * COMPOSE2_STEP_US <
+           (double)model_waves(2 * (G - 1) * pairs) * COMPOSE_STEP_US;
+}
 
 // (groups, chunks per group) for a scan over nch chunks with about g groups: every group but the last full
 int64_t scan_len(int64_t nch, int g) { return (nch + g - 1) / g; }
@@ -199,7 +209,6 @@ int scan_groups(int N, int64_t T, int H, bool varlen)
         return 1;
     if (KDA_SCAN_GROUPS_FORCE > 1)
         return scan_groups_of(nch, (int)std::min<int64_t>(KDA_SCAN_GROUPS_FORCE, nch));
-    auto waves = [](int64_t ctas) { return (double)((ctas + MODEL_SMS - 1) / MODEL_SMS); };
     // the serial chain, with what the pieces hide behind it
     const double recur_us = CHUNK_STEP_US * (double)nch;
     const double prep_us = 5.9 * (double)nch * (double)pairs / MODEL_SMS;
@@ -211,8 +220,10 @@ int scan_groups(int N, int64_t T, int H, bool varlen)
     for (int g = 2; g <= SCAN_MAX_GROUPS && g <= nch; ++g) {
         const int G = scan_groups_of(nch, g);
         const double L = (double)scan_len(nch, g);
-        const double t = waves(2 * (G - 1) * pairs) * L * COMPOSE_STEP_US + (G - 1) * SCAN_STEP_US +
-                         waves(G * pairs) * L * CHUNK_STEP_US + SCAN_FIXED_US;
+        const double compose = compose_two_tiles(pairs, G) ? model_waves((G - 1) * pairs) * COMPOSE2_STEP_US
+                                                           : model_waves(2 * (G - 1) * pairs) * COMPOSE_STEP_US;
+        const double t = compose * L + (G - 1) * SCAN_STEP_US + model_waves(G * pairs) * L * CHUNK_STEP_US +
+                         SCAN_FIXED_US;
         if (t < best) {
             best = t;
             best_g = G;
@@ -465,7 +476,7 @@ cudaError_t run_scan(const Problem &p, int groups, int state_kind, kda_dtype_t s
     float *last = ss + (size_t)(groups - 2) * pairs * mat;
     q.fin = bf16 ? (p.fin ? last : nullptr) : p.fin;
     if (e == cudaSuccess)
-        e = launch_compose(q, stream);
+        e = launch_compose(q, compose_two_tiles((int64_t)pairs, groups), stream);
     if (e == cudaSuccess)
         e = launch_scan_states(init0, ma, mb, ss, (int)pairs, groups, stream);
     if (e == cudaSuccess)

@@ -51,7 +51,8 @@ cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream);
 // The chunk-transition scan: each group's transition (recurrence kernel, compose form; groups 0 .. p.groups - 2
 // into p.sc_a / p.sc_b), then the group start states, serially over the groups (p.sc_s, from the fp32 initial
 // state init0 or zeros).
-cudaError_t launch_compose(const Problem &p, cudaStream_t stream);
+// two_tiles: one CTA per (group, sequence, head) carries both the transition and the offset; otherwise two CTAs.
+cudaError_t launch_compose(const Problem &p, bool two_tiles, cudaStream_t stream);
 cudaError_t launch_scan_states(const float *init0, const float *a, const float *b, float *s, int pairs, int groups,
                                cudaStream_t stream);
 // Token-recurrent kernel, persistent over the N x H x 2 (sequence, head, value half) items; no workspace.

@@ -67,6 +67,24 @@ __device__ __forceinline__ void tmem_ld_s_ofrag(uint32_t taddr_s, uint32_t (&u)[
                    "=r"(o[24]), "=r"(o[25]), "=r"(o[26]), "=r"(o[27]), "=r"(o[28]), "=r"(o[29]), "=r"(o[30]), "=r"(o[31])
                  : "r"(taddr_s), "r"(taddr_o), "r"(taddr_o + (16u << 16)));
 }
+// 64 columns of this warp's 32 lanes (one value per lane and column), waited for
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&u)[64])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+                 "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+                 "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+                   "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
+                   "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]),
+                   "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31]),
+                   "=r"(u[32]), "=r"(u[33]), "=r"(u[34]), "=r"(u[35]), "=r"(u[36]), "=r"(u[37]), "=r"(u[38]), "=r"(u[39]),
+                   "=r"(u[40]), "=r"(u[41]), "=r"(u[42]), "=r"(u[43]), "=r"(u[44]), "=r"(u[45]), "=r"(u[46]), "=r"(u[47]),
+                   "=r"(u[48]), "=r"(u[49]), "=r"(u[50]), "=r"(u[51]), "=r"(u[52]), "=r"(u[53]), "=r"(u[54]), "=r"(u[55]),
+                   "=r"(u[56]), "=r"(u[57]), "=r"(u[58]), "=r"(u[59]), "=r"(u[60]), "=r"(u[61]), "=r"(u[62]), "=r"(u[63])
+                 : "r"(taddr));
+}
 // stmatrix.trans: four 8x8 16-bit matrices from mma-fragment registers, each stored transposed (matrix m:
 // rows at the addresses of lanes 8m .. 8m + 7)
 __device__ __forceinline__ void stsm_x4_t(uint32_t addr, const uint32_t (&r)[4])
@@ -109,11 +127,14 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 //
 // Fixed length, p.groups > 1 (the chunk-transition scan): CTA (group g, sequence n, head h) runs chunks
 // g group_len .. of sequence n from the start state of group g (the initial state for g = 0, else sc_s) and
-// stores a final state for the last group only.  COMPOSE: the scan's first level, two CTAs per (group, n, h)
-// and no outputs: the group's chunks map a start state S to M S + B (M = the product of the chunks'
-// Diag(Gamma_C) - K~^T W, B = the state reached from S = 0); tile 0 runs from S = I with U0 taken as 0 and
-// leaves M, tile 1 runs from S = 0 and leaves B, both stored transposed like a state (sc_a / sc_b).
-template <int STATE, bool VARLEN, bool BSTATE, bool COMPOSE>
+// stores a final state for the last group only.  COMPOSE > 0: the scan's first level, no outputs: the group's
+// chunks map a start state S to M S + B (M = the product of the chunks' Diag(Gamma_C) - K~^T W, B = the state
+// reached from S = 0).  Tile 0 runs from S = I with U0 taken as 0 (leaving M), tile 1 from S = 0 (leaving B),
+// both stored transposed like a state (sc_a / sc_b).  COMPOSE = 1: one tile per CTA (two CTAs per (group, n,
+// h), the tile in the low bit of the CTA index), tensor memory as in the recurrence.  COMPOSE = 2: one CTA per
+// (group, n, h) carries both tiles; tensor memory: X^T of tile t at 64 t, S^T at 128 + 128 t, its fp16 copy at
+// 384 + 64 t, where U^T (fp16) also goes once the first product has read the copy.
+template <int STATE, bool VARLEN, bool BSTATE, int COMPOSE>
 __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 {
     extern __shared__ __align__(128) unsigned char sm[];
@@ -122,8 +143,8 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     asm volatile("griddepcontrol.launch_dependents;");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = p.H;
-    const int tile = COMPOSE ? (int)(blockIdx.x & 1u) : 0;
-    const int cta = COMPOSE ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int ctile = COMPOSE == 1 ? (int)(blockIdx.x & 1u) : 0;   // the tile of a one-tile compose CTA
+    const int cta = COMPOSE == 1 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int NH = p.N * H;
     const int grp = VARLEN ? 0 : cta / NH;   // group of the scan (0 without one)
     const int pr = cta - grp * NH;
@@ -140,7 +161,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         fin = nullptr;
     if (COMPOSE) {
         init = nullptr;
-        fin = (tile ? p.sc_b : p.sc_a) + (size_t)grp * NH * D * D;
+        fin = nullptr;   // sc_a / sc_b per tile
     }
     int64_t bos, len, slot0;
     if (VARLEN) {
@@ -170,11 +191,10 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     auto buf_of = [&](int c) -> unsigned char * { return sm + (c % NBUF) * SLOT_BYTES; };
     // one thread: the first / second part of the slot of chunk c into buffer c % 3 (both complete one phase
     // of that buffer's mbarrier)
-    // COMPOSE reads only what the state update needs: W (QW rows 0 .. 63), K~^T (KA rows 64 .. 191) and Gamma_C,
-    // and U0^T in tile 1 (tile 0 takes U0 as 0)
+    // COMPOSE reads only what the state updates need: W (QW rows 0 .. 63), K~^T (KA rows 64 .. 191), U0^T and
+    // Gamma_C
     constexpr int CMP_W = CH * D * 2, CMP_K = D * CH * 2, CMP_KOFF = SLOT_KA + (CH / 8) * KA_SBO;
-    const uint32_t tx_bytes = !COMPOSE ? (uint32_t)SLOT_BYTES
-                                       : (uint32_t)(CMP_W + CMP_K + (tile ? SLOT_BYTES - SLOT_U0 : D * 4));
+    constexpr uint32_t tx_bytes = !COMPOSE ? (uint32_t)SLOT_BYTES : (uint32_t)(CMP_W + CMP_K + SLOT_BYTES - SLOT_U0);
     auto issue_head = [&](int c) {
         const uint32_t mb = mbarL + 8 * (c % NBUF);
         mbar_expect_tx(mb, tx_bytes);
@@ -187,8 +207,8 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     };
     auto issue_tail = [&](int c) {
         fence_async_smem();   // the buffer's generic-proxy readers and writers finished before a barrier
-        const int off = COMPOSE && tile == 0 ? SLOT_GC : SLOT_HEAD;
-        bulk_g2s(smem_u32(buf_of(c) + off), slot_ptr(c) + off, SLOT_BYTES - off, mbarL + 8 * (c % NBUF));
+        bulk_g2s(smem_u32(buf_of(c) + SLOT_HEAD), slot_ptr(c) + SLOT_HEAD, SLOT_BYTES - SLOT_HEAD,
+                 mbarL + 8 * (c % NBUF));
     };
 
     if (warp == 0) {
@@ -221,14 +241,28 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     const uint32_t trow = tbase + ((uint32_t)(q4 * 32) << 16);
     const size_t srow = ((size_t)n * H + h) * D * D + (size_t)vrow * D + half * 64;
 
+    // tensor-memory columns of tile t (COMPOSE carries two states; otherwise t = 0)
+    auto col_x = [](int t) -> uint32_t { return COMPOSE == 2 ? 64u * t : (uint32_t)TM_X; };
+    auto col_s = [](int t) -> uint32_t { return COMPOSE == 2 ? 128u + 128u * t : (uint32_t)TM_S; };
+    auto col_s16 = [](int t) -> uint32_t { return COMPOSE == 2 ? 384u + 64u * t : (uint32_t)TM_S16; };
+    auto col_u16 = [](int t) -> uint32_t { return COMPOSE == 2 ? 384u + 64u * t : (uint32_t)TM_U16; };
+    constexpr int TILES = COMPOSE == 2 ? 2 : 1;
+    auto tile_of = [&](int t) { return COMPOSE == 2 ? t : ctile; };   // 0: M, 1: B
+
     // -------- initial state -> S^T (row v, key columns 64 half .. + 63)
+#pragma unroll
+    for (int t = 0; t < TILES; ++t)
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
         uint32_t u[32];
-        if (COMPOSE && tile == 0) {
+        if (COMPOSE && tile_of(t) == 0) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 u[e] = half * 64 + 32 * part + e == vrow ? 0x3f800000u : 0u;   // S = I
+        } else if (COMPOSE) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                u[e] = 0u;   // S = 0
         } else if (STATE == 2 && init) {
             const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(init) + srow + 32 * part);
 #pragma unroll
@@ -257,7 +291,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             for (int e = 0; e < 32; ++e)
                 u[e] = 0u;
         }
-        tmem_st32(trow + TM_S + half * 64 + 32 * part, u);
+        tmem_st32(trow + col_s(t) + half * 64 + 32 * part, u);
     }
     tc_fence_before();
 
@@ -325,26 +359,32 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         //      tensor-memory load of S^T and O^T; the stores complete together before the barrier)
         {
             const float *gam = reinterpret_cast<const float *>(sb + SLOT_GC) + half * 64;
-            uint32_t u[64], o[32];
-            tmem_ld_s_ofrag(trow + TM_S + half * 64, u, trow + TM_O + half * 32, o);   // O^T unused at c = 0
-            if (BSTATE) {
+#pragma unroll 1
+            for (int t = 0; t < TILES; ++t) {
+                uint32_t u[64], o[32];
+                if (COMPOSE)
+                    tmem_ld64(trow + col_s(t) + half * 64, u);
+                else
+                    tmem_ld_s_ofrag(trow + TM_S + half * 64, u, trow + TM_O + half * 32, o);   // O^T unused at c = 0
+                if (BSTATE) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        u[e] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(u[e]))));
+                }
+                {
+                    uint32_t hv[32];
+#pragma unroll
+                    for (int m = 0; m < 32; ++m)
+                        hv[m] = pack_half2(__uint_as_float(u[2 * m]), __uint_as_float(u[2 * m + 1]));
+                    tmem_st32_nw(trow + col_s16(t) + half * 32, hv);
+                }
 #pragma unroll
                 for (int e = 0; e < 64; ++e)
-                    u[e] = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(u[e]))));
+                    u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[e]);
+                tmem_st64_nw(trow + col_s(t) + half * 64, u);
+                if (!COMPOSE && c > 0)
+                    write_out(ost, o);
             }
-            {
-                uint32_t hv[32];
-#pragma unroll
-                for (int m = 0; m < 32; ++m)
-                    hv[m] = pack_half2(__uint_as_float(u[2 * m]), __uint_as_float(u[2 * m + 1]));
-                tmem_st32_nw(trow + TM_S16 + half * 32, hv);
-            }
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-                u[e] = __float_as_uint(__uint_as_float(u[e]) * gam[e]);
-            tmem_st64_nw(trow + TM_S + half * 64, u);
-            if (!COMPOSE && c > 0)
-                write_out(ost, o);
             tmem_wait_st();
         }
         tc_fence_before();
@@ -359,10 +399,12 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-                mma_f16_ts(tbase + TM_X, tbase + TM_S16 + 8 * s,
-                           umma_desc(s_buf + SLOT_QW + s * 2 * CORE_LBO, CORE_LBO, QW_SBO),
-                           idesc_f16(128, COMPOSE ? CH : 128), s > 0);   // [W ; Q~] rows (W only: no outputs)
+            for (int t = 0; t < TILES; ++t)
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s)
+                    mma_f16_ts(tbase + col_x(t), tbase + col_s16(t) + 8 * s,
+                               umma_desc(s_buf + SLOT_QW + s * 2 * CORE_LBO, CORE_LBO, QW_SBO),
+                               idesc_f16(128, COMPOSE ? CH : 128), s > 0);   // [W ; Q~] rows (W only: no outputs)
             umma_commit(mbarQ);
         }
         ++nq;
@@ -375,9 +417,10 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         if (!mbar_wait(mbarQ, c & 1, p.wait_polls))
             *hang_flag = 1u;
         tc_fence_after();
-        {
+#pragma unroll 1
+        for (int t = 0; t < TILES; ++t) {
             uint32_t x[32], hv[16];
-            tmem_ld32(trow + TM_X + half * 32, x);
+            tmem_ld32(trow + col_x(t) + half * 32, x);
             const unsigned char *u0row = sb + SLOT_U0 + vrow * (CH * 2);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -386,13 +429,14 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&ww[e]));
-                if (COMPOSE && tile == 0)
-                    f = make_float2(0.f, 0.f);   // the linear part: U = -X
+                    if (COMPOSE && tile_of(t) == 0)
+                        f = make_float2(0.f, 0.f);   // the linear part: U = -X
                     hv[4 * m + e] = pack_half2(f.x - __uint_as_float(x[8 * m + 2 * e]),
                                                f.y - __uint_as_float(x[8 * m + 2 * e + 1]));
                 }
             }
-            tmem_st16(trow + TM_U16 + half * 16, hv);
+            // (two-tile compose: over the tile's fp16 state copy, which the completed first product has read)
+            tmem_st16(trow + col_u16(t) + half * 16, hv);
         }
         tc_fence_before();
         __syncthreads();
@@ -404,11 +448,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             tc_fence_after();
 #pragma unroll
             for (int s = 0; s < CH / 16; ++s)
-                if (COMPOSE)   // the state update alone: B = the K~^T rows of KA (rows 64 ..)
-                    mma_f16_ts(tbase + TM_S, tbase + TM_U16 + 8 * s,
-                               umma_desc(s_buf + SLOT_KA + (CH / 8) * KA_SBO + s * 2 * CORE_LBO, CORE_LBO, KA_SBO),
-                               idesc_f16(128, D), 1);
-                else
+                if (COMPOSE) {   // the state updates alone: B = the K~^T rows of KA (rows 64 ..)
+#pragma unroll
+                    for (int t = 0; t < TILES; ++t)
+                        mma_f16_ts(tbase + col_s(t), tbase + col_u16(t) + 8 * s,
+                                   umma_desc(s_buf + SLOT_KA + (CH / 8) * KA_SBO + s * 2 * CORE_LBO, CORE_LBO, KA_SBO),
+                                   idesc_f16(128, D), 1);
+                } else
                     mma_f16_ts(tbase + TM_O, tbase + TM_U16 + 8 * s,
                                umma_desc(s_buf + SLOT_KA + s * 2 * CORE_LBO, CORE_LBO, KA_SBO), idesc_f16(128, 64 + D), 1);
             umma_commit(mbarB);
@@ -457,14 +503,23 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         // that overflowed (or an inf / NaN input) leaves the fp32 state non-finite from that chunk on
         tc_fence_after();
         bool bad = false;
+#pragma unroll 1
+        for (int t = 0; t < TILES; ++t)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             uint32_t u[32];
-            tmem_ld32(trow + TM_S + half * 64 + 32 * part, u);
+            tmem_ld32(trow + col_s(t) + half * 64 + 32 * part, u);
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 bad |= !(fabsf(__uint_as_float(u[e])) <= 3.402823466e38f);
-            if (STATE == 2 && fin) {
+            if (COMPOSE) {   // M (tile 0) or B (tile 1) of this group
+                float4 *dst = reinterpret_cast<float4 *>((tile_of(t) ? p.sc_b : p.sc_a) + (size_t)grp * NH * D * D +
+                                                         srow + 32 * part);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                         __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
+            } else if (STATE == 2 && fin) {
                 float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(fin) + srow + 32 * part);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
@@ -496,7 +551,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     }
 }
 
-template <int STATE, bool VARLEN, bool BSTATE, bool COMPOSE>
+template <int STATE, bool VARLEN, bool BSTATE, int COMPOSE>
 cudaError_t launch_recur_t(const Problem &p, int grid, cudaStream_t stream)
 {
     static bool configured[64] = {};
@@ -523,13 +578,13 @@ cudaError_t launch_recur_b(const Problem &p, int state_kind, cudaStream_t stream
 {
     const int grid = p.N * p.H;
     if (p.cu)
-        return state_kind == 2 ? launch_recur_t<2, true, BSTATE, false>(p, grid, stream)
-             : state_kind == 1 ? launch_recur_t<1, true, BSTATE, false>(p, grid, stream)
-                               : launch_recur_t<0, true, BSTATE, false>(p, grid, stream);
+        return state_kind == 2 ? launch_recur_t<2, true, BSTATE, 0>(p, grid, stream)
+             : state_kind == 1 ? launch_recur_t<1, true, BSTATE, 0>(p, grid, stream)
+                               : launch_recur_t<0, true, BSTATE, 0>(p, grid, stream);
     const int fgrid = grid * p.groups;
-    return state_kind == 2 ? launch_recur_t<2, false, BSTATE, false>(p, fgrid, stream)
-         : state_kind == 1 ? launch_recur_t<1, false, BSTATE, false>(p, fgrid, stream)
-                           : launch_recur_t<0, false, BSTATE, false>(p, fgrid, stream);
+    return state_kind == 2 ? launch_recur_t<2, false, BSTATE, 0>(p, fgrid, stream)
+         : state_kind == 1 ? launch_recur_t<1, false, BSTATE, 0>(p, fgrid, stream)
+                           : launch_recur_t<0, false, BSTATE, 0>(p, fgrid, stream);
 }
 
 }  // namespace
@@ -540,9 +595,11 @@ cudaError_t launch_recur(const Problem &p, int state_kind, cudaStream_t stream)
                                             : launch_recur_b<false>(p, state_kind, stream);
 }
 
-cudaError_t launch_compose(const Problem &p, cudaStream_t stream)
+cudaError_t launch_compose(const Problem &p, bool two_tiles, cudaStream_t stream)
 {
-    return launch_recur_t<2, false, false, true>(p, 2 * (p.groups - 1) * p.N * p.H, stream);
+    const int grid = (p.groups - 1) * p.N * p.H;
+    return two_tiles ? launch_recur_t<2, false, false, 2>(p, grid, stream)
+                     : launch_recur_t<2, false, false, 1>(p, 2 * grid, stream);
 }
 
 size_t recur_smem_bytes() { return RECUR_SMEM; }

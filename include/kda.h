@@ -151,7 +151,7 @@ int kda_fwd_pieces(int N, int64_t T, int H, int varlen);
 /*
  * Number of groups G of the chunk-transition scan along T in which kda_fwd, kda_fwd_ws and
  * kda_fwd_noalloc run a problem of this size (see kda_fwd): 1 when the recurrence runs as one serial
- * chain per (sequence, head) pair, 2 to 16 otherwise.  Depends on N, T, H and varlen only (the
+ * chain per (sequence, head) pair, 2 to 32 otherwise.  Depends on N, T, H and varlen only (the
  * workspace holds the scan's matrices: (1 + 3 (G - 1)) x N x H x 64 KiB ahead of the operand slots).
  * 0 for invalid sizes.  Launches nothing.
  */

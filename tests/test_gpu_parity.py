@@ -297,8 +297,9 @@ def test_pieces_in_place_state(state):
 def test_scan_along_t_matches_oracle(B, T, H, state, with_initial, lb):
     """Few (sequence, head) pairs and long sequences take the chunk-transition scan along T (groups composed in
     parallel, their start states chained in fp32, the groups run in parallel): within the parity tolerances
-    of the oracle and close to the serial chain of kda_fwd_ws_profiled, for every state kind and 7 to 16
-    groups with ragged last groups and chunks; and work that the caller enqueues on the same stream after
+    of the oracle and close to the serial chain of kda_fwd_ws_profiled, for every state kind, 7 to 28 groups
+    with ragged last groups and chunks and both compose forms (two CTAs per group and pair, or one carrying
+    both states); and work that the caller enqueues on the same stream after
     the call sees the finished results.  With lower_bound = -5 the state forgets a chunk's start within the
     chunk (its decay underflows), so each group's transition is exactly zero and the scan gives the serial
     chain's bits; with -0.05 and 0 (no decay) the state carries across many chunks and groups."""
