@@ -7,13 +7,16 @@
 // back on a copy-out stream, so the copies of neighbouring pieces overlap the kernels.  Because the
 // pieces start at chunk boundaries and the chained state is fp32 (the state the recurrence keeps
 // internally), the results are bit-identical to one kda_fwd call over the whole problem.  Varlen
-// problems (cu_seqlens) run as one piece.
+// problems (cu_seqlens) are cut into pieces of whole sequences, which share no state: each piece is a
+// varlen call of its own, with its cu_seqlens shifted to start at 0 and its sequences' slices of the
+// states, so the results are again the bits of one call (every (sequence, head) pair is computed alone).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -110,6 +113,132 @@ cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cu
     return cudaGetLastError();
 }
 
+namespace {
+
+// Varlen pipeline: pieces of whole sequences [sb[p], sb[p + 1]), each about T / P tokens (P at most
+// HOST_MAX_PIECES, pieces of at least HOST_MIN_PIECE tokens where the lengths allow).  Piece p's token rows
+// [cu[s0], cu[s1]) are contiguous in every token tensor, its states are the contiguous slices of sequences s0 ..
+// s1 - 1, and its cu_seqlens is cu[s0 .. s1] - cu[s0] (all pieces' arrays go to the device in one copy).
+kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const void *v, const void *g, const void *beta,
+                             float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                             const void *initial_state, void *final_state, kda_dtype_t state_dtype,
+                             const int64_t *cu, int N, int64_t T, int H)
+{
+    const size_t row = (size_t)H * D;                  // elements of one token's q / k / v / g / out
+    const size_t smat = (size_t)H * D * D;             // state elements of one sequence
+    const size_t sbytes = state_dtype == KDA_DTYPE_FP32 ? 4 : 2;
+    const int64_t want = std::min<int64_t>(std::min<int64_t>(HOST_MAX_PIECES, N), (T + HOST_MIN_PIECE - 1) / HOST_MIN_PIECE);
+    const int64_t target = (T + want - 1) / std::max<int64_t>(want, 1);
+    std::vector<int> sb{0};
+    for (int s = 1; s < N; ++s)
+        if (cu[s] - cu[sb.back()] >= target && (int64_t)sb.size() < want)
+            sb.push_back(s);
+    sb.push_back(N);
+    const int pieces = (int)sb.size() - 1;
+    std::vector<int64_t> cus;
+    std::vector<size_t> cu_off;
+    int64_t max_t = 0;
+    int max_n = 0;
+    size_t max_ws = 0;
+    for (int p = 0; p < pieces; ++p) {
+        const int s0 = sb[p], s1 = sb[p + 1];
+        cu_off.push_back(cus.size());
+        for (int s = s0; s <= s1; ++s)
+            cus.push_back(cu[s] - cu[s0]);
+        const int64_t pt = cu[s1] - cu[s0];
+        max_t = std::max(max_t, pt);
+        max_n = std::max(max_n, s1 - s0);
+        max_ws = std::max(max_ws, workspace_bytes(s1 - s0, pt, H, true));
+    }
+    const int ring = pieces > 1 ? HOST_RING : 1;
+
+    cudaStream_t sc = c->s_comp;
+    DevBufs bufs;
+    bufs.s = sc;
+    void *dq[HOST_RING] = {}, *dk[HOST_RING] = {}, *dv[HOST_RING] = {}, *dg[HOST_RING] = {}, *db[HOST_RING] = {},
+         *dout[HOST_RING] = {}, *dinit[HOST_RING] = {}, *dfin[HOST_RING] = {};
+    void *dalog = nullptr, *ddt = nullptr, *dcu = nullptr, *dws = nullptr;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < ring && e == cudaSuccess; ++i) {
+        e = bufs.get(&dq[i], (size_t)max_t * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&dk[i], (size_t)max_t * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&dv[i], (size_t)max_t * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&dg[i], (size_t)max_t * row * 2);
+        if (e == cudaSuccess) e = bufs.get(&db[i], (size_t)max_t * H * 2);
+        if (e == cudaSuccess) e = bufs.get(&dout[i], (size_t)max_t * row * 2);
+        if (e == cudaSuccess && initial_state) e = bufs.get(&dinit[i], (size_t)max_n * smat * sbytes);
+        if (e == cudaSuccess && final_state) e = bufs.get(&dfin[i], (size_t)max_n * smat * sbytes);
+    }
+    if (e == cudaSuccess) e = bufs.get(&dalog, (size_t)H * 4);
+    if (e == cudaSuccess) e = bufs.get(&ddt, (size_t)H * D * 4);
+    if (e == cudaSuccess) e = bufs.get(&dcu, cus.size() * 8);
+    if (e == cudaSuccess) e = bufs.get(&dws, max_ws);
+    // parameters and every piece's cu_seqlens (compute stream), then the copy streams start
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dalog, A_log, (size_t)H * 4, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ddt, dt_bias, (size_t)H * D * 4, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dcu, cus.data(), cus.size() * 8, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess) e = cudaEventRecord(c->e_start, sc);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_in, c->e_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_start, 0);
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(sc);
+        return KDA_ERR_CUDA;
+    }
+
+    const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k);
+    const char *hv = static_cast<const char *>(v), *hg = static_cast<const char *>(g);
+    const char *hb = static_cast<const char *>(beta), *hi = static_cast<const char *>(initial_state);
+    char *ho = static_cast<char *>(out), *hf = static_cast<char *>(final_state);
+    kda_status_t st = KDA_OK;
+    for (int p = 0; p < pieces && st == KDA_OK; ++p) {
+        const int slot = p % ring, s0 = sb[p], np = sb[p + 1] - s0;
+        const int64_t t0 = cu[s0], pt = cu[sb[p + 1]] - t0;
+        const size_t w = (size_t)pt * row * 2, o = (size_t)t0 * row * 2;
+        const size_t sw = (size_t)np * smat * sbytes, so = (size_t)s0 * smat * sbytes;
+        // copy in (after the slot's previous piece has been computed)
+        if (p >= ring) e = cudaStreamWaitEvent(c->s_in, c->e_comp[slot], 0);
+        if (pt > 0) {
+            if (e == cudaSuccess) e = cudaMemcpyAsync(dq[slot], hq + o, w, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(dk[slot], hk + o, w, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(dv[slot], hv + o, w, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(dg[slot], hg + o, w, cudaMemcpyHostToDevice, c->s_in);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(db[slot], hb + (size_t)t0 * H * 2, (size_t)pt * H * 2, cudaMemcpyHostToDevice, c->s_in);
+        }
+        if (e == cudaSuccess && initial_state)
+            e = cudaMemcpyAsync(dinit[slot], hi + so, sw, cudaMemcpyHostToDevice, c->s_in);
+        if (e == cudaSuccess) e = cudaEventRecord(c->e_in[slot], c->s_in);
+        // compute (after the copy in, and after the slot's previous results have been copied out)
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, c->e_in[slot], 0);
+        if (e == cudaSuccess && p >= ring) e = cudaStreamWaitEvent(sc, c->e_out[slot], 0);
+        if (e != cudaSuccess) {
+            st = KDA_ERR_CUDA;
+            break;
+        }
+        st = run(dq[slot], dk[slot], dv[slot], dg[slot], db[slot], scale, dout[slot], static_cast<const float *>(dalog),
+                 static_cast<const float *>(ddt), lower_bound, dinit[slot], dfin[slot],
+                 (initial_state || final_state) ? state_dtype : KDA_DTYPE_NONE,
+                 static_cast<const int64_t *>(dcu) + cu_off[p], np, pt, H, static_cast<unsigned char *>(dws), sc);
+        if (st != KDA_OK)
+            break;
+        e = cudaEventRecord(c->e_comp[slot], sc);
+        // copy out
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_comp[slot], 0);
+        if (e == cudaSuccess && pt > 0) e = cudaMemcpyAsync(ho + o, dout[slot], w, cudaMemcpyDeviceToHost, c->s_out);
+        if (e == cudaSuccess && final_state) e = cudaMemcpyAsync(hf + so, dfin[slot], sw, cudaMemcpyDeviceToHost, c->s_out);
+        if (e == cudaSuccess) e = cudaEventRecord(c->e_out[slot], c->s_out);
+        if (e != cudaSuccess)
+            st = KDA_ERR_CUDA;
+    }
+    const cudaError_t e1 = cudaStreamSynchronize(sc), e2 = cudaStreamSynchronize(c->s_out),
+                      e3 = cudaStreamSynchronize(c->s_in);
+    if (st == KDA_OK && (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess))
+        st = KDA_ERR_CUDA;
+    return st;
+}
+
+}  // namespace
+
 kda_status_t run_host(const void *q, const void *k, const void *v, const void *g, const void *beta, float scale,
                       void *out, const float *A_log, const float *dt_bias, float lower_bound, const void *initial_state,
                       void *final_state, kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H)
@@ -122,6 +251,9 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     if (host_ctx(dev, &c) != cudaSuccess)
         return KDA_ERR_CUDA;
     const bool varlen = cu_seqlens != nullptr;
+    if (varlen && N > 1 && T > HOST_MIN_PIECE)
+        return run_host_varlen(c, q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
+                               state_dtype, cu_seqlens, N, T, H);
     const int B = varlen ? 1 : N;
     const size_t row = (size_t)H * D;                  // elements of one token's q / k / v / g / out
     const size_t state_elems = (size_t)N * H * D * D;

@@ -269,9 +269,10 @@ kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, cons
  * alignments.  The library copies the inputs to the current device, runs the forward pass there
  * and copies out (and final_state) back, and returns when the results are in host memory.  The
  * FlashKDA pages have no counterpart: it is this library's end-to-end entry point.  Fixed-length
- * problems are cut into pieces of whole 64-token chunks and the copies of neighbouring pieces
- * overlap the kernels on three streams of the library's own; the state passes between pieces in
- * fp32, so the results are bit-identical to kda_fwd on the same data.  Page-locked (pinned) host
+ * problems are cut into pieces of whole 64-token chunks, varlen problems into pieces of whole
+ * sequences, and the copies of neighbouring pieces overlap the kernels on three streams of the
+ * library's own; the state passes between fixed-length pieces in fp32 (varlen pieces share none),
+ * so the results are bit-identical to kda_fwd on the same data.  Page-locked (pinned) host
  * memory lets the copies run asynchronously; pageable memory works but the copies do not overlap.
  * Device memory comes from the library's pool (see kda_workspace_trim).  Calls are serialised per
  * device.  Errors: those of kda_fwd (cu_seqlens is also checked, on the host, as

@@ -1,6 +1,7 @@
 """The host-buffer entry point kda_fwd_host against kda_fwd on the device: the pipelined pieces
-(whole 64-token chunks, state chained in fp32) give the same bits as one device call, for every state
-dtype and presence, ragged last pieces, batches, varlen problems, pageable memory and T = 0."""
+(whole 64-token chunks with the state chained in fp32; for varlen problems, whole sequences) give the
+same bits as one device call, for every state dtype and presence, ragged last pieces, batches, varlen
+problems (in place too), pageable memory and T = 0."""
 import numpy as np
 import pytest
 import torch
@@ -64,9 +65,30 @@ def test_batch_rows_are_strided_copies():
     assert_same(make_problem(B=3, T=1100, H=4, seed=412))
 
 
-def test_varlen_runs_as_one_piece():
-    cu = np.array([0, 5, 5, 700, 1800, 1801], dtype=np.int64)
-    assert_same(make_problem(B=1, T=1801, H=3, seed=413, cu_seqlens=cu))
+@pytest.mark.parametrize("cu", [
+    [0, 5, 5, 700, 1800, 1801],                       # empty sequences, a one-token last piece
+    [0, 2000, 2010, 2020],                            # one sequence dominates
+    list(np.cumsum([0] + [97 * (i % 5) + 31 for i in range(20)])),   # more sequences than pieces
+    [0, 300, 600]])                                   # too short to cut
+@pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
+def test_varlen_pieces_of_whole_sequences(cu, state):
+    """Varlen problems run in pieces of whole sequences (each its own varlen call, no state between them)."""
+    cu = np.array(cu, dtype=np.int64)
+    assert_same(make_problem(B=1, T=int(cu[-1]), H=3, seed=413, cu_seqlens=cu, state_dtype=state,
+                             lower_bound=-0.05))
+
+
+def test_varlen_pieces_in_place_state():
+    """In place (final_state = initial_state, host memory): each piece reads its sequences' initial states
+    before its final states overwrite them, and no two pieces share a sequence."""
+    cu = np.array(np.cumsum([0] + [300, 700, 64, 900, 1, 600]), dtype=np.int64)
+    p = make_problem(B=1, T=int(cu[-1]), H=2, seed=416, cu_seqlens=cu, lower_bound=-0.05)
+    h = host_tensors(p)
+    kda_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], p.scale, h["out"], h["A_log"], h["dt_bias"],
+                 p.lower_bound, initial_state=h["init"], final_state=h["init"], cu_seqlens=h["cu"])
+    out_d, fin_d = run_gpu(p)
+    assert np.array_equal(h["out"].float().numpy(), out_d)
+    assert np.array_equal(h["init"].float().numpy(), fin_d)
 
 
 def test_pageable_memory():
