@@ -411,32 +411,38 @@ def test_values_beyond_fp16_operand_range_are_reported():
     device_status()   # cleared
 
 
-def test_wait_that_gives_up_is_reported_and_the_next_call_is_correct():
+@pytest.mark.parametrize("B,T,H,cu", [(1, 200, 2, None), (1, 200, 2, np.array([0, 70, 200])),
+                                      (1, 4097, 40, None), (2, 8200, 8, None), (1, 2049, 3, None)])
+def test_wait_that_gives_up_is_reported_and_the_next_call_is_correct(B, T, H, cu):
     """With a zero wait budget every wait of the chunked kernels gives up at once: the kernels drain their
     own work in flight, free their tensor memory and return, kda_device_status reports KDA_ERR_TIMEOUT once,
     and a following call with the default budget is correct against the oracle.  Nothing waits without a
-    limit at any point."""
+    limit at any point.  The last three problems run in pieces (the next piece's prep kernel waiting, in the
+    hardware, for a recurrence that gives up) and with the scan along T (both compose forms)."""
     from gated_delta_rule_23_gb300 import KDAError, _native, device_status
     from gated_delta_rule_23_gb300._native import KDA_DEFAULT_WAIT_POLLS, KDA_ERR_TIMEOUT
     lib = _native.load()
-    for cu in (None, np.array([0, 70, 200])):
-        p = make_problem(B=1, T=200, H=2, seed=71, cu_seqlens=cu)
-        dev = to_device(p)
-        out = torch.empty_like(dev["q"])
-        fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda")
-        try:
-            lib.kda_set_wait_limit(0)
-            kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"],
-                    dev["dt_bias"], p.lower_bound, initial_state=dev["init"], final_state=fin,
-                    cu_seqlens=dev["cu"])
-            with pytest.raises(KDAError) as e:
-                device_status()
-            assert e.value.status == KDA_ERR_TIMEOUT
-        finally:
-            lib.kda_set_wait_limit(KDA_DEFAULT_WAIT_POLLS)
-        device_status()   # the report was cleared
-        out, fin = run_gpu(p, dev)
-        assert_parity(out, fin, *oracle_run(p))
+    if (B, T, H) == (1, 4097, 40):
+        assert lib.kda_fwd_pieces(B, T, H, 0) >= 2
+    if T > 2000 and H <= 8:
+        assert lib.kda_fwd_scan_groups(B, T, H, 0) >= 2
+    p = make_problem(B=B, T=T, H=H, seed=71, cu_seqlens=cu, lower_bound=-0.05)
+    dev = to_device(p)
+    out = torch.empty_like(dev["q"])
+    fin = torch.empty((p.N, p.H, 128, 128), dtype=dev["sdt"], device="cuda")
+    try:
+        lib.kda_set_wait_limit(0)
+        kda_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], p.scale, out, dev["A_log"],
+                dev["dt_bias"], p.lower_bound, initial_state=dev["init"], final_state=fin,
+                cu_seqlens=dev["cu"])
+        with pytest.raises(KDAError) as e:
+            device_status()
+        assert e.value.status == KDA_ERR_TIMEOUT
+    finally:
+        lib.kda_set_wait_limit(KDA_DEFAULT_WAIT_POLLS)
+    device_status()   # the report was cleared
+    out, fin = run_gpu(p, dev)
+    assert_parity(out, fin, *oracle_run(p))
 
 
 @pytest.mark.parametrize("variant", [1, 2, 3])
