@@ -467,3 +467,33 @@ def test_measurement_variants_within_parity(variant, lb):
         o_ref, f_ref = oracle_run(p)
         r = assert_parity(o, f, o_ref, f_ref)
         print(f"variant {variant} lb {lb} varlen {cu is not None}: {parity_report(o, f, o_ref, f_ref)}")
+
+
+def _random_cases(n=16, seed=2024):
+    """Seeded random shapes across the schedules: fixed length with and without pieces or the scan along T,
+    varlen with empty and ragged sequences; random state dtype, initial state and lower bound."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        varlen = i % 4 == 3
+        H = int(rng.choice([1, 2, 3, 5, 8, 12, 24, 40]))
+        if varlen:
+            N = int(rng.integers(2, 9))
+            cu = np.concatenate([[0], np.cumsum(rng.integers(0, 1500, size=N))]).astype(np.int64)
+            B, T = 1, int(cu[-1])
+        else:
+            cu = None
+            B, T = int(rng.integers(1, 3)), int(rng.choice([65, 700, 2049, 3000, 4100, 6000, 8200]))
+        state = [STATE_NONE, STATE_BF16, STATE_FP32][int(rng.integers(0, 3))]
+        cases.append(dict(B=B, T=T, H=H, cu=cu, state=state, with_initial=bool(rng.integers(0, 2)),
+                          lb=float(rng.choice([-5.0, -1.0, -0.05])), seed=1000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: f"B{c['B']}T{c['T']}H{c['H']}{'v' if c['cu'] is not None else ''}")
+def test_random_shapes(case):
+    """Random shapes against the oracle, whichever schedule each takes (single launch, pieces, scan, varlen)."""
+    p = make_problem(B=case["B"], T=case["T"], H=case["H"], seed=case["seed"], cu_seqlens=case["cu"],
+                     state_dtype=case["state"], with_initial=case["with_initial"], lower_bound=case["lb"])
+    out, fin = run_gpu(p)
+    assert_parity(out, fin, *oracle_run(p))
