@@ -68,11 +68,13 @@ constexpr int OFF_TP = OFF_TM + CH * PA * 4;        // fp16 [64 t][64 j] T' (swi
 constexpr int OFF_ZW = OFF_TP + CH * CH * 2;        // fp32 [8 warps][16][8] off-diagonal partial products
 constexpr int OFF_AQS = OFF_ZW + 8 * 16 * 8 * 4;  // Aqk rows of the slot (KA rows 0..63), staged for a bulk copy
 static_assert(OFF_AQS + 64 * CH * 2 <= OPS_BYTES, "post-product overlay");
-// after T' is formed, the W and U0^T parts of the slot are staged over Akk / Tm for bulk copies
-constexpr int OFF_WS = OFF_AKK, OFF_US = OFF_AKK + 64 * D * 2;
-static_assert(OFF_US + D * CH * 2 <= OFF_TP, "W / U0 staging overlaps T'");
 constexpr int OFF_KG = 65536;                       // fp16 [64 j][128 c] K^ . Gamma (kg_off swizzle)
 constexpr int OFF_V = OFF_KG + CH * D * 2;          // bf16 [64 j][128 v] (swizzled)
+// once the WY products have read K^.Gamma and V, the W and U0^T parts of the slot are staged over them for bulk
+// copies, which may still be reading while the next item stages its q, k, g (the next item's first write to
+// these tiles is in its gate pass, after a wait for those copies)
+constexpr int OFF_WS = OFF_KG, OFF_US = OFF_V;
+static_assert(64 * D * 2 <= CH * D * 2 && D * CH * 2 <= CH * D * 2, "W / U0 staging fits K^.Gamma / V");
 constexpr int OFF_RQ = OFF_V + CH * D * 2;          // fp32 pairs [68][2] 1 / |q| (both halves; norm_slot order)
 constexpr int OFF_RK = OFF_RQ + 544;                // fp32 pairs [68][2] 1 / |k|
 constexpr int OFF_BT = OFF_RK + 544;                // fp32 [64] b = sigmoid(beta), 0 past the end
@@ -275,6 +277,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         bt[tid] = tid < L ? sigmoid_fast(__bfloat162float(bval)) : 0.f;
     const float eA = expf(alog);
     cp_async_wait_all();
+    if (tid == 0)
+        bulk_wait_read_all();   // the previous item's W / U0^T copies have read K^.Gamma / V
     __syncthreads();
     // this thread's q, k, g words: tokens t0 + j, channels 64 ps + 8 warp + 2 cpl + {0, 1} (bf16 pairs)
     uint32_t qw[2][8], kw[2][8], gw[2][8];
@@ -761,6 +765,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
                 mma_f16(accu[2 * mt + 1], vf, af[1], af[3]);   // tokens 16 mt + 8 .. + 15
             }
         }
+        __syncthreads();   // every warp has read K^.Gamma and V: their tiles take the staging
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
@@ -783,12 +788,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
-        // W rows (QW rows 0..63) and U0^T of the slot: bulk copies.  The next item may overwrite the shared
-        // memory once every copy has read it; the writes complete before the kernel does.
+        // W rows (QW rows 0..63) and U0^T of the slot: bulk copies, left reading while the next item starts.
+        // The Aqk copy (this item's older group) has read its staging before the next item's q, k, g land
+        // over it; the writes complete before the kernel does.
         bulk_s2g(slot + SLOT_QW, smem_u32(sm + OFF_WS), 64 * D * 2);
         bulk_s2g(slot + SLOT_U0, smem_u32(sm + OFF_US), D * CH * 2);
         bulk_commit();
-        bulk_wait_read_all();
+        bulk_wait_read_but_last();
     }
     // the next item's tensor-core product reuses the accumulator columns this item read out
     tc_fence_before();
@@ -806,6 +812,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 2) kda_prep_kernel(const Problem
         mbar_wait(mbarD, 0);
         atomicOr(&g_kda_prep_error, DEVERR_TIMEOUT);
     }
+    if (tid == 0)
+        bulk_wait_read_all();   // the last item's copies have read their staging
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
