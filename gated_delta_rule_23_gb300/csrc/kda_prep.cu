@@ -108,6 +108,8 @@ __device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a0, uint32_t a1
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+// all but the most recently committed bulk group have read their shared-memory source
+__device__ __forceinline__ void bulk_wait_read_but_last() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 __device__ __forceinline__ f2 f2_add(f2 a, f2 b)
 {
