@@ -570,7 +570,7 @@ def launches_per_step(p):
     conversions into and out of the fp32 states they pass on."""
     if p.cu_seqlens is not None:
         return 3
-    if 1 <= p.T <= 4:
+    if 1 <= p.T <= 16:   # the token-recurrent kernels
         return 1
     conv = int(p.state_dtype == STATE_BF16) * (int(p.initial_state is not None) + int(p.want_final))
     if scan_groups_per_step(p) > 1:

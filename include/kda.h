@@ -103,9 +103,10 @@ typedef enum {
  *
  * When T == 0 (no tokens at all) q, k, v, g, beta and out may be NULL.
  *
- * Fixed-length problems of 1 to 4 tokens per sequence (decode steps) are evaluated token by
- * token, as kda_fwd_recurrent does (same kernels, same bits, no workspace); everything else
- * takes the chunked form.
+ * Fixed-length problems of 1 to 16 tokens per sequence (decode steps, short speculative runs)
+ * are evaluated token by token, as kda_fwd_recurrent does (same kernels, same bits, no
+ * workspace), where that is faster than the chunked form; everything else takes the chunked
+ * form.
  *
  * Fixed-length problems with N x H <= 16 pairs and at least 32 chunks per sequence replace the
  * serial chain of the recurrence by a scan along T when its cost model says it is faster
@@ -136,7 +137,7 @@ kda_status_t kda_fwd(const void *q, const void *k, const void *v, const void *g,
 /*
  * Bytes of workspace kda_fwd_ws needs for this problem size (an upper bound that depends
  * only on N, T, H and whether cu_seqlens is given: varlen != 0).  0 for invalid sizes and for
- * the fixed-length problems of 1 to 4 tokens per sequence, which need none.
+ * the fixed-length problems of 1 to 16 tokens per sequence, which need none.
  */
 size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen);
 
@@ -199,7 +200,7 @@ kda_status_t kda_fwd_ws_profiled(const void *q, const void *k, const void *v, co
  * this hardware: the bf16 state is less precise (its rounding accumulates over the chunks) and the
  * Neumann product costs more tensor-core steps; neither is faster here.  Same arguments, layouts and
  * errors as kda_fwd_ws, plus KDA_ERR_INVALID_ARGUMENT for unknown variant bits.  Fixed-length
- * problems of 1 to 4 tokens per sequence take the token-recurrent kernels whatever the variant.
+ * problems of 1 to 16 tokens per sequence take the token-recurrent kernels whatever the variant.
  */
 kda_status_t kda_fwd_ws_variant(const void *q, const void *k, const void *v, const void *g, const void *beta,
                                 float scale, void *out, const float *A_log, const float *dt_bias,
@@ -229,7 +230,7 @@ kda_status_t kda_fwd_ws_variant(const void *q, const void *k, const void *v, con
  *     before reading it, so nothing has to be cleared between calls.
  *   - Problems whose workspace (kda_fwd_workspace_size(N, T, H, cu_seqlens != NULL)) exceeds
  *     KDA_NOALLOC_SCRATCH_BYTES (a single 8192-token sequence with 96 heads does) are rejected
- *     with KDA_ERR_UNSUPPORTED before any CUDA call.  Fixed-length problems of 1 to 4 tokens per
+ *     with KDA_ERR_UNSUPPORTED before any CUDA call.  Fixed-length problems of 1 to 16 tokens per
  *     sequence need no workspace and make no lookup.
  *
  * Same arguments, results and other errors as kda_fwd; KDA_ERR_CUDA if the address lookup fails.

@@ -119,10 +119,12 @@ def test_workspace_size(lib):
     hdr = -(-(-(-(9 * 8 + 8 * 4) // 16) * 16 + mc * 16) // 256) * 256
     assert lib.kda_fwd_workspace_size(8, 8192, 96, 1) == hdr + mc * 96 * slot
     assert lib.kda_fwd_workspace_size(0, 10, 1, 0) == 0
-    # fixed-length problems of 1-4 tokens per sequence take the token-recurrent kernels: no workspace
+    # fixed-length problems of 1-16 tokens per sequence take the token-recurrent kernels: no workspace
     assert lib.kda_fwd_workspace_size(256, 1, 96, 0) == 0
     assert lib.kda_fwd_workspace_size(256, 4, 96, 0) == 0
-    assert lib.kda_fwd_workspace_size(256, 5, 96, 0) == 256 * 96 * slot
+    assert lib.kda_fwd_workspace_size(256, 16, 96, 0) == 0
+    assert lib.kda_fwd_workspace_size(256, 17, 96, 0) == 256 * 96 * slot
+    assert lib.kda_fwd_workspace_size(1, 5, 96, 1) > 0   # varlen: always the chunked form
 
 
 def test_scan_groups_and_workspace(lib):

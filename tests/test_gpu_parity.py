@@ -34,8 +34,11 @@ def test_workload_parity(idx):
 
 
 @pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 31, 63, 64, 65, 127, 128, 129, 200, 333])
-def test_lengths_across_chunk_and_subblock_edges(T):
-    p = make_problem(B=1, T=T, H=3, seed=100 + T)
+@pytest.mark.parametrize("varlen", [False, True])
+def test_lengths_across_chunk_and_subblock_edges(T, varlen):
+    """Every length across the 16-token sub-blocks and the 64-token chunks; as one varlen sequence the chunked
+    kernels take every length (fixed-length problems of up to 16 tokens take the token-recurrent kernels)."""
+    p = make_problem(B=1, T=T, H=3, seed=100 + T, cu_seqlens=np.array([0, T]) if varlen else None)
     out, fin = run_gpu(p)
     assert_parity(out, fin, *oracle_run(p))
 
@@ -67,7 +70,7 @@ def test_fixed_length_batch():
 def test_varlen_bitexact_against_separate_calls():
     """One varlen call equals separate per-sequence calls bit for bit (cu_seqlens indexing).  The separate
     calls are one-sequence varlen calls, so that every call takes the chunked form (fixed-length calls of
-    1-4 tokens take the token-recurrent kernels)."""
+    1-16 tokens take the token-recurrent kernels)."""
     lens = [5, 0, 64, 131, 1, 17]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     p = make_problem(B=1, T=int(cu[-1]), H=3, seed=10, cu_seqlens=cu)
@@ -358,10 +361,10 @@ def test_workspace_too_small_rejected():
         _call(p, dev, out, None, workspace=ws)
 
 
-@pytest.mark.parametrize("T", [1, 3, 4])
+@pytest.mark.parametrize("T", [1, 3, 4, 5, 12, 16])
 @pytest.mark.parametrize("state", [STATE_NONE, STATE_BF16, STATE_FP32])
 def test_short_fixed_length_takes_the_token_recurrent_kernels(T, state):
-    """kda_fwd on fixed-length problems of 1-4 tokens gives the bits of kda_fwd_recurrent (the same
+    """kda_fwd on fixed-length problems of 1-16 tokens gives the bits of kda_fwd_recurrent (the same
     kernels) and meets the oracle."""
     p = make_problem(B=6, T=T, H=3, seed=60 + T, state_dtype=state)
     a = run_gpu(p)
