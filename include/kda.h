@@ -164,6 +164,14 @@ int kda_fwd_scan_groups(int N, int64_t T, int H, int varlen);
  * NULL when that size is 0).  The workspace must not be used by anything else until the
  * call has completed on `stream`.  Same arguments, results and errors as kda_fwd, plus
  * KDA_ERR_INVALID_ARGUMENT for a missing, misaligned or too small workspace.
+ *
+ * CUDA graphs: a kda_fwd_ws call (like a kda_fwd_recurrent call) can be captured from `stream`
+ * into a CUDA graph once a call of any size has run on the device outside a capture (the first
+ * call on a device sets the kernels' attributes and caches device properties).  The graph holds
+ * the call's launches and copies for whichever schedule the size selects (one launch of each
+ * kernel, pieces with programmatic dependent launches, the scan along T, varlen, the
+ * token-recurrent kernels) and its replays give the bits of direct calls on the data then in the
+ * captured buffers (tests/test_gpu_graph.py).
  */
 kda_status_t kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,
                         float scale, void *out, const float *A_log, const float *dt_bias,
