@@ -27,6 +27,9 @@ namespace {
 constexpr int HOST_RING = 2;            // device piece buffers in flight
 constexpr int64_t HOST_MAX_PIECES = 8;
 constexpr int64_t HOST_MIN_PIECE = 512; // tokens
+// the last fixed-length piece about 1 / HOST_TAIL of the others, so that less compute and copy-out follows the
+// last copy in (T=8192 H=96: 4.46 -> 4.43 ms per call)
+constexpr int64_t HOST_TAIL = 4;
 
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16 *src, float *dst, size_t n)
 {
@@ -265,6 +268,10 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     if (!varlen && T > HOST_MIN_PIECE) {
         pieces = std::min<int64_t>(HOST_MAX_PIECES, (T + HOST_MIN_PIECE - 1) / HOST_MIN_PIECE);
         PT = ((T + pieces - 1) / pieces + CH - 1) / CH * CH;
+        if (pieces > 1) {   // T = (pieces - 1) PT + PT / HOST_TAIL
+            const int64_t den = (pieces - 1) * HOST_TAIL + 1;
+            PT = ((T * HOST_TAIL + den - 1) / den + CH - 1) / CH * CH;
+        }
         pieces = (T + PT - 1) / PT;
     }
     const int ring = pieces > 1 ? HOST_RING : 1;
