@@ -1,5 +1,5 @@
 // KDA decode kernel: the per-token gated delta rule (guancyxx.cn FlashKDA article, section 一) for
-// fixed-length problems of 1 to 4 tokens per sequence -- decode steps, and short speculative runs.
+// fixed-length problems of 1 to 8 tokens per sequence -- decode steps, and short speculative runs.
 //
 // Per token (state S in R^{K x V}, stored transposed [V][K]):
 //   S' = Diag(alpha) S,   u = b (v - S'^T k^),   S = S' + k^ u^T,   o = scale S^T q^
@@ -29,7 +29,10 @@ constexpr int DC_CONSUMER_WARPS = 8;
 constexpr int DC_THREADS = (DC_CONSUMER_WARPS + 1) * 32;
 constexpr int DC_VALUES = 64;      // values per item
 constexpr int DC_RING = 3;         // slots
-constexpr int DC_MAX_T = 4;
+#ifndef KDA_DC_MAX_T
+#define KDA_DC_MAX_T 8
+#endif
+constexpr int DC_MAX_T = KDA_DC_MAX_T;   // one stage of the token-recurrent kernel at most (same bits)
 
 struct DcHdr {
     long long tok0;                // first token of the item's sequence
@@ -372,22 +375,31 @@ cudaError_t launch_decode_t(const Problem &p, cudaStream_t stream)
         if (dev < 64)
             configured[dev] = true;
     }
+    // persistent: as many CTAs per SM as their shared memory allows (two up to 4 tokens with an fp32 state)
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_decode_kernel<S>, DC_THREADS, smem);
+    if (err != cudaSuccess)
+        return err;
+    per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
     const int n_items = 2 * p.N * p.H;   // the entry point checks 2 N H <= INT32_MAX
-    const int grid = n_items < 2 * nsm ? n_items : 2 * nsm;
+    const int grid = n_items < per_sm * nsm ? n_items : per_sm * nsm;
     kda_decode_kernel<S><<<grid, DC_THREADS, smem, stream>>>(p, n_items, lay.bytes);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// Fixed-length problems of 1-4 tokens.  Both kernels give the same bits; the choice is by measurement on
-// GB300: for one token with an fp32 state (64 KB of state traffic per item) the staged kernel streams the
-// state slightly faster (0.493 against 0.519 ms at 256 sequences x 96 heads); for bf16 states (0.252 against
-// 0.394 ms) and for 2-4 tokens (64 sequences x 4 tokens: 0.180 / 0.164 against 0.211 / 0.187 ms for fp32 /
-// bf16 states) the decode kernel is faster.
+// Fixed-length problems of up to DC_MAX_T tokens.  Both kernels give the same bits; the choice is by measurement
+// on GB300 (64 and 256 sequences x 96 heads, decode kernel against the staged kernel):
+//   fp32 state: 1 token 0.493 against 0.494 ms (the staged kernel streams the state as fast); 2-5 tokens faster
+//     (1.15x at 5); from 6 tokens slower (0.8x: the three-slot ring of 8 tokens and a 32 KB state leaves one
+//     CTA per SM);
+//   bf16 state: faster up to 7 tokens (1.65x at 1, 1.11x at 5, 1.03x at 7), the same at 8.
 bool decode_applies(const Problem &p, int state_kind)
 {
-    return p.cu == nullptr && p.T >= 1 && p.T <= DC_MAX_T && !(state_kind == 2 && p.T == 1);
+    if (p.cu != nullptr || p.T < 1)
+        return false;
+    return state_kind == 2 ? (p.T >= 2 && p.T <= 5) : p.T <= 7;
 }
 
 cudaError_t launch_decode(const Problem &p, int state_kind, cudaStream_t stream)

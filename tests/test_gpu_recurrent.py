@@ -171,12 +171,12 @@ def test_repeat_calls_are_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-@pytest.mark.parametrize("T", [1, 2, 4])
+@pytest.mark.parametrize("T", [1, 2, 4, 5, 7, 8])
 @pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
 def test_decode_kernel_matches_staged_kernel(T, state):
-    """Fixed-length problems of 1-4 tokens take the barrier-free decode kernel; the same tokens as varlen
-    sequences take the staged kernel.  Both evaluate the tokens as one stage with the same rounding: the
-    bits agree."""
+    """Fixed-length problems of up to 7 tokens (5 with an fp32 state) take the barrier-free decode kernel; the
+    same tokens as varlen sequences take the staged kernel.  Both evaluate the tokens as one stage with the
+    same rounding: the bits agree."""
     p = make_problem(B=5, T=T, H=3, seed=320 + T, state_dtype=state)
     o_dec, f_dec = run_rec(p)
     cu = np.arange(0, 5 * T + 1, T, dtype=np.int64)
