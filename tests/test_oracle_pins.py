@@ -192,6 +192,21 @@ def test_chunked_form_equals_recurrence(C, inverse):
     assert rel_l2(oc, out) < 1e-10 and rel_l2(fc, fin) < 1e-10
 
 
+@pytest.mark.parametrize("groups", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("lb", [-0.05, 0.0])
+def test_scan_along_t_equals_recurrence(groups, lb):
+    """The chunk-transition scan along T (group maps S -> M S + B composed from S = I with U0 = 0 and from
+    S = 0, start states chained, groups re-run) equals the token recurrence, with ragged last groups and chunks;
+    with slow or no decay the group transitions stay far above the tolerance (a mistake in the chaining would
+    show at their size), so the chaining is exercised."""
+    p = inputs.make_problem(B=2, T=1000, H=1, seed=31, lower_bound=lb)
+    out, fin = run(p)
+    oc, fc, Ms = chunked_ref.scan_form(p, groups)
+    assert rel_l2(oc, out) < 1e-10 and rel_l2(fc, fin) < 1e-10
+    if groups > 1:
+        assert min(np.linalg.norm(M) for M in Ms) > (1.0 if lb == 0.0 else 1e-6)
+
+
 def test_subblock_factorised_chunked_form_equals_recurrence():
     """The 16-row sub-block factorisation of the decay (no overflow at lower_bound = -5, C = 64)."""
     p = inputs.make_problem(B=1, T=200, H=2, seed=13, cu_seqlens=np.array([0, 1, 64, 65, 200]))
