@@ -35,7 +35,7 @@ constexpr int TM_X = 0, TM_O = 64, TM_S = 128, TM_S16 = 256, TM_U16 = 320;
 constexpr int NBUF = 3;
 constexpr int SLOT_HEAD = SLOT_U0;          // bytes of the first copy
 constexpr int OFF_BAR = NBUF * SLOT_BYTES;
-constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load 0..2, product X|O, update; tmem slot; flag
+constexpr int RECUR_SMEM = OFF_BAR + 64;    // mbarriers: load 0..2, product X|O, update; tmem slot
 static_assert(RECUR_SMEM <= 232448, "shared memory budget");
 static_assert(SLOT_BYTES % 128 == 0 && SLOT_HEAD % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SLOT_BYTES - SLOT_HEAD >= CH * D * 2, "output staging fits in U0^T and Gamma_C");
@@ -182,7 +182,6 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
     const int nch = (int)((len + CH - 1) / CH);
 
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 40);
-    volatile uint32_t *hang_flag = reinterpret_cast<volatile uint32_t *>(sm + OFF_BAR + 44);
     const uint32_t mbarL = smem_u32(sm + OFF_BAR);   // + 8 b: slot of buffer b landed
     const uint32_t mbarQ = smem_u32(sm + OFF_BAR + 24), mbarB = smem_u32(sm + OFF_BAR + 32);
     auto slot_ptr = [&](int c) -> const unsigned char * {
@@ -222,7 +221,6 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             mbar_init(mbarL + 8 * b, 1);
         mbar_init(mbarQ, 1);
         mbar_init(mbarB, 1);
-        *hang_flag = 0u;
         mbar_fence_init();
     }
     __syncthreads();
@@ -344,15 +342,13 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         const int64_t rem = len - (int64_t)c * CH;
         const int L = (int)(rem < CH ? rem : CH);
 
-        // the previous update is complete and this chunk's slot has landed
+        // the previous update is complete and this chunk's slot has landed (each thread waits; no barrier here: a
+        // wait that gave up is reduced over the CTA at P1's barrier, which every thread reaches either way)
         bool ok = true;
         if (c > 0)
             ok = mbar_wait(mbarB, (c - 1) & 1, p.wait_polls);
         ok = ok && mbar_wait(mbarL + 8 * (c % NBUF), (c / NBUF) & 1, p.wait_polls);
-        if (__syncthreads_or(!ok)) {
-            hung = true;
-            break;
-        }
+        __syncwarp();   // the warp's lanes leave their waits together before the warp-wide tensor-memory loads
         tc_fence_after();
 
         // ---- P1: fp16 copy of S^T (A operand), S^T <- S^T Diag(Gamma_C), previous output read-out (one
@@ -388,7 +384,10 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             tmem_wait_st();
         }
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(!ok)) {   // a wait above gave up in some thread
+            hung = true;
+            break;
+        }
         // QW and KA of chunk c + 2 into chunk c - 1's buffer (only chunk c - 1's products, complete, read them), by
         // another warp while the first product is issued
         if (c + 2 < nch) {
@@ -413,9 +412,8 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
 
         // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
         // (no barrier: each thread waits for the product itself; a wait that gave up is reported through the
-        // flag, which every thread reads after the next barrier)
-        if (!mbar_wait(mbarQ, c & 1, p.wait_polls))
-            *hang_flag = 1u;
+        // reduction of the next barrier)
+        const bool qok = mbar_wait(mbarQ, c & 1, p.wait_polls);
         tc_fence_after();
 #pragma unroll 1
         for (int t = 0; t < TILES; ++t) {
@@ -439,8 +437,7 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
             tmem_st16(trow + col_u16(t) + half * 16, hv);
         }
         tc_fence_before();
-        __syncthreads();
-        if (*hang_flag) {
+        if (__syncthreads_or(!qok)) {
             hung = true;
             break;
         }
