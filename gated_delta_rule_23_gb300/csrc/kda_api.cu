@@ -141,7 +141,7 @@ int64_t max_chunks(int N, int64_t T, bool varlen)
 // recurrence over piece i (one CTA per pair, on a part of the SMs) runs beside the prep kernel of piece
 // i + 1 on the SMs it leaves free, and the state passes from piece to piece in fp32, exactly as the
 // recurrence keeps it between chunks, so the results are the same bits as one launch over all chunks.
-// With P pieces the overlap hides about (1 - 1/P) of the shorter of two times: the recurrence's (≈1.52 us
+// With P pieces the overlap hides about (1 - 1/P) of the shorter of two times: the recurrence's (≈1.43 us
 // per chunk step on GB300) scaled by the fraction of SMs it leaves free, and the prep kernel's (≈5.9 us
 // per (chunk, head) item per SM); each piece costs about 12 us (the prep kernel's last wave and the
 // recurrence's start), so the best P is near sqrt(hidden time / 12 us), rounded down.  With more than 64
@@ -154,6 +154,7 @@ int64_t max_chunks(int N, int64_t T, bool varlen)
 #endif
 constexpr int MAX_PIECES = 8;
 constexpr int64_t PIECE_MIN_CHUNKS = 16;   // chunks per piece at least
+constexpr double CHUNK_STEP_US = 1.43;     // the recurrence's chain per 64-token chunk, measured on GB300
 
 bool piece_mode(int N, int64_t T, int H, bool varlen)
 {
@@ -166,7 +167,7 @@ int piece_count(int64_t nch, int64_t pairs, int nsm)
     const int64_t most = std::min<int64_t>(MAX_PIECES, nch / PIECE_MIN_CHUNKS);
     int64_t n = KDA_PIECES_FORCE;
     if (n <= 0 && nsm > 0) {
-        const double recur_us = 1.52 * (double)nch * (double)std::max<int64_t>(nsm - pairs, 0) / nsm;
+        const double recur_us = CHUNK_STEP_US * (double)nch * (double)std::max<int64_t>(nsm - pairs, 0) / nsm;
         const double prep_us = 5.9 * (double)nch * (double)pairs / nsm;
         n = (int64_t)std::sqrt(std::min(recur_us, prep_us) / 12.0);
     }
@@ -178,7 +179,7 @@ int piece_count(int64_t nch, int64_t pairs, int nsm)
 // parallel (2 (G - 1) CTAs per pair at ≈1.38 us per chunk step, or G - 1 CTAs that carry both states at ≈2.32 us,
 // whichever finishes first in waves of 152 CTAs), chained serially (G - 1 fp32 steps of ≈1.7 us), then run in
 // parallel (G CTAs per pair).  G comes from a cost model of those three launches against the
-// serial chain (≈1.52 us per chunk, less what the pieces hide) on the 152 SMs of a GB300, with the step
+// serial chain (≈1.43 us per chunk, less what the pieces hide) on the 152 SMs of a GB300, with the step
 // costs measured there; it depends only on N, T and H, like the workspace that holds the scan's matrices.
 #ifndef KDA_SCAN_GROUPS_FORCE
 #define KDA_SCAN_GROUPS_FORCE 0   // > 0: this many groups wherever the scan may run (measurement builds)
@@ -186,8 +187,7 @@ int piece_count(int64_t nch, int64_t pairs, int nsm)
 constexpr int SCAN_MAX_PAIRS = 16;
 constexpr int SCAN_MAX_GROUPS = 32;
 constexpr int MODEL_SMS = 152;
-constexpr double CHUNK_STEP_US = 1.52, COMPOSE_STEP_US = 1.38, COMPOSE2_STEP_US = 2.32, SCAN_STEP_US = 1.7,
-                 SCAN_FIXED_US = 10.0;
+constexpr double COMPOSE_STEP_US = 1.38, COMPOSE2_STEP_US = 2.32, SCAN_STEP_US = 1.7, SCAN_FIXED_US = 10.0;
 
 int64_t model_waves(int64_t ctas) { return (ctas + MODEL_SMS - 1) / MODEL_SMS; }
 // the compose form for G groups: true = one CTA per (group, pair) carrying both states

@@ -134,7 +134,7 @@ def test_scan_groups_and_workspace(lib):
     assert lib.kda_fwd_scan_groups(2, 8200, 8, 0) == 9      # 129 chunks: 9 groups of 15 (the last 9)
     assert lib.kda_fwd_scan_groups(1, 2049, 3, 0) == 7      # 33 chunks: 7 groups of 5 (the last 3)
     assert lib.kda_fwd_scan_groups(1, 32768, 8, 0) == 19    # 512 chunks: 19 groups of 27 (the last 26)
-    assert lib.kda_fwd_scan_groups(1, 32768, 1, 0) == 32
+    assert lib.kda_fwd_scan_groups(1, 32768, 1, 0) == 27    # 512 chunks: 27 groups of 19 (the last 18)
     assert lib.kda_fwd_scan_groups(1, 8192, 17, 0) == 1     # more than 16 pairs
     assert lib.kda_fwd_scan_groups(1, 1984, 1, 0) == 1      # fewer than 32 chunks
     assert lib.kda_fwd_scan_groups(8, 8192, 1, 1) == 1      # varlen
