@@ -25,11 +25,33 @@ namespace kda {
 namespace {
 
 constexpr int HOST_RING = 2;            // device piece buffers in flight
-constexpr int64_t HOST_MAX_PIECES = 8;
+constexpr int64_t HOST_MAX_PIECES = 8;  // varlen pieces; fixed-length big pieces
 constexpr int64_t HOST_MIN_PIECE = 512; // tokens
-// the last fixed-length piece about 1 / HOST_TAIL of the others, so that less compute and copy-out follows the
-// last copy in (T=8192 H=96: 4.46 -> 4.43 ms per call)
-constexpr int64_t HOST_TAIL = 4;
+constexpr int64_t HOST_TAIL_MIN = 2;    // chunks of the last fixed-length piece
+
+// Chunks per fixed-length piece.  Copying a token in takes about twice as long as computing it and copying its
+// output back, so a piece's compute and copy-out hide behind the copy-in of the pieces after it only if those
+// are at least about half its size: up to HOST_MAX_PIECES big pieces of about nch / 8 chunks (at least
+// HOST_MIN_PIECE tokens), then a tail that halves down to HOST_TAIL_MIN chunks, so that little work follows the
+// last copy in.  One piece when T <= HOST_MIN_PIECE.
+std::vector<int64_t> host_piece_chunks(int64_t nch)
+{
+    if (nch * CH <= HOST_MIN_PIECE)
+        return {nch};
+    const int64_t big = std::max<int64_t>(HOST_MIN_PIECE / CH, (nch + HOST_MAX_PIECES - 1) / HOST_MAX_PIECES);
+    std::vector<int64_t> tail;
+    int64_t tail_sum = 0;
+    for (int64_t t = HOST_TAIL_MIN; t < big && tail_sum + t <= nch - big; t *= 2) {
+        tail.push_back(t);
+        tail_sum += t;
+    }
+    const int64_t rest = nch - tail_sum, nbig = (rest + big - 1) / big;
+    std::vector<int64_t> plan;
+    for (int64_t i = 0; i < nbig; ++i)
+        plan.push_back(rest / nbig + (i < rest % nbig ? 1 : 0));
+    plan.insert(plan.end(), tail.rbegin(), tail.rend());
+    return plan;
+}
 
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16 *src, float *dst, size_t n)
 {
@@ -263,17 +285,19 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     const size_t sbytes = state_dtype == KDA_DTYPE_FP32 ? 4 : 2;
     const bool has_state = initial_state || final_state;
 
-    // pieces: whole 64-token chunks, at most HOST_MAX_PIECES, at least HOST_MIN_PIECE tokens each
-    int64_t pieces = 1, PT = T;
+    // pieces of whole 64-token chunks (host_piece_chunks); piece p starts at token first[p]
+    std::vector<int64_t> first{0};
+    int64_t PT = T;   // tokens of the largest piece
     if (!varlen && T > HOST_MIN_PIECE) {
-        pieces = std::min<int64_t>(HOST_MAX_PIECES, (T + HOST_MIN_PIECE - 1) / HOST_MIN_PIECE);
-        PT = ((T + pieces - 1) / pieces + CH - 1) / CH * CH;
-        if (pieces > 1) {   // T = (pieces - 1) PT + PT / HOST_TAIL
-            const int64_t den = (pieces - 1) * HOST_TAIL + 1;
-            PT = ((T * HOST_TAIL + den - 1) / den + CH - 1) / CH * CH;
+        PT = 0;
+        for (int64_t ch : host_piece_chunks((T + CH - 1) / CH)) {
+            PT = std::max(PT, ch * CH);
+            first.push_back(first.back() + ch * CH);
         }
-        pieces = (T + PT - 1) / PT;
+    } else {
+        first.push_back(T);
     }
+    const int64_t pieces = (int64_t)first.size() - 1;
     const int ring = pieces > 1 ? HOST_RING : 1;
     const size_t tok_cap = (size_t)B * (size_t)PT;     // tokens of one piece (all batch rows)
 
@@ -304,7 +328,10 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     if (e == cudaSuccess && !chain && final_state) e = bufs.get(&dfin, state_elems * sbytes);
     if (e == cudaSuccess && chain && initial_state && state_dtype == KDA_DTYPE_BF16) e = bufs.get(&dinit, state_elems * 2);
     if (e == cudaSuccess && chain && final_state && state_dtype == KDA_DTYPE_BF16) e = bufs.get(&dfin, state_elems * 2);
-    if (e == cudaSuccess) e = bufs.get(&dws, workspace_bytes(N, PT, H, varlen));
+    size_t ws_bytes = 0;   // the largest of the pieces' workspaces (a shorter piece may take another schedule)
+    for (int64_t p = 0; p < pieces; ++p)
+        ws_bytes = std::max(ws_bytes, workspace_bytes(N, varlen ? T : std::min<int64_t>(first[p + 1], T) - first[p], H, varlen));
+    if (e == cudaSuccess) e = bufs.get(&dws, ws_bytes);
     if (e == cudaSuccess) e = cudaEventRecord(c->e_start, sc);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_in, c->e_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_start, 0);
@@ -339,7 +366,7 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     kda_status_t st = KDA_OK;
     for (int64_t p = 0; p < pieces && st == KDA_OK; ++p) {
         const int slot = (int)(p % ring);
-        const int64_t t0 = p * PT, pt = std::min<int64_t>(PT, T - t0);
+        const int64_t t0 = first[p], pt = std::min<int64_t>(first[p + 1], T) - t0;
         const size_t w = (size_t)pt * row * 2, wb = (size_t)pt * H * 2;                 // bytes per batch row
         const size_t sp = (size_t)T * row * 2, spb = (size_t)T * H * 2;                 // host pitches
         const size_t o = (size_t)t0 * row * 2, ob = (size_t)t0 * H * 2;                 // host offsets

@@ -281,7 +281,12 @@ kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, cons
  * problems are cut into pieces of whole 64-token chunks, varlen problems into pieces of whole
  * sequences, and the copies of neighbouring pieces overlap the kernels on three streams of the
  * library's own; the state passes between fixed-length pieces in fp32 (varlen pieces share none),
- * so the results are bit-identical to kda_fwd on the same data.  Page-locked (pinned) host
+ * so the results are bit-identical to kda_fwd on the same data -- except where kda_fwd, or a
+ * piece, runs the scan along T (kda_fwd_scan_groups > 1: at most 16 (sequence, head) pairs with
+ * long sequences), whose grouping of the chunks differs: there the two agree within the parity
+ * tolerances of the oracle (and bit for bit when the decay is strong enough that a chunk forgets
+ * its start state, as with lower_bound = -5).  The fixed-length pieces are up to 8 big pieces of
+ * about T / 8 tokens, then a tail that halves down to 128 tokens.  Page-locked (pinned) host
  * memory lets the copies run asynchronously; pageable memory works but the copies do not overlap.
  * Device memory comes from the library's pool (see kda_workspace_trim).  Calls are serialised per
  * device.  Errors: those of kda_fwd (cu_seqlens is also checked, on the host, as

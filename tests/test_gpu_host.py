@@ -1,14 +1,16 @@
 """The host-buffer entry point kda_fwd_host against kda_fwd on the device: the pipelined pieces
 (whole 64-token chunks with the state chained in fp32; for varlen problems, whole sequences) give the
 same bits as one device call, for every state dtype and presence, ragged last pieces, batches, varlen
-problems (in place too), pageable memory and T = 0."""
+problems (in place too), pageable memory and T = 0; where the device call runs the scan along T (at most
+16 (sequence, head) pairs, long sequences) and the decay is slow, the two agree within the parity bar."""
 import numpy as np
 import pytest
 import torch
 
-from gated_delta_rule_23_gb300 import kda_fwd_host
+import oracle
+from gated_delta_rule_23_gb300 import _native, kda_fwd_host
 from gated_delta_rule_23_gb300.inputs import STATE_BF16, STATE_FP32, STATE_NONE, make_problem
-from tests.gpu_util import bf16_tensor, run_gpu
+from tests.gpu_util import assert_parity, bf16_tensor, rel_l2, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +51,28 @@ def assert_same(p, pinned=True):
 @pytest.mark.parametrize("T", [1, 64, 512, 513, 2500, 4096])
 def test_pieces_equal_one_device_call(T):
     assert_same(make_problem(B=1, T=T, H=3, seed=400 + T))
+
+
+@pytest.mark.parametrize("T", [2500, 8200])
+def test_pieces_equal_one_device_call_slow_decay(T):
+    """Slow decay (the state carries across every piece) with 17 heads: more than 16 pairs, so the device call
+    runs one chain per pair (in pieces beside the prep kernel); the host pieces, ending in a tail of 16, 8, 4
+    and 2 chunks at T = 8200 (the last chunk 8 tokens), give its bits."""
+    assert _native.load().kda_fwd_scan_groups(1, T, 17, 0) == 1
+    assert_same(make_problem(B=1, T=T, H=17, seed=420 + T, state_dtype=STATE_FP32, lower_bound=-0.05))
+
+
+def test_scan_problem_within_parity_of_device_call():
+    """Three heads, T = 4096, slow decay: the device call runs the scan along T, the host pieces (8 chunks and
+    fewer) one chain per pair; both match the oracle within the parity bar and each other closely."""
+    p = make_problem(B=1, T=4096, H=3, seed=421, state_dtype=STATE_FP32, lower_bound=-0.05)
+    assert _native.load().kda_fwd_scan_groups(1, 4096, 3, 0) > 1
+    out_h, fin_h = run_host(p)
+    out_d, fin_d = run_gpu(p)
+    o_ref, f_ref = oracle.kda_fwd_problem(p)
+    assert_parity(out_h, fin_h, o_ref, f_ref)
+    assert_parity(out_d, fin_d, o_ref, f_ref)
+    assert rel_l2(out_h, out_d) < 2e-3 and rel_l2(fin_h, fin_d) < 2e-3
 
 
 @pytest.mark.parametrize("state", [STATE_NONE, STATE_BF16, STATE_FP32])
