@@ -140,10 +140,22 @@ cudaError_t launch_convert(const void *src, void *dst, size_t n, bool to_f32, cu
 
 namespace {
 
-// Varlen pipeline: pieces of whole sequences [sb[p], sb[p + 1]), each about T / P tokens (P at most
-// HOST_MAX_PIECES, pieces of at least HOST_MIN_PIECE tokens where the lengths allow).  Piece p's token rows
-// [cu[s0], cu[s1]) are contiguous in every token tensor, its states are the contiguous slices of sequences s0 ..
-// s1 - 1, and its cu_seqlens is cu[s0 .. s1] - cu[s0] (all pieces' arrays go to the device in one copy).
+// Varlen pipeline: pieces of whole sequences [s0, s1), each about T / P tokens (P at most HOST_MAX_PIECES, pieces
+// of at least HOST_MIN_PIECE tokens where the lengths allow).  A piece's token rows [cu[s0], cu[s1]) are contiguous
+// in every token tensor, its states are the contiguous slices of sequences s0 .. s1 - 1, and its cu_seqlens is
+// cu[s0 .. s1] - cu[s0] (all pieces' arrays go to the device in one copy).  The longest sequence (the last of equals),
+// when it spans at least 2 HOST_TAIL_MIN chunks, is in no such piece: it comes last, as a halving tail of pieces of
+// whole chunks (each a one-sequence varlen call), its state chained between them in fp32 as in the fixed-length
+// pipeline, so that little compute and copy-out follows the last copy in; its chunks start where the sequence's do,
+// so the results are the bits of one call.
+struct VarlenPiece {
+    int64_t t0, pt;   // token rows
+    int s0, ns;       // sequences (a tail piece: the last sequence, ns = 1)
+    size_t cu_off;    // its cu_seqlens in the device array
+    bool tail;        // a part of the last sequence, state in the fp32 chain
+    bool first_tail, last_tail;
+};
+
 kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const void *v, const void *g, const void *beta,
                              float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
                              const void *initial_state, void *final_state, kda_dtype_t state_dtype,
@@ -152,37 +164,78 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
     const size_t row = (size_t)H * D;                  // elements of one token's q / k / v / g / out
     const size_t smat = (size_t)H * D * D;             // state elements of one sequence
     const size_t sbytes = state_dtype == KDA_DTYPE_FP32 ? 4 : 2;
-    const int64_t want = std::min<int64_t>(std::min<int64_t>(HOST_MAX_PIECES, N), (T + HOST_MIN_PIECE - 1) / HOST_MIN_PIECE);
-    const int64_t target = (T + want - 1) / std::max<int64_t>(want, 1);
-    std::vector<int> sb{0};
+    // the longest sequence's chunks, cut into a halving tail, when it has enough of them
+    int star = 0;
     for (int s = 1; s < N; ++s)
-        if (cu[s] - cu[sb.back()] >= target && (int64_t)sb.size() < want)
-            sb.push_back(s);
-    sb.push_back(N);
-    const int pieces = (int)sb.size() - 1;
+        if (cu[s + 1] - cu[s] >= cu[star + 1] - cu[star])
+            star = s;
+    std::vector<int64_t> tail_chunks;
+    {
+        int64_t rem = (cu[star + 1] - cu[star] + CH - 1) / CH;
+        if (rem >= 2 * HOST_TAIL_MIN) {
+            for (; rem >= 2 * HOST_TAIL_MIN; rem /= 2)
+                tail_chunks.push_back(rem - rem / 2);
+            tail_chunks.push_back(rem);
+        } else {
+            star = -1;
+        }
+    }
+    // pieces of whole sequences around it, closed once they reach about 1 / want of the tokens left
+    const int64_t Tv = T - (star >= 0 ? cu[star + 1] - cu[star] : 0);
+    const int Nv = N - (star >= 0 ? 1 : 0);
+    const int64_t want = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(HOST_MAX_PIECES, Nv),
+                                                                (Tv + HOST_MIN_PIECE - 1) / HOST_MIN_PIECE));
+    const int64_t target = (Tv + want - 1) / want;
+    std::vector<std::pair<int, int>> ranges;
+    {
+        int s0 = 0;
+        for (int s = 0; s < N; ++s) {
+            if (s == star) {
+                if (s > s0)
+                    ranges.push_back({s0, s});
+                s0 = s + 1;
+            } else if (s > s0 && cu[s] - cu[s0] >= target && (int64_t)ranges.size() + 1 < want) {
+                ranges.push_back({s0, s});
+                s0 = s;
+            }
+        }
+        if (N > s0)
+            ranges.push_back({s0, N});
+    }
+    std::vector<VarlenPiece> pl;
     std::vector<int64_t> cus;
-    std::vector<size_t> cu_off;
+    for (const auto &r : ranges) {
+        const int s0 = r.first, s1 = r.second;
+        pl.push_back({cu[s0], cu[s1] - cu[s0], s0, s1 - s0, cus.size(), false, false, false});
+        for (int s = s0; s <= s1; ++s)
+            cus.push_back(cu[s] - cu[s0]);
+    }
+    for (size_t i = 0; i < tail_chunks.size(); ++i) {
+        const int64_t t = i == 0 ? cu[star] : pl.back().t0 + pl.back().pt;
+        const int64_t pt = std::min<int64_t>(tail_chunks[i] * CH, cu[star + 1] - t);
+        pl.push_back({t, pt, star, 1, cus.size(), true, i == 0, i + 1 == tail_chunks.size()});
+        cus.push_back(0);
+        cus.push_back(pt);
+    }
     int64_t max_t = 0;
     int max_n = 0;
     size_t max_ws = 0;
-    for (int p = 0; p < pieces; ++p) {
-        const int s0 = sb[p], s1 = sb[p + 1];
-        cu_off.push_back(cus.size());
-        for (int s = s0; s <= s1; ++s)
-            cus.push_back(cu[s] - cu[s0]);
-        const int64_t pt = cu[s1] - cu[s0];
-        max_t = std::max(max_t, pt);
-        max_n = std::max(max_n, s1 - s0);
-        max_ws = std::max(max_ws, workspace_bytes(s1 - s0, pt, H, true));
+    for (const VarlenPiece &pc : pl) {
+        max_t = std::max(max_t, pc.pt);
+        if (!pc.tail)
+            max_n = std::max(max_n, pc.ns);
+        max_ws = std::max(max_ws, workspace_bytes(pc.ns, pc.pt, H, true));
     }
+    const int pieces = (int)pl.size();
     const int ring = pieces > 1 ? HOST_RING : 1;
+    const bool chain = !tail_chunks.empty();
 
     cudaStream_t sc = c->s_comp;
     DevBufs bufs;
     bufs.s = sc;
     void *dq[HOST_RING] = {}, *dk[HOST_RING] = {}, *dv[HOST_RING] = {}, *dg[HOST_RING] = {}, *db[HOST_RING] = {},
          *dout[HOST_RING] = {}, *dinit[HOST_RING] = {}, *dfin[HOST_RING] = {};
-    void *dalog = nullptr, *ddt = nullptr, *dcu = nullptr, *dws = nullptr;
+    void *dalog = nullptr, *ddt = nullptr, *dcu = nullptr, *dws = nullptr, *dchain = nullptr, *dtail16 = nullptr;
     cudaError_t e = cudaSuccess;
     for (int i = 0; i < ring && e == cudaSuccess; ++i) {
         e = bufs.get(&dq[i], (size_t)max_t * row * 2);
@@ -198,10 +251,26 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
     if (e == cudaSuccess) e = bufs.get(&ddt, (size_t)H * D * 4);
     if (e == cudaSuccess) e = bufs.get(&dcu, cus.size() * 8);
     if (e == cudaSuccess) e = bufs.get(&dws, max_ws);
-    // parameters and every piece's cu_seqlens (compute stream), then the copy streams start
+    // the last sequence's state between its tail pieces (fp32), and its bf16 image at the ends
+    if (e == cudaSuccess && chain) e = bufs.get(&dchain, smat * 4);
+    if (e == cudaSuccess && chain && state_dtype == KDA_DTYPE_BF16 && (initial_state || final_state))
+        e = bufs.get(&dtail16, smat * 2);
+    // parameters, every piece's cu_seqlens and the last sequence's initial state (compute stream), then the copy
+    // streams start
     if (e == cudaSuccess) e = cudaMemcpyAsync(dalog, A_log, (size_t)H * 4, cudaMemcpyHostToDevice, sc);
     if (e == cudaSuccess) e = cudaMemcpyAsync(ddt, dt_bias, (size_t)H * D * 4, cudaMemcpyHostToDevice, sc);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dcu, cus.data(), cus.size() * 8, cudaMemcpyHostToDevice, sc);
+    const char *hi = static_cast<const char *>(initial_state);
+    char *hf = static_cast<char *>(final_state);
+    if (e == cudaSuccess && chain && initial_state) {
+        const char *src = hi + (size_t)star * smat * sbytes;
+        if (state_dtype == KDA_DTYPE_FP32) {
+            e = cudaMemcpyAsync(dchain, src, smat * 4, cudaMemcpyHostToDevice, sc);
+        } else {
+            e = cudaMemcpyAsync(dtail16, src, smat * 2, cudaMemcpyHostToDevice, sc);
+            if (e == cudaSuccess) e = launch_convert(dtail16, dchain, smat, true, sc);
+        }
+    }
     if (e == cudaSuccess) e = cudaEventRecord(c->e_start, sc);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_in, c->e_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_start, 0);
@@ -212,14 +281,15 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
 
     const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k);
     const char *hv = static_cast<const char *>(v), *hg = static_cast<const char *>(g);
-    const char *hb = static_cast<const char *>(beta), *hi = static_cast<const char *>(initial_state);
-    char *ho = static_cast<char *>(out), *hf = static_cast<char *>(final_state);
+    const char *hb = static_cast<const char *>(beta);
+    char *ho = static_cast<char *>(out);
     kda_status_t st = KDA_OK;
     for (int p = 0; p < pieces && st == KDA_OK; ++p) {
-        const int slot = p % ring, s0 = sb[p], np = sb[p + 1] - s0;
-        const int64_t t0 = cu[s0], pt = cu[sb[p + 1]] - t0;
+        const VarlenPiece &pc = pl[p];
+        const int slot = p % ring;
+        const int64_t t0 = pc.t0, pt = pc.pt;
         const size_t w = (size_t)pt * row * 2, o = (size_t)t0 * row * 2;
-        const size_t sw = (size_t)np * smat * sbytes, so = (size_t)s0 * smat * sbytes;
+        const size_t sw = (size_t)pc.ns * smat * sbytes, so = (size_t)pc.s0 * smat * sbytes;
         // copy in (after the slot's previous piece has been computed)
         if (p >= ring) e = cudaStreamWaitEvent(c->s_in, c->e_comp[slot], 0);
         if (pt > 0) {
@@ -230,7 +300,7 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(db[slot], hb + (size_t)t0 * H * 2, (size_t)pt * H * 2, cudaMemcpyHostToDevice, c->s_in);
         }
-        if (e == cudaSuccess && initial_state)
+        if (e == cudaSuccess && initial_state && !pc.tail)
             e = cudaMemcpyAsync(dinit[slot], hi + so, sw, cudaMemcpyHostToDevice, c->s_in);
         if (e == cudaSuccess) e = cudaEventRecord(c->e_in[slot], c->s_in);
         // compute (after the copy in, and after the slot's previous results have been copied out)
@@ -240,17 +310,29 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
             st = KDA_ERR_CUDA;
             break;
         }
+        const void *init_p = pc.tail ? ((pc.first_tail && !initial_state) ? nullptr : dchain) : dinit[slot];
+        void *fin_p = pc.tail ? dchain : dfin[slot];
+        const kda_dtype_t sdt = pc.tail ? KDA_DTYPE_FP32
+                                        : ((initial_state || final_state) ? state_dtype : KDA_DTYPE_NONE);
         st = run(dq[slot], dk[slot], dv[slot], dg[slot], db[slot], scale, dout[slot], static_cast<const float *>(dalog),
-                 static_cast<const float *>(ddt), lower_bound, dinit[slot], dfin[slot],
-                 (initial_state || final_state) ? state_dtype : KDA_DTYPE_NONE,
-                 static_cast<const int64_t *>(dcu) + cu_off[p], np, pt, H, static_cast<unsigned char *>(dws), sc);
+                 static_cast<const float *>(ddt), lower_bound, init_p, fin_p, sdt,
+                 static_cast<const int64_t *>(dcu) + pc.cu_off, pc.ns, pt, H, static_cast<unsigned char *>(dws), sc);
         if (st != KDA_OK)
             break;
-        e = cudaEventRecord(c->e_comp[slot], sc);
+        // the last sequence's final state, once its last tail piece is computed (compute stream)
+        e = cudaSuccess;
+        if (pc.last_tail && final_state) {
+            if (state_dtype == KDA_DTYPE_BF16) e = launch_convert(dchain, dtail16, smat, false, sc);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(hf + so, state_dtype == KDA_DTYPE_BF16 ? dtail16 : dchain, smat * sbytes,
+                                    cudaMemcpyDeviceToHost, sc);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(c->e_comp[slot], sc);
         // copy out
         if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_comp[slot], 0);
         if (e == cudaSuccess && pt > 0) e = cudaMemcpyAsync(ho + o, dout[slot], w, cudaMemcpyDeviceToHost, c->s_out);
-        if (e == cudaSuccess && final_state) e = cudaMemcpyAsync(hf + so, dfin[slot], sw, cudaMemcpyDeviceToHost, c->s_out);
+        if (e == cudaSuccess && final_state && !pc.tail)
+            e = cudaMemcpyAsync(hf + so, dfin[slot], sw, cudaMemcpyDeviceToHost, c->s_out);
         if (e == cudaSuccess) e = cudaEventRecord(c->e_out[slot], c->s_out);
         if (e != cudaSuccess)
             st = KDA_ERR_CUDA;

@@ -279,8 +279,9 @@ kda_status_t kda_fwd_recurrent(const void *q, const void *k, const void *v, cons
  * and copies out (and final_state) back, and returns when the results are in host memory.  The
  * FlashKDA pages have no counterpart: it is this library's end-to-end entry point.  Fixed-length
  * problems are cut into pieces of whole 64-token chunks, varlen problems into pieces of whole
- * sequences, and the copies of neighbouring pieces overlap the kernels on three streams of the
- * library's own; the state passes between fixed-length pieces in fp32 (varlen pieces share none),
+ * sequences (the longest, from 4 chunks on, last and in pieces of whole chunks), and the copies of
+ * neighbouring pieces overlap the kernels on three streams of the library's own; the state passes
+ * between pieces of one sequence in fp32 (pieces of whole sequences share none),
  * so the results are bit-identical to kda_fwd on the same data -- except where kda_fwd, or a
  * piece, runs the scan along T (kda_fwd_scan_groups > 1: at most 16 (sequence, head) pairs with
  * long sequences), whose grouping of the chunks differs: there the two agree within the parity

@@ -96,10 +96,26 @@ def test_batch_rows_are_strided_copies():
     [0, 300, 600]])                                   # too short to cut
 @pytest.mark.parametrize("state", [STATE_BF16, STATE_FP32])
 def test_varlen_pieces_of_whole_sequences(cu, state):
-    """Varlen problems run in pieces of whole sequences (each its own varlen call, no state between them)."""
+    """Varlen problems run in pieces of whole sequences (each its own varlen call, no state between them); a last
+    longest sequence of 4 chunks or more is cut into a halving tail of chunk pieces, its state chained in fp32."""
     cu = np.array(cu, dtype=np.int64)
     assert_same(make_problem(B=1, T=int(cu[-1]), H=3, seed=413, cu_seqlens=cu, state_dtype=state,
                              lower_bound=-0.05))
+
+
+@pytest.mark.parametrize("cu,state,with_initial", [
+    ([1024 * i for i in range(9)], STATE_FP32, True),            # 8 equal sequences: the last one in 8, 4, 2, 2 chunks
+    ([1024 * i for i in range(9)], STATE_BF16, True),
+    ([0, 100, 150, 3000], STATE_BF16, False),                   # a long last sequence, no initial state
+    ([0, 2000, 2000, 2000, 2193], STATE_FP32, True),            # the first sequence longest, then empty ones
+    ([0, 43, 124, 208, 481, 1355, 3852, 3931, 4584, 4747, 7102, 8070, 8192], STATE_FP32, True),  # irregular
+    ([0, 700, 1400, 1657], STATE_NONE, False)])                 # no states; last chunk ragged
+def test_varlen_longest_sequence_in_a_tail(cu, state, with_initial):
+    """The longest sequence (the last of equals) comes last, in tail pieces of whole chunks that chain its state
+    in fp32: the bits of one call, at slow decay, wherever it sits among the others."""
+    cu = np.array(cu, dtype=np.int64)
+    assert_same(make_problem(B=1, T=int(cu[-1]), H=3, seed=417, cu_seqlens=cu, state_dtype=state,
+                             with_initial=with_initial, lower_bound=-0.05))
 
 
 def test_varlen_pieces_in_place_state():
