@@ -149,10 +149,10 @@ namespace {
 // pipeline, so that little compute and copy-out follows the last copy in; its chunks start where the sequence's do,
 // so the results are the bits of one call.
 struct VarlenPiece {
-    int64_t t0, pt;   // token rows
-    int s0, ns;       // sequences (a tail piece: the last sequence, ns = 1)
+    int64_t t0, pt;   // token rows [t0, t0 + pt)
+    int s0, ns;       // sequences s0 .. s0 + ns - 1 (a tail piece: the longest sequence, ns = 1)
     size_t cu_off;    // its cu_seqlens in the device array
-    bool tail;        // a part of the last sequence, state in the fp32 chain
+    bool tail;        // a part of the longest sequence, its state in the fp32 chain
     bool first_tail, last_tail;
 };
 
