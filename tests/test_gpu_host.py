@@ -118,6 +118,31 @@ def test_varlen_longest_sequence_in_a_tail(cu, state, with_initial):
                              with_initial=with_initial, lower_bound=-0.05))
 
 
+def _random_host_cases(n=10):
+    """Seeded varlen mixes: 2 to 14 sequences of log-uniform lengths (with empty ones), 1 to 5 heads, every
+    state kind, slow or strong decay."""
+    rng = np.random.default_rng(4242)
+    cases = []
+    for i in range(n):
+        nseq = int(rng.integers(2, 15))
+        lens = np.exp(rng.uniform(np.log(1), np.log(1500), nseq)).astype(np.int64)
+        lens[rng.random(nseq) < 0.15] = 0
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        if cu[-1] <= 512:   # below that the host call is one piece
+            cu[-1] += 600
+        cases.append(dict(cu=cu, H=int(rng.integers(1, 6)), seed=500 + i,
+                          state=[STATE_NONE, STATE_BF16, STATE_FP32][i % 3], with_initial=bool(i % 2),
+                          lb=[-0.05, -5.0][i % 2]))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_host_cases(), ids=lambda c: f"N{len(c['cu']) - 1}T{c['cu'][-1]}H{c['H']}")
+def test_random_varlen_mixes(case):
+    """Seeded random varlen mixes through the host pipeline: the bits of one device call."""
+    assert_same(make_problem(B=1, T=int(case["cu"][-1]), H=case["H"], seed=case["seed"], cu_seqlens=case["cu"],
+                             state_dtype=case["state"], with_initial=case["with_initial"], lower_bound=case["lb"]))
+
+
 def test_varlen_pieces_in_place_state():
     """In place (final_state = initial_state, host memory): each piece reads its sequences' initial states
     before its final states overwrite them, and no two pieces share a sequence."""
