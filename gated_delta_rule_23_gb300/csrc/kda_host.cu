@@ -255,22 +255,12 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
     if (e == cudaSuccess && chain) e = bufs.get(&dchain, smat * 4);
     if (e == cudaSuccess && chain && state_dtype == KDA_DTYPE_BF16 && (initial_state || final_state))
         e = bufs.get(&dtail16, smat * 2);
-    // parameters, every piece's cu_seqlens and the last sequence's initial state (compute stream), then the copy
-    // streams start
+    // parameters and every piece's cu_seqlens (compute stream), then the copy streams start
     if (e == cudaSuccess) e = cudaMemcpyAsync(dalog, A_log, (size_t)H * 4, cudaMemcpyHostToDevice, sc);
     if (e == cudaSuccess) e = cudaMemcpyAsync(ddt, dt_bias, (size_t)H * D * 4, cudaMemcpyHostToDevice, sc);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dcu, cus.data(), cus.size() * 8, cudaMemcpyHostToDevice, sc);
     const char *hi = static_cast<const char *>(initial_state);
     char *hf = static_cast<char *>(final_state);
-    if (e == cudaSuccess && chain && initial_state) {
-        const char *src = hi + (size_t)star * smat * sbytes;
-        if (state_dtype == KDA_DTYPE_FP32) {
-            e = cudaMemcpyAsync(dchain, src, smat * 4, cudaMemcpyHostToDevice, sc);
-        } else {
-            e = cudaMemcpyAsync(dtail16, src, smat * 2, cudaMemcpyHostToDevice, sc);
-            if (e == cudaSuccess) e = launch_convert(dtail16, dchain, smat, true, sc);
-        }
-    }
     if (e == cudaSuccess) e = cudaEventRecord(c->e_start, sc);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_in, c->e_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_start, 0);
@@ -302,10 +292,16 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
         }
         if (e == cudaSuccess && initial_state && !pc.tail)
             e = cudaMemcpyAsync(dinit[slot], hi + so, sw, cudaMemcpyHostToDevice, c->s_in);
+        // the tail sequence's initial state with its first piece (into the fp32 chain, or its bf16 image)
+        if (e == cudaSuccess && initial_state && pc.first_tail)
+            e = cudaMemcpyAsync(state_dtype == KDA_DTYPE_FP32 ? dchain : dtail16, hi + so, smat * sbytes,
+                                cudaMemcpyHostToDevice, c->s_in);
         if (e == cudaSuccess) e = cudaEventRecord(c->e_in[slot], c->s_in);
         // compute (after the copy in, and after the slot's previous results have been copied out)
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, c->e_in[slot], 0);
         if (e == cudaSuccess && p >= ring) e = cudaStreamWaitEvent(sc, c->e_out[slot], 0);
+        if (e == cudaSuccess && initial_state && pc.first_tail && state_dtype == KDA_DTYPE_BF16)
+            e = launch_convert(dtail16, dchain, smat, true, sc);
         if (e != cudaSuccess) {
             st = KDA_ERR_CUDA;
             break;
@@ -414,28 +410,14 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     for (int64_t p = 0; p < pieces; ++p)
         ws_bytes = std::max(ws_bytes, workspace_bytes(N, varlen ? T : std::min<int64_t>(first[p + 1], T) - first[p], H, varlen));
     if (e == cudaSuccess) e = bufs.get(&dws, ws_bytes);
+    // parameters and cu_seqlens (compute stream) before the copy streams start: issued after the first piece's
+    // inputs, the copy engine could serve them only after those, and the first compute would wait for it
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dalog, A_log, (size_t)H * 4, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ddt, dt_bias, (size_t)H * D * 4, cudaMemcpyHostToDevice, sc);
+    if (e == cudaSuccess && varlen) e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(N + 1) * 8, cudaMemcpyHostToDevice, sc);
     if (e == cudaSuccess) e = cudaEventRecord(c->e_start, sc);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_in, c->e_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->s_out, c->e_start, 0);
-    if (e != cudaSuccess) {
-        cudaStreamSynchronize(sc);
-        return KDA_ERR_CUDA;
-    }
-
-    // parameters, cu_seqlens and the initial state (compute stream)
-    e = cudaMemcpyAsync(dalog, A_log, (size_t)H * 4, cudaMemcpyHostToDevice, sc);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ddt, dt_bias, (size_t)H * D * 4, cudaMemcpyHostToDevice, sc);
-    if (e == cudaSuccess && varlen) e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(N + 1) * 8, cudaMemcpyHostToDevice, sc);
-    if (e == cudaSuccess && initial_state) {
-        if (!chain) {
-            e = cudaMemcpyAsync(dinit, initial_state, state_elems * sbytes, cudaMemcpyHostToDevice, sc);
-        } else if (state_dtype == KDA_DTYPE_FP32) {
-            e = cudaMemcpyAsync(dstate, initial_state, state_elems * 4, cudaMemcpyHostToDevice, sc);
-        } else {
-            e = cudaMemcpyAsync(dinit, initial_state, state_elems * 2, cudaMemcpyHostToDevice, sc);
-            if (e == cudaSuccess) e = launch_convert(dinit, dstate, state_elems, true, sc);
-        }
-    }
     if (e != cudaSuccess) {
         cudaStreamSynchronize(sc);
         return KDA_ERR_CUDA;
@@ -461,10 +443,16 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
             if (e == cudaSuccess) e = cudaMemcpy2DAsync(dg[slot], w, hg + o, sp, w, B, cudaMemcpyHostToDevice, c->s_in);
             if (e == cudaSuccess) e = cudaMemcpy2DAsync(db[slot], wb, hb + ob, spb, wb, B, cudaMemcpyHostToDevice, c->s_in);
         }
+        // the initial state with the first piece's inputs (into the fp32 chain, or its bf16 image, converted below)
+        void *init_dst = !chain ? dinit : (state_dtype == KDA_DTYPE_FP32 ? dstate : dinit);
+        if (e == cudaSuccess && p == 0 && initial_state)
+            e = cudaMemcpyAsync(init_dst, initial_state, state_elems * sbytes, cudaMemcpyHostToDevice, c->s_in);
         if (e == cudaSuccess) e = cudaEventRecord(c->e_in[slot], c->s_in);
         // compute (after the copy in, and after the slot's previous output has been copied out)
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, c->e_in[slot], 0);
         if (e == cudaSuccess && p >= ring) e = cudaStreamWaitEvent(sc, c->e_out[slot], 0);
+        if (e == cudaSuccess && p == 0 && initial_state && chain && state_dtype == KDA_DTYPE_BF16)
+            e = launch_convert(dinit, dstate, state_elems, true, sc);
         if (e != cudaSuccess) {
             st = KDA_ERR_CUDA;
             break;
