@@ -413,16 +413,23 @@ __global__ void __launch_bounds__(RT, 1) kda_recur_kernel(const Problem p)
         // ---- P2: U^T = U0^T - X^T as fp16 into tensor memory
         // (no barrier: each thread waits for the product itself; a wait that gave up is reported through the
         // reduction of the next barrier)
+        // this thread's U0^T row of the slot (landed with it), read before the wait for the first product
+        uint4 u0w[4];
+        {
+            const unsigned char *u0row = sb + SLOT_U0 + vrow * (CH * 2);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                u0w[m] = *reinterpret_cast<const uint4 *>(u0row + (((half * 4 + m) ^ (vrow & 7)) << 4));
+        }
         const bool qok = mbar_wait(mbarQ, c & 1, p.wait_polls);
         tc_fence_after();
 #pragma unroll 1
         for (int t = 0; t < TILES; ++t) {
             uint32_t x[32], hv[16];
             tmem_ld32(trow + col_x(t) + half * 32, x);
-            const unsigned char *u0row = sb + SLOT_U0 + vrow * (CH * 2);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(u0row + (((half * 4 + m) ^ (vrow & 7)) << 4));
+                const uint4 w = u0w[m];
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
