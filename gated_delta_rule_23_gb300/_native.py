@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd_recurrent.restype = I
         lib.kda_fwd_host.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I]
         lib.kda_fwd_host.restype = I
+        lib.kda_fwd_host_plan.argtypes = [I, I64, P, P, P, P, P, I]
+        lib.kda_fwd_host_plan.restype = I
         lib.kda_fwd_ws.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t, P]
         lib.kda_fwd_ws.restype = I
         lib.kda_fwd_ws_profiled.argtypes = [P, P, P, P, P, F, P, P, P, F, P, P, I, P, I, I64, I, P, ctypes.c_size_t,

@@ -53,6 +53,20 @@ std::vector<int64_t> host_piece_chunks(int64_t nch)
     return plan;
 }
 
+// Token starts of the pieces of a problem of T tokens per batch row: host_piece_chunks when `split`, else one
+// piece; the last entry is the end (T, or past it when the last chunk is partial).
+std::vector<int64_t> piece_starts(int64_t T, bool split)
+{
+    std::vector<int64_t> first{0};
+    if (split) {
+        for (int64_t ch : host_piece_chunks((T + CH - 1) / CH))
+            first.push_back(first.back() + ch * CH);
+    } else {
+        first.push_back(T);
+    }
+    return first;
+}
+
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16 *src, float *dst, size_t n)
 {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
@@ -156,14 +170,10 @@ struct VarlenPiece {
     bool first_tail, last_tail;
 };
 
-kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const void *v, const void *g, const void *beta,
-                             float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
-                             const void *initial_state, void *final_state, kda_dtype_t state_dtype,
-                             const int64_t *cu, int N, int64_t T, int H)
+// The pieces of a varlen call (N > 1 sequences) in pipeline order, and their cu_seqlens arrays one after another;
+// returns the sequence cut into the tail (-1: none).
+int varlen_plan(const int64_t *cu, int N, int64_t T, std::vector<VarlenPiece> &pl, std::vector<int64_t> &cus)
 {
-    const size_t row = (size_t)H * D;                  // elements of one token's q / k / v / g / out
-    const size_t smat = (size_t)H * D * D;             // state elements of one sequence
-    const size_t sbytes = state_dtype == KDA_DTYPE_FP32 ? 4 : 2;
     // the longest sequence's chunks, cut into a halving tail, when it has enough of them
     int star = 0;
     for (int s = 1; s < N; ++s)
@@ -202,8 +212,6 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
         if (N > s0)
             ranges.push_back({s0, N});
     }
-    std::vector<VarlenPiece> pl;
-    std::vector<int64_t> cus;
     for (const auto &r : ranges) {
         const int s0 = r.first, s1 = r.second;
         pl.push_back({cu[s0], cu[s1] - cu[s0], s0, s1 - s0, cus.size(), false, false, false});
@@ -217,6 +225,20 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
         cus.push_back(0);
         cus.push_back(pt);
     }
+    return star;
+}
+
+kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const void *v, const void *g, const void *beta,
+                             float scale, void *out, const float *A_log, const float *dt_bias, float lower_bound,
+                             const void *initial_state, void *final_state, kda_dtype_t state_dtype,
+                             const int64_t *cu, int N, int64_t T, int H)
+{
+    const size_t row = (size_t)H * D;                  // elements of one token's q / k / v / g / out
+    const size_t smat = (size_t)H * D * D;             // state elements of one sequence
+    const size_t sbytes = state_dtype == KDA_DTYPE_FP32 ? 4 : 2;
+    std::vector<VarlenPiece> pl;
+    std::vector<int64_t> cus;
+    const int star = varlen_plan(cu, N, T, pl, cus);
     int64_t max_t = 0;
     int max_n = 0;
     size_t max_ws = 0;
@@ -228,7 +250,7 @@ kda_status_t run_host_varlen(HostCtx *c, const void *q, const void *k, const voi
     }
     const int pieces = (int)pl.size();
     const int ring = pieces > 1 ? HOST_RING : 1;
-    const bool chain = !tail_chunks.empty();
+    const bool chain = star >= 0;   // the tail sequence's state passes between its pieces
 
     cudaStream_t sc = c->s_comp;
     DevBufs bufs;
@@ -364,18 +386,11 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
     const bool has_state = initial_state || final_state;
 
     // pieces of whole 64-token chunks (host_piece_chunks); piece p starts at token first[p]
-    std::vector<int64_t> first{0};
-    int64_t PT = T;   // tokens of the largest piece
-    if (!varlen && T > HOST_MIN_PIECE) {
-        PT = 0;
-        for (int64_t ch : host_piece_chunks((T + CH - 1) / CH)) {
-            PT = std::max(PT, ch * CH);
-            first.push_back(first.back() + ch * CH);
-        }
-    } else {
-        first.push_back(T);
-    }
+    const std::vector<int64_t> first = piece_starts(T, !varlen && T > HOST_MIN_PIECE);
     const int64_t pieces = (int64_t)first.size() - 1;
+    int64_t PT = 0;   // tokens of the largest piece
+    for (int64_t p = 0; p < pieces; ++p)
+        PT = std::max(PT, first[p + 1] - first[p]);
     const int ring = pieces > 1 ? HOST_RING : 1;
     const size_t tok_cap = (size_t)B * (size_t)PT;     // tokens of one piece (all batch rows)
 
@@ -503,3 +518,36 @@ kda_status_t run_host(const void *q, const void *k, const void *v, const void *g
 }
 
 }  // namespace kda
+
+extern "C" int kda_fwd_host_plan(int N, int64_t T, const int64_t *cu_seqlens, int64_t *first_token, int64_t *tokens,
+                                 int *first_seq, int *seqs, int max_pieces)
+{
+    using namespace kda;
+    if (N < 1 || T < 0 || T > ((int64_t)1 << 40) || max_pieces < 0 ||
+        (max_pieces > 0 && (!first_token || !tokens || !first_seq || !seqs)))
+        return -1;
+    if (cu_seqlens && kda_check_cu_seqlens(cu_seqlens, N, T) != KDA_OK)
+        return -1;
+    int n = 0;
+    auto put = [&](int64_t t0, int64_t pt, int s0, int ns) {
+        if (n < max_pieces) {
+            first_token[n] = t0;
+            tokens[n] = pt;
+            first_seq[n] = s0;
+            seqs[n] = ns;
+        }
+        ++n;
+    };
+    if (cu_seqlens && N > 1 && T > HOST_MIN_PIECE) {   // the choice run_host makes
+        std::vector<VarlenPiece> pl;
+        std::vector<int64_t> cus;
+        varlen_plan(cu_seqlens, N, T, pl, cus);
+        for (const VarlenPiece &pc : pl)
+            put(pc.t0, pc.pt, pc.s0, pc.ns);
+    } else {
+        const std::vector<int64_t> first = piece_starts(T, !cu_seqlens && T > HOST_MIN_PIECE);
+        for (size_t p = 0; p + 1 < first.size(); ++p)
+            put(first[p], std::min<int64_t>(first[p + 1], T) - first[p], 0, N);
+    }
+    return n;
+}

@@ -299,6 +299,20 @@ kda_status_t kda_fwd_host(const void *q, const void *k, const void *v, const voi
                           kda_dtype_t state_dtype, const int64_t *cu_seqlens, int N, int64_t T, int H);
 
 /*
+ * kda_fwd_host_plan -- the pieces kda_fwd_host cuts a problem of N sequences and T tokens into, in
+ * the order it copies them in (a host-side query: it touches no device).  cu_seqlens is a HOST
+ * pointer (varlen) or NULL (fixed length, T tokens per batch row).  Piece i covers token rows
+ * [first_token[i], first_token[i] + tokens[i]) (of every batch row, fixed length) and sequences
+ * [first_seq[i], first_seq[i] + seqs[i]) (fixed length: 0 and N); a piece of the longest varlen
+ * sequence covers one sequence (seqs = 1) in part, starting at a multiple of 64 tokens from the
+ * sequence's start.  Writes at most max_pieces entries (the four arrays may be NULL when it is 0)
+ * and returns the number of pieces, or -1 for N < 1, T outside [0, 2^40], or a cu_seqlens that
+ * kda_check_cu_seqlens rejects.  The plan depends on N, T and cu_seqlens only.
+ */
+int kda_fwd_host_plan(int N, int64_t T, const int64_t *cu_seqlens, int64_t *first_token, int64_t *tokens,
+                      int *first_seq, int *seqs, int max_pieces);
+
+/*
  * Returns the workspace memory kda_fwd's pools hold but no call is using to the driver.
  * KDA_ERR_CUDA if a pool could not be trimmed.
  */
