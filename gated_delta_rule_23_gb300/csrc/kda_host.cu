@@ -1,15 +1,18 @@
 // Host-buffer entry point (kda_fwd_host): the forward pass on host memory, with the host-to-device
 // copies, the kernels and the device-to-host copies pipelined over pieces of the sequence.
 //
-// Fixed-length problems are cut into pieces of whole 64-token chunks.  Piece p's rows of q, k, v, g,
-// beta go to a device ring slot on a copy-in stream, the forward pass for the piece runs on a
-// compute stream with the state chained between pieces in fp32, and the piece's output rows go
-// back on a copy-out stream, so the copies of neighbouring pieces overlap the kernels.  Because the
-// pieces start at chunk boundaries and the chained state is fp32 (the state the recurrence keeps
-// internally), the results are bit-identical to one kda_fwd call over the whole problem.  Varlen
-// problems (cu_seqlens) are cut into pieces of whole sequences, which share no state: each piece is a
-// varlen call of its own, with its cu_seqlens shifted to start at 0 and its sequences' slices of the
-// states, so the results are again the bits of one call (every (sequence, head) pair is computed alone).
+// Fixed-length problems are cut into pieces of whole 64-token chunks (big pieces, then a tail that
+// halves, so that little work follows the last copy in).  Piece p's rows of q, k, v, g, beta go to a
+// device ring slot on a copy-in stream, the forward pass for the piece runs on a compute stream with
+// the state chained between pieces in fp32, and the piece's output rows go back on a copy-out stream,
+// so the copies of neighbouring pieces overlap the kernels.  Because the pieces start at chunk
+// boundaries and the chained state is fp32 (the state the recurrence keeps internally), the results
+// are bit-identical to one kda_fwd call over the whole problem (unless either takes the scan along T,
+// whose grouping differs).  Varlen problems (cu_seqlens) are cut into pieces of whole sequences, which
+// share no state: each piece is a varlen call of its own, with its cu_seqlens shifted to start at 0 and
+// its sequences' slices of the states; the longest sequence comes last, in pieces of whole chunks with
+// its state chained in fp32.  The results are again the bits of one call (every (sequence, head) pair
+// is computed alone, its chunks where one call puts them).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
