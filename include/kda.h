@@ -117,8 +117,8 @@ typedef enum {
  * order of operations) but within the same tolerances.
  *
  * Otherwise, fixed-length problems with N x H <= 64 (sequence, head) pairs and at least 32 chunks of 64
- * tokens per sequence run in up to 8 pieces of whole chunks along T (more for longer sequences
- * and fewer pairs; at least 16 chunks each), all on `stream`: the prep kernel
+ * tokens per sequence run in 2 to 8 pieces of whole chunks along T (more pieces for longer
+ * sequences and fewer pairs; at least 16 chunks each; kda_fwd_pieces), all on `stream`: the prep kernel
  * of the next piece is launched as a programmatic dependent of the recurrence over the current
  * one (it reads nothing that recurrence writes), so the two run side by side on different SMs;
  * the prep kernel completes only after that recurrence has.  The state passes between pieces in
