@@ -117,8 +117,9 @@ typedef enum {
  * order of operations) but within the same tolerances.
  *
  * Otherwise, fixed-length problems with N x H <= 64 (sequence, head) pairs and at least 32 chunks of 64
- * tokens per sequence run in 2 to 8 pieces of whole chunks along T (more pieces for longer
- * sequences and fewer pairs; at least 16 chunks each; kda_fwd_pieces), all on `stream`: the prep kernel
+ * tokens per sequence run in pieces of whole chunks along T where the overlap pays for a piece's
+ * cost (kda_fwd_pieces: up to 8, more for longer sequences and fewer pairs; at least 16 chunks
+ * each), all on `stream`: the prep kernel
  * of the next piece is launched as a programmatic dependent of the recurrence over the current
  * one (it reads nothing that recurrence writes), so the two run side by side on different SMs;
  * the prep kernel completes only after that recurrence has.  The state passes between pieces in
@@ -144,7 +145,8 @@ size_t kda_fwd_workspace_size(int N, int64_t T, int H, int varlen);
 /*
  * Number of pieces along T in which kda_fwd, kda_fwd_ws and kda_fwd_noalloc run a problem of this
  * size on the current device (see kda_fwd): 1 when the call runs without pieces (every varlen
- * problem, and the fixed-length problems outside the piece rule), 2 to 8 otherwise.  0 for invalid
+ * problem, the fixed-length problems outside the piece rule, and those whose overlap would not pay
+ * for a second piece), 2 to 8 otherwise.  0 for invalid
  * sizes, or when the device's SM count cannot be read.  Launches nothing.
  */
 int kda_fwd_pieces(int N, int64_t T, int H, int varlen);
