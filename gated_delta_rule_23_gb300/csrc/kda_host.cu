@@ -30,7 +30,7 @@ namespace {
 constexpr int HOST_RING = 2;            // device piece buffers in flight
 constexpr int64_t HOST_MAX_PIECES = 8;  // varlen pieces; fixed-length big pieces
 constexpr int64_t HOST_MIN_PIECE = 512; // tokens
-constexpr int64_t HOST_TAIL_MIN = 2;    // chunks of the last fixed-length piece
+constexpr int64_t HOST_TAIL_MIN = 2;    // chunks of the last piece of a halving tail
 
 // Chunks per fixed-length piece.  Copying a token in takes about twice as long as computing it and copying its
 // output back, so a piece's compute and copy-out hide behind the copy-in of the pieces after it only if those
