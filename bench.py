@@ -481,9 +481,14 @@ def run_ours(args, p, idx, rank, world):
     if world > 1:
         dist.barrier()
     t_e0 = time.perf_counter()
+    e2e_calls = []
     for _ in range(n_e2e):
+        t_c = time.perf_counter()
         e2e_step()
+        e2e_calls.append((time.perf_counter() - t_c) * 1e3)
     e2e_ms = max_over_ranks((time.perf_counter() - t_e0) * 1e3 / n_e2e, world, "cuda")
+    e2e_calls.sort()
+    e2e_median = e2e_calls[len(e2e_calls) // 2]
     h2d_bytes = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h_bytes = sum(t.numel() * t.element_size() for t in (out_h, fin_h) if t is not None)
     link = measure_link(h2d_bytes, d2h_bytes) if rank == 0 else None
@@ -540,7 +545,9 @@ def run_ours(args, p, idx, rank, world):
                 # the host link as the bound of the end-to-end call: one plain copy of the step's input bytes
                 # and one of its output bytes (pinned memory, CUDA events), alone and both directions at once;
                 # the floor is the slower of the concurrent pair, frac = floor / e2e time
-                "link": link, "link_frac": None if link is None else link["floor_ms"] / e2e_ms},
+                "link": link, "link_frac": None if link is None else link["floor_ms"] / e2e_ms,
+                # the per-call spread (rank 0): a mean above the median means slow single calls (the host is shared)
+                "median_call_ms": e2e_median, "max_call_ms": e2e_calls[-1]},
         "clocks": sampler.summary(),
         "variants_ms_per_step": variant_ms,
         "pieces_per_step": pieces_per_step(p),
