@@ -240,3 +240,37 @@ def scan_form(p, groups, C=64):
                     S = S_next
             final[n, h] = S.T
     return out, final, Ms
+
+
+def lookahead_form(p, C=64):
+    """The chunk recurrence with a two-chunk lookahead: the product X_{c+1} = W_{c+1} S_{c+1} that the next chunk's
+    U = U0 - X needs is formed from chunk c's start state and U instead of from S_{c+1}:
+        X_{c+1} = (W_{c+1} Diag(Gamma_C,c)) S_c + (W_{c+1} K~_c^T) U_c,
+    which follows from S_{c+1} = Diag(Gamma_C,c) S_c + K~_c^T U_c.  Chunks restart at every sequence.  Returns
+    (out, final) like chunked_direct and, per chunk after the first of a sequence, the relative size
+    |P_{c+1} U_c| / |X_{c+1}| of the lookahead term."""
+    qh, kh, v, b, a = prepare(p)
+    H = p.H
+    out = np.zeros(qh.shape)
+    final = np.zeros((p.N, H, 128, 128))
+    init = p.initial_state_f64()
+    shares = []
+    for n, bos, eos in seq_ranges(p):
+        bidx = 0 if p.cu_seqlens is not None else n
+        for h in range(H):
+            S = np.zeros((128, 128)) if init is None else init[n, h].T.copy()
+            starts = list(range(bos, eos, C))
+            ops = [_chunk_operands(qh, kh, v, b, a, (bidx, slice(c0, min(eos, c0 + C)), h), C, p.scale)
+                   for c0 in starts]
+            X = ops[0]["W"] @ S if ops else None
+            for i, (c0, op) in enumerate(zip(starts, ops)):
+                U = op["U0"] - X
+                out[bidx, c0:c0 + op["W"].shape[0], h] = op["Qg"] @ S + p.scale * (op["Aqk"] @ U)
+                if i + 1 < len(ops):
+                    Wn = ops[i + 1]["W"]
+                    PU = (Wn @ op["Kt"].T) @ U
+                    X = (Wn * op["gl"][None, :]) @ S + PU
+                    shares.append(np.linalg.norm(PU) / max(np.linalg.norm(X), 1e-300))
+                S = op["gl"][:, None] * S + op["Kt"].T @ U
+            final[n, h] = S.T
+    return out, final, shares

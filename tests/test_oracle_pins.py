@@ -207,6 +207,20 @@ def test_scan_along_t_equals_recurrence(groups, lb):
         assert min(np.linalg.norm(M) for M in Ms) > (1.0 if lb == 0.0 else 1e-6)
 
 
+@pytest.mark.parametrize("lb", [-0.05, 0.0, -5.0])
+def test_lookahead_form_equals_recurrence(lb):
+    """The two-chunk lookahead of the chunk recurrence (the next chunk's W S formed as W Diag(Gamma_C) S_c +
+    (W K~^T) U_c from this chunk's start state) equals the token recurrence, varlen with ragged and one-chunk
+    sequences; with slow or no decay the lookahead term carries a large part of the product, so a mistake in it
+    (a transposed or missing factor) would show."""
+    p = inputs.make_problem(B=1, T=600, H=1, seed=33, lower_bound=lb, cu_seqlens=np.array([0, 40, 300, 600]))
+    out, fin = run(p)
+    oc, fc, shares = chunked_ref.lookahead_form(p)
+    assert rel_l2(oc, out) < 1e-10 and rel_l2(fc, fin) < 1e-10
+    if lb > -1.0:
+        assert len(shares) >= 5 and min(shares) > 0.05
+
+
 def test_subblock_factorised_chunked_form_equals_recurrence():
     """The 16-row sub-block factorisation of the decay (no overflow at lower_bound = -5, C = 64)."""
     p = inputs.make_problem(B=1, T=200, H=2, seed=13, cu_seqlens=np.array([0, 1, 64, 65, 200]))
