@@ -477,7 +477,7 @@ def run_ours(args, p, idx, rank, world):
 
     for _ in range(3):   # the first call of a process also reserves the pool's memory
         e2e_step()
-    n_e2e = max(3, min(args.steps, 50))   # a mean over 50 calls: one slow call (a host-side stall) moves it little
+    n_e2e = max(3, min(args.steps, 50))   # a mean over 50 calls: one slow call moves it little
     if world > 1:
         dist.barrier()
     t_e0 = time.perf_counter()
@@ -546,7 +546,7 @@ def run_ours(args, p, idx, rank, world):
                 # and one of its output bytes (pinned memory, CUDA events), alone and both directions at once;
                 # the floor is the slower of the concurrent pair, frac = floor / e2e time
                 "link": link, "link_frac": None if link is None else link["floor_ms"] / e2e_ms,
-                # the per-call spread (rank 0): a mean above the median means slow single calls (the host is shared)
+                # the per-call spread (rank 0): a mean well above the median marks slow single calls
                 "median_call_ms": e2e_median, "max_call_ms": e2e_calls[-1]},
         "clocks": sampler.summary(),
         "variants_ms_per_step": variant_ms,
